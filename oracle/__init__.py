@@ -1,0 +1,212 @@
+"""CPU oracle for the DFlash2 draft-proposal hot path — TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg (and its ``--impl reference`` arm) may import this package.  The product
+library never links, loads or calls it, and it imports nothing from the
+product package: the two implementations share no code.
+
+The arithmetic lives in ``oracle.c`` (plain C, double accumulation, one
+rounding at each output).  This module compiles it with gcc on first use and
+marshals numpy arrays through ctypes.  bf16 tensors travel as ``uint16`` bit
+patterns.
+
+Every function is pinned by ``tests/test_oracle_*.py`` against brute force,
+closed forms, invariants or library special cases; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32 = 0
+BF16 = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc, OpenMP, no FP contraction)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off",
+           "-fno-fast-math", "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.c_void_p
+            i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+            lib.oracle_round_bf16.argtypes = [f64]
+            lib.oracle_round_bf16.restype = ctypes.c_uint16
+            lib.oracle_conv.argtypes = [P, P, P, i64, P, i64, i32, i32, i32, i32, i32]
+            lib.oracle_conv.restype = ctypes.c_int
+            lib.oracle_unary_rows.argtypes = [P, P, P, i64, i32, i64, i64, f64, f64, i32, P]
+            lib.oracle_unary_rows.restype = None
+            lib.oracle_topk.argtypes = [P, i64, i64, i32, P, P]
+            lib.oracle_topk.restype = ctypes.c_int
+            lib.oracle_project.argtypes = [P, P, i64, i32, i32, i32, P]
+            lib.oracle_project.restype = None
+            lib.oracle_lattice.argtypes = [P, P, P, i64, P, P, P, i32, i32, i32, i32, i32, P]
+            lib.oracle_lattice.restype = i64
+            lib.oracle_walk.argtypes = [P, P, P, P, P, i32, i32, i32, P, P, P]
+            lib.oracle_walk.restype = None
+            lib.oracle_d2t.argtypes = [P, P, i64, i64, i64, P]
+            lib.oracle_d2t.restype = i64
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _elem(a: np.ndarray):
+    """Return (contiguous array, dtype code) for a float32 or bf16-bits array."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float32:
+        return a, F32
+    if a.dtype == np.uint16:
+        return a, BF16
+    raise TypeError(f"oracle takes float32 or uint16 (bf16 bits), got {a.dtype}")
+
+
+def _same(code, *arrays):
+    for a in arrays:
+        if _elem(a)[1] != code:
+            raise TypeError("all floating inputs of one call must share a dtype")
+
+
+def round_bf16(v: float) -> int:
+    """Nearest bf16 bit pattern of a double, ties to even, one rounding."""
+    return int(_load().oracle_round_bf16(float(v)))
+
+
+def conv(x, base, delta, block_size: int, group_size: int, taps: int,
+         delta_row_stride: int | None = None):
+    """Grouped dynamic depthwise conv; returns out with x's dtype."""
+    x, code = _elem(x)
+    base, _ = _elem(base)
+    delta, _ = _elem(delta)
+    _same(code, base, delta)
+    n, hidden = x.shape
+    groups = hidden // group_size
+    if delta_row_stride is None:
+        delta_row_stride = taps * groups
+    out = np.empty_like(x)
+    rc = _load().oracle_conv(_ptr(x), _ptr(base), _ptr(delta), delta_row_stride,
+                             _ptr(out), n, hidden, group_size, taps, block_size, code)
+    if rc:
+        raise ValueError("oracle_conv rejected its arguments")
+    return out
+
+
+def unary_rows(h, lm_head, target_vocab: int, mult: float, cap: float,
+               rows=None) -> np.ndarray:
+    """u (double) for the selected rows of h over the whole draft vocab."""
+    h, code = _elem(h)
+    lm_head, _ = _elem(lm_head)
+    _same(code, lm_head)
+    hidden = h.shape[1]
+    vd = lm_head.shape[0]
+    if rows is None:
+        sel, n_sel = None, h.shape[0]
+    else:
+        sel = np.ascontiguousarray(rows, dtype=np.int64)
+        n_sel = sel.shape[0]
+    u = np.empty((n_sel, vd), dtype=np.float64)
+    _load().oracle_unary_rows(_ptr(h), _ptr(lm_head), _ptr(sel), n_sel, hidden, vd,
+                              target_vocab, float(mult), float(cap), code, _ptr(u))
+    return u
+
+
+def topk(u: np.ndarray, k: int):
+    """Top-K (ids int64, values float32) per row of a double u matrix."""
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    n, vd = u.shape
+    ids = np.empty((n, k), dtype=np.int64)
+    vals = np.empty((n, k), dtype=np.float32)
+    if _load().oracle_topk(_ptr(u), n, vd, k, _ptr(ids), _ptr(vals)):
+        raise ValueError("oracle_topk failed")
+    return ids, vals
+
+
+def project(h, proj) -> np.ndarray:
+    """g = h . proj^T in double; proj is [rank, hidden]."""
+    h, code = _elem(h)
+    proj, _ = _elem(proj)
+    _same(code, proj)
+    rows, hidden = h.shape
+    rank = proj.shape[0]
+    g = np.empty((rows, rank), dtype=np.float64)
+    _load().oracle_project(_ptr(h), _ptr(proj), rows, hidden, rank, code, _ptr(g))
+    return g
+
+
+def lattice(g, A, B, anchors, cand, cand_u):
+    """Full [batch, slots, K, K] fp32 edge lattice and the out-of-range count."""
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    A, code = _elem(A)
+    B, _ = _elem(B)
+    _same(code, B)
+    cand = np.ascontiguousarray(cand, dtype=np.int64)
+    batch, slots, k = cand.shape
+    anchors = np.ascontiguousarray(anchors, dtype=np.int64)
+    cand_u = np.ascontiguousarray(cand_u, dtype=np.float32)
+    rank = A.shape[1]
+    scores = np.empty((batch, slots, k, k), dtype=np.float32)
+    errors = _load().oracle_lattice(_ptr(g), _ptr(A), _ptr(B), A.shape[0], _ptr(anchors),
+                                    _ptr(cand), _ptr(cand_u), batch, slots, rank, k,
+                                    code, _ptr(scores))
+    return scores, int(errors)
+
+
+def walk(scores, cand, uniforms, temperatures, greedy):
+    """Walk a lattice; returns (tokens int64 [B,S], q float32 [B,S,K], index int32 [B,S])."""
+    scores = np.ascontiguousarray(scores, dtype=np.float32)
+    cand = np.ascontiguousarray(cand, dtype=np.int64)
+    batch, slots, k = cand.shape
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32)
+    temperatures = np.ascontiguousarray(temperatures, dtype=np.float32)
+    greedy = np.ascontiguousarray(greedy, dtype=np.uint8)
+    tokens = np.empty((batch, slots), dtype=np.int64)
+    q = np.empty((batch, slots, k), dtype=np.float32)
+    chosen = np.empty((batch, slots), dtype=np.int32)
+    _load().oracle_walk(_ptr(scores), _ptr(cand), _ptr(uniforms), _ptr(temperatures),
+                        _ptr(greedy), batch, slots, k, _ptr(tokens), _ptr(q), _ptr(chosen))
+    return tokens, q, chosen
+
+
+def d2t(draft_ids, table, draft_vocab: int, target_vocab: int):
+    """Draft-to-target remap; returns (target ids, error count)."""
+    ids = np.ascontiguousarray(draft_ids, dtype=np.int64)
+    tbl = None if table is None else np.ascontiguousarray(table, dtype=np.int64)
+    out = np.empty_like(ids)
+    errors = _load().oracle_d2t(_ptr(ids), _ptr(tbl), ids.size, draft_vocab,
+                                target_vocab, _ptr(out))
+    return out, int(errors)
+
+
+def selector(h, proj, A, B, anchors, cand, cand_u, uniforms, temperatures, greedy):
+    """Projection, lattice and walk chained: the selector stage end to end."""
+    batch, slots, _ = np.shape(cand)
+    g = project(np.asarray(h).reshape(batch * slots, -1), proj)
+    scores, errors = lattice(g, A, B, anchors, cand, cand_u)
+    tokens, q, chosen = walk(scores, cand, uniforms, temperatures, greedy)
+    return dict(g=g, scores=scores, errors=errors, tokens=tokens, q=q, chosen=chosen)

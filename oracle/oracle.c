@@ -1,0 +1,392 @@
+/*
+ * Plain, slow CPU oracle for the DFlash2 draft-proposal hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: it exists so that tests, the smoke check and the benchmark's
+ * CPU-baseline leg can compare the CUDA library against an obviously correct
+ * restatement of the method.  It shares no code, header, table or helper with
+ * the CUDA library.
+ *
+ * Conventions
+ *   - Every floating-point accumulation runs in double from the exact input
+ *     values (bf16 and fp32 inputs widen exactly to double) and is rounded once
+ *     at the output.
+ *   - Where floating point decides an integer (top-K membership, the walk's
+ *     argmax and inverse-CDF draw) the decision is taken in fp32, the precision
+ *     of the sglang Triton walk ("[Spec] DFlash2: local convolution + candidate
+ *     selector", _selector_walk_kernel, which loads the scores as float32).
+ *   - dtype 0 = fp32 (float arrays), dtype 1 = bf16 (uint16 bit patterns).
+ *   - Parallelism is OpenMP over independent rows only; it cannot change a
+ *     result because no reduction crosses threads.
+ *
+ * Every function below is pinned by the CPU tests (tests/test_oracle_*.py)
+ * against brute force, closed forms, invariants or library special cases.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_F32 0
+#define ORACLE_BF16 1
+
+/* ---- element access ---------------------------------------------------- */
+
+static double bf16_bits_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double load_elem(const void *p, int64_t i, int dtype)
+{
+    if (dtype == ORACLE_BF16)
+        return bf16_bits_to_double(((const uint16_t *)p)[i]);
+    return (double)((const float *)p)[i];
+}
+
+/*
+ * Round a double to the nearest bf16 (ties to even) in ONE step.  Going
+ * through float first would round twice.  The value is scaled by a power of
+ * two so that it carries exactly 8 significant bits before the binary point;
+ * nearbyint() then rounds half-to-even in the default rounding mode.  Power of
+ * two scaling is exact, so the only rounding is the one in nearbyint().
+ */
+uint16_t oracle_round_bf16(double v)
+{
+    if (isnan(v))
+        return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return sign | 0x7F80;
+    int e;
+    frexp(a, &e); /* a = f * 2^e with f in [0.5, 1) */
+    int sh = 8 - e; /* a * 2^sh lies in [128, 256) */
+    if (e - 8 < -133)
+        sh = 133; /* below the normal range bf16 steps by 2^-133 */
+    double q = nearbyint(ldexp(a, sh));
+    double r = ldexp(q, -sh);
+    const double bf16_max = 3.3895313892515355e38; /* (2 - 2^-7) * 2^127 */
+    if (r > bf16_max)
+        return sign | 0x7F80;
+    float f = (float)r; /* exact: r has at most 8 significant bits */
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    return sign | (uint16_t)(bits >> 16);
+}
+
+static void store_elem(void *p, int64_t i, double v, int dtype)
+{
+    if (dtype == ORACLE_BF16)
+        ((uint16_t *)p)[i] = oracle_round_bf16(v);
+    else
+        ((float *)p)[i] = (float)v; /* one round-to-nearest-even */
+}
+
+/* ---- (1) block-causal grouped dynamic depthwise conv --------------------
+ * sglang "[Spec] DFlash2: local convolution + candidate selector",
+ * _grouped_conv: hidden is split into (groups, group_size); the coefficient of
+ * tap t for channel c of token i is base[t, c] + delta[i, t, c / group_size];
+ * tap t reads the token t rows earlier and is zeroed unless the in-block
+ * position (i mod block_size) is at least t.
+ *
+ *   out[i, c] = sum_{t < taps, pos(i) >= t} (base[t,c] + delta[i,t,c/gs]) * x[i-t, c]
+ *
+ * x, out: [n, hidden]; base: [taps, hidden]; delta row i starts at
+ * i * delta_row_stride and holds [taps, hidden / gs].
+ */
+int oracle_conv(const void *x, const void *base, const void *delta,
+                int64_t delta_row_stride, void *out, int64_t n, int32_t hidden,
+                int32_t group_size, int32_t taps, int32_t block_size,
+                int32_t dtype)
+{
+    if (n < 0 || hidden <= 0 || group_size <= 0 || hidden % group_size ||
+        taps <= 0 || block_size <= 0)
+        return 1;
+    const int64_t groups = hidden / group_size;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t pos = i % block_size;
+        for (int32_t c = 0; c < hidden; ++c) {
+            double acc = 0.0;
+            for (int32_t t = 0; t < taps; ++t) {
+                if (pos < t)
+                    continue; /* this tap would cross the block start */
+                double coef =
+                    load_elem(base, (int64_t)t * hidden + c, dtype) +
+                    load_elem(delta,
+                              i * delta_row_stride + (int64_t)t * groups +
+                                  c / group_size,
+                              dtype);
+                acc += coef * load_elem(x, (i - t) * hidden + c, dtype);
+            }
+            store_elem(out, i * hidden + c, acc, dtype);
+        }
+    }
+    return 0;
+}
+
+/* ---- (2)+(3) unary logits ------------------------------------------------
+ * z[m, v] = sum_j h[m, j] * lm_head[v, j]   (lm_head in nn.Linear layout)
+ * u = cap * tanh(mult * z / cap) when cap > 0, else mult * z
+ *   (output_multiplier / final_logit_softcapping of the DFlash2 draft config;
+ *   the pages name the two fields, the formula is the stated reading)
+ * u = -inf for padded vocab rows v >= target_vocab: the vLLM DSpark
+ *   padded-vocab review asks that [target_vocab, draft_vocab) be masked
+ *   before any top-k.
+ * Rows listed in `rows` (all rows when rows == NULL) are evaluated; u_out is
+ * [n_sel, draft_vocab] doubles.
+ */
+void oracle_unary_rows(const void *h, const void *lm_head, const int64_t *rows,
+                       int64_t n_sel, int32_t hidden, int64_t draft_vocab,
+                       int64_t target_vocab, double mult, double cap,
+                       int32_t dtype, double *u_out)
+{
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t r = 0; r < n_sel; ++r) {
+        for (int64_t v = 0; v < draft_vocab; ++v) {
+            const int64_t m = rows ? rows[r] : r;
+            double u;
+            if (v >= target_vocab) {
+                u = -INFINITY;
+            } else {
+                double z = 0.0;
+                for (int32_t j = 0; j < hidden; ++j)
+                    z += load_elem(h, m * hidden + j, dtype) *
+                         load_elem(lm_head, v * hidden + j, dtype);
+                u = cap > 0.0 ? cap * tanh(mult * z / cap) : mult * z;
+            }
+            u_out[r * draft_vocab + v] = u;
+        }
+    }
+}
+
+/* ---- (4) top-K ------------------------------------------------------------
+ * Per row, the K best (u, id) pairs with u taken in fp32: a full sort by u
+ * descending, equal u by smaller vocab id first, then the first K.  The order
+ * matters downstream: the walk's greedy tie rule picks the lowest candidate
+ * index and its inverse-CDF scans candidates in index order.
+ */
+typedef struct {
+    float u;
+    int64_t id;
+} oracle_pair;
+
+static int pair_order(const void *pa, const void *pb)
+{
+    const oracle_pair *a = (const oracle_pair *)pa;
+    const oracle_pair *b = (const oracle_pair *)pb;
+    if (a->u > b->u)
+        return -1;
+    if (a->u < b->u)
+        return 1;
+    return (a->id > b->id) - (a->id < b->id);
+}
+
+int oracle_topk(const double *u, int64_t n_rows, int64_t draft_vocab,
+                int32_t k, int64_t *ids, float *vals)
+{
+    if (k <= 0 || k > draft_vocab)
+        return 1;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        oracle_pair *p =
+            (oracle_pair *)malloc((size_t)draft_vocab * sizeof(oracle_pair));
+        if (!p) {
+#pragma omp atomic write
+            bad = 1;
+            continue;
+        }
+        for (int64_t v = 0; v < draft_vocab; ++v) {
+            p[v].u = (float)u[r * draft_vocab + v];
+            p[v].id = v;
+        }
+        qsort(p, (size_t)draft_vocab, sizeof(oracle_pair), pair_order);
+        for (int32_t i = 0; i < k; ++i) {
+            ids[r * k + i] = p[i].id;
+            vals[r * k + i] = p[i].u;
+        }
+        free(p);
+    }
+    return bad;
+}
+
+/* ---- (5) selector projection -----------------------------------------------
+ * project(h) of the selector edge formula, read as an nn.Linear(hidden, rank)
+ * without bias: g[m, j] = sum_i h[m, i] * proj[j, i], proj stored [rank, hidden].
+ */
+void oracle_project(const void *h, const void *proj, int64_t rows,
+                    int32_t hidden, int32_t rank, int32_t dtype, double *g)
+{
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t m = 0; m < rows; ++m) {
+        for (int32_t j = 0; j < rank; ++j) {
+            double acc = 0.0;
+            for (int32_t i = 0; i < hidden; ++i)
+                acc += load_elem(h, m * hidden + i, dtype) *
+                       load_elem(proj, (int64_t)j * hidden + i, dtype);
+            g[m * rank + j] = acc;
+        }
+    }
+}
+
+/* ---- (6) selector lattice ------------------------------------------------
+ * The sglang DFlash2 PR body scores adjacent transitions as
+ *   edge(p -> c) = < A[p] (elementwise *) project(h), B[c] > + unary[c].
+ * scores[b, s, kp, kc] is the edge from predecessor kp to candidate kc of
+ * slot s, matching the [batch, slots, K, K] layout the Triton walk indexes
+ * ((row*slots + slot)*K + previous)*K + k.  Slot 0's predecessor is the
+ * verified anchor token, so every kp row of slot 0 holds the anchor's edges.
+ * A and B are [table_rows, rank] indexed by draft ids.  An id outside
+ * [0, table_rows) counts as an error and contributes a zero table row.
+ * Returns the number of out-of-range ids met.
+ */
+int64_t oracle_lattice(const double *g, const void *A, const void *B,
+                       int64_t table_rows, const int64_t *anchors,
+                       const int64_t *cand, const float *cand_u, int32_t batch,
+                       int32_t slots, int32_t rank, int32_t k, int32_t dtype,
+                       float *scores)
+{
+    int64_t errors = 0;
+#pragma omp parallel for collapse(2) schedule(static) reduction(+ : errors)
+    for (int32_t b = 0; b < batch; ++b) {
+        for (int32_t s = 0; s < slots; ++s) {
+            const int64_t bs_row = (int64_t)b * slots + s;
+            for (int32_t kp = 0; kp < k; ++kp) {
+                int64_t p = s == 0 ? anchors[b] : cand[(bs_row - 1) * k + kp];
+                int p_ok = p >= 0 && p < table_rows;
+                if (!p_ok && (s > 0 || kp == 0))
+                    errors += 1;
+                for (int32_t kc = 0; kc < k; ++kc) {
+                    int64_t c = cand[bs_row * k + kc];
+                    int c_ok = c >= 0 && c < table_rows;
+                    if (!c_ok && kp == 0)
+                        errors += 1;
+                    double acc = 0.0;
+                    if (p_ok && c_ok) {
+                        for (int32_t j = 0; j < rank; ++j)
+                            acc += load_elem(A, p * rank + j, dtype) *
+                                   g[bs_row * rank + j] *
+                                   load_elem(B, c * rank + j, dtype);
+                    }
+                    acc += (double)cand_u[bs_row * k + kc];
+                    scores[(bs_row * k + kp) * k + kc] = (float)acc;
+                }
+            }
+        }
+    }
+    return errors;
+}
+
+/* ---- (7) selector walk -------------------------------------------------------
+ * Follows the sglang _selector_walk_kernel step by step, in fp32:
+ *   previous = 0 (the anchor row) at slot 0;
+ *   scores = lattice row `previous` of this slot;
+ *   greedy row:  index = smallest k with scores[k] == max(scores); q = one-hot;
+ *   sampled row: scaled = scores / T; e = exp(scaled - max(scaled));
+ *                p = e / sum(e); cdf = cumulative sum of p;
+ *                index = #{k : uniform >= cdf[k]}, capped at K - 1; q = p;
+ *   token = candidate[index]; previous = index.
+ * T is first clamped to at least 1e-5 (stage_sampling_params of the same PR).
+ * The sums run left to right in fp32; exp is taken in double and rounded to
+ * fp32 once (a correctly rounded fp32 exp for all practical purposes).
+ * chosen (nullable) receives the candidate index per (b, s).
+ */
+void oracle_walk(const float *scores, const int64_t *cand, const float *uniforms,
+                 const float *temperatures, const uint8_t *greedy, int32_t batch,
+                 int32_t slots, int32_t k, int64_t *tokens, float *q,
+                 int32_t *chosen)
+{
+#pragma omp parallel for schedule(static)
+    for (int32_t b = 0; b < batch; ++b) {
+        float t = temperatures[b];
+        if (!(t >= 1e-5f))
+            t = 1e-5f;
+        const int is_greedy = greedy[b] != 0;
+        float *scaled = (float *)malloc((size_t)k * sizeof(float));
+        int32_t previous = 0;
+        for (int32_t s = 0; s < slots; ++s) {
+            const int64_t bs_row = (int64_t)b * slots + s;
+            const float *row = scores + (bs_row * k + previous) * k;
+            float *qr = q + bs_row * k;
+            int32_t index = 0;
+            if (is_greedy) {
+                float best = row[0];
+                for (int32_t i = 1; i < k; ++i)
+                    if (row[i] > best)
+                        best = row[i];
+                index = k;
+                for (int32_t i = 0; i < k; ++i)
+                    if (row[i] == best && i < index)
+                        index = i;
+                for (int32_t i = 0; i < k; ++i)
+                    qr[i] = i == index ? 1.0f : 0.0f;
+            } else {
+                float mx = -INFINITY;
+                for (int32_t i = 0; i < k; ++i) {
+                    scaled[i] = row[i] / t;
+                    if (scaled[i] > mx)
+                        mx = scaled[i];
+                }
+                float total = 0.0f;
+                for (int32_t i = 0; i < k; ++i) {
+                    float d = scaled[i] - mx;
+                    qr[i] = (float)exp((double)d);
+                    total += qr[i];
+                }
+                for (int32_t i = 0; i < k; ++i)
+                    qr[i] = qr[i] / total;
+                const float uni = uniforms[bs_row];
+                float cdf = 0.0f;
+                index = 0;
+                for (int32_t i = 0; i < k; ++i) {
+                    cdf += qr[i];
+                    if (uni >= cdf)
+                        index += 1;
+                }
+                if (index > k - 1)
+                    index = k - 1;
+            }
+            tokens[bs_row] = cand[bs_row * k + index];
+            if (chosen)
+                chosen[bs_row] = index;
+            previous = index;
+        }
+        free(scaled);
+    }
+}
+
+/* ---- (8) draft-to-target id remap -----------------------------------------
+ * vLLM Qwen3DSparkForCausalLM.map_draft_to_target: d2t holds OFFSETS, so the
+ * target id is draft + d2t[draft]; with no table (draft vocab >= target vocab,
+ * the padded-vocab case) the map is the identity.  Ids that are not valid
+ * draft ids, or that land outside [0, target_vocab), count as errors and are
+ * written as 0.  Returns the number of errors.
+ */
+int64_t oracle_d2t(const int64_t *draft_ids, const int64_t *d2t, int64_t n,
+                   int64_t draft_vocab, int64_t target_vocab, int64_t *out)
+{
+    int64_t errors = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t d = draft_ids[i];
+        if (d < 0 || d >= draft_vocab) {
+            out[i] = 0;
+            errors += 1;
+            continue;
+        }
+        int64_t t = d2t ? d + d2t[d] : d;
+        if (t < 0 || t >= target_vocab) {
+            out[i] = 0;
+            errors += 1;
+            continue;
+        }
+        out[i] = t;
+    }
+    return errors;
+}

@@ -1,0 +1,24 @@
+"""Shared pytest setup.
+
+Markers: ``gpu`` marks tests that launch CUDA kernels through the C ABI; the
+CPU suite runs with ``-m "not gpu"``.
+"""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and libdflash2.so")
+
+
+@pytest.fixture(scope="session")
+def ora():
+    import oracle
+    oracle.build()
+    return oracle
