@@ -1,0 +1,313 @@
+// Persistent warp-specialised bf16 GEMM on the 5th-generation tensor cores.
+//
+//   C[m, v] = sum_j h[m, j] * w[v, j]      (w: lm_head or selector projection)
+//
+// Swap-AB: the weight rows are the MMA's M side (128-row tiles) and the
+// tokens its N side (bn-column tiles, bn <= 256), so the fp32 accumulator of
+// one tile is 128 TMEM lanes x bn columns and each epilogue thread owns one
+// weight row (one vocab id) across the tile's tokens.
+//
+// Roles (192 threads, one CTA per SM, persistent over work items):
+//   warp 0  lane 0: TMA producer (cp.async.bulk.tensor, 128-byte swizzle)
+//   warp 1  lane 0: MMA issuer (tcgen05.mma kind::f16, accumulator in TMEM)
+//   warps 2-5     : epilogue (tcgen05.ld; 4 warps cover the 128 TMEM lanes)
+// Shared-memory stages are handed over with mbarriers (full: TMA bytes
+// landed; empty: the MMAs reading the stage completed).  Two TMEM
+// accumulators alternate so the epilogue of one tile overlaps the MMAs of
+// the next.  Every wait is bounded (common.cuh).
+//
+// Work items are ordered with the token tile fastest, so the CTAs that run
+// at the same time share weight tiles in L2 and the weight matrix streams
+// from HBM about once.
+#include "kernels.h"
+
+namespace dflash2 {
+namespace {
+
+constexpr uint32_t kWTileBytes = kGemmTileW * kGemmTileK * 2;  // 16 KiB
+
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+// Which weight tile the j-th tile of this launch's pass is.
+__device__ __forceinline__ int pass_tile(const GemmParams &p, int j) {
+    if (p.mode == kGemmPilot) return j * p.pilot_stride;
+    if (p.mode == kGemmFilter) {
+        const int per = p.pilot_stride - 1;  // non-pilot tiles between two pilot tiles
+        const int in_blocks = p.n_pilot * per;
+        if (per > 0 && j < in_blocks) return (j / per) * p.pilot_stride + 1 + (j % per);
+        return p.n_pilot * p.pilot_stride + (j - in_blocks);
+    }
+    return j;
+}
+
+struct Item {
+    int wt, nt, ks, j;
+};
+__device__ __forceinline__ Item decode(const GemmParams &p, int w) {
+    Item it;
+    it.ks = w % p.k_splits;
+    const int rest = w / p.k_splits;
+    it.nt = rest % p.n_tok_tiles;
+    it.j = rest / p.n_tok_tiles;
+    it.wt = pass_tile(p, it.j);
+    return it;
+}
+
+// Epilogue of 32 accumulator columns (tokens m0 .. m0+31) of one weight row v.
+__device__ __forceinline__ void epilogue_chunk(const GemmParams &p, const float (&z)[32], int64_t v,
+                                               int row_in_tile, int m0, int ncols, const Item &it,
+                                               int lane) {
+    if (p.mode == kGemmStore) {
+        if (v < p.rows_w) {
+            float *o = p.out + (int64_t)it.ks * p.split_stride + v;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int m = m0 + i;
+                if (i < ncols && m < p.rows_h) o[(int64_t)m * p.ldo] = z[i];
+            }
+        }
+    } else if (p.mode == kGemmPilot) {
+        const bool valid = v < p.rows_w && v < p.target_vocab;
+        float *o = p.out + (int64_t)it.j * kGemmTileW + row_in_tile;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int m = m0 + i;
+            if (i < ncols && m < p.rows_h)
+                o[(int64_t)m * p.ldo] = valid ? unary_transform(z[i], p.mult, p.cap) : -INFINITY;
+        }
+    } else {
+        const bool valid_v = v < p.rows_w && v < p.target_vocab;
+        const int my_m = m0 + lane;
+        const uint64_t th_lane = (lane < ncols && my_m < p.rows_h) ? p.theta[my_m] : ~0ull;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int m = m0 + i;
+            const uint64_t th = shfl_u64(th_lane, i);
+            bool pass = false;
+            uint64_t key = 0;
+            if (valid_v && i < ncols && m < p.rows_h) {
+                key = make_key(unary_transform(z[i], p.mult, p.cap), (uint32_t)v);
+                pass = key >= th;
+            }
+            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
+            if (bal) {
+                const int leader = __ffs(bal) - 1;
+                uint32_t base = 0;
+                if (lane == leader) base = atomicAdd(p.cnt + m, (uint32_t)__popc(bal));
+                base = __shfl_sync(0xFFFFFFFFu, base, leader);
+                if (pass) {
+                    const uint32_t slot = base + (uint32_t)__popc(bal & ((1u << lane) - 1u));
+                    if (slot < (uint32_t)p.cand_cap) p.cand[(int64_t)m * p.cand_cap + slot] = key;
+                }
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_h,
+                   const GemmParams p) {
+    extern __shared__ uint8_t dsmem[];
+    __shared__ uint64_t full_bar[kGemmMaxStages];
+    __shared__ uint64_t empty_bar[kGemmMaxStages];
+    __shared__ uint64_t acc_full[2];
+    __shared__ uint64_t acc_empty[2];
+    __shared__ uint64_t drain_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t h_bytes = (uint32_t)p.bn * kGemmTileK * 2;
+    uint8_t *w_smem = smem;
+    uint8_t *h_smem = smem + (size_t)p.stages * kWTileBytes;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t tmem_cols = 2 * p.acc_cols;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], 4);
+        }
+        mbar_init(&drain_bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_slot, tmem_cols);
+        tmem_relinquish();
+    }
+    if (warp == 1 && lane == 0) {
+        prefetch_tmap(&tm_w);
+        prefetch_tmap(&tm_h);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const int total = p.pass_tiles * p.n_tok_tiles * p.k_splits;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                const Item item = decode(p, w);
+                const int kb0 = item.ks * p.kb_per_split;
+                const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int s = (int)(it % (uint32_t)p.stages);
+                    const uint32_t par = ((it / (uint32_t)p.stages) & 1u) ^ 1u;
+                    if (!mbar_wait(&empty_bar[s], par, &abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full_bar[s], kWTileBytes + h_bytes);
+                    tma_load_2d(w_smem + (size_t)s * kWTileBytes, &tm_w, &full_bar[s],
+                                kb * kGemmTileK, item.wt * kGemmTileW);
+                    tma_load_2d(h_smem + (size_t)s * h_bytes, &tm_h, &full_bar[s],
+                                kb * kGemmTileK, item.nt * p.bn);
+                }
+            }
+            // Never leave the CTA with copies still landing in its shared memory.
+            const uint32_t st = (uint32_t)p.stages;
+            for (uint32_t n = it > st ? it - st : 0; n < it; ++n)
+                mbar_wait_drain(&full_bar[n % st], (n / st) & 1u);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(kGemmTileW, p.bn);
+            uint32_t it = 0;
+            int t = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < total; w += gridDim.x, ++t) {
+                const Item item = decode(p, w);
+                const int kb0 = item.ks * p.kb_per_split;
+                const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+                const int a = t & 1;
+                if (!mbar_wait(&acc_empty[a], (((uint32_t)t >> 1) & 1u) ^ 1u, &abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)a * p.acc_cols;
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int s = (int)(it % (uint32_t)p.stages);
+                    if (!mbar_wait(&full_bar[s], (it / (uint32_t)p.stages) & 1u, &abort_flag,
+                                   p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t wa = smem_u32(w_smem + (size_t)s * kWTileBytes);
+                    const uint32_t ha = smem_u32(h_smem + (size_t)s * h_bytes);
+#pragma unroll
+                    for (int kk = 0; kk < kGemmTileK / 16; ++kk)
+                        tc_mma_bf16(d_tmem, sw128_desc(wa + kk * 32), sw128_desc(ha + kk * 32),
+                                    idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                    tc_commit(&empty_bar[s]);
+                }
+                if (!ok) break;
+                tc_commit(&acc_full[a]);
+            }
+            if (!ok) {
+                // let the MMAs already issued finish before TMEM is released
+                tc_commit(&drain_bar);
+                mbar_wait_drain(&drain_bar, 0);
+            }
+        }
+    } else {
+        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const int row_in_tile = quarter * 32 + lane;
+        int t = 0;
+        for (int w = blockIdx.x; w < total; w += gridDim.x, ++t) {
+            const Item item = decode(p, w);
+            const int a = t & 1;
+            if (!mbar_wait(&acc_full[a], ((uint32_t)t >> 1) & 1u, &abort_flag, p.err)) break;
+            tc_fence_after();
+            const int64_t v = (int64_t)item.wt * kGemmTileW + row_in_tile;
+            const int m_tile = item.nt * p.bn;
+            const uint32_t tbase = tmem + (uint32_t)a * p.acc_cols + ((uint32_t)(quarter * 32) << 16);
+            for (int c0 = 0; c0 < p.bn; c0 += 32) {
+                float z[32];
+                tmem_ld32_wait(tbase + (uint32_t)c0, z);
+                epilogue_chunk(p, z, v, row_in_tile, m_tile + c0, min(32, p.bn - c0), item, lane);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[a]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, tmem_cols);
+    }
+}
+
+int g_smem_set[64];
+
+}  // namespace
+
+dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h, GemmParams p,
+                              cudaStream_t st) {
+    if (p.bn < 16 || p.bn > 256 || p.bn % 16 != 0 || p.k_splits < 1) return DFLASH2_ERR_INVALID_ARG;
+    if (p.rows_h <= 0 || p.rows_w <= 0 || p.hidden <= 0) return DFLASH2_OK;
+    p.n_tok_tiles = (p.rows_h + p.bn - 1) / p.bn;
+    p.num_kb = (p.hidden + kGemmTileK - 1) / kGemmTileK;
+    p.kb_per_split = (p.num_kb + p.k_splits - 1) / p.k_splits;
+    p.k_splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;  // every split gets >= 1 block
+    p.n_wtiles = (p.rows_w + kGemmTileW - 1) / kGemmTileW;
+    pilot_layout(p.n_wtiles, &p.n_pilot, &p.pilot_stride);
+    if (p.mode == kGemmPilot)
+        p.pass_tiles = p.n_pilot;
+    else if (p.mode == kGemmFilter)
+        p.pass_tiles = p.n_wtiles - p.n_pilot;
+    else
+        p.pass_tiles = p.n_wtiles;
+    if (p.pass_tiles <= 0) return DFLASH2_OK;
+    if (p.mode != kGemmStore) p.k_splits = 1;
+    uint32_t acc = 32;
+    while (acc < (uint32_t)p.bn) acc <<= 1;
+    p.acc_cols = acc;
+    const uint32_t stage_bytes = kWTileBytes + (uint32_t)p.bn * kGemmTileK * 2;
+    int stages = (int)((200u * 1024u) / stage_bytes);
+    if (stages > kGemmMaxStages) stages = kGemmMaxStages;
+    p.stages = stages;
+    const size_t smem = (size_t)stages * stage_bytes + 1024;
+
+    CUtensorMap tm_w, tm_h;
+    dflash2_status s = encode_tmap_bf16(&tm_w, w, (uint64_t)p.rows_w, (uint64_t)p.hidden, kGemmTileW);
+    if (s != DFLASH2_OK) return s;
+    s = encode_tmap_bf16(&tm_h, h, (uint64_t)p.rows_h, (uint64_t)p.hidden, (uint32_t)p.bn);
+    if (s != DFLASH2_OK) return s;
+
+    if (di.device >= 0 && di.device < 64 && !g_smem_set[di.device]) {
+        if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 210 * 1024) != cudaSuccess) {
+            cudaGetLastError();
+            return DFLASH2_ERR_CUDA;
+        }
+        g_smem_set[di.device] = 1;
+    }
+    const int64_t total = (int64_t)p.pass_tiles * p.n_tok_tiles * p.k_splits;
+    const int grid = (int)(total < di.sm_count ? total : di.sm_count);
+    gemm_tc_kernel<<<grid, 192, smem, st>>>(tm_w, tm_h, p);
+    return launch_status();
+}
+
+}  // namespace dflash2

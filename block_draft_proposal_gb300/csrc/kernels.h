@@ -1,0 +1,67 @@
+// Internal launch interfaces shared between the translation units.
+#pragma once
+
+#include "common.cuh"
+
+namespace dflash2 {
+
+// ---- tcgen05 GEMM (gemm_tc.cu) ----------------------------------------------
+// C[m, v] = sum_j h[m, j] * w[v, j] with w and h row-major bf16 (K-major).
+// The weight rows form the MMA's M side in tiles of 128 rows; the h rows
+// (tokens) form the N side in tiles of `bn` rows.
+enum GemmMode : int32_t {
+    kGemmStore = 0,   // write fp32 C (split-K partials) to out
+    kGemmPilot = 1,   // write the transformed, masked u of the pilot tiles to out
+    kGemmFilter = 2,  // append (u, id) keys that reach the row's threshold
+};
+
+constexpr int kGemmTileW = 128;  // weight rows per tile (MMA M)
+constexpr int kGemmTileK = 64;   // hidden elements per pipeline stage (one 128-byte swizzle row)
+constexpr int kGemmMaxStages = 8;
+constexpr int kPilotTiles = 32;  // pilot weight tiles sampled across the vocab
+
+struct GemmParams {
+    // problem
+    int32_t rows_w;  // weight rows (draft vocab, or selector rank)
+    int32_t rows_h;  // token rows
+    int32_t hidden;
+    int32_t mode;
+    // tiling (filled by launch_gemm_tc except bn / k_splits)
+    int32_t bn;       // token tile, multiple of 16 in [16, 256]
+    int32_t k_splits; // store mode: number of hidden splits (>= 1)
+    int32_t n_tok_tiles;
+    int32_t num_kb;
+    int32_t kb_per_split;
+    int32_t n_wtiles;
+    int32_t n_pilot;
+    int32_t pilot_stride;
+    int32_t pass_tiles;
+    int32_t stages;
+    uint32_t acc_cols;
+    // epilogue
+    int64_t target_vocab;
+    float mult;
+    float cap;
+    float *out;            // store: [k_splits][rows_h][ldo]; pilot: [rows_h][ldo]
+    int64_t ldo;
+    int64_t split_stride;
+    const uint64_t *theta; // filter: per-row threshold key
+    uint32_t *cnt;         // filter: per-row candidate count
+    uint64_t *cand;        // filter: [rows_h][cand_cap] keys
+    int32_t cand_cap;
+    int32_t *err;
+};
+
+// Pilot tiling of a weight matrix with n_wtiles tiles: n_pilot tiles spaced
+// pilot_stride apart, starting at tile 0.
+inline void pilot_layout(int64_t n_wtiles, int32_t *n_pilot, int32_t *stride) {
+    int64_t np = n_wtiles < kPilotTiles ? n_wtiles : kPilotTiles;
+    if (np < 1) np = 1;
+    *n_pilot = (int32_t)np;
+    *stride = (int32_t)(n_wtiles / np);
+}
+
+dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h, GemmParams p,
+                              cudaStream_t st);
+
+}  // namespace dflash2

@@ -1,0 +1,455 @@
+// Unary candidates: lm_head GEMM + softcap transform + padded-vocab mask +
+// per-row top-K (sglang DFlash2 PR: compute_candidates, _transform_unary_logits,
+// _radix_topk; vLLM DSpark padded-vocab review: mask [target_vocab, draft_vocab)).
+//
+// bf16 pipeline (four launches, no full logit matrix in HBM):
+//   1. pilot GEMM: u for 32 weight tiles spread over the vocab (<= 4096 rows)
+//      is written to the workspace;
+//   2. pilot select: per row, the K-th best (u, id) key of the pilot is a
+//      lower bound of the row's true K-th best key (it is the K-th best of a
+//      subset), so it is a safe threshold; the pilot's own top K keys seed the
+//      row's candidate list;
+//   3. filter GEMM over the remaining tiles: the epilogue appends every key
+//      that reaches the threshold to the row's candidate list;
+//   4. finalize: exact radix select + sort of each row's candidates.  A row
+//      whose list overflowed is recomputed exactly on CUDA cores (rare: only
+//      adversarial weights defeat the pilot threshold).
+// fp32 pipeline: one CUDA-core kernel per row (the same exact routine as the
+// overflow path), fp32 FMA accumulation.
+//
+// Keys order (u descending, id ascending) as one uint64 (common.cuh), so the
+// selection is a plain "K largest keys" problem with no ties.
+#include "kernels.h"
+
+namespace dflash2 {
+namespace {
+
+constexpr int kSelThreads = 256;
+constexpr int kMaxTopK = 128;
+constexpr int kMaxCandCap = 16384;
+constexpr int kSmemKeys = 4096;     // candidate keys staged in shared memory
+constexpr int kDirectBuf = 2048;    // keys buffered by the exact CUDA-core path
+constexpr int kDirectRows = 64;     // vocab rows per buffered batch (8 warps x 8)
+
+struct SelectShared {
+    uint32_t hist[256];
+    uint32_t bcast[4];
+    uint32_t count;
+    uint64_t top[kMaxTopK];
+};
+
+// Exact k-th largest of keys[0, n) (1 <= k <= n), by 8-bit radix passes from
+// the top byte.  All threads of the block call it; every thread gets the
+// result.  keys may live in shared or global memory.
+__device__ uint64_t block_kth_largest(const uint64_t *keys, int n, int k, SelectShared &sh) {
+    uint64_t prefix = 0, mask = 0;
+    uint32_t remaining = (uint32_t)k;
+    const int lane = threadIdx.x & 31;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) sh.hist[i] = 0;
+        __syncthreads();
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            const uint64_t key = keys[i];
+            if ((key & mask) == prefix) atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            uint32_t c[8], tot = 0;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                c[b] = sh.hist[lane * 8 + b];
+                tot += c[b];
+            }
+            uint32_t suf = tot;  // keys in bins of this lane and all higher lanes
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, suf, o);
+                if (lane + o < 32) suf += y;
+            }
+            const uint32_t above = suf - tot;
+            if (above < remaining && remaining <= above + tot) {
+                uint32_t acc = above;
+                for (int b = 7; b >= 0; --b) {
+                    if (acc + c[b] >= remaining) {
+                        sh.bcast[0] = (uint32_t)(lane * 8 + b);
+                        sh.bcast[1] = remaining - acc;
+                        sh.bcast[2] = c[b];
+                        break;
+                    }
+                    acc += c[b];
+                }
+            }
+        }
+        __syncthreads();
+        const uint32_t digit = sh.bcast[0];
+        remaining = sh.bcast[1];
+        const uint32_t in_bin = sh.bcast[2];
+        prefix |= (uint64_t)digit << shift;
+        mask |= (uint64_t)0xFFu << shift;
+        __syncthreads();
+        if (in_bin == 1 && shift > 0) {
+            // one key carries this prefix: it is the answer
+            for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                const uint64_t key = keys[i];
+                if ((key & mask) == prefix) sh.bcast[3] = i;
+            }
+            __syncthreads();
+            const uint64_t kth = keys[sh.bcast[3]];
+            __syncthreads();
+            return kth;
+        }
+    }
+    return prefix;
+}
+
+// Collects the keys >= kth (nonzero) into sh.top (at most k of them), sorts
+// them descending and returns how many there are.
+__device__ int block_collect_sorted(const uint64_t *keys, int n, uint64_t kth, int k,
+                                    SelectShared &sh) {
+    if (threadIdx.x == 0) sh.count = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const uint64_t key = keys[i];
+        if (key != 0 && key >= kth) {
+            const uint32_t slot = atomicAdd(&sh.count, 1u);
+            if (slot < (uint32_t)k) sh.top[slot] = key;
+        }
+    }
+    __syncthreads();
+    const int got = min((int)sh.count, k);
+    int kpad = 1;
+    while (kpad < k) kpad <<= 1;
+    for (int i = got + threadIdx.x; i < kpad; i += blockDim.x) sh.top[i] = 0;
+    __syncthreads();
+    for (int size = 2; size <= kpad; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < kpad; i += blockDim.x) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const uint64_t a = sh.top[i], b = sh.top[j];
+                    const bool desc = (i & size) == 0;
+                    if (desc ? (a < b) : (a > b)) {
+                        sh.top[i] = b;
+                        sh.top[j] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    return got;
+}
+
+__device__ void write_row(const SelectShared &sh, int got, int k, int64_t row, int64_t *ids,
+                          float *vals, int32_t *err) {
+    for (int i = threadIdx.x; i < k; i += blockDim.x) {
+        if (i < got) {
+            ids[row * k + i] = (int64_t)key_id(sh.top[i]);
+            vals[row * k + i] = key_u(sh.top[i]);
+        } else {
+            ids[row * k + i] = 0;
+            vals[row * k + i] = -INFINITY;
+        }
+    }
+    if (got < k && threadIdx.x == 0 && err) atomicOr(err, DFLASH2_DEVERR_SHORT);
+}
+
+template <typename T> __device__ __forceinline__ float to_f(T v);
+template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) {
+    return __bfloat162float(v);
+}
+
+// Exact top-k of one row on CUDA cores: every vocab row's u is computed in
+// fp32 (lane-strided FMA over hidden, then a warp tree sum), keys that reach
+// the running threshold are buffered in shared memory, and a full buffer is
+// cut back to its k best (whose k-th key becomes the new threshold).  Leaves
+// the sorted result in sh.top and returns how many keys it holds.
+template <typename T>
+__device__ int direct_row_topk(const T *__restrict__ hrow, const T *__restrict__ w, int hidden,
+                               int64_t draft_vocab, int64_t target_vocab, float mult, float cap,
+                               int k, float *hs, uint64_t *buf, SelectShared &sh) {
+    for (int j = threadIdx.x; j < hidden; j += blockDim.x) hs[j] = to_f(hrow[j]);
+    if (threadIdx.x == 0) sh.count = 0;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
+    const int64_t vmax = draft_vocab < target_vocab ? draft_vocab : target_vocab;
+    uint64_t theta = 0;
+    for (int64_t v0 = 0; v0 < vmax; v0 += kDirectRows) {
+        for (int r = warp; r < kDirectRows; r += nwarps) {
+            const int64_t v = v0 + r;
+            if (v >= vmax) break;
+            const T *wr = w + v * hidden;
+            float acc = 0.0f;
+            for (int j = lane; j < hidden; j += 32) acc = fmaf(hs[j], to_f(wr[j]), acc);
+            acc = warp_sum(acc);
+            if (lane == 0) {
+                const uint64_t key = make_key(unary_transform(acc, mult, cap), (uint32_t)v);
+                if (key >= theta) {
+                    const uint32_t slot = atomicAdd(&sh.count, 1u);
+                    buf[slot] = key;  // slot < kDirectBuf: the buffer is cut below
+                }
+            }
+        }
+        __syncthreads();
+        const int n = (int)sh.count;
+        if (n > kDirectBuf - kDirectRows && n > k) {
+            const uint64_t kth = block_kth_largest(buf, n, k, sh);
+            const int got = block_collect_sorted(buf, n, kth, k, sh);
+            for (int i = threadIdx.x; i < got; i += blockDim.x) buf[i] = sh.top[i];
+            theta = kth;
+            __syncthreads();
+            if (threadIdx.x == 0) sh.count = (uint32_t)got;
+            __syncthreads();
+        }
+    }
+    const int n = (int)sh.count;
+    const uint64_t kth = n > k ? block_kth_largest(buf, n, k, sh) : 1;
+    return block_collect_sorted(buf, n, kth, k, sh);
+}
+
+// Shared-memory layout of the kernels that may take the exact path:
+// [SelectShared][hidden floats][kDirectBuf keys] (and the staged candidates
+// reuse the float + key area).
+__host__ __device__ inline size_t direct_smem_bytes(int hidden) {
+    return (((size_t)hidden * 4 + 15) & ~(size_t)15) + (size_t)kDirectBuf * 8;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kSelThreads)
+    direct_topk_kernel(const T *__restrict__ h, const T *__restrict__ w, int hidden,
+                       int64_t draft_vocab, int64_t target_vocab, float mult, float cap, int k,
+                       int64_t *ids, float *vals, int32_t *err) {
+    __shared__ SelectShared sh;
+    extern __shared__ __align__(16) uint8_t dyn[];
+    float *hs = reinterpret_cast<float *>(dyn);
+    uint64_t *buf = reinterpret_cast<uint64_t *>(dyn + (((size_t)hidden * 4 + 15) & ~(size_t)15));
+    const int64_t row = blockIdx.x;
+    const int got = direct_row_topk<T>(h + row * hidden, w, hidden, draft_vocab, target_vocab, mult,
+                                       cap, k, hs, buf, sh);
+    write_row(sh, got, k, row, ids, vals, err);
+}
+
+// Pilot select: threshold and seed candidates of each row from its pilot u.
+__global__ void __launch_bounds__(kSelThreads)
+    pilot_select_kernel(const float *__restrict__ pilot_u, int n_pilot, int pilot_stride, int k,
+                        uint64_t *theta, uint32_t *cnt, uint64_t *cand, int cand_cap) {
+    __shared__ SelectShared sh;
+    extern __shared__ __align__(16) uint8_t dyn[];
+    uint64_t *keys = reinterpret_cast<uint64_t *>(dyn);
+    const int64_t row = blockIdx.x;
+    const int n = n_pilot * kGemmTileW;
+    const float *pu = pilot_u + row * n;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const float u = pu[i];
+        const uint32_t v = (uint32_t)((i / kGemmTileW) * pilot_stride * kGemmTileW + (i % kGemmTileW));
+        keys[i] = (u == -INFINITY) ? 0ull : make_key(u, v);
+    }
+    __syncthreads();
+    const uint64_t kth = block_kth_largest(keys, n, k, sh);
+    const int got = block_collect_sorted(keys, n, kth, k, sh);
+    for (int i = threadIdx.x; i < got; i += blockDim.x) cand[row * cand_cap + i] = sh.top[i];
+    if (threadIdx.x == 0) {
+        theta[row] = kth;  // 0 when the pilot holds fewer than k valid entries
+        cnt[row] = (uint32_t)got;
+    }
+}
+
+// Final exact top-k of each row's candidate list (or the exact CUDA-core
+// recomputation of the row when its list overflowed).
+__global__ void __launch_bounds__(kSelThreads)
+    finalize_kernel(const uint32_t *__restrict__ cnt, const uint64_t *__restrict__ cand,
+                    int cand_cap, int k, int64_t *ids, float *vals, int32_t *err,
+                    const __nv_bfloat16 *__restrict__ h, const __nv_bfloat16 *__restrict__ w,
+                    int hidden, int64_t draft_vocab, int64_t target_vocab, float mult, float cap) {
+    __shared__ SelectShared sh;
+    extern __shared__ __align__(16) uint8_t dyn[];
+    const int64_t row = blockIdx.x;
+    const uint32_t n = cnt[row];
+    if (n > (uint32_t)cand_cap) {
+        float *hs = reinterpret_cast<float *>(dyn);
+        uint64_t *buf =
+            reinterpret_cast<uint64_t *>(dyn + (((size_t)hidden * 4 + 15) & ~(size_t)15));
+        const int got = direct_row_topk<__nv_bfloat16>(h + row * hidden, w, hidden, draft_vocab,
+                                                       target_vocab, mult, cap, k, hs, buf, sh);
+        write_row(sh, got, k, row, ids, vals, err);
+        if (threadIdx.x == 0 && err) atomicOr(err, DFLASH2_DEVINFO_TOPK_FALLBACK);
+        return;
+    }
+    const uint64_t *src = cand + row * cand_cap;
+    const uint64_t *keys = src;
+    if (n <= (uint32_t)kSmemKeys) {
+        uint64_t *st = reinterpret_cast<uint64_t *>(dyn);
+        for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) st[i] = src[i];
+        __syncthreads();
+        keys = st;
+    }
+    const int kk = (int)n < k ? (int)n : k;
+    const uint64_t kth = kk > 0 ? block_kth_largest(keys, (int)n, kk, sh) : ~0ull;
+    const int got = block_collect_sorted(keys, (int)n, kth, k, sh);
+    write_row(sh, got, k, row, ids, vals, err);
+}
+
+// ---- workspace layout (bf16) -------------------------------------------------
+struct TopkLayout {
+    int32_t n_wtiles, n_pilot, pilot_stride, cap;
+    size_t theta_off, cnt_off, pilot_off, cand_off, fixed_bytes;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+inline TopkLayout topk_layout(int64_t rows, int64_t draft_vocab) {
+    TopkLayout L{};
+    L.n_wtiles = (int32_t)((draft_vocab + kGemmTileW - 1) / kGemmTileW);
+    pilot_layout(L.n_wtiles, &L.n_pilot, &L.pilot_stride);
+    L.theta_off = 0;
+    L.cnt_off = align256(L.theta_off + (size_t)rows * 8);
+    L.pilot_off = align256(L.cnt_off + (size_t)rows * 4);
+    L.cand_off = align256(L.pilot_off + (size_t)rows * L.n_pilot * kGemmTileW * 4);
+    L.fixed_bytes = L.cand_off;
+    return L;
+}
+
+inline int64_t recommended_cap(const TopkLayout &L, int k) {
+    const int64_t rest = L.n_wtiles - L.n_pilot;
+    int64_t cap = k + 4LL * k * ((rest + L.n_pilot - 1) / L.n_pilot) + 256;
+    cap = (cap + 63) / 64 * 64;
+    if (cap > kMaxCandCap) cap = kMaxCandCap;
+    if (cap < k) cap = k;
+    return cap;
+}
+
+bool g_topk_attr[64];
+
+dflash2_status set_select_attrs(int device) {
+    if (device < 0 || device >= 64) return DFLASH2_ERR_CUDA;
+    if (g_topk_attr[device]) return DFLASH2_OK;
+    const int bytes = 160 * 1024;
+    if (cudaFuncSetAttribute(finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(pilot_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(direct_topk_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(direct_topk_kernel<__nv_bfloat16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return DFLASH2_ERR_CUDA;
+    }
+    g_topk_attr[device] = true;
+    return DFLASH2_OK;
+}
+
+constexpr int kMaxHidden = 32768;  // the exact path stages one h row as fp32 in shared memory
+
+}  // namespace
+}  // namespace dflash2
+
+using namespace dflash2;
+
+extern "C" size_t dflash2_unary_topk_workspace_size(int64_t rows, int64_t draft_vocab, int32_t top_k,
+                                                    int32_t dtype) {
+    if (rows <= 0 || draft_vocab <= 0 || top_k <= 0) return 0;
+    if (dtype == DFLASH2_F32) return 0;
+    const TopkLayout L = topk_layout(rows, draft_vocab);
+    return L.fixed_bytes + (size_t)rows * recommended_cap(L, top_k) * 8;
+}
+
+extern "C" size_t dflash2_unary_topk_workspace_min(int64_t rows, int64_t draft_vocab, int32_t top_k,
+                                                   int32_t dtype) {
+    if (rows <= 0 || draft_vocab <= 0 || top_k <= 0) return 0;
+    if (dtype == DFLASH2_F32) return 0;
+    const TopkLayout L = topk_layout(rows, draft_vocab);
+    return L.fixed_bytes + (size_t)rows * top_k * 8;
+}
+
+extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head, int64_t rows,
+                                             int32_t hidden, int64_t draft_vocab,
+                                             int64_t target_vocab, float mult, float cap,
+                                             int32_t top_k, int32_t dtype, int64_t *cand_ids,
+                                             float *cand_u, void *workspace, size_t ws_bytes,
+                                             int32_t *err_word, void *stream) {
+    if (dtype != DFLASH2_F32 && dtype != DFLASH2_BF16) return DFLASH2_ERR_UNSUPPORTED_DTYPE;
+    if (rows < 0 || rows > INT32_MAX || hidden <= 0 || hidden > kMaxHidden || draft_vocab <= 0 ||
+        draft_vocab > INT32_MAX || target_vocab <= 0 || top_k <= 0 || top_k > kMaxTopK ||
+        top_k > target_vocab || top_k > draft_vocab || !(cap >= 0.0f))
+        return DFLASH2_ERR_INVALID_ARG;
+    if (rows == 0) return DFLASH2_OK;
+    if (!h || !lm_head || !cand_ids || !cand_u) return DFLASH2_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(cand_ids) % 8 != 0 || reinterpret_cast<uintptr_t>(cand_u) % 4 != 0)
+        return DFLASH2_ERR_MISALIGNED;
+    DeviceInfo di;
+    dflash2_status s = current_device(&di);
+    if (s != DFLASH2_OK) return s;
+    s = set_select_attrs(di.device);
+    if (s != DFLASH2_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t dsm = direct_smem_bytes(hidden);
+
+    if (dtype == DFLASH2_F32) {
+        if ((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(lm_head)) % 4 != 0)
+            return DFLASH2_ERR_MISALIGNED;
+        direct_topk_kernel<float><<<(unsigned)rows, kSelThreads, dsm, st>>>(
+            static_cast<const float *>(h), static_cast<const float *>(lm_head), hidden, draft_vocab,
+            target_vocab, mult, cap, top_k, cand_ids, cand_u, err_word);
+        return launch_status();
+    }
+
+    if (hidden % 8 != 0 || !aligned16(h) || !aligned16(lm_head)) return DFLASH2_ERR_MISALIGNED;
+    const TopkLayout L = topk_layout(rows, draft_vocab);
+    if (!workspace || ws_bytes < L.fixed_bytes + (size_t)rows * top_k * 8)
+        return DFLASH2_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return DFLASH2_ERR_MISALIGNED;
+    int64_t cap_keys = (int64_t)((ws_bytes - L.fixed_bytes) / ((size_t)rows * 8));
+    if (cap_keys > kMaxCandCap) cap_keys = kMaxCandCap;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint64_t *theta = reinterpret_cast<uint64_t *>(ws + L.theta_off);
+    uint32_t *cnt = reinterpret_cast<uint32_t *>(ws + L.cnt_off);
+    float *pilot_u = reinterpret_cast<float *>(ws + L.pilot_off);
+    uint64_t *cand = reinterpret_cast<uint64_t *>(ws + L.cand_off);
+
+    // token tile: split the rows into near-equal tiles of at most 256
+    const int64_t n_tiles = (rows + 255) / 256;
+    int bn = (int)(((rows + n_tiles - 1) / n_tiles + 15) / 16 * 16);
+
+    GemmParams p{};
+    p.rows_w = (int32_t)draft_vocab;
+    p.rows_h = (int32_t)rows;
+    p.hidden = hidden;
+    p.bn = bn;
+    p.k_splits = 1;
+    p.target_vocab = target_vocab;
+    p.mult = mult;
+    p.cap = cap;
+    p.err = err_word;
+
+    p.mode = kGemmPilot;
+    p.out = pilot_u;
+    p.ldo = (int64_t)L.n_pilot * kGemmTileW;
+    s = launch_gemm_tc(di, lm_head, h, p, st);
+    if (s != DFLASH2_OK) return s;
+
+    const size_t pilot_smem = (size_t)L.n_pilot * kGemmTileW * 8;
+    pilot_select_kernel<<<(unsigned)rows, kSelThreads, pilot_smem, st>>>(
+        pilot_u, L.n_pilot, L.pilot_stride, top_k, theta, cnt, cand, (int)cap_keys);
+    s = launch_status();
+    if (s != DFLASH2_OK) return s;
+
+    p.mode = kGemmFilter;
+    p.out = nullptr;
+    p.theta = theta;
+    p.cnt = cnt;
+    p.cand = cand;
+    p.cand_cap = (int32_t)cap_keys;
+    s = launch_gemm_tc(di, lm_head, h, p, st);
+    if (s != DFLASH2_OK) return s;
+
+    size_t fin_smem = (size_t)(cap_keys < kSmemKeys ? cap_keys : kSmemKeys) * 8;
+    if (fin_smem < dsm) fin_smem = dsm;
+    finalize_kernel<<<(unsigned)rows, kSelThreads, fin_smem, st>>>(
+        cnt, cand, (int)cap_keys, top_k, cand_ids, cand_u, err_word,
+        static_cast<const __nv_bfloat16 *>(h), static_cast<const __nv_bfloat16 *>(lm_head), hidden,
+        draft_vocab, target_vocab, mult, cap);
+    return launch_status();
+}

@@ -1,0 +1,297 @@
+"""Thin ctypes binding of libdflash2.so (declared in include/dflash2.h).
+
+Argument marshalling only: each function checks shapes and dtypes of torch
+CUDA tensors, passes their data pointers and the current CUDA stream to the
+C entry point of the same name, and raises :class:`Dflash2Error` on a
+non-OK status.  Every step of the hot path runs in the library's kernels;
+there is no fallback.  If the shared library is missing the first call
+raises: build it with ``python -c "import __graft_entry__ as g; g.build()"``.
+
+PyTorch provides device memory and streams only.  Workspaces are caller-owned
+device buffers; the helpers here allocate them with torch when not given.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdflash2.so")
+_lock = threading.Lock()
+_lib = None
+
+OK = 0
+F32, BF16 = 0, 1
+DEVERR_ID_RANGE = 0x1
+DEVERR_TIMEOUT = 0x2
+DEVERR_SHORT = 0x4
+DEVINFO_TOPK_FALLBACK = 0x100
+ABI_VERSION = 1
+
+# Every symbol include/dflash2.h declares.
+EXPORTS = (
+    "dflash2_status_string", "dflash2_abi_version", "dflash2_grouped_conv",
+    "dflash2_unary_topk_workspace_size", "dflash2_unary_topk_workspace_min",
+    "dflash2_unary_topk", "dflash2_selector_walk_workspace_size", "dflash2_selector_walk",
+    "dflash2_d2t_remap",
+)
+
+
+class Dflash2Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = library().dflash2_status_string(status).decode()
+        super().__init__(f"{fn}: {msg} (status {status})")
+
+
+def library():
+    """Load libdflash2.so once and declare the C signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: the CUDA extension is not built "
+                "(run `python -c \"import __graft_entry__ as g; g.build()\"`)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                ctypes.c_float, ctypes.c_size_t)
+        lib.dflash2_status_string.argtypes = [i32]
+        lib.dflash2_status_string.restype = ctypes.c_char_p
+        lib.dflash2_abi_version.argtypes = []
+        lib.dflash2_abi_version.restype = i32
+        lib.dflash2_grouped_conv.argtypes = [P, P, P, i64, P, i64, i32, i32, i32, i32, i32, P]
+        lib.dflash2_grouped_conv.restype = i32
+        lib.dflash2_unary_topk_workspace_size.argtypes = [i64, i64, i32, i32]
+        lib.dflash2_unary_topk_workspace_size.restype = sz
+        lib.dflash2_unary_topk_workspace_min.argtypes = [i64, i64, i32, i32]
+        lib.dflash2_unary_topk_workspace_min.restype = sz
+        lib.dflash2_unary_topk.argtypes = [P, P, i64, i32, i64, i64, f32, f32, i32, i32, P, P, P,
+                                           sz, P, P]
+        lib.dflash2_unary_topk.restype = i32
+        lib.dflash2_selector_walk_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        lib.dflash2_selector_walk_workspace_size.restype = sz
+        lib.dflash2_selector_walk.argtypes = [P, P, P, P, i64, P, P, P, P, P, P, i32, i32, i32,
+                                              i32, i32, i32, P, P, P, P, sz, P, P]
+        lib.dflash2_selector_walk.restype = i32
+        lib.dflash2_d2t_remap.argtypes = [P, P, i64, i64, i64, P, P, P]
+        lib.dflash2_d2t_remap.restype = i32
+        if lib.dflash2_abi_version() != ABI_VERSION:
+            raise RuntimeError("libdflash2.so ABI version mismatch; rebuild it")
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, status: int):
+    if status != OK:
+        raise Dflash2Error(fn, status)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: fp32 or bf16 only")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+# ---- entry points -----------------------------------------------------------------
+
+def grouped_conv(x, base, delta, block_size: int, group_size: int, taps: int, out=None,
+                 delta_row_stride: int | None = None, stream=None):
+    """dflash2_grouped_conv: x [n, hidden], base [taps, hidden], delta rows of
+    [taps, hidden/group_size] (row stride delta_row_stride elements)."""
+    n, hidden = x.shape
+    for t, nm in ((x, "x"), (base, "base"), (delta, "delta")):
+        _need(t, nm, x.dtype)
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", x.dtype, x.shape)
+    groups = hidden // group_size
+    if delta_row_stride is None:
+        delta_row_stride = taps * groups
+    if delta.numel() < (n - 1) * delta_row_stride + taps * groups if n else False:
+        raise ValueError("delta is too small for n rows at this row stride")
+    _check("dflash2_grouped_conv", library().dflash2_grouped_conv(
+        _ptr(x), _ptr(base), _ptr(delta), delta_row_stride, _ptr(out), n, hidden, group_size,
+        taps, block_size, _dtype_code(x), _stream(stream)))
+    return out
+
+
+def unary_topk_workspace_size(rows: int, draft_vocab: int, top_k: int, dtype_code: int) -> int:
+    return int(library().dflash2_unary_topk_workspace_size(rows, draft_vocab, top_k, dtype_code))
+
+
+def unary_topk_workspace_min(rows: int, draft_vocab: int, top_k: int, dtype_code: int) -> int:
+    return int(library().dflash2_unary_topk_workspace_min(rows, draft_vocab, top_k, dtype_code))
+
+
+def unary_topk(h, lm_head, target_vocab: int, mult: float, cap: float, top_k: int,
+               cand_ids=None, cand_u=None, workspace=None, err=None, stream=None):
+    """dflash2_unary_topk: top_k (ids, u) per row of h against lm_head."""
+    rows, hidden = h.shape
+    draft_vocab = lm_head.shape[0]
+    _need(h, "h")
+    _need(lm_head, "lm_head", h.dtype)
+    code = _dtype_code(h)
+    dev = h.device
+    if cand_ids is None:
+        cand_ids = torch.empty((rows, top_k), dtype=torch.int64, device=dev)
+    if cand_u is None:
+        cand_u = torch.empty((rows, top_k), dtype=torch.float32, device=dev)
+    _need(cand_ids, "cand_ids", torch.int64)
+    _need(cand_u, "cand_u", torch.float32)
+    if workspace is None:
+        workspace = torch.empty(max(1, unary_topk_workspace_size(rows, draft_vocab, top_k, code)),
+                                dtype=torch.uint8, device=dev)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check("dflash2_unary_topk", library().dflash2_unary_topk(
+        _ptr(h), _ptr(lm_head), rows, hidden, draft_vocab, target_vocab, float(mult),
+        float(cap), top_k, code, _ptr(cand_ids), _ptr(cand_u), _ptr(workspace),
+        workspace.numel(), _ptr(err), _stream(stream)))
+    return cand_ids, cand_u, err
+
+
+def selector_walk_workspace_size(batch: int, slots: int, hidden: int, rank: int,
+                                 dtype_code: int) -> int:
+    return int(library().dflash2_selector_walk_workspace_size(batch, slots, hidden, rank,
+                                                              dtype_code))
+
+
+def selector_walk(h, proj, A, B, anchor_ids, cand_ids, cand_u, temperatures, greedy, uniforms,
+                  tokens=None, q=None, path_scores=None, workspace=None, err=None,
+                  with_path_scores: bool = False, stream=None):
+    """dflash2_selector_walk over [batch, slots, top_k] candidates."""
+    batch, slots, top_k = cand_ids.shape
+    hidden = h.shape[-1]
+    rank = proj.shape[0]
+    code = _dtype_code(h)
+    dev = h.device
+    for t, nm in ((h, "h"), (proj, "proj"), (A, "A"), (B, "B")):
+        _need(t, nm, h.dtype)
+    _need(anchor_ids, "anchor_ids", torch.int64, (batch,))
+    _need(cand_ids, "cand_ids", torch.int64)
+    _need(cand_u, "cand_u", torch.float32, (batch, slots, top_k))
+    _need(temperatures, "temperatures", torch.float32, (batch,))
+    _need(greedy, "greedy", torch.uint8, (batch,))
+    _need(uniforms, "uniforms", torch.float32, (batch, slots))
+    if A.shape != B.shape or A.shape[1] != rank:
+        raise ValueError("A and B must both be [table_rows, rank]")
+    if tokens is None:
+        tokens = torch.empty((batch, slots), dtype=torch.int64, device=dev)
+    if q is None:
+        q = torch.empty((batch, slots, top_k), dtype=torch.float32, device=dev)
+    if path_scores is None and with_path_scores:
+        path_scores = torch.empty((batch, slots, top_k), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(1, selector_walk_workspace_size(batch, slots, hidden, rank, code)),
+                                dtype=torch.uint8, device=dev)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check("dflash2_selector_walk", library().dflash2_selector_walk(
+        _ptr(h), _ptr(proj), _ptr(A), _ptr(B), A.shape[0], _ptr(anchor_ids), _ptr(cand_ids),
+        _ptr(cand_u), _ptr(temperatures), _ptr(greedy), _ptr(uniforms), batch, slots, hidden,
+        rank, top_k, code, _ptr(tokens), _ptr(q), _ptr(path_scores), _ptr(workspace),
+        workspace.numel(), _ptr(err), _stream(stream)))
+    return tokens, q, path_scores, err
+
+
+def d2t_remap(draft_ids, d2t, draft_vocab: int, target_vocab: int, out=None, err=None,
+              stream=None):
+    """dflash2_d2t_remap: target = draft + d2t[draft] (identity when d2t is None)."""
+    _need(draft_ids, "draft_ids", torch.int64)
+    if d2t is not None:
+        _need(d2t, "d2t", torch.int64, (draft_vocab,))
+    if out is None:
+        out = torch.empty_like(draft_ids)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=draft_ids.device)
+    _check("dflash2_d2t_remap", library().dflash2_d2t_remap(
+        _ptr(draft_ids), _ptr(d2t), draft_ids.numel(), draft_vocab, target_vocab, _ptr(out),
+        _ptr(err), _stream(stream)))
+    return out, err
+
+
+# ---- host <-> device helpers (plumbing) ----------------------------------------------
+
+def to_device(a: np.ndarray, device) -> torch.Tensor:
+    """numpy -> torch on `device`; uint16 arrays are bf16 bit patterns."""
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def to_host_bits(t: torch.Tensor) -> np.ndarray:
+    """torch -> numpy; bf16 comes back as uint16 bit patterns."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+class ProposalBuffers:
+    """Caller-owned outputs and workspaces of one proposal step (allocated once)."""
+
+    def __init__(self, w, device):
+        code = F32 if w.dtype == "f32" else BF16
+        fdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+        self.conv_out = torch.empty((w.n_tokens, w.hidden), dtype=fdt, device=device)
+        self.cand_ids = torch.empty((w.rows, w.top_k), dtype=torch.int64, device=device)
+        self.cand_u = torch.empty((w.rows, w.top_k), dtype=torch.float32, device=device)
+        self.tokens = torch.empty((w.batch, w.slots), dtype=torch.int64, device=device)
+        self.q = torch.empty((w.batch, w.slots, w.top_k), dtype=torch.float32, device=device)
+        self.target_ids = torch.empty((w.batch, w.slots), dtype=torch.int64, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.ws_topk = torch.empty(max(1, unary_topk_workspace_size(w.rows, w.draft_vocab, w.top_k, code)),
+                                   dtype=torch.uint8, device=device)
+        self.ws_walk = torch.empty(max(1, selector_walk_workspace_size(w.batch, w.slots, w.hidden, w.rank, code)),
+                                   dtype=torch.uint8, device=device)
+
+
+def proposal_step(w, t: dict, bufs: ProposalBuffers | None = None, stream=None) -> dict:
+    """One pass of the hot path: conv, unary candidates, selector walk, d2t remap.
+
+    `t` holds the device tensors of synth.make(w) (bf16 tensors as torch.bfloat16).
+    Returns the output tensors (no synchronisation)."""
+    dev = t["h"].device
+    if bufs is None:
+        bufs = ProposalBuffers(w, dev)
+    grouped_conv(t["x"], t["base"], t["delta"], w.block_size, w.group_size, w.taps,
+                 out=bufs.conv_out, stream=stream)
+    unary_topk(t["h"], t["lm_head"], w.target_vocab, w.mult, w.cap, w.top_k,
+               cand_ids=bufs.cand_ids, cand_u=bufs.cand_u, workspace=bufs.ws_topk, err=bufs.err,
+               stream=stream)
+    selector_walk(t["h"], t["proj"], t["A"], t["B"], t["anchors"],
+                  bufs.cand_ids.view(w.batch, w.slots, w.top_k),
+                  bufs.cand_u.view(w.batch, w.slots, w.top_k), t["temperatures"], t["greedy"],
+                  t["uniforms"], tokens=bufs.tokens, q=bufs.q, workspace=bufs.ws_walk,
+                  err=bufs.err, stream=stream)
+    d2t_remap(bufs.tokens, t.get("d2t"), w.draft_vocab, w.target_vocab, out=bufs.target_ids,
+              err=bufs.err, stream=stream)
+    return dict(conv_out=bufs.conv_out, cand_ids=bufs.cand_ids, cand_u=bufs.cand_u,
+                tokens=bufs.tokens, q=bufs.q, target_ids=bufs.target_ids, err=bufs.err)

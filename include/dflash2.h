@@ -1,0 +1,201 @@
+/*
+ * dflash2.h — C ABI of the GB300 (sm_103a) DFlash2 draft-proposal hot path.
+ *
+ * The method is the one of sglang PR "[Spec] DFlash2: local convolution +
+ * candidate selector" (a block-causal grouped dynamic conv, unary candidate
+ * logits with a top-K, and a low-rank selector lattice walked slot by slot),
+ * plus the draft-to-target id remap of vLLM PR "DSpark padded-vocab drafts no
+ * longer wrongly demand a d2t table" (map_draft_to_target).
+ *
+ * General rules for every entry point
+ *   - Pointers named as device pointers must point to device memory that the
+ *     caller allocated and keeps alive until the work queued on `stream`
+ *     completes.  The library allocates nothing, keeps no per-call state,
+ *     never synchronises and never falls back to the CPU.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
+ *     work is queued on it asynchronously, in call order.
+ *   - Arguments are validated on the host before anything is queued; a bad
+ *     argument returns a non-OK status and queues nothing.
+ *   - `err_word` (device int32, caller-owned, may be NULL where noted) is
+ *     OR-ed with DFLASH2_DEVERR_* bits by the kernels when they meet data
+ *     they cannot process (for example an id outside its table); the kernels
+ *     then write a defined value (id 0, a zero table row) and carry on.  The
+ *     caller clears it and reads it back when it synchronises.
+ *   - dtype is DFLASH2_F32 or DFLASH2_BF16 and applies to every floating
+ *     tensor of the call unless stated otherwise.  Ids are int64.
+ *   - The kernels are built for sm_103a only; on any other device every
+ *     compute entry point returns DFLASH2_ERR_UNSUPPORTED_DEVICE.
+ */
+#ifndef DFLASH2_H
+#define DFLASH2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DFLASH2_ABI_VERSION 1
+
+typedef enum {
+    DFLASH2_OK = 0,
+    DFLASH2_ERR_INVALID_ARG = 1,        /* a null pointer, a size out of range */
+    DFLASH2_ERR_UNSUPPORTED_DTYPE = 2,  /* dtype not fp32/bf16 (e.g. a quantised head) */
+    DFLASH2_ERR_MISALIGNED = 3,         /* a pointer or stride breaks an alignment rule */
+    DFLASH2_ERR_WORKSPACE = 4,          /* workspace null or smaller than the minimum */
+    DFLASH2_ERR_CUDA = 5,               /* a CUDA runtime call failed (launch, attribute) */
+    DFLASH2_ERR_UNSUPPORTED_DEVICE = 6  /* current device is not sm_103 */
+} dflash2_status;
+
+typedef enum { DFLASH2_F32 = 0, DFLASH2_BF16 = 1 } dflash2_dtype;
+
+/* Bits OR-ed into *err_word by the kernels. */
+#define DFLASH2_DEVERR_ID_RANGE 0x1  /* an id outside [0, rows of its table) */
+#define DFLASH2_DEVERR_TIMEOUT 0x2   /* a bounded pipeline wait gave up; outputs invalid */
+#define DFLASH2_DEVERR_SHORT 0x4     /* fewer than K selectable vocab entries */
+/* Informational (not an error): a top-K row overflowed its candidate list and
+ * was recomputed exactly on CUDA cores. */
+#define DFLASH2_DEVINFO_TOPK_FALLBACK 0x100
+
+/* Human-readable name of a status code (static storage). */
+const char *dflash2_status_string(int32_t status);
+
+/* DFLASH2_ABI_VERSION of the loaded library. */
+int32_t dflash2_abi_version(void);
+
+/*
+ * Block-causal grouped dynamic depthwise convolution.
+ * sglang DFlash2 PR, _grouped_conv and DFlashGroupedConv: hidden is split into
+ * groups of `group_size` channels; tap t of token i uses the coefficient
+ * base[t, c] + delta[i, t, c / group_size] on x[i - t, c], and is zeroed unless
+ * the in-block position i mod block_size is at least t:
+ *
+ *   out[i, c] = sum_{t < taps, (i mod block_size) >= t}
+ *               (base[t, c] + delta[i, t, c / group_size]) * x[i - t, c]
+ *
+ * x, out      device, [n_tokens, hidden] row-major, token-major; each request's
+ *             block of block_size rows is contiguous (the last block may be short).
+ * base        device, [taps, hidden] (one side of the module's [2, taps, hidden]).
+ * delta       device; row i starts at delta + i * delta_row_stride elements and
+ *             holds [taps, hidden / group_size].  delta_row_stride >= taps * groups
+ *             lets side 0 of a [n, 2, taps, groups] projection be read in place.
+ * Arithmetic: fp32 (coefficient formed in fp32, fp32 multiply-add, taps in
+ *             order 0..taps-1); out is rounded to dtype.
+ * Errors:     hidden % group_size != 0, taps < 1, block_size < 1, n_tokens < 0,
+ *             delta_row_stride < taps * groups -> INVALID_ARG.  n_tokens == 0
+ *             queues nothing.  out must not overlap x.
+ * The fast path wants x, base and out 16-byte aligned and group_size a multiple
+ * of 8 (bf16) or 4 (fp32); other layouts take a scalar path.
+ */
+dflash2_status dflash2_grouped_conv(const void *x, const void *base, const void *delta,
+                                    int64_t delta_row_stride, void *out, int64_t n_tokens,
+                                    int32_t hidden, int32_t group_size, int32_t taps,
+                                    int32_t block_size, int32_t dtype, void *stream);
+
+/*
+ * Unary candidates: lm_head GEMM, output transform, padded-vocab mask, top-K.
+ * sglang DFlash2 PR, DFlash2DraftModel.compute_candidates / _transform_unary_logits
+ * / _radix_topk and _selector_lattice (the rows are the flattened
+ * [batch, slots] proposals); vLLM DSpark padded-vocab review (mask
+ * [target_vocab, draft_vocab) before top-k).
+ *
+ *   z[m, v] = sum_j h[m, j] * lm_head[v, j]
+ *   u[m, v] = cap * tanh(mult * z / cap)  if cap > 0,  mult * z  otherwise
+ *   u[m, v] = -inf                        for v >= target_vocab
+ *   cand_ids[m, :], cand_u[m, :] = the top_k (u, v) of row m, ordered by u
+ *                                  descending, equal u by smaller v
+ *
+ * h           device, [rows, hidden] row-major (proposal positions only).
+ * lm_head     device, [draft_vocab, hidden] row-major (nn.Linear weight layout).
+ * cand_ids    device int64 [rows, top_k];  cand_u device float [rows, top_k].
+ * workspace   device, ws_bytes >= dflash2_unary_topk_workspace_min(...);
+ *             dflash2_unary_topk_workspace_size(...) is the recommended size.
+ *             Its contents need no initialisation and are clobbered.
+ * err_word    device int32, may be NULL.
+ * Arithmetic: bf16 -> tcgen05 tensor-core GEMM with fp32 accumulation; fp32 ->
+ *             fp32 FMA on CUDA cores (no TF32).  The transform runs in fp32
+ *             (tanhf), and selection compares the fp32 u.
+ * Errors:     rows < 0, hidden < 1, top_k < 1, top_k > 128, top_k > target_vocab,
+ *             target_vocab > draft_vocab ... see validation: INVALID_ARG;
+ *             bf16 needs hidden % 8 == 0 and 16-byte aligned h and lm_head
+ *             (MISALIGNED).  rows == 0 queues nothing.
+ */
+size_t dflash2_unary_topk_workspace_size(int64_t rows, int64_t draft_vocab, int32_t top_k,
+                                         int32_t dtype);
+size_t dflash2_unary_topk_workspace_min(int64_t rows, int64_t draft_vocab, int32_t top_k,
+                                        int32_t dtype);
+dflash2_status dflash2_unary_topk(const void *h, const void *lm_head, int64_t rows,
+                                  int32_t hidden, int64_t draft_vocab, int64_t target_vocab,
+                                  float mult, float cap, int32_t top_k, int32_t dtype,
+                                  int64_t *cand_ids, float *cand_u, void *workspace,
+                                  size_t ws_bytes, int32_t *err_word, void *stream);
+
+/*
+ * Selector lattice and walk.
+ * sglang DFlash2 PR: the PR body's edge formula
+ *   edge(p -> c) = < A[p] (elementwise *) project(h), B[c] > + unary[c]
+ * and _selector_walk_kernel / stage_sampling_params.  project(h) = h . proj^T
+ * (proj is an nn.Linear(hidden, rank) weight).  Per request b, slot s:
+ *   p      = anchor_ids[b] at s = 0, else cand_ids[b, s-1, previous]
+ *   e[k]   = sum_j A[p, j] * g[b, s, j] * B[cand_ids[b, s, k], j] + cand_u[b, s, k]
+ *   greedy[b] != 0:  index = smallest k with e[k] == max e;  q = one-hot(index)
+ *   otherwise:       T = max(temperatures[b], 1e-5);  q = softmax(e / T);
+ *                    index = min(#{k : uniforms[b, s] >= cumsum(q)[k]}, top_k - 1)
+ *   tokens[b, s] = cand_ids[b, s, index];  previous = index
+ *
+ * h             device, [batch * slots, hidden] (same rows as unary_topk's h).
+ * proj          device, [rank, hidden].
+ * A, B          device, [table_rows, rank], indexed by draft ids.
+ * anchor_ids    device int64 [batch]: the verified token at block position 0.
+ * cand_ids      device int64 [batch, slots, top_k]; cand_u device float, same shape
+ *               (the outputs of dflash2_unary_topk).
+ * temperatures  device float [batch]; greedy device uint8 [batch];
+ * uniforms      device float [batch, slots] in [0, 1).
+ * tokens        device int64 [batch, slots]; q device float [batch, slots, top_k].
+ * path_scores   device float [batch, slots, top_k] or NULL: the edges e[k] of the
+ *               lattice row the walk actually read at each slot.
+ * workspace     device, ws_bytes >= dflash2_selector_walk_workspace_size(...).
+ * Arithmetic: g in fp32 (bf16: tcgen05 GEMM; fp32: CUDA-core FMA), edges,
+ *             softmax (expf) and the running sum in fp32.
+ * Errors:     top_k < 1 or > 128, rank < 1 or > 256, rank % 8 != 0 (bf16) or
+ *             % 4 != 0 (fp32), batch/slots < 0 -> INVALID_ARG.  An anchor or
+ *             candidate id outside [0, table_rows) sets DFLASH2_DEVERR_ID_RANGE
+ *             and uses a zero table row.
+ */
+size_t dflash2_selector_walk_workspace_size(int32_t batch, int32_t slots, int32_t hidden,
+                                            int32_t rank, int32_t dtype);
+dflash2_status dflash2_selector_walk(const void *h, const void *proj, const void *A,
+                                     const void *B, int64_t table_rows,
+                                     const int64_t *anchor_ids, const int64_t *cand_ids,
+                                     const float *cand_u, const float *temperatures,
+                                     const uint8_t *greedy, const float *uniforms,
+                                     int32_t batch, int32_t slots, int32_t hidden,
+                                     int32_t rank, int32_t top_k, int32_t dtype,
+                                     int64_t *tokens, float *q, float *path_scores,
+                                     void *workspace, size_t ws_bytes, int32_t *err_word,
+                                     void *stream);
+
+/*
+ * Draft-to-target id remap.
+ * vLLM Qwen3DSparkForCausalLM.map_draft_to_target: d2t holds offsets, so
+ *   target_ids[i] = draft_ids[i] + d2t[draft_ids[i]];
+ * with d2t == NULL the map is the identity.  A table exists exactly for a
+ * pruned draft (draft_vocab < target_vocab, the `<` predicate of the same PR).
+ *
+ * draft_ids, target_ids  device int64 [n] (may alias: in-place is allowed).
+ * d2t                    device int64 [draft_vocab] or NULL.
+ * Errors: d2t == NULL while draft_vocab < target_vocab, or d2t != NULL while
+ *         draft_vocab >= target_vocab -> INVALID_ARG.  An id outside
+ *         [0, draft_vocab) or a result outside [0, target_vocab) writes 0 and
+ *         sets DFLASH2_DEVERR_ID_RANGE.
+ */
+dflash2_status dflash2_d2t_remap(const int64_t *draft_ids, const int64_t *d2t, int64_t n,
+                                 int64_t draft_vocab, int64_t target_vocab,
+                                 int64_t *target_ids, int32_t *err_word, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH2_H */

@@ -22,3 +22,29 @@ def ora():
     import oracle
     oracle.build()
     return oracle
+
+
+def pytest_collection_modifyitems(config, items):
+    # GPU tests need a CUDA device; on a machine without one they are skipped.
+    # On a GPU machine a missing or broken extension fails loudly instead.
+    try:
+        import torch
+        has_gpu = torch.cuda.is_available()
+    except Exception:  # pragma: no cover
+        has_gpu = False
+    if has_gpu:
+        return
+    skip = pytest.mark.skip(reason="no CUDA device on this machine")
+    for item in items:
+        if "gpu" in item.keywords:
+            item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def cuda():
+    import torch
+    import __graft_entry__ as g
+    g.build_library()
+    from block_draft_proposal_gb300 import dflash2
+    dflash2.library()
+    return torch.device("cuda:0")

@@ -1,0 +1,85 @@
+"""The C ABI: libdflash2.so loads on a machine without a GPU, exports every
+entry point include/dflash2.h declares, and rejects bad arguments on the host
+before touching CUDA.  No compute call is made here."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dflash2.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+    g.build_library()
+    from block_draft_proposal_gb300 import dflash2
+    return dflash2.library()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dflash2_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    from block_draft_proposal_gb300 import dflash2
+    assert _declared() == sorted(dflash2.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (dflash2_\w+)", out))
+    for name in _declared():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_status_strings_and_version(lib):
+    assert lib.dflash2_abi_version() == 1
+    assert lib.dflash2_status_string(0) == b"ok"
+    for s in range(1, 7):
+        assert lib.dflash2_status_string(s) not in (b"ok", b"unknown status")
+    assert lib.dflash2_status_string(99) == b"unknown status"
+
+
+def test_host_validation_rejects_before_any_launch(lib):
+    null = None
+    # conv: bad dtype, hidden not divisible by group size, short delta stride, empty input
+    assert lib.dflash2_grouped_conv(null, null, null, 0, null, 8, 64, 8, 4, 8, 7, null) == 2
+    assert lib.dflash2_grouped_conv(null, null, null, 32, null, 8, 60, 8, 4, 8, 1, null) == 1
+    assert lib.dflash2_grouped_conv(null, null, null, 31, null, 8, 64, 8, 4, 8, 1, null) == 1
+    assert lib.dflash2_grouped_conv(null, null, null, 32, null, 0, 64, 8, 4, 8, 1, null) == 0
+    assert lib.dflash2_grouped_conv(null, null, null, 32, null, 8, 64, 8, 0, 8, 1, null) == 1
+    # unary top-k: K out of range, K above the target vocab, a quantised dtype
+    args = (null, null, 7, 256, 4096, 4096, 1.0, 0.0)
+    assert lib.dflash2_unary_topk(*args, 0, 1, null, null, null, 0, null, null) == 1
+    assert lib.dflash2_unary_topk(*args, 129, 1, null, null, null, 0, null, null) == 1
+    assert lib.dflash2_unary_topk(null, null, 7, 256, 4096, 4, 1.0, 0.0, 8, 1, null, null, null, 0,
+                                  null, null) == 1
+    assert lib.dflash2_unary_topk(*args, 8, 3, null, null, null, 0, null, null) == 2
+    assert lib.dflash2_unary_topk(null, null, 0, 256, 4096, 4096, 1.0, 0.0, 8, 1, null, null, null,
+                                  0, null, null) == 0
+    # selector walk: rank not a multiple of 8 (bf16), K too large
+    w = (null,) * 4
+    assert lib.dflash2_selector_walk(*w, 10, *(null,) * 6, 2, 3, 64, 12, 8, 1, null, null, null,
+                                     null, 0, null, null) == 1
+    assert lib.dflash2_selector_walk(*w, 10, *(null,) * 6, 2, 3, 64, 16, 200, 1, null, null, null,
+                                     null, 0, null, null) == 1
+    # d2t: a table exists exactly when the draft vocab is smaller than the target
+    assert lib.dflash2_d2t_remap(null, null, 4, 100, 200, null, null, null) == 1
+    assert lib.dflash2_d2t_remap(null, ctypes.c_void_p(64), 4, 200, 100, null, null, null) == 1
+    assert lib.dflash2_d2t_remap(null, null, 0, 201, 200, null, null, null) == 0
+
+
+def test_workspace_sizes_are_host_arithmetic(lib):
+    rec = lib.dflash2_unary_topk_workspace_size(480, 151936, 16, 1)
+    mn = lib.dflash2_unary_topk_workspace_min(480, 151936, 16, 1)
+    assert rec > mn > 0
+    assert lib.dflash2_unary_topk_workspace_size(7, 4096, 8, 0) == 0   # fp32 path needs none
+    assert lib.dflash2_selector_walk_workspace_size(32, 15, 4096, 64, 1) >= 32 * 15 * 64 * 4

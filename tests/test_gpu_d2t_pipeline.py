@@ -1,0 +1,98 @@
+"""GPU parity of dflash2_d2t_remap (bit-exact), and of the whole proposal step
+end to end (conv, candidates, walk, remap) against the chained oracle,
+including replay from a captured CUDA graph."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_draft_proposal_gb300 import dflash2, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def test_d2t_identity_and_padded_ids(cuda):
+    ids = torch.tensor([0, 5, 199, 200, 250, -1], dtype=torch.int64, device=cuda)
+    out, err = dflash2.d2t_remap(ids, None, draft_vocab=256, target_vocab=200)
+    torch.cuda.synchronize()
+    ref, nerr = oracle.d2t(ids.cpu().numpy(), None, 256, 200)
+    np.testing.assert_array_equal(out.cpu().numpy(), ref)
+    assert nerr == 3 and int(err.item()) & dflash2.DEVERR_ID_RANGE
+
+
+def test_d2t_table_matches_oracle_bit_exact(cuda):
+    w = synth.BY_NAME["reduced-vocab-bs12-bf16"]
+    table = synth.d2t_table(w)
+    rng = np.random.default_rng(110)
+    ids = rng.integers(0, w.draft_vocab, size=100_003).astype(np.int64)
+    ids[::997] = w.draft_vocab + 3                          # sprinkle invalid ids
+    t_ids = torch.from_numpy(ids).to(cuda)
+    out, err = dflash2.d2t_remap(t_ids, torch.from_numpy(table).to(cuda), w.draft_vocab,
+                                 w.target_vocab)
+    torch.cuda.synchronize()
+    ref, nerr = oracle.d2t(ids, table, w.draft_vocab, w.target_vocab)
+    np.testing.assert_array_equal(out.cpu().numpy(), ref)
+    assert nerr > 0 and int(err.item()) & dflash2.DEVERR_ID_RANGE
+    # in place
+    dflash2.d2t_remap(t_ids, torch.from_numpy(table).to(cuda), w.draft_vocab, w.target_vocab,
+                      out=t_ids)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(t_ids.cpu().numpy(), ref)
+
+
+def _pipeline_oracle(w, inp):
+    u = oracle.unary_rows(inp["h"], inp["lm_head"], w.target_vocab, w.mult, w.cap)
+    ids, vals = oracle.topk(u, w.top_k)
+    sel = oracle.selector(inp["h"], inp["proj"], inp["A"], inp["B"], inp["anchors"],
+                          ids.reshape(w.batch, w.slots, w.top_k),
+                          vals.reshape(w.batch, w.slots, w.top_k), inp["uniforms"],
+                          inp["temperatures"], inp["greedy"])
+    tgt, errors = oracle.d2t(sel["tokens"].reshape(-1), inp["d2t"], w.draft_vocab, w.target_vocab)
+    return ids, sel, tgt.reshape(w.batch, w.slots), errors
+
+
+@pytest.mark.parametrize("name,scale", [("tiny-fp32", {}),
+                                        ("reduced-vocab-bs12-bf16", dict(batch=6)),
+                                        ("padded-vocab-bf16", dict(batch=2))])
+def test_proposal_step_end_to_end(cuda, name, scale):
+    w = synth.BY_NAME[name].scaled(**scale)
+    inp = synth.make(w)
+    t = {k: dflash2.to_device(v, cuda) for k, v in inp.items() if v is not None}
+    out = dflash2.proposal_step(w, t)
+    torch.cuda.synchronize()
+    assert int(out["err"].item()) & ~dflash2.DEVINFO_TOPK_FALLBACK == 0
+    ids, sel, tgt, errors = _pipeline_oracle(w, inp)
+    assert errors == 0
+    agree_ids = (out["cand_ids"].cpu().numpy() == ids).mean()
+    agree_tok = (out["tokens"].cpu().numpy() == sel["tokens"]).mean()
+    print(f"{name}: end-to-end agreement ids {agree_ids:.4f} tokens {agree_tok:.4f}")
+    # end to end, an accepted top-K near-tie may change a path; the staged
+    # tests pin each stage exactly.  Here most of the batch must agree.
+    assert agree_ids >= 0.99 and agree_tok >= 0.9
+    # the remap of the GPU's own tokens is exact
+    ref_tgt, _ = oracle.d2t(out["tokens"].cpu().numpy().reshape(-1), inp["d2t"], w.draft_vocab,
+                            w.target_vocab)
+    np.testing.assert_array_equal(out["target_ids"].cpu().numpy().reshape(-1), ref_tgt)
+
+
+def test_captured_graph_replays_the_eager_step(cuda):
+    w = synth.BY_NAME["qwen3-8b-bf16"].scaled(batch=4, draft_vocab=20000, target_vocab=20000)
+    inp = synth.make(w)
+    t = {k: dflash2.to_device(v, cuda) for k, v in inp.items() if v is not None}
+    bufs = dflash2.ProposalBuffers(w, cuda)
+    eager = {k: v.clone() for k, v in dflash2.proposal_step(w, t, bufs).items()}
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        dflash2.proposal_step(w, t, bufs)        # warm the stream before capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            dflash2.proposal_step(w, t, bufs)
+    for v in (bufs.tokens, bufs.q, bufs.cand_ids):
+        v.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for key in ("cand_ids", "cand_u", "tokens", "q", "target_ids", "conv_out"):
+        assert torch.equal(getattr(bufs, key), eager[key]), key

@@ -1,0 +1,160 @@
+"""GPU parity of dflash2_unary_topk (lm_head GEMM, transform, padded mask, top-K).
+
+Ids must equal the oracle's except documented near-ties (see parity.py);
+cand_u must lie within the fp32 forward-error bound of the exact u.  Small
+cases cover several tiles with ragged tails in every dimension; the named
+workloads run at full size with the oracle evaluated on sampled rows; the
+candidate-list overflow path, adversarial vocab orders, high padded logits and
+K equal to the logical vocab are covered explicitly."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_draft_proposal_gb300 import dflash2, synth
+from parity import check_topk_row, u_error_bound
+
+pytestmark = pytest.mark.gpu
+
+
+def _f64(a):
+    return (synth.bf16_bits_to_f32(a) if a.dtype == np.uint16 else a).astype(np.float64)
+
+
+def _check(h, W, target_vocab, mult, cap, k, ids, vals, rows):
+    u = oracle.unary_rows(h, W, target_vocab, mult, cap, rows=rows)
+    ora_ids, _ = oracle.topk(u, k)
+    ties = 0
+    for r, m in enumerate(rows):
+        h64 = _f64(h[m])
+
+        def bound(sel, h64=h64, r=r):
+            sel = np.asarray(sel)
+            return u_error_bound(h64, _f64(W[sel]), np.arange(len(sel)), u[r][sel], mult)
+
+        ties += check_topk_row(ids[m], vals[m], ora_ids[r], u[r], bound, k)
+        assert np.all(ids[m] < target_vocab)
+        assert np.all(np.diff(vals[m]) <= 0)
+    return ties
+
+
+def _run(dev, h, W, target_vocab, mult, cap, k, ws_bytes=None):
+    th, tw = dflash2.to_device(h, dev), dflash2.to_device(W, dev)
+    ws = None
+    if ws_bytes is not None:
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ids, vals, err = dflash2.unary_topk(th, tw, target_vocab, mult, cap, k, workspace=ws)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), vals.cpu().numpy(), int(err.item())
+
+
+SMALL = [
+    # rows, hidden, draft_vocab, target_vocab, k, mult, cap, dtype
+    (37, 200, 5000, 4900, 16, 0.5, 30.0, "bf16"),      # ragged in every dimension, pilot-only
+    (300, 264, 40000, 39990, 32, 1.0, 0.0, "bf16"),    # filter pass active, two token tiles
+    (7, 512, 70000, 70000, 64, 1.0, 30.0, "bf16"),
+    (513, 128, 9000, 8800, 8, 2.0, 0.0, "bf16"),       # three token tiles
+    (5, 96, 3000, 2999, 128, 1.0, 0.0, "bf16"),        # K at its maximum
+    (9, 136, 1100, 1000, 16, 1.0, 10.0, "f32"),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"m{c[0]}-h{c[1]}-v{c[2]}-k{c[4]}-{c[7]}")
+def test_unary_topk_small(cuda, case):
+    rows, hidden, vd, vt, k, mult, cap, dtype = case
+    w = synth.CONFIGS[0].scaled(batch=rows, block_size=2, hidden=hidden, draft_vocab=vd,
+                                target_vocab=vt, top_k=k, mult=mult, cap=cap, dtype=dtype, seed=91)
+    inp = synth.make(w, parts=("h", "lm_head"))
+    ids, vals, err = _run(cuda, inp["h"], inp["lm_head"], vt, mult, cap, k)
+    assert err & ~dflash2.DEVINFO_TOPK_FALLBACK == 0
+    ties = _check(inp["h"], inp["lm_head"], vt, mult, cap, k, ids, vals, list(range(rows)))
+    print(f"near-ties accepted: {ties}")
+
+
+@pytest.mark.parametrize("name", [c.name for c in synth.CONFIGS])
+def test_unary_topk_named_workloads(cuda, name):
+    w = synth.BY_NAME[name]
+    inp = synth.make(w, parts=("h", "lm_head"))
+    ids, vals, err = _run(cuda, inp["h"], inp["lm_head"], w.target_vocab, w.mult, w.cap, w.top_k)
+    assert err == 0, hex(err)
+    rng = np.random.default_rng(5)
+    rows = sorted({0, w.rows - 1, *rng.integers(0, w.rows, size=2).tolist()})
+    ties = _check(inp["h"], inp["lm_head"], w.target_vocab, w.mult, w.cap, w.top_k, ids, vals, rows)
+    # properties that hold for every row
+    assert np.all(ids >= 0) and np.all(ids < w.target_vocab)
+    assert np.all(np.diff(vals, axis=1) <= 0)
+    assert all(len(set(r)) == w.top_k for r in ids.tolist())
+    print(f"{name}: near-ties accepted {ties}")
+
+
+def test_overflowing_candidate_lists_fall_back_exactly(cuda):
+    # the minimum workspace leaves room for K candidates per row: every row
+    # that meets a filter-pass survivor overflows and is recomputed exactly
+    rows, hidden, vd, vt, k = 24, 128, 20000, 19900, 16
+    w = synth.CONFIGS[0].scaled(batch=rows, block_size=2, hidden=hidden, draft_vocab=vd,
+                                target_vocab=vt, top_k=k, dtype="bf16", seed=92)
+    inp = synth.make(w, parts=("h", "lm_head"))
+    ws = dflash2.unary_topk_workspace_min(rows, vd, k, dflash2.BF16)
+    ids, vals, err = _run(cuda, inp["h"], inp["lm_head"], vt, 1.0, 0.0, k, ws_bytes=ws)
+    assert err & dflash2.DEVINFO_TOPK_FALLBACK
+    assert err & ~dflash2.DEVINFO_TOPK_FALLBACK == 0
+    _check(inp["h"], inp["lm_head"], vt, 1.0, 0.0, k, ids, vals, list(range(rows)))
+
+
+def test_logits_rising_with_id_defeat_the_pilot_but_stay_exact(cuda):
+    # lm_head rows aligned with h and scaled up with the vocab id: the pilot
+    # tiles see small logits, the threshold is weak and the lists overflow
+    rows, hidden, vd, k = 6, 64, 30000, 32
+    rng = np.random.default_rng(93)
+    h = rng.standard_normal((rows, hidden)).astype(np.float32)
+    direction = h.mean(0)
+    W = (np.linspace(0.0, 1.0, vd)[:, None] * direction[None, :] +
+         0.01 * rng.standard_normal((vd, hidden))).astype(np.float32)
+    h16, W16 = synth.to_bf16_bits(h), synth.to_bf16_bits(W)
+    ids, vals, err = _run(cuda, h16, W16, vd, 1.0, 0.0, k)
+    assert err & ~dflash2.DEVINFO_TOPK_FALLBACK == 0
+    _check(h16, W16, vd, 1.0, 0.0, k, ids, vals, list(range(rows)))
+
+
+def test_high_padded_logits_are_never_chosen(cuda):
+    rows, hidden, vd, vt, k = 16, 128, 6000, 5500, 32
+    rng = np.random.default_rng(94)
+    h = (np.abs(rng.standard_normal((rows, hidden))) + 0.1).astype(np.float32)
+    W = (0.02 * rng.standard_normal((vd, hidden))).astype(np.float32)
+    W[vt:] = 1.0                                   # padded rows carry the largest logits
+    h16, W16 = synth.to_bf16_bits(h), synth.to_bf16_bits(W)
+    ids, vals, err = _run(cuda, h16, W16, vt, 1.0, 0.0, k)
+    assert err == 0
+    assert ids.max() < vt and np.all(np.isfinite(vals))
+    _check(h16, W16, vt, 1.0, 0.0, k, ids, vals, list(range(rows)))
+
+
+def test_k_equal_to_target_vocab_returns_every_valid_id(cuda):
+    rows, hidden, vd, vt = 4, 64, 130, 100
+    w = synth.CONFIGS[0].scaled(batch=rows, block_size=2, hidden=hidden, draft_vocab=vd,
+                                target_vocab=vt, top_k=vt, dtype="bf16", seed=95)
+    inp = synth.make(w, parts=("h", "lm_head"))
+    ids, vals, err = _run(cuda, inp["h"], inp["lm_head"], vt, 1.0, 0.0, vt)
+    assert err == 0
+    for r in range(rows):
+        assert sorted(ids[r].tolist()) == list(range(vt))
+    _check(inp["h"], inp["lm_head"], vt, 1.0, 0.0, vt, ids, vals, list(range(rows)))
+
+
+def test_zero_multiplier_ties_resolve_to_smallest_ids(cuda):
+    rows, hidden, vd, k = 3, 64, 9000, 20
+    w = synth.CONFIGS[0].scaled(batch=rows, block_size=2, hidden=hidden, draft_vocab=vd,
+                                target_vocab=vd, top_k=k, dtype="bf16", seed=96)
+    inp = synth.make(w, parts=("h", "lm_head"))
+    ids, vals, err = _run(cuda, inp["h"], inp["lm_head"], vd, 0.0, 0.0, k)
+    assert err == 0
+    for r in range(rows):
+        np.testing.assert_array_equal(ids[r], np.arange(k))
+        assert np.all(vals[r] == 0)
+
+
+def test_zero_rows_is_a_no_op(cuda):
+    h = torch.empty((0, 64), dtype=torch.bfloat16, device=cuda)
+    W = torch.zeros((256, 64), dtype=torch.bfloat16, device=cuda)
+    ids, vals, err = dflash2.unary_topk(h, W, 256, 1.0, 0.0, 8)
+    assert ids.shape == (0, 8)

@@ -1,0 +1,185 @@
+"""GPU parity of dflash2_selector_walk (projection, lattice edges, walk).
+
+Staged parity: the oracle's projection, lattice and walk run on the GPU's own
+candidates and unary values, so a near-tie in the top-K cannot cascade.
+Tokens must equal the oracle's along each request until an accepted near-tie
+(documented in parity.py); the edges the walk read (path_scores) must match
+the oracle lattice row of the predecessor the GPU chose; q must match within
+tolerance; greedy q is exactly one-hot and sampled q sums to one."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_draft_proposal_gb300 import dflash2, synth
+
+pytestmark = pytest.mark.gpu
+EPS = 2.0 ** -24
+
+
+def _f64(a):
+    return (synth.bf16_bits_to_f32(a) if a.dtype == np.uint16 else a).astype(np.float64)
+
+
+def _edge_bound(inp, cand, anchors, hidden):
+    """Per-edge forward-error bound [B, S, K(prev), K(cur)] of the fp32 edges."""
+    batch, slots, k = cand.shape
+    A, B = _f64(inp["A"]), _f64(inp["B"])
+    r = A.shape[1]
+    habs = np.abs(_f64(inp["h"]))
+    gabs = habs @ np.abs(_f64(inp["proj"])).T                  # sum_i |h_i P_ji|
+    g = _f64(inp["h"]) @ _f64(inp["proj"]).T
+    gerr = (hidden + 2) * EPS * gabs                           # |g_gpu - g|
+    out = np.empty((batch, slots, k, k))
+    for b in range(batch):
+        for s in range(slots):
+            prev = np.full(k, anchors[b]) if s == 0 else cand[b, s - 1]
+            prev = np.clip(prev, 0, A.shape[0] - 1)
+            pa = np.abs(A[prev])                               # [k, r]
+            cb = np.abs(B[np.clip(cand[b, s], 0, B.shape[0] - 1)])
+            row = b * slots + s
+            lat = (pa * np.abs(g[row])[None, :]) @ cb.T        # sum |A g B|
+            lat_g = (pa * gerr[row][None, :]) @ cb.T
+            out[b, s] = (r + 4) * EPS * lat + lat_g
+    return out
+
+
+def _run_walk(dev, inp, cand, cand_u, with_ws=None):
+    t = {k: dflash2.to_device(v, dev) for k, v in inp.items() if v is not None}
+    tc = torch.from_numpy(np.ascontiguousarray(cand)).to(dev)
+    tu = torch.from_numpy(np.ascontiguousarray(cand_u)).to(dev)
+    tokens, q, ps, err = dflash2.selector_walk(t["h"], t["proj"], t["A"], t["B"], t["anchors"], tc,
+                                               tu, t["temperatures"], t["greedy"], t["uniforms"],
+                                               with_path_scores=True)
+    torch.cuda.synchronize()
+    return tokens.cpu().numpy(), q.cpu().numpy(), ps.cpu().numpy(), int(err.item())
+
+
+def _compare(inp, cand, cand_u, tokens, q, ps, dtype, hidden):
+    batch, slots, k = cand.shape
+    ora = oracle.selector(inp["h"], inp["proj"], inp["A"], inp["B"], inp["anchors"], cand, cand_u,
+                          inp["uniforms"], inp["temperatures"], inp["greedy"])
+    bound = _edge_bound(inp, cand, inp["anchors"], hidden) + np.abs(cand_u)[:, :, None, :] * EPS
+    scores = ora["scores"]
+    q_tol = 1e-5 if dtype == "f32" else 2e-2
+    ties = 0
+    for b in range(batch):
+        greedy = bool(inp["greedy"][b])
+        prev = 0
+        diverged = False
+        for s in range(slots):
+            row = cand[b, s]
+            gi = int(np.nonzero(row == tokens[b, s])[0][0])     # GPU index (ids are distinct)
+            # edges the GPU read: the oracle lattice row of the GPU's predecessor
+            e_ref = scores[b, s, prev].astype(np.float64)
+            tol = bound[b, s, prev] + np.abs(e_ref) * EPS
+            assert np.all(np.abs(ps[b, s].astype(np.float64) - e_ref) <= tol), (b, s)
+            if greedy:
+                np.testing.assert_array_equal(q[b, s], np.eye(k, dtype=np.float32)[gi])
+            else:
+                assert abs(q[b, s].astype(np.float64).sum() - 1.0) <= 1e-6 * k
+            if not diverged:
+                oi = int(ora["chosen"][b, s])
+                if gi != oi:
+                    if greedy:
+                        gap = abs(float(e_ref[gi]) - float(e_ref[oi]))
+                        assert gap <= tol[gi] + tol[oi], (b, s, gi, oi, gap)
+                    else:
+                        t = max(float(inp["temperatures"][b]), 1e-5)
+                        p = ora["q"][b, s].astype(np.float64)
+                        cdf = np.cumsum(p)
+                        lo, hi = min(gi, oi), max(gi, oi)
+                        slack = k * 2.0 ** -23 + 4 * float(tol.max()) / t
+                        assert np.all(np.abs(inp["uniforms"][b, s] - cdf[lo:hi]) <= slack), (b, s)
+                    ties += 1
+                    diverged = True
+                else:
+                    assert abs(q[b, s] - ora["q"][b, s]).max() <= q_tol
+            prev = gi
+    return ties
+
+
+def _named(name):
+    w = synth.BY_NAME[name]
+    inp = synth.make(w)
+    return w, inp
+
+
+@pytest.mark.parametrize("name", [c.name for c in synth.CONFIGS])
+def test_walk_staged_parity_on_named_workloads(cuda, name):
+    w, inp = _named(name)
+    th, tw = dflash2.to_device(inp["h"], cuda), dflash2.to_device(inp["lm_head"], cuda)
+    ids, vals, err = dflash2.unary_topk(th, tw, w.target_vocab, w.mult, w.cap, w.top_k)
+    cand = ids.cpu().numpy().reshape(w.batch, w.slots, w.top_k)
+    cand_u = vals.cpu().numpy().reshape(w.batch, w.slots, w.top_k)
+    del th, tw
+    tokens, q, ps, err2 = _run_walk(cuda, inp, cand, cand_u)
+    assert int(err.item()) == 0 and err2 == 0
+    ties = _compare(inp, cand, cand_u, tokens, q, ps, w.dtype, w.hidden)
+    print(f"{name}: walk near-ties accepted {ties}")
+
+
+def _random_candidates(w, seed, scale_ab=1.0):
+    rng = np.random.default_rng(seed)
+    inp = synth.make(w, parts=("h", "A", "B", "proj", "uniforms", "anchors"))
+    if scale_ab != 1.0:
+        for p in ("A", "B"):
+            a = (synth.bf16_bits_to_f32(inp[p]) if w.dtype == "bf16" else inp[p]) * scale_ab
+            inp[p] = synth.to_bf16_bits(a) if w.dtype == "bf16" else a.astype(np.float32)
+    cand = np.stack([rng.choice(w.draft_vocab, size=w.top_k, replace=False)
+                     for _ in range(w.rows)]).reshape(w.batch, w.slots, w.top_k).astype(np.int64)
+    cand_u = np.sort(rng.standard_normal((w.batch, w.slots, w.top_k)).astype(np.float32),
+                     axis=-1)[..., ::-1].copy()
+    return inp, cand, cand_u
+
+
+WALK_CASES = [
+    dict(batch=6, block_size=9, hidden=192, rank=8, top_k=20, dtype="bf16", sampling="mixed", temperature=0.9),
+    dict(batch=4, block_size=5, hidden=96, rank=16, top_k=1, dtype="bf16", sampling="sampled", temperature=1.0),
+    dict(batch=5, block_size=17, hidden=128, rank=256, top_k=128, dtype="bf16", sampling="mixed", temperature=0.5),
+    dict(batch=3, block_size=2, hidden=64, rank=32, top_k=33, dtype="f32", sampling="sampled", temperature=2.0),
+    dict(batch=7, block_size=8, hidden=256, rank=16, top_k=8, dtype="f32", sampling="mixed", temperature=1e-7),
+]
+
+
+@pytest.mark.parametrize("case", WALK_CASES, ids=lambda c: f"r{c['rank']}-k{c['top_k']}-{c['dtype']}")
+def test_walk_small_shapes(cuda, case):
+    w = synth.CONFIGS[0].scaled(draft_vocab=3000, target_vocab=3000, seed=97, **case)
+    inp, cand, cand_u = _random_candidates(w, 98, scale_ab=20.0)
+    tokens, q, ps, err = _run_walk(cuda, inp, cand, cand_u)
+    assert err == 0
+    _compare(inp, cand, cand_u, tokens, q, ps, w.dtype, w.hidden)
+
+
+def test_out_of_range_ids_set_the_error_bit_and_use_zero_rows(cuda):
+    w = synth.CONFIGS[0].scaled(batch=3, block_size=4, hidden=64, rank=16, top_k=8, dtype="bf16",
+                                draft_vocab=500, target_vocab=500, sampling="greedy", seed=99)
+    inp, cand, cand_u = _random_candidates(w, 100, scale_ab=30.0)
+    inp["anchors"] = inp["anchors"].copy()
+    inp["anchors"][1] = 10_000
+    cand[2, 1, 3] = -5
+    tokens, q, ps, err = _run_walk(cuda, inp, cand, cand_u)
+    assert err & dflash2.DEVERR_ID_RANGE
+    ora = oracle.selector(inp["h"], inp["proj"], inp["A"], inp["B"], inp["anchors"], cand, cand_u,
+                          inp["uniforms"], inp["temperatures"], inp["greedy"])
+    assert ora["errors"] > 0
+    # request 1's first slot falls back to the unary values alone
+    np.testing.assert_allclose(ps[1, 0], cand_u[1, 0], rtol=0, atol=0)
+    _compare(inp, cand, cand_u, tokens, q, ps, w.dtype, w.hidden)
+
+
+def test_greedy_rows_do_not_depend_on_other_rows(cuda):
+    w = synth.CONFIGS[0].scaled(batch=8, block_size=10, hidden=128, rank=32, top_k=16, dtype="bf16",
+                                draft_vocab=2000, target_vocab=2000, sampling="mixed",
+                                temperature=0.7, seed=101)
+    inp, cand, cand_u = _random_candidates(w, 102, scale_ab=10.0)
+    t1, q1, _, _ = _run_walk(cuda, inp, cand, cand_u)
+    rng = np.random.default_rng(103)
+    inp2 = dict(inp)
+    inp2["uniforms"] = rng.random(inp["uniforms"].shape, dtype=np.float32)
+    inp2["temperatures"] = np.where(inp["greedy"] == 1, np.float32(1.0),
+                                    rng.uniform(0.1, 3.0, w.batch).astype(np.float32)).astype(np.float32)
+    t2, q2, _, _ = _run_walk(cuda, inp2, cand, cand_u)
+    g = inp["greedy"] == 1
+    np.testing.assert_array_equal(t1[g], t2[g])
+    np.testing.assert_array_equal(q1[g], q2[g])
