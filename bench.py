@@ -1,0 +1,451 @@
+"""Benchmark of the DFlash2 draft-proposal hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+grouped conv, unary candidates (lm_head GEMM + transform + padded mask +
+top-K), selector walk (projection + edges + walk) and d2t remap, all through
+the C ABI on one stream, replayed from one captured CUDA graph.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload NAME]
+
+The default workload is the Qwen3-8B-shaped bf16 draft (batch 32, block 16,
+hidden 4096, vocab 151936, rank 64, top-K 16, cap 30; even rows greedy, odd
+rows T = 0.7).  The metric is proposals per second (batch x slots proposed /
+step time).  L2 is flushed (a 256 MiB write) before every timed step and the
+flush is outside the timed events.  Prints ONE JSON line (rank 0).
+
+`--impl reference` times the CPU oracle (the method restated in plain C,
+double accumulation) on a bounded sample of the same workload on the host
+cores; it never touches the GPU.  Under torchrun every rank runs its own
+replica of the workload (weak scaling; requests are independent, so there is
+no data-path collective) and the step time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft blocks/sec (batch×slots proposed/s) + % HBM / tensor roofline per kernel"
+UNIT = "proposals/s"
+DEFAULT_WORKLOAD = "qwen3-8b-bf16"
+L2_FLUSH_BYTES = 256 << 20
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "unary_topk_qwen3-8b-bf16.md")
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p["bf16_tflops_sustained"], "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def algorithmic_work(w):
+    """Per-call algorithmic work of each stage (bytes moved at minimum, or flops)."""
+    e = 2 if w.dtype == "bf16" else 4
+    n, hdim, g = w.n_tokens, w.hidden, w.groups
+    conv_bytes = 2 * n * hdim * e + n * w.taps * g * e + w.taps * hdim * e
+    gemm_flops = 2 * w.rows * w.draft_vocab * hdim
+    # walk incl. projection: h and proj once, per slot K candidate B rows + one A
+    # row, the unary values, ids, uniforms; outputs q and tokens
+    walk_bytes = (w.rows * hdim * e + w.rank * hdim * e
+                  + w.rows * (w.top_k + 1) * w.rank * e
+                  + w.rows * w.top_k * (4 + 8) + w.rows * 4
+                  + w.rows * w.top_k * 4 + w.rows * 8)
+    d2t_bytes = w.rows * (8 + 8 + (8 if w.uses_d2t else 0))
+    return dict(conv_bytes=conv_bytes, gemm_flops=gemm_flops, walk_bytes=walk_bytes,
+                d2t_bytes=d2t_bytes)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _profile_traffic(kernel_sources):
+    """DRAM bytes per launch of the filter GEMM from the committed ncu summary,
+    or None when the kernel sources changed since the capture."""
+    import hashlib
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    hm = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    if not m or not hm:
+        return None
+    h = hashlib.sha256()
+    for path in kernel_sources:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    if h.hexdigest()[:16] != hm.group(1)[:16]:
+        return None
+    return float(m.group(1))
+
+
+def kernel_source_hash():
+    import hashlib
+    srcs = [os.path.join(ROOT, "block_draft_proposal_gb300", "csrc", f)
+            for f in ("gemm_tc.cu", "common.cuh", "kernels.h")]
+    h = hashlib.sha256()
+    for path in srcs:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16], srcs
+
+
+# ---------------------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline leg)
+# ---------------------------------------------------------------------------------------
+
+def oracle_sample_time(w, inp, n_requests: int):
+    """Time the oracle chain over the first n_requests requests of the workload."""
+    import oracle
+    rows = n_requests * w.slots
+    t0 = time.perf_counter()
+    nt = n_requests * w.block_size
+    oracle.conv(inp["x"][:nt], inp["base"], inp["delta"][:nt], w.block_size, w.group_size, w.taps)
+    u = oracle.unary_rows(inp["h"], inp["lm_head"], w.target_vocab, w.mult, w.cap,
+                          rows=list(range(rows)))
+    ids, vals = oracle.topk(u, w.top_k)
+    sel = oracle.selector(inp["h"][:rows], inp["proj"], inp["A"], inp["B"], inp["anchors"][:n_requests],
+                          ids.reshape(n_requests, w.slots, w.top_k),
+                          vals.reshape(n_requests, w.slots, w.top_k), inp["uniforms"][:n_requests],
+                          inp["temperatures"][:n_requests], inp["greedy"][:n_requests])
+    oracle.d2t(sel["tokens"].reshape(-1), inp["d2t"], w.draft_vocab, w.target_vocab)
+    return time.perf_counter() - t0
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, w):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return 0
+    from block_draft_proposal_gb300 import synth
+    inp = synth.make(w)
+    n_req = 1
+    for _ in range(args.warmup):
+        oracle_sample_time(w, inp, n_req)
+    times = [oracle_sample_time(w, inp, n_req) for _ in range(args.steps)]
+    t = statistics.mean(times)
+    value = n_req * w.slots / t
+    sample = (f"{n_req} request ({n_req * w.slots} proposal rows) of {w.name} per step: conv of its "
+              f"block, unary logits over the full vocab, full-sort top-K, lattice + walk, d2t")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(w):
+    return {"workload": w.name, "batch": w.batch, "block_size": w.block_size, "slots": w.slots,
+            "hidden": w.hidden, "group_size": w.group_size, "taps": w.taps,
+            "draft_vocab": w.draft_vocab, "target_vocab": w.target_vocab, "rank": w.rank,
+            "top_k": w.top_k, "mult": w.mult, "cap": w.cap, "sampling": w.sampling,
+            "temperature": w.temperature,
+            "l2": "flushed before every timed step (256 MiB write, outside the timed events)",
+            "graph": "one CUDA graph per step (replayed)"}
+
+
+# ---------------------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------------------
+
+def run_gpu(args, w):
+    import numpy as np
+    import torch
+
+    rank, world, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__ as g
+    g.build_library()
+    from block_draft_proposal_gb300 import dflash2, synth
+
+    inp = synth.make(w)
+    t = {k: dflash2.to_device(v, dev) for k, v in inp.items() if v is not None}
+    bufs = dflash2.ProposalBuffers(w, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+
+    def step(record: bool):
+        if record:
+            ev[0].record(stream)
+        dflash2.grouped_conv(t["x"], t["base"], t["delta"], w.block_size, w.group_size, w.taps,
+                             out=bufs.conv_out, stream=stream)
+        if record:
+            ev[1].record(stream)
+        dflash2.unary_topk(t["h"], t["lm_head"], w.target_vocab, w.mult, w.cap, w.top_k,
+                           cand_ids=bufs.cand_ids, cand_u=bufs.cand_u, workspace=bufs.ws_topk,
+                           err=bufs.err, stream=stream)
+        if record:
+            ev[2].record(stream)
+        dflash2.selector_walk(t["h"], t["proj"], t["A"], t["B"], t["anchors"],
+                              bufs.cand_ids.view(w.batch, w.slots, w.top_k),
+                              bufs.cand_u.view(w.batch, w.slots, w.top_k), t["temperatures"],
+                              t["greedy"], t["uniforms"], tokens=bufs.tokens, q=bufs.q,
+                              workspace=bufs.ws_walk, err=bufs.err, stream=stream)
+        if record:
+            ev[3].record(stream)
+        dflash2.d2t_remap(bufs.tokens, t.get("d2t"), w.draft_vocab, w.target_vocab,
+                          out=bufs.target_ids, err=bufs.err, stream=stream)
+        if record:
+            ev[4].record(stream)
+
+    # capture one step into a graph (stage events cannot be timed inside a graph)
+    with torch.cuda.stream(stream):
+        step(False)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    use_graph = True
+    try:
+        with torch.cuda.graph(graph, stream=stream):
+            step(False)
+    except Exception:
+        use_graph = False
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            graph.replay() if use_graph else step(False)
+            flush.zero_()
+            step(True)
+    stream.synchronize()
+
+    # timed region: K graph replays (the value), then K eager steps with stage
+    # events (the per-stage breakdown and the roofline); L2 flushed before each
+    stage_ms = {k: [] for k in ("conv", "unary_topk", "walk", "d2t", "step")}
+    graph_ms = []
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                flush.zero_()
+                g0.record(stream)
+                graph.replay() if use_graph else step(False)
+                g1.record(stream)
+                stream.synchronize()
+                graph_ms.append(g0.elapsed_time(g1))
+            for _ in range(args.steps):
+                flush.zero_()
+                step(True)
+                stream.synchronize()
+                stage_ms["conv"].append(ev[0].elapsed_time(ev[1]))
+                stage_ms["unary_topk"].append(ev[1].elapsed_time(ev[2]))
+                stage_ms["walk"].append(ev[2].elapsed_time(ev[3]))
+                stage_ms["d2t"].append(ev[3].elapsed_time(ev[4]))
+                stage_ms["step"].append(ev[0].elapsed_time(ev[4]))
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = statistics.mean(graph_ms)
+    eager_ms = statistics.mean(stage_ms["step"])
+    err = int(bufs.err.item())
+
+    # end to end through the public API: inputs from pinned host memory, outputs back
+    host_in = {k: torch.from_numpy(inp[k].view(np.int16) if inp[k].dtype == np.uint16 else inp[k])
+               .pin_memory() for k in ("x", "delta", "h", "uniforms", "temperatures", "greedy", "anchors")}
+    dev_in = {k: t[k] for k in host_in}
+    host_tok = torch.empty(bufs.target_ids.shape, dtype=torch.int64).pin_memory()
+    host_q = torch.empty(bufs.q.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_tok.numel() * 8 + host_q.numel() * 4
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            e0.record(stream)
+            for k, hv in host_in.items():
+                dv = dev_in[k]
+                if dv.dtype == torch.bfloat16:
+                    dv = dv.view(torch.int16)
+                dv.copy_(hv, non_blocking=True)
+            graph.replay() if use_graph else step(False)
+            host_tok.copy_(bufs.target_ids, non_blocking=True)
+            host_q.copy_(bufs.q, non_blocking=True)
+            e1.record(stream)
+            stream.synchronize()
+            if i >= args.warmup:
+                e2e_ms.append(e0.elapsed_time(e1))
+    e2e = statistics.mean(e2e_ms)
+
+    # max over ranks
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms, e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms, e2e = float(tt[0]), float(tt[1])
+
+    launches_per_step = 1 + 4 + 2 + 1
+    if w.dtype == "f32":
+        launches_per_step = 1 + 1 + 2 + 1
+    elif (w.draft_vocab + 127) // 128 <= 32:
+        launches_per_step = 1 + 3 + 2 + 1
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    hbm, tf_burst, tf_sust, peak_kind = _peaks()
+    work = algorithmic_work(w)
+    unary_ms = statistics.mean(stage_ms["unary_topk"])
+    achieved_tf = work["gemm_flops"] / (unary_ms * 1e-3) / 1e12
+    src_hash, srcs = kernel_source_hash()
+    traffic = _profile_traffic(srcs)
+    conv_ms = statistics.mean(stage_ms["conv"])
+    walk_ms = statistics.mean(stage_ms["walk"])
+    stages = {
+        "conv": {"ms": conv_ms, "GB/s": work["conv_bytes"] / (conv_ms * 1e-3) / 1e9,
+                 "frac_hbm": work["conv_bytes"] / (conv_ms * 1e-3) / 1e9 / hbm},
+        "unary_topk": {"ms": unary_ms, "TFLOP/s": achieved_tf, "frac_bf16_burst": achieved_tf / tf_burst,
+                       "frac_bf16_sustained": achieved_tf / tf_sust},
+        "walk": {"ms": walk_ms, "GB/s": work["walk_bytes"] / (walk_ms * 1e-3) / 1e9,
+                 "frac_hbm": work["walk_bytes"] / (walk_ms * 1e-3) / 1e9 / hbm},
+        "d2t": {"ms": statistics.mean(stage_ms["d2t"])},
+    }
+
+    # CPU baseline: the oracle as it stands on a bounded sample (rank 0, N = 1)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        n_req = max(1, min(w.batch, 20))   # about 10-30 s of CPU work on 16 cores
+        tc = oracle_sample_time(w, inp, n_req)
+        cpu = {"value": n_req * w.slots / tc, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+               "sample": f"{n_req} requests ({n_req * w.slots} proposal rows) of {w.name}: the "
+                         f"whole oracle chain, {tc:.1f} s"}
+
+    value = world * w.rows / (ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded; weights N(0,0.02), "
+        "activations N(0,1), uniforms U[0,1))", "config": _config(w),
+        "roofline": {"bound": "tensor", "achieved": achieved_tf, "peak": tf_burst,
+                     "unit": "TFLOP/s", "frac": achieved_tf / tf_burst, "traffic": traffic,
+                     "kernel": "unary_topk stage (pilot GEMM + pilot select + filter GEMM + "
+                               "finalize), 2*M*V*H flops over the stage time",
+                     "peak_kind": f"{peak_kind} bf16 burst"},
+        "stages": stages,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * w.rows / (e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps * 2,  # graph phase + eager phase
+        "clocks": clocks.summary(),
+        "device_err_word": err,
+        "graph": use_graph,
+        "eager_ms_per_step": eager_ms,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    from block_draft_proposal_gb300 import synth
+    w = synth.BY_NAME[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
