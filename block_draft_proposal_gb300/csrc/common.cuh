@@ -241,6 +241,18 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// One fp32 TMEM column of this warp's 32 lanes (one value per thread), waited.
+__device__ __forceinline__ float tmem_ld1_wait(uint32_t taddr) {
+    uint32_t r;
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r)
+        : "r"(taddr)
+        : "memory");
+    return __uint_as_float(r);
+}
+
 // Shared-memory matrix descriptor for a K-major bf16 tile written by TMA with
 // 128-byte swizzle: rows of 128 bytes (64 elements), 8-row groups 1024 bytes
 // apart.  Advancing K by 16 elements inside the 128-byte row adds 32 bytes

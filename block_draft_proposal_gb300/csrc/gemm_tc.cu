@@ -25,6 +25,7 @@ namespace dflash2 {
 namespace {
 
 constexpr uint32_t kWTileBytes = kGemmTileW * kGemmTileK * 2;  // 16 KiB
+constexpr size_t kGemmSmemBytes = 220 * 1024;                   // dynamic shared memory cap
 
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
     const uint64_t t0 = global_timer_ns();
@@ -81,31 +82,80 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams &p, const float 
             if (i < ncols && m < p.rows_h)
                 o[(int64_t)m * p.ldo] = valid ? unary_transform(z[i], p.mult, p.cap) : -INFINITY;
         }
-    } else {
-        const bool valid_v = v < p.rows_w && v < p.target_vocab;
-        const int my_m = m0 + lane;
-        const uint64_t th_lane = (lane < ncols && my_m < p.rows_h) ? p.theta[my_m] : ~0ull;
+    }
+}
+
+// Per-epilogue-warp shared scratch of the filter mode: the thresholds of the
+// current tile's tokens and a buffer of survivors waiting for their global
+// slots.
+constexpr int kEpiBuf = 128;
+struct EpiScratch {
+    float pre[256];
+    uint64_t th[256];
+    uint64_t key[kEpiBuf];
+    int32_t row[kEpiBuf];
+};
+
+// Moves the buffered survivors to their rows' candidate lists: one global
+// atomic per survivor, issued by all lanes together.
+__device__ __noinline__ void flush_survivors(const GemmParams &p, EpiScratch &es, int n, int lane) {
+    __syncwarp();
+#pragma unroll 4
+    for (int e = lane; e < n; e += 32) {
+        const int row = es.row[e];
+        const uint32_t slot = atomicAdd(p.cnt + row, 1u);
+        if (slot < (uint32_t)p.cand_cap) p.cand[(int64_t)row * p.cand_cap + slot] = es.key[e];
+    }
+    __syncwarp();
+}
+
+// Filter epilogue of 32 columns (tokens m0 .. m0+31, tile columns c0 ..).
+// fl(mult * z), the first rounding step of the transform, is compared with
+// the token's pre-threshold; only where some lane passes is the exact key
+// formed and compared with the threshold key (pilot_select_kernel shows the
+// pre-threshold never drops a key that reaches it).  The rare columns with a
+// hit are visited in a compact loop that re-reads the one column from TMEM,
+// which keeps the code small.  Keys that pass are buffered in shared memory;
+// nbuf counts them (warp-uniform).
+__device__ __forceinline__ void filter_chunk(const GemmParams &p, const float (&z)[32], int64_t v,
+                                             int m0, int c0, uint32_t tcol, EpiScratch &es,
+                                             int &nbuf, int lane) {
+    const bool valid_v = v < p.rows_w && v < p.target_vocab;
+    const float pre_lane = es.pre[c0 + lane];
+    uint32_t hits = 0;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int m = m0 + i;
-            const uint64_t th = shfl_u64(th_lane, i);
-            bool pass = false;
-            uint64_t key = 0;
-            if (valid_v && i < ncols && m < p.rows_h) {
-                key = make_key(unary_transform(z[i], p.mult, p.cap), (uint32_t)v);
-                pass = key >= th;
+    for (int i = 0; i < 32; ++i) {
+        const float pre = __shfl_sync(0xFFFFFFFFu, pre_lane, i);
+        hits |= (valid_v && p.mult * z[i] >= pre) ? (1u << i) : 0u;
+    }
+    uint32_t cols = __reduce_or_sync(0xFFFFFFFFu, hits);
+    if (cols == 0) return;
+    const uint64_t th_lane = es.th[c0 + lane];
+    const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll 1
+    while (cols) {  // warp-uniform
+        const int i = __ffs(cols) - 1;
+        cols &= cols - 1;
+        const float zi = tmem_ld1_wait(tcol + (uint32_t)i);
+        const uint64_t th = shfl_u64(th_lane, i);
+        bool pass = false;
+        uint64_t key = 0;
+        if ((hits >> i) & 1u) {
+            key = make_key(unary_transform(zi, p.mult, p.cap), (uint32_t)v);
+            pass = key >= th;
+        }
+        const uint32_t b = __ballot_sync(0xFFFFFFFFu, pass);
+        if (b) {
+            if (nbuf + 32 > kEpiBuf) {
+                flush_survivors(p, es, nbuf, lane);
+                nbuf = 0;
             }
-            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pass);
-            if (bal) {
-                const int leader = __ffs(bal) - 1;
-                uint32_t base = 0;
-                if (lane == leader) base = atomicAdd(p.cnt + m, (uint32_t)__popc(bal));
-                base = __shfl_sync(0xFFFFFFFFu, base, leader);
-                if (pass) {
-                    const uint32_t slot = base + (uint32_t)__popc(bal & ((1u << lane) - 1u));
-                    if (slot < (uint32_t)p.cand_cap) p.cand[(int64_t)m * p.cand_cap + slot] = key;
-                }
+            if (pass) {
+                const int pos = nbuf + __popc(b & lt);
+                es.key[pos] = key;
+                es.row[pos] = m0 + i;
             }
+            nbuf += __popc(b);
         }
     }
 }
@@ -127,6 +177,7 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t h_bytes = (uint32_t)p.bn * kGemmTileK * 2;
     uint8_t *w_smem = smem;
     uint8_t *h_smem = smem + (size_t)p.stages * kWTileBytes;
+    EpiScratch *epi = reinterpret_cast<EpiScratch *>(h_smem + (size_t)p.stages * h_bytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -231,21 +282,37 @@ __global__ void __launch_bounds__(192, 1)
     } else {
         const int quarter = warp & 3;  // TMEM lanes this warp may access
         const int row_in_tile = quarter * 32 + lane;
+        EpiScratch &es = epi[warp - 2];
         int t = 0;
         for (int w = blockIdx.x; w < total; w += gridDim.x, ++t) {
             const Item item = decode(p, w);
             const int a = t & 1;
+            const int m_tile = item.nt * p.bn;
+            if (p.mode == kGemmFilter) {
+                // the tile's thresholds, fetched while its MMAs still run
+                for (int c = lane; c < 256; c += 32) {
+                    const int m = m_tile + c;
+                    const bool ok = c < p.bn && m < p.rows_h;
+                    es.pre[c] = ok ? p.theta_pre[m] : INFINITY;
+                    es.th[c] = ok ? p.theta[m] : ~0ull;
+                }
+                __syncwarp();
+            }
             if (!mbar_wait(&acc_full[a], ((uint32_t)t >> 1) & 1u, &abort_flag, p.err)) break;
             tc_fence_after();
             const int64_t v = (int64_t)item.wt * kGemmTileW + row_in_tile;
-            const int m_tile = item.nt * p.bn;
             const uint32_t tbase = tmem + (uint32_t)a * p.acc_cols + ((uint32_t)(quarter * 32) << 16);
+            int nbuf = 0;
             for (int c0 = 0; c0 < p.bn; c0 += 32) {
                 float z[32];
                 tmem_ld32_wait(tbase + (uint32_t)c0, z);
-                epilogue_chunk(p, z, v, row_in_tile, m_tile + c0, min(32, p.bn - c0), item, lane);
+                if (p.mode == kGemmFilter)
+                    filter_chunk(p, z, v, m_tile + c0, c0, tbase + (uint32_t)c0, es, nbuf, lane);
+                else
+                    epilogue_chunk(p, z, v, row_in_tile, m_tile + c0, min(32, p.bn - c0), item, lane);
             }
             tc_fence_before();
+            if (p.mode == kGemmFilter && nbuf > 0) flush_survivors(p, es, nbuf, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[a]);
         }
@@ -285,10 +352,11 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     while (acc < (uint32_t)p.bn) acc <<= 1;
     p.acc_cols = acc;
     const uint32_t stage_bytes = kWTileBytes + (uint32_t)p.bn * kGemmTileK * 2;
-    int stages = (int)((200u * 1024u) / stage_bytes);
+    const size_t epi_bytes = p.mode == kGemmFilter ? 4 * sizeof(EpiScratch) : 0;
+    int stages = (int)((kGemmSmemBytes - 1024 - epi_bytes) / stage_bytes);
     if (stages > kGemmMaxStages) stages = kGemmMaxStages;
     p.stages = stages;
-    const size_t smem = (size_t)stages * stage_bytes + 1024;
+    const size_t smem = (size_t)stages * stage_bytes + epi_bytes + 1024;
 
     CUtensorMap tm_w, tm_h;
     dflash2_status s = encode_tmap_bf16(&tm_w, w, (uint64_t)p.rows_w, (uint64_t)p.hidden, kGemmTileW);
@@ -298,7 +366,7 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
 
     if (di.device >= 0 && di.device < 64 && !g_smem_set[di.device]) {
         if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 210 * 1024) != cudaSuccess) {
+                                 (int)kGemmSmemBytes) != cudaSuccess) {
             cudaGetLastError();
             return DFLASH2_ERR_CUDA;
         }

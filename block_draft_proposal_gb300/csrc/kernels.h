@@ -46,6 +46,7 @@ struct GemmParams {
     int64_t ldo;
     int64_t split_stride;
     const uint64_t *theta; // filter: per-row threshold key
+    const float *theta_pre; // filter: per-row bound on mult * z below which u cannot reach theta
     uint32_t *cnt;         // filter: per-row candidate count
     uint64_t *cand;        // filter: [rows_h][cand_cap] keys
     int32_t cand_cap;

@@ -232,9 +232,18 @@ __global__ void __launch_bounds__(kSelThreads)
 }
 
 // Pilot select: threshold and seed candidates of each row from its pilot u.
+//
+// theta_pre: for mult > 0 and a positive threshold u_th, the transform obeys
+// u <= mult * z (1 + 2^-21) after rounding: tanh(x) <= x for x >= 0, tanhf is
+// within 2 ulp, and the divide and the two multiplies round once each (for
+// mult * z < 0, u < 0 < u_th).  So any entry whose computed u reaches u_th has
+// fl(mult * z) >= u_th (1 - 2^-21) > u_th (1 - 2^-18) = theta_pre, and the
+// filter may skip the transform wherever fl(mult * z) < theta_pre.  With no
+// threshold, mult <= 0 or u_th <= 0, theta_pre is -inf (every entry checked).
 __global__ void __launch_bounds__(kSelThreads)
     pilot_select_kernel(const float *__restrict__ pilot_u, int n_pilot, int pilot_stride, int k,
-                        uint64_t *theta, uint32_t *cnt, uint64_t *cand, int cand_cap) {
+                        float mult, uint64_t *theta, float *theta_pre, uint32_t *cnt,
+                        uint64_t *cand, int cand_cap) {
     __shared__ SelectShared sh;
     extern __shared__ __align__(16) uint8_t dyn[];
     uint64_t *keys = reinterpret_cast<uint64_t *>(dyn);
@@ -252,6 +261,9 @@ __global__ void __launch_bounds__(kSelThreads)
     for (int i = threadIdx.x; i < got; i += blockDim.x) cand[row * cand_cap + i] = sh.top[i];
     if (threadIdx.x == 0) {
         theta[row] = kth;  // 0 when the pilot holds fewer than k valid entries
+        const float u_th = key_u(kth);
+        theta_pre[row] = (kth != 0 && mult > 0.0f && u_th > 0.0f) ? u_th * (1.0f - 0x1p-18f)
+                                                                  : -INFINITY;
         cnt[row] = (uint32_t)got;
     }
 }
@@ -294,7 +306,7 @@ __global__ void __launch_bounds__(kSelThreads)
 // ---- workspace layout (bf16) -------------------------------------------------
 struct TopkLayout {
     int32_t n_wtiles, n_pilot, pilot_stride, cap;
-    size_t theta_off, cnt_off, pilot_off, cand_off, fixed_bytes;
+    size_t theta_off, pre_off, cnt_off, pilot_off, cand_off, fixed_bytes;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -304,7 +316,8 @@ inline TopkLayout topk_layout(int64_t rows, int64_t draft_vocab) {
     L.n_wtiles = (int32_t)((draft_vocab + kGemmTileW - 1) / kGemmTileW);
     pilot_layout(L.n_wtiles, &L.n_pilot, &L.pilot_stride);
     L.theta_off = 0;
-    L.cnt_off = align256(L.theta_off + (size_t)rows * 8);
+    L.pre_off = align256(L.theta_off + (size_t)rows * 8);
+    L.cnt_off = align256(L.pre_off + (size_t)rows * 4);
     L.pilot_off = align256(L.cnt_off + (size_t)rows * 4);
     L.cand_off = align256(L.pilot_off + (size_t)rows * L.n_pilot * kGemmTileW * 4);
     L.fixed_bytes = L.cand_off;
@@ -405,6 +418,7 @@ extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head,
     if (cap_keys > kMaxCandCap) cap_keys = kMaxCandCap;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     uint64_t *theta = reinterpret_cast<uint64_t *>(ws + L.theta_off);
+    float *theta_pre = reinterpret_cast<float *>(ws + L.pre_off);
     uint32_t *cnt = reinterpret_cast<uint32_t *>(ws + L.cnt_off);
     float *pilot_u = reinterpret_cast<float *>(ws + L.pilot_off);
     uint64_t *cand = reinterpret_cast<uint64_t *>(ws + L.cand_off);
@@ -424,21 +438,32 @@ extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head,
     p.cap = cap;
     p.err = err_word;
 
+    // The pilot covers at most 32 weight tiles: smaller token tiles spread
+    // its work items over the SMs.
     p.mode = kGemmPilot;
     p.out = pilot_u;
     p.ldo = (int64_t)L.n_pilot * kGemmTileW;
+    {
+        int64_t want_tiles = di.sm_count / L.n_pilot;  // one wave of work items
+        if (want_tiles < 1) want_tiles = 1;
+        int64_t per = (rows + want_tiles - 1) / want_tiles;
+        per = (per + 15) / 16 * 16;
+        p.bn = (int)(per < 16 ? 16 : (per > bn ? bn : per));
+    }
     s = launch_gemm_tc(di, lm_head, h, p, st);
     if (s != DFLASH2_OK) return s;
+    p.bn = bn;
 
     const size_t pilot_smem = (size_t)L.n_pilot * kGemmTileW * 8;
     pilot_select_kernel<<<(unsigned)rows, kSelThreads, pilot_smem, st>>>(
-        pilot_u, L.n_pilot, L.pilot_stride, top_k, theta, cnt, cand, (int)cap_keys);
+        pilot_u, L.n_pilot, L.pilot_stride, top_k, mult, theta, theta_pre, cnt, cand, (int)cap_keys);
     s = launch_status();
     if (s != DFLASH2_OK) return s;
 
     p.mode = kGemmFilter;
     p.out = nullptr;
     p.theta = theta;
+    p.theta_pre = theta_pre;
     p.cnt = cnt;
     p.cand = cand;
     p.cand_cap = (int32_t)cap_keys;
