@@ -7,23 +7,26 @@
 //   greedy: index = smallest argmax e, q = one-hot;  sampled: q = softmax(e / T),
 //   index = min(#{k : uniform >= cumsum(q)[k]}, K - 1);  token = c_index.
 //
-// One CTA per request walks its slots in order.  The lattice is never
-// materialised: only the K edges leaving the chosen predecessor are formed.
-// The B rows of a slot's K candidates do not depend on the path, so the rows
-// of slot s+1 are fetched (cp.async) while slot s is being walked; only the
-// predecessor's A row sits on the serial chain.  The K edges are reduced by
-// one warp with shuffles (argmax, max, sum, prefix sum, count).
+// One warp walks one request, as the Triton walk runs one single-warp program
+// per request; a CTA holds several independent requests and no block-wide
+// barrier is used.  The lattice is never materialised: only the K edges
+// leaving the chosen predecessor are formed.  The rows a slot needs do not
+// depend on the path, so they are fetched ahead with 1-D TMA bulk copies into
+// a ring of shared-memory buffers: group s holds the B rows of slot s's
+// candidates and, when shared memory allows, the A rows of its possible
+// predecessors (the anchor at slot 0, else slot s-1's candidates).  The
+// serial chain of a slot then touches shared memory and registers only.
 #include "kernels.h"
 
 namespace dflash2 {
 namespace {
 
-constexpr int kWalkThreads = 128;
-constexpr int kWalkWarps = kWalkThreads / 32;
 constexpr int kMaxK = 128;
 constexpr int kMaxRank = 256;
-constexpr int kPerLane = kMaxK / 32;
-constexpr int kWalkMaxSmem = 200 * 1024;  // two buffers of K candidate B rows
+constexpr int kMaxWarpsPerCta = 4;
+constexpr int kMaxSplits = 8;   // hidden splits of the tensor-core projection
+constexpr int kMaxRing = 8;     // prefetch groups per warp
+constexpr size_t kWalkSmemBytes = 224 * 1024;
 
 struct WalkParams {
     const float *g;        // [k_splits][rows][rank] partial projections
@@ -38,19 +41,59 @@ struct WalkParams {
     const float *temps;
     const uint8_t *greedy;
     const float *uniforms;
-    int32_t slots, rank, k;
+    int32_t batch, slots, rank, k;
+    bool bulk_ids;
     int64_t *tokens;
     float *q;
     float *path_scores;
     int32_t *err;
 };
 
-template <typename T> __device__ __forceinline__ float2 ld2(const T *p);
-template <> __device__ __forceinline__ float2 ld2<float>(const float *p) {
-    return *reinterpret_cast<const float2 *>(p);
+// Per-warp shared-memory layout (byte offsets from the warp's base).
+struct WalkLayout {
+    int row_bytes;  // rank * sizeof(T): one table row
+    int nbuf;       // prefetch ring size
+    size_t bars, ids, cu, uni, gs, w, bbuf, abuf, scratch_bytes, total;
+};
+
+__host__ __device__ inline size_t pad16(size_t x) { return (x + 15) & ~(size_t)15; }
+
+__host__ __device__ inline WalkLayout walk_layout(int slots, int k, int rank, int esz, bool prefetch_a,
+                                                  int nbuf, int k_splits) {
+    WalkLayout L;
+    L.row_bytes = rank * esz;
+    L.nbuf = nbuf;
+    L.bars = 0;                                        // nbuf + 1 mbarriers
+    L.ids = pad16((size_t)(kMaxRing + 1) * 8);
+    L.cu = L.ids + pad16((size_t)slots * k * 8);
+    L.uni = L.cu + pad16((size_t)slots * k * 4);
+    L.gs = L.uni + pad16((size_t)slots * 4);
+    L.w = L.gs + pad16((size_t)slots * rank * 4);
+    L.bbuf = L.w + pad16((size_t)rank * 4);
+    L.abuf = L.bbuf + (size_t)nbuf * k * L.row_bytes;
+    size_t end = L.abuf + (prefetch_a ? (size_t)nbuf * k * L.row_bytes : 0);
+    // the projection partials land in the ring buffers before the first group
+    L.scratch_bytes = (size_t)k_splits * slots * rank * 4;
+    if (L.bbuf + L.scratch_bytes > end) end = L.bbuf + L.scratch_bytes;
+    L.total = pad16(end);
+    return L;
 }
-template <> __device__ __forceinline__ float2 ld2<__nv_bfloat16>(const __nv_bfloat16 *p) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+
+template <typename T> __device__ __forceinline__ void unpack16(const uint4 &v, float (&f)[16 / sizeof(T)]);
+template <> __device__ __forceinline__ void unpack16<__nv_bfloat16>(const uint4 &v, float (&f)[8]) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = __bfloat1622float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+template <> __device__ __forceinline__ void unpack16<float>(const uint4 &v, float (&f)[4]) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
 }
 template <typename T> __device__ __forceinline__ float ld1(const T *p);
 template <> __device__ __forceinline__ float ld1<float>(const float *p) { return *p; }
@@ -58,176 +101,271 @@ template <> __device__ __forceinline__ float ld1<__nv_bfloat16>(const __nv_bfloa
     return __bfloat162float(*p);
 }
 
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool valid) {
-    const uint32_t n = valid ? 16u : 0u;  // 0 source bytes: the 16 bytes are zero-filled
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)),
-                 "l"(gmem), "r"(n)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N> __device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// 1-D TMA bulk copy global -> this CTA's shared memory, completing on `bar`.
+// Both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
 }
 
-// Issue the copies of slot s's K candidate B rows into buffer `dst`.
-template <typename T>
-__device__ __forceinline__ void fetch_b_rows(const WalkParams &p, int64_t bs_row, T *dst) {
-    const int chunks = p.rank * (int)sizeof(T) / 16;  // 16-byte pieces per row
-    const T *B = static_cast<const T *>(p.B);
-    for (int idx = threadIdx.x; idx < p.k * chunks; idx += kWalkThreads) {
-        const int kk = idx / chunks;
-        const int ch = idx - kk * chunks;
-        const int64_t c = p.cand[bs_row * p.k + kk];
-        const bool ok = c >= 0 && c < p.table_rows;
-        const T *src = ok ? B + c * p.rank : B;
-        cp_async16(reinterpret_cast<uint8_t *>(dst + (int64_t)kk * p.rank) + ch * 16,
-                   reinterpret_cast<const uint8_t *>(src) + ch * 16, ok);
-        if (!ok && ch == 0 && p.err) atomicOr(p.err, DFLASH2_DEVERR_ID_RANGE);
+// Bounded wait on a warp's own mbarrier.  After the limit the error bit is
+// raised and *timed_out makes later waits return at once (the outputs are
+// then invalid, but the kernel ends).
+__device__ __forceinline__ void warp_bar_wait(uint64_t *bar, uint32_t parity, bool &timed_out,
+                                              int32_t *err) {
+    if (timed_out || mbar_try_wait(bar, parity)) return;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            timed_out = true;
+            if (err) atomicOr(err, DFLASH2_DEVERR_TIMEOUT);
+            return;
+        }
     }
-    cp_async_commit();
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kWalkThreads) walk_kernel(const WalkParams p) {
-    extern __shared__ __align__(16) uint8_t dyn[];
-    T *bbuf[2];
-    bbuf[0] = reinterpret_cast<T *>(dyn);
-    bbuf[1] = bbuf[0] + (size_t)p.k * p.rank;
-    __shared__ float w[kMaxRank];
-    __shared__ float e[kMaxK];
-    __shared__ int chosen;
+__device__ __forceinline__ bool id_ok(int64_t c, int64_t rows) { return c >= 0 && c < rows; }
 
-    const int b = blockIdx.x;
+__device__ __forceinline__ void prefetch_l2_row(const void *row, int bytes) {
+    for (int o = 0; o < bytes; o += 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const uint8_t *>(row) + o));
+}
+
+// Group s of the prefetch ring: one bulk copy per valid row (rows with an
+// id outside the table are zero-filled with plain stores).  Lane 0 arms the
+// group's mbarrier with the byte count before any copy is issued.
+template <typename T, bool PA>
+__device__ __forceinline__ void issue_group(const WalkParams &p, const WalkLayout &L, uint8_t *base,
+                                            const int64_t *ids, int64_t anchor, int s, int lane) {
+    const int K = p.k;
+    const int buf = s % L.nbuf;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(base + L.bars) + buf;
+    uint8_t *bdst = base + L.bbuf + (size_t)buf * K * L.row_bytes;
+    uint8_t *adst = base + L.abuf + (size_t)buf * K * L.row_bytes;
+    const int64_t *bid = ids + (int64_t)s * K;
+    const int64_t *aid = ids + (int64_t)(s - 1) * K;
+    const int na = PA ? (s == 0 ? 1 : K) : 0;
+    uint32_t valid = 0;
+    for (int r = lane; r < K + na; r += 32) {
+        const int64_t c = r < K ? bid[r] : (s == 0 ? anchor : aid[r - K]);
+        valid += id_ok(c, p.table_rows) ? 1u : 0u;
+    }
+    for (int o = 16; o > 0; o >>= 1) valid += __shfl_xor_sync(0xFFFFFFFFu, valid, o);
+    // order this buffer's earlier generic-proxy accesses before the copies
+    fence_proxy_async_smem();
+    if (lane == 0) mbar_arrive_expect_tx(bar, valid * (uint32_t)L.row_bytes);
+    __syncwarp();
+    const T *A = static_cast<const T *>(p.A);
+    const T *B = static_cast<const T *>(p.B);
+    for (int r = lane; r < K + na; r += 32) {
+        const bool is_b = r < K;
+        const int64_t c = is_b ? bid[r] : (s == 0 ? anchor : aid[r - K]);
+        uint8_t *dst = is_b ? bdst + (size_t)r * L.row_bytes : adst + (size_t)(r - K) * L.row_bytes;
+        if (id_ok(c, p.table_rows)) {
+            bulk_copy(dst, (is_b ? B : A) + c * p.rank, (uint32_t)L.row_bytes, bar);
+        } else {
+            for (int o = 0; o < L.row_bytes; o += 16) *reinterpret_cast<uint4 *>(dst + o) = make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+template <typename T, bool PA, int E>
+__global__ void __launch_bounds__(kMaxWarpsPerCta * 32)
+    walk_kernel(const WalkParams p, int warps_per_cta, WalkLayout L) {
+    extern __shared__ __align__(16) uint8_t dyn[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x * warps_per_cta + warp;
+    if (b >= p.batch) return;
     const int S = p.slots, K = p.k, R = p.rank;
-    const bool is_greedy = p.greedy[b] != 0;
+    const int NB = L.nbuf;
+    uint8_t *base = dyn + (size_t)warp * L.total;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + L.bars);
+    int64_t *ids = reinterpret_cast<int64_t *>(base + L.ids);  // raw candidate ids
+    float *cu = reinterpret_cast<float *>(base + L.cu);
+    float *uni = reinterpret_cast<float *>(base + L.uni);
+    float *gs = reinterpret_cast<float *>(base + L.gs);
+    float *w = reinterpret_cast<float *>(base + L.w);
+    const int64_t row0 = (int64_t)b * S;
+    bool timed_out = false;
+
+    if (lane == 0) {
+        for (int i = 0; i <= NB; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    // ---- prologue: ids, unary values and projection partials by bulk copy
+    // (plain loads where the request's slice is not 16-byte aligned)
+    uint64_t *pro = &bars[NB];
+    float *scratch = reinterpret_cast<float *>(base + L.bbuf);
+    const uint32_t part_bytes = (uint32_t)(S * R * 4);
+    const bool bulk_ids = p.bulk_ids;  // the request's id and value slices are 16-byte aligned
+    if (lane == 0)
+        mbar_arrive_expect_tx(pro, (uint32_t)p.k_splits * part_bytes +
+                                       (bulk_ids ? (uint32_t)(S * K * 12) : 0u));
+    __syncwarp();
+    if (lane < p.k_splits)
+        bulk_copy(scratch + (size_t)lane * S * R, p.g + lane * p.split_stride + row0 * R, part_bytes,
+                  pro);
+    if (bulk_ids) {
+        if (lane == 31) bulk_copy(ids, p.cand + row0 * K, (uint32_t)(S * K * 8), pro);
+        if (lane == 30) bulk_copy(cu, p.cand_u + row0 * K, (uint32_t)(S * K * 4), pro);
+    } else {
+#pragma unroll 4
+        for (int t = lane; t < S * K; t += 32) {
+            ids[t] = p.cand[row0 * K + t];
+            cu[t] = p.cand_u[row0 * K + t];
+        }
+    }
+    for (int t = lane; t < S; t += 32) uni[t] = p.uniforms[row0 + t];
+    const int64_t anchor = p.anchors[b];
+    const bool greedy = p.greedy[b] != 0;
     float temp = p.temps[b];
     if (!(temp >= 1e-5f)) temp = 1e-5f;
-    const T *A = static_cast<const T *>(p.A);
+    warp_bar_wait(pro, 0, timed_out, p.err);
+    __syncwarp();
+    // fixed-order sum of the partials
+    for (int t = lane; t < S * R; t += 32) {
+        float acc = scratch[t];
+        for (int ks = 1; ks < p.k_splits; ++ks) acc += scratch[(size_t)ks * S * R + t];
+        gs[t] = acc;
+    }
+    bool bad = !id_ok(anchor, p.table_rows);
+    for (int t = lane; t < S * K; t += 32) bad |= !id_ok(ids[t], p.table_rows);
+    if (__any_sync(0xFFFFFFFFu, bad) && lane == 0 && p.err) atomicOr(p.err, DFLASH2_DEVERR_ID_RANGE);
+    __syncwarp();  // scratch (ring buffers) is free again
 
-    if (S > 0) fetch_b_rows<T>(p, (int64_t)b * S, bbuf[0]);
+    for (int s0 = 0; s0 < NB - 1 && s0 < S; ++s0) issue_group<T, PA>(p, L, base, ids, anchor, s0, lane);
+
+    constexpr int VN = 16 / sizeof(T);
+    const T *A = static_cast<const T *>(p.A);
     int prev = 0;
     for (int s = 0; s < S; ++s) {
-        const int64_t bs_row = (int64_t)b * S + s;
-        if (s + 1 < S) {
-            fetch_b_rows<T>(p, bs_row + 1, bbuf[(s + 1) & 1]);
-            cp_async_wait<1>();
+        const int64_t row = row0 + s;
+        if (s + NB - 1 < S) issue_group<T, PA>(p, L, base, ids, anchor, s + NB - 1, lane);
+        const int buf = s % NB;
+        warp_bar_wait(&bars[buf], (uint32_t)(s / NB) & 1u, timed_out, p.err);
+        __syncwarp();
+        if (!PA && s + 1 < S) {
+            // warm L2 with the A rows the next slot may need
+            for (int t = lane; t < K; t += 32) {
+                const int64_t c = ids[(int64_t)s * K + t];
+                if (id_ok(c, p.table_rows)) prefetch_l2_row(A + c * R, L.row_bytes);
+            }
+        }
+        // w = A[predecessor] (elementwise *) g
+        const float *gsl = gs + (size_t)s * R;
+        if (PA) {
+            const T *arow = reinterpret_cast<const T *>(base + L.abuf + (size_t)buf * K * L.row_bytes +
+                                                        (size_t)(s == 0 ? 0 : prev) * L.row_bytes);
+            for (int j = lane; j < R; j += 32) w[j] = ld1<T>(arow + j) * gsl[j];
         } else {
-            cp_async_wait<0>();
+            const int64_t pid = s == 0 ? anchor : ids[(int64_t)(s - 1) * K + prev];
+            const bool ok = id_ok(pid, p.table_rows);
+            for (int j = lane; j < R; j += 32) w[j] = (ok ? ld1<T>(A + pid * R + j) : 0.0f) * gsl[j];
         }
-        // predecessor: the anchor at slot 0, else the previous slot's choice
-        const int64_t pid = s == 0 ? p.anchors[b] : p.cand[(bs_row - 1) * K + prev];
-        const bool p_ok = pid >= 0 && pid < p.table_rows;
-        if (!p_ok && threadIdx.x == 0 && p.err) atomicOr(p.err, DFLASH2_DEVERR_ID_RANGE);
-        for (int j = threadIdx.x; j < R; j += kWalkThreads) {
-            float gj = 0.0f;
-            for (int ks = 0; ks < p.k_splits; ++ks) gj += p.g[ks * p.split_stride + bs_row * R + j];
-            const float a = p_ok ? ld1<T>(A + pid * R + j) : 0.0f;
-            w[j] = a * gj;
-        }
-        __syncthreads();
-        // edges: one warp per candidate, lanes over the rank in pairs
-        const T *brow = bbuf[s & 1];
-        for (int kk = warp; kk < K; kk += kWalkWarps) {
-            const T *bk = brow + (int64_t)kk * R;
-            float acc = 0.0f;
-            for (int j = 2 * lane; j < R; j += 64) {
-                const float2 bv = ld2<T>(bk + j);
-                acc = fmaf(w[j], bv.x, acc);
-                acc = fmaf(w[j + 1], bv.y, acc);
-            }
-            acc = warp_sum(acc);
-            if (lane == 0) e[kk] = acc + p.cand_u[bs_row * K + kk];
-        }
-        __syncthreads();
-        if (warp == 0) {
-            const int E = (K + 31) >> 5;  // consecutive edges per lane
-            float ev[kPerLane];
-            bool valid[kPerLane];
+        __syncwarp();
+        // edges: lane owns candidates k = lane + 32 i (two FMA chains each)
+        const uint8_t *brows = base + L.bbuf + (size_t)buf * K * L.row_bytes;
+        float ev[E];
+        bool valid[E];
 #pragma unroll
-            for (int i = 0; i < kPerLane; ++i) {
-                const int kk = lane * E + i;
-                valid[i] = i < E && kk < K;
-                ev[i] = valid[i] ? e[kk] : -INFINITY;
-            }
-            float qv[kPerLane];
-            int index;
-            if (is_greedy) {
-                float best = -INFINITY;
-                int bi = INT32_MAX;
+        for (int i = 0; i < E; ++i) {
+            const int kk = lane + 32 * i;
+            valid[i] = kk < K;
+            ev[i] = -INFINITY;
+            if (valid[i]) {
+                // rotate the starting vector by the lane so that lanes reading
+                // different rows touch different banks
+                const uint8_t *brow = brows + (size_t)kk * L.row_bytes;
+                const int nvec = R / VN;
+                float acc0 = 0.0f, acc1 = 0.0f;
+                int v = lane % nvec;
+                for (int n = 0; n < nvec; ++n, v = (v + 1 == nvec) ? 0 : v + 1) {
+                    float bv[VN];
+                    unpack16<T>(*reinterpret_cast<const uint4 *>(brow + v * 16), bv);
+                    const float *wv = w + v * VN;
 #pragma unroll
-                for (int i = 0; i < kPerLane; ++i)
-                    if (valid[i] && (bi == INT32_MAX || ev[i] > best)) {
-                        best = ev[i];
-                        bi = lane * E + i;
-                    }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-                    const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-                    if (oi != INT32_MAX && (bi == INT32_MAX || ob > best || (ob == best && oi < bi))) {
-                        best = ob;
-                        bi = oi;
+                    for (int e = 0; e < VN; e += 2) {
+                        acc0 = fmaf(wv[e], bv[e], acc0);
+                        acc1 = fmaf(wv[e + 1], bv[e + 1], acc1);
                     }
                 }
-                index = bi;
+                ev[i] = (acc0 + acc1) + cu[(int64_t)s * K + kk];
+            }
+        }
+        // selection (warp shuffles only)
+        float qv[E];
+        int index;
+        if (greedy) {
+            float best = -INFINITY;
+            int bi = INT32_MAX;
 #pragma unroll
-                for (int i = 0; i < kPerLane; ++i) qv[i] = (lane * E + i) == index ? 1.0f : 0.0f;
-            } else {
-                float sc[kPerLane];
-                float mx = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < kPerLane; ++i) {
-                    sc[i] = valid[i] ? ev[i] / temp : -INFINITY;
-                    mx = fmaxf(mx, sc[i]);
+            for (int i = 0; i < E; ++i)
+                if (valid[i] && (bi == INT32_MAX || ev[i] > best)) {
+                    best = ev[i];
+                    bi = lane + 32 * i;
                 }
-                mx = warp_max(mx);
-                float local = 0.0f;
 #pragma unroll
-                for (int i = 0; i < kPerLane; ++i) {
-                    qv[i] = valid[i] ? expf(sc[i] - mx) : 0.0f;
-                    local += qv[i];
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+                const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+                if (oi != INT32_MAX && (bi == INT32_MAX || ob > best || (ob == best && oi < bi))) {
+                    best = ob;
+                    bi = oi;
                 }
-                const float total = warp_sum(local);
-                float run = 0.0f, cdf[kPerLane];
+            }
+            index = bi;
 #pragma unroll
-                for (int i = 0; i < kPerLane; ++i) {
-                    qv[i] = qv[i] / total;
-                    run += qv[i];
-                    cdf[i] = run;
-                }
-                float incl = run;  // inclusive scan of the lane totals
+            for (int i = 0; i < E; ++i) qv[i] = (lane + 32 * i) == index ? 1.0f : 0.0f;
+        } else {
+            float sc[E];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < E; ++i) {
+                sc[i] = valid[i] ? ev[i] / temp : -INFINITY;
+                mx = fmaxf(mx, sc[i]);
+            }
+            mx = warp_max(mx);
+            float local = 0.0f;
+#pragma unroll
+            for (int i = 0; i < E; ++i) {
+                qv[i] = valid[i] ? expf(sc[i] - mx) : 0.0f;
+                local += qv[i];
+            }
+            const float total = warp_sum(local);
+            const float u = uni[s];
+            float offset = 0.0f;  // mass of the previous 32-candidate blocks
+            int count = 0;
+#pragma unroll
+            for (int i = 0; i < E; ++i) {
+                qv[i] = qv[i] / total;
+                float incl = qv[i];
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
                     if (lane >= o) incl += y;
                 }
-                float excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
-                if (lane == 0) excl = 0.0f;
-                const float uni = p.uniforms[bs_row];
-                int count = 0;
-#pragma unroll
-                for (int i = 0; i < kPerLane; ++i)
-                    if (valid[i] && uni >= excl + cdf[i]) ++count;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) count += __shfl_xor_sync(0xFFFFFFFFu, count, o);
-                index = count < K - 1 ? count : K - 1;
+                const float cdf = offset + incl;
+                count += __popc(__ballot_sync(0xFFFFFFFFu, valid[i] && u >= cdf));
+                if (i + 1 < E) offset = offset + __shfl_sync(0xFFFFFFFFu, incl, 31);
             }
+            index = count < K - 1 ? count : K - 1;
+        }
 #pragma unroll
-            for (int i = 0; i < kPerLane; ++i) {
-                const int kk = lane * E + i;
-                if (valid[i]) {
-                    p.q[bs_row * K + kk] = qv[i];
-                    if (p.path_scores) p.path_scores[bs_row * K + kk] = ev[i];
-                }
-            }
-            if (lane == 0) {
-                p.tokens[bs_row] = p.cand[bs_row * K + index];
-                chosen = index;
+        for (int i = 0; i < E; ++i) {
+            const int kk = lane + 32 * i;
+            if (valid[i]) {
+                p.q[row * K + kk] = qv[i];
+                if (p.path_scores) p.path_scores[row * K + kk] = ev[i];
             }
         }
-        __syncthreads();
-        prev = chosen;
+        if (lane == 0) p.tokens[row] = ids[(int64_t)s * K + index];
+        prev = index;
+        __syncwarp();  // w and this slot's buffer are rewritten next
     }
 }
 
@@ -248,18 +386,17 @@ __global__ void __launch_bounds__(128)
 }
 
 // Split of the hidden dimension for the tensor-core projection, so that
-// small batches still spread over the SMs.  Depends on the shape only, so
-// the workspace size does not depend on the device.
+// small batches still spread over the SMs; the walk sums the partials in a
+// fixed order.  Depends on the shape only, so the workspace size does not
+// depend on the device.
 inline void proj_tiling(int64_t rows, int hidden, int *bn, int *k_splits) {
-    *bn = rows >= 4096 ? 64 : 32;
+    *bn = rows >= 4096 ? 64 : 16;
     const int64_t tiles = (rows + *bn - 1) / *bn;
     const int num_kb = (hidden + kGemmTileK - 1) / kGemmTileK;
     int64_t ks = (148 + tiles - 1) / tiles;
     if (ks > num_kb) ks = num_kb;
-    if (ks > 16) ks = 16;
+    if (ks > 8) ks = 8;
     if (ks < 1) ks = 1;
-    // the GEMM launcher trims k_splits so that every split has work; size
-    // the workspace for the requested count
     *k_splits = (int)ks;
 }
 
@@ -291,9 +428,7 @@ extern "C" dflash2_status dflash2_selector_walk(
     if (batch < 0 || slots < 0 || hidden <= 0 || rank <= 0 || rank > kMaxRank ||
         rank % rank_mult != 0 || top_k <= 0 || top_k > kMaxK || table_rows <= 0)
         return DFLASH2_ERR_INVALID_ARG;
-    const size_t esz = dtype == DFLASH2_BF16 ? 2 : 4;
-    const size_t smem = 2 * (size_t)top_k * rank * esz;
-    if (smem > (size_t)kWalkMaxSmem) return DFLASH2_ERR_INVALID_ARG;
+    const int esz = dtype == DFLASH2_BF16 ? 2 : 4;
     if (batch == 0 || slots == 0) return DFLASH2_OK;
     if (!h || !proj || !A || !B || !anchor_ids || !cand_ids || !cand_u || !temperatures || !greedy ||
         !uniforms || !tokens || !q)
@@ -305,6 +440,49 @@ extern "C" dflash2_status dflash2_selector_walk(
     DeviceInfo di;
     dflash2_status s = current_device(&di);
     if (s != DFLASH2_OK) return s;
+    // projection tiling decides how many partials the walk sums
+    int ksplits = 1;
+    if (dtype == DFLASH2_BF16) {
+        int bn_unused;
+        proj_tiling((int64_t)batch * slots, hidden, &bn_unused, &ksplits);
+        const int num_kb = (hidden + kGemmTileK - 1) / kGemmTileK;
+        const int per = (num_kb + ksplits - 1) / ksplits;
+        ksplits = (num_kb + per - 1) / per;  // the count the GEMM launcher keeps
+    }
+    // One warp per request.  Among the shared-memory layouts that fit, take
+    // the fewest waves of CTAs, then A-row prefetch, then the deepest
+    // prefetch ring (every slot in flight at most).
+    bool prefetch_a = false;
+    WalkLayout L{};
+    int warps = 0;
+    {
+        const int max_ring = slots < 2 ? 2 : (slots < kMaxRing ? slots : kMaxRing);
+        int64_t best_waves = INT64_MAX;
+        int best_pa = -1;
+        for (int pa = 1; pa >= 0; --pa) {
+            for (int nb = max_ring; nb >= 2; --nb) {
+                const WalkLayout c = walk_layout(slots, top_k, rank, esz, pa != 0, nb, ksplits);
+                int wpc = (int)(kWalkSmemBytes / c.total);
+                if (wpc < 1) continue;
+                if (wpc > kMaxWarpsPerCta) wpc = kMaxWarpsPerCta;
+                const int64_t ctas = (batch + wpc - 1) / wpc;
+                int64_t per_sm = (int64_t)(227 * 1024) / (int64_t)(wpc * c.total + 1024);
+                if (per_sm < 1) per_sm = 1;
+                const int64_t waves = (ctas + di.sm_count * per_sm - 1) / (di.sm_count * per_sm);
+                if (waves < best_waves) {  // ties keep the earlier (A prefetch, deeper ring)
+                    best_waves = waves;
+                    best_pa = pa;
+                    L = c;
+                    warps = wpc;
+                }
+            }
+        }
+        if (best_pa < 0) return DFLASH2_ERR_INVALID_ARG;  // one request's state exceeds shared memory
+        // one mbarrier phase counts fewer than 2^20 transaction bytes
+        if ((int64_t)ksplits * slots * rank * 4 + (int64_t)slots * top_k * 12 >= (1 << 20))
+            return DFLASH2_ERR_INVALID_ARG;
+        prefetch_a = best_pa != 0;
+    }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t rows = (int64_t)batch * slots;
     float *g = static_cast<float *>(workspace);
@@ -360,19 +538,54 @@ extern "C" dflash2_status dflash2_selector_walk(
     wp.path_scores = path_scores;
     wp.err = err_word;
     if (di.device >= 0 && di.device < 64 && !g_walk_attr[di.device]) {
-        if (cudaFuncSetAttribute(walk_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kWalkMaxSmem) != cudaSuccess ||
-            cudaFuncSetAttribute(walk_kernel<__nv_bfloat16>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kWalkMaxSmem) != cudaSuccess) {
+        const int bytes = (int)kWalkSmemBytes;
+        cudaError_t e = cudaSuccess;
+#define DFLASH2_WALK_ATTR(T_, PA_, E_)                                                          \
+    if (e == cudaSuccess)                                                                      \
+        e = cudaFuncSetAttribute(walk_kernel<T_, PA_, E_>,                                     \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
+        DFLASH2_WALK_ATTR(__nv_bfloat16, true, 1); DFLASH2_WALK_ATTR(__nv_bfloat16, true, 2);
+        DFLASH2_WALK_ATTR(__nv_bfloat16, true, 4); DFLASH2_WALK_ATTR(__nv_bfloat16, false, 1);
+        DFLASH2_WALK_ATTR(__nv_bfloat16, false, 2); DFLASH2_WALK_ATTR(__nv_bfloat16, false, 4);
+        DFLASH2_WALK_ATTR(float, true, 1); DFLASH2_WALK_ATTR(float, true, 2);
+        DFLASH2_WALK_ATTR(float, true, 4); DFLASH2_WALK_ATTR(float, false, 1);
+        DFLASH2_WALK_ATTR(float, false, 2); DFLASH2_WALK_ATTR(float, false, 4);
+#undef DFLASH2_WALK_ATTR
+        if (e != cudaSuccess) {
             cudaGetLastError();
             return DFLASH2_ERR_CUDA;
         }
         g_walk_attr[di.device] = true;
     }
-    if (dtype == DFLASH2_BF16)
-        walk_kernel<__nv_bfloat16><<<(unsigned)batch, kWalkThreads, smem, st>>>(wp);
-    else
-        walk_kernel<float><<<(unsigned)batch, kWalkThreads, smem, st>>>(wp);
+    wp.batch = batch;
+    wp.bulk_ids = ((int64_t)slots * top_k) % 4 == 0 && aligned16(cand_ids) && aligned16(cand_u);
+    const unsigned grid = (unsigned)((batch + warps - 1) / warps);
+    const size_t smem = L.total * warps;
+    const int threads = 32 * warps;
+#define DFLASH2_WALK_LAUNCH(T_, PA_, E_) \
+    walk_kernel<T_, PA_, E_><<<grid, threads, smem, st>>>(wp, warps, L)
+    const int E = top_k <= 32 ? 1 : (top_k <= 64 ? 2 : 4);
+    if (dtype == DFLASH2_BF16) {
+        if (prefetch_a) {
+            if (E == 1) DFLASH2_WALK_LAUNCH(__nv_bfloat16, true, 1);
+            else if (E == 2) DFLASH2_WALK_LAUNCH(__nv_bfloat16, true, 2);
+            else DFLASH2_WALK_LAUNCH(__nv_bfloat16, true, 4);
+        } else {
+            if (E == 1) DFLASH2_WALK_LAUNCH(__nv_bfloat16, false, 1);
+            else if (E == 2) DFLASH2_WALK_LAUNCH(__nv_bfloat16, false, 2);
+            else DFLASH2_WALK_LAUNCH(__nv_bfloat16, false, 4);
+        }
+    } else {
+        if (prefetch_a) {
+            if (E == 1) DFLASH2_WALK_LAUNCH(float, true, 1);
+            else if (E == 2) DFLASH2_WALK_LAUNCH(float, true, 2);
+            else DFLASH2_WALK_LAUNCH(float, true, 4);
+        } else {
+            if (E == 1) DFLASH2_WALK_LAUNCH(float, false, 1);
+            else if (E == 2) DFLASH2_WALK_LAUNCH(float, false, 2);
+            else DFLASH2_WALK_LAUNCH(float, false, 4);
+        }
+    }
+#undef DFLASH2_WALK_LAUNCH
     return launch_status();
 }
