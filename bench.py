@@ -48,6 +48,22 @@ def _dist():
     return rank, world, local
 
 
+def reduce_max_over_ranks(values, device="cpu"):
+    """Element-wise maximum of a list of floats over all ranks of the default
+    process group (the step time of a job is its slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_value(world: int, rows_per_rank: int, ms: float) -> float:
+    """Proposals per second of the whole job: every rank proposes rows_per_rank
+    rows per step (weak scaling) and the step takes the slowest rank's time."""
+    return world * rows_per_rank / (ms * 1e-3)
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -128,8 +144,9 @@ class ClockSampler:
 
 
 def _profile_traffic(kernel_sources):
-    """DRAM bytes per launch of the filter GEMM from the committed ncu summary,
-    or None when the kernel sources changed since the capture."""
+    """DRAM bytes (read + write) of one unary_topk stage (its four launches)
+    from the committed ncu summary, or None when the kernel sources changed
+    since the capture."""
     import hashlib
     try:
         text = open(PROFILE_SUMMARY).read()
@@ -151,7 +168,7 @@ def _profile_traffic(kernel_sources):
 def kernel_source_hash():
     import hashlib
     srcs = [os.path.join(ROOT, "block_draft_proposal_gb300", "csrc", f)
-            for f in ("gemm_tc.cu", "common.cuh", "kernels.h")]
+            for f in ("gemm_tc.cu", "topk.cu", "common.cuh", "kernels.h")]
     h = hashlib.sha256()
     for path in srcs:
         with open(path, "rb") as f:
@@ -359,10 +376,7 @@ def run_gpu(args, w):
 
     # max over ranks
     if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms, e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms, e2e = float(tt[0]), float(tt[1])
+        ms, e2e = reduce_max_over_ranks([ms, e2e], device=dev)
 
     launches_per_step = 1 + 4 + 2 + 1
     if w.dtype == "f32":
@@ -402,7 +416,7 @@ def run_gpu(args, w):
                "sample": f"{n_req} requests ({n_req * w.slots} proposal rows) of {w.name}: the "
                          f"whole oracle chain, {tc:.1f} s"}
 
-    value = world * w.rows / (ms * 1e-3)
+    value = job_value(world, w.rows, ms)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -415,7 +429,7 @@ def run_gpu(args, w):
                      "peak_kind": f"{peak_kind} bf16 burst"},
         "stages": stages,
         "cpu_baseline": cpu,
-        "e2e": {"value": world * w.rows / (e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_value(world, w.rows, e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps * 2,  # graph phase + eager phase
         "clocks": clocks.summary(),

@@ -14,8 +14,8 @@ on (sizes in the docstring of :data:`CONFIGS`).  Weights are N(0, 0.02); the
 conv input x is N(0, 0.02) for the tiny fp32 case and N(0, 1) for the bf16
 cases; the proposal hidden states h are N(0, 1).  Sampling uses the even
 batch rows as greedy rows and the odd rows as sampled rows for the "mixed"
-workloads.  Synthetic draws stand in for the GSM8K runs the pages quote:
-no dataset item is used.
+workloads.  Synthetic draws stand in for the GSM8K runs that the DFlash2 PR
+quotes for acceptance and speed-up: no dataset item is used.
 """
 from __future__ import annotations
 

@@ -134,8 +134,9 @@ int oracle_conv(const void *x, const void *base, const void *delta,
 /* ---- (2)+(3) unary logits ------------------------------------------------
  * z[m, v] = sum_j h[m, j] * lm_head[v, j]   (lm_head in nn.Linear layout)
  * u = cap * tanh(mult * z / cap) when cap > 0, else mult * z
- *   (output_multiplier / final_logit_softcapping of the DFlash2 draft config;
- *   the pages name the two fields, the formula is the stated reading)
+ *   (output_multiplier / final_logit_softcapping of DFlashDraftConfig in the
+ *   DFlash2 PR, which names the two fields but prints no formula; this is
+ *   the soft-capping reading used throughout)
  * u = -inf for padded vocab rows v >= target_vocab: the vLLM DSpark
  *   padded-vocab review asks that [target_vocab, draft_vocab) be masked
  *   before any top-k.
