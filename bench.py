@@ -316,32 +316,35 @@ def run_gpu(args, w):
 
     # timed region: K graph replays (the value), then K eager steps with stage
     # events (the per-stage breakdown and the roofline); L2 flushed before each
-    stage_ms = {k: [] for k in ("conv", "unary_topk", "walk", "d2t", "step")}
-    graph_ms = []
+    # step, outside the events.  Events are read after one final synchronize.
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         with torch.cuda.stream(stream):
-            for _ in range(args.steps):
+            for i in range(args.steps):
                 flush.zero_()
-                g0.record(stream)
+                gev[i][0].record(stream)
                 graph.replay() if use_graph else step(False)
-                g1.record(stream)
-                stream.synchronize()
-                graph_ms.append(g0.elapsed_time(g1))
-            for _ in range(args.steps):
+                gev[i][1].record(stream)
+            for i in range(args.steps):
                 flush.zero_()
+                ev[:] = sev[i]
                 step(True)
-                stream.synchronize()
-                stage_ms["conv"].append(ev[0].elapsed_time(ev[1]))
-                stage_ms["unary_topk"].append(ev[1].elapsed_time(ev[2]))
-                stage_ms["walk"].append(ev[2].elapsed_time(ev[3]))
-                stage_ms["d2t"].append(ev[3].elapsed_time(ev[4]))
-                stage_ms["step"].append(ev[0].elapsed_time(ev[4]))
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
+    graph_ms = [a.elapsed_time(b) for a, b in gev]
+    stage_ms = {
+        "conv": [e[0].elapsed_time(e[1]) for e in sev],
+        "unary_topk": [e[1].elapsed_time(e[2]) for e in sev],
+        "walk": [e[2].elapsed_time(e[3]) for e in sev],
+        "d2t": [e[3].elapsed_time(e[4]) for e in sev],
+        "step": [e[0].elapsed_time(e[4]) for e in sev],
+    }
     ms = statistics.mean(graph_ms)
     eager_ms = statistics.mean(stage_ms["step"])
     err = int(bufs.err.item())
@@ -446,8 +449,8 @@ def run_gpu(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")

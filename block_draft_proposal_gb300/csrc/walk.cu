@@ -101,6 +101,18 @@ template <> __device__ __forceinline__ float ld1<__nv_bfloat16>(const __nv_bfloa
     return __bfloat162float(*p);
 }
 
+// 16-byte asynchronous copy global -> shared; invalid sources are zero-filled.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool valid) {
+    const uint32_t n = valid ? 16u : 0u;  // 0 source bytes: the 16 bytes are zero-filled
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)),
+                 "l"(gmem), "r"(n)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // 1-D TMA bulk copy global -> this CTA's shared memory, completing on `bar`.
 // Both addresses 16-byte aligned, size a multiple of 16.
 __device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
@@ -369,6 +381,230 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Lattice mode (top_k <= 32): one CTA per request.  Slot s's possible
+// predecessors are exactly slot s-1's candidates (the anchor at slot 0), so
+// every slot's K x K edges and the draw from every lattice row can be formed
+// in parallel before the walk; the walk itself is then a chase through the
+// per-row choices.  Each (slot, predecessor) row is reduced by one thread in
+// candidate order, as the sequential sums of the walk's definition.
+// ---------------------------------------------------------------------------
+constexpr int kLatThreads = 256;
+
+struct LatLayout {
+    int a_stride;   // bytes per staged A row (rank * esz + 16)
+    int b_stride;   // bytes per staged B row (rank * esz + 16)
+    int b_slot;     // bytes per slot of B rows (k * b_stride + 16)
+    size_t ids, cu, uni, gs, brow, arow, lat, stat, nxt, path, scratch_bytes, total;
+};
+
+__host__ __device__ inline LatLayout lat_layout(int slots, int k, int rank, int esz, int k_splits) {
+    LatLayout L;
+    L.a_stride = rank * esz + 16;
+    L.b_stride = rank * esz + 16;
+    L.b_slot = k * L.b_stride + 16;
+    L.ids = 0;
+    L.cu = L.ids + pad16((size_t)slots * k * 8);
+    L.uni = L.cu + pad16((size_t)slots * k * 4);
+    L.gs = L.uni + pad16((size_t)slots * 4);
+    L.brow = L.gs + pad16((size_t)slots * rank * 4);
+    L.arow = L.brow + (size_t)slots * L.b_slot;
+    L.lat = L.arow + pad16((size_t)(1 + (slots - 1) * k) * L.a_stride);
+    L.stat = L.lat + pad16((size_t)slots * k * k * 4);
+    L.nxt = L.stat + pad16((size_t)slots * k * 8);
+    L.path = L.nxt + pad16((size_t)slots * k * 4);
+    L.total = L.path + pad16((size_t)slots * 4);
+    L.scratch_bytes = 0;
+    (void)k_splits;
+    return L;
+}
+
+// Row staged for predecessor kp of slot s: the anchor (row 0) at slot 0,
+// else slot s-1's candidate kp.
+__device__ __forceinline__ int lat_arow(int s, int kp, int K) { return s == 0 ? 0 : 1 + (s - 1) * K + kp; }
+
+template <typename T, int KM>
+__global__ void __launch_bounds__(kLatThreads) walk_lattice_kernel(const WalkParams p, LatLayout L) {
+    extern __shared__ __align__(16) uint8_t dyn[];
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int S = p.slots, K = p.k, R = p.rank;
+    int64_t *ids = reinterpret_cast<int64_t *>(dyn + L.ids);
+    float *cu = reinterpret_cast<float *>(dyn + L.cu);
+    float *uni = reinterpret_cast<float *>(dyn + L.uni);
+    float *gs = reinterpret_cast<float *>(dyn + L.gs);
+    uint8_t *brow = dyn + L.brow;
+    uint8_t *arow = dyn + L.arow;
+    float *lat = reinterpret_cast<float *>(dyn + L.lat);
+    float2 *stat = reinterpret_cast<float2 *>(dyn + L.stat);   // (max of e/T, sum of exp) per row
+    int32_t *nxt = reinterpret_cast<int32_t *>(dyn + L.nxt);
+    int32_t *path = reinterpret_cast<int32_t *>(dyn + L.path);
+    const int64_t row0 = (int64_t)b * S;
+    const T *A = static_cast<const T *>(p.A);
+    const T *B = static_cast<const T *>(p.B);
+
+    // ---- prologue
+    bool bad = false;
+    for (int t = tid; t < S * K; t += kLatThreads) {
+        const int64_t c = p.cand[row0 * K + t];
+        bad |= !id_ok(c, p.table_rows);
+        ids[t] = c;
+        cu[t] = p.cand_u[row0 * K + t];
+    }
+    for (int t = tid; t < S; t += kLatThreads) uni[t] = p.uniforms[row0 + t];
+    {
+        const float4 *g4 = reinterpret_cast<const float4 *>(p.g + row0 * R);
+        const int64_t stride4 = p.split_stride / 4;
+        float4 *gs4 = reinterpret_cast<float4 *>(gs);
+        for (int t = tid; t < S * R / 4; t += kLatThreads) {
+            float4 acc = g4[t];
+            for (int ks = 1; ks < p.k_splits; ++ks) {
+                const float4 v = g4[ks * stride4 + t];
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            gs4[t] = acc;
+        }
+    }
+    const int64_t anchor = p.anchors[b];
+    bad |= !id_ok(anchor, p.table_rows);
+    if (__syncthreads_or(bad) && tid == 0 && p.err) atomicOr(p.err, DFLASH2_DEVERR_ID_RANGE);
+
+    // ---- gather the rows of the whole request (16-byte copies, zero rows for bad ids)
+    const int chunks = R * (int)sizeof(T) / 16;
+    const int n_b = S * K, n_a = 1 + (S - 1) * K;
+    for (int t = tid; t < (n_b + n_a) * chunks; t += kLatThreads) {
+        const int r = t / chunks;
+        const int ch = t - r * chunks;
+        if (r < n_b) {
+            const int s = r / K, kk = r - s * K;
+            const int64_t c = ids[r];
+            const bool ok = id_ok(c, p.table_rows);
+            cp_async16(brow + (size_t)s * L.b_slot + (size_t)kk * L.b_stride + ch * 16,
+                       reinterpret_cast<const uint8_t *>(ok ? B + c * R : B) + ch * 16, ok);
+        } else {
+            const int ar = r - n_b;
+            const int64_t c = ar == 0 ? anchor : ids[ar - 1];  // row 1 + (s-1)K + kp = ids[(s-1)K + kp]
+            const bool ok = id_ok(c, p.table_rows);
+            cp_async16(arow + (size_t)ar * L.a_stride + ch * 16,
+                       reinterpret_cast<const uint8_t *>(ok ? A + c * R : A) + ch * 16, ok);
+        }
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // ---- every lattice row: K edges, then the row's draw
+    const bool greedy = p.greedy[b] != 0;
+    float temp = p.temps[b];
+    if (!(temp >= 1e-5f)) temp = 1e-5f;
+    constexpr int VN = 16 / sizeof(T);
+    const int n_rows = 1 + (S - 1) * K;  // slot 0 has the anchor row only
+    for (int pr = tid; pr < n_rows; pr += kLatThreads) {
+        const int s = pr == 0 ? 0 : 1 + (pr - 1) / K;
+        const int kp = pr == 0 ? 0 : (pr - 1) - (s - 1) * K;
+        const uint8_t *ar = arow + (size_t)lat_arow(s, kp, K) * L.a_stride;
+        const uint8_t *bs = brow + (size_t)s * L.b_slot;
+        const float *gsl = gs + (size_t)s * R;
+        float acc[KM];
+#pragma unroll
+        for (int kk = 0; kk < KM; ++kk) acc[kk] = 0.0f;
+        for (int v = 0; v < R / VN; ++v) {
+            float av[VN], w[VN];
+            unpack16<T>(*reinterpret_cast<const uint4 *>(ar + v * 16), av);
+#pragma unroll
+            for (int e = 0; e < VN; ++e) w[e] = av[e] * gsl[v * VN + e];
+#pragma unroll
+            for (int kk = 0; kk < KM; ++kk) {
+                if (kk < K) {
+                    float bv[VN];
+                    unpack16<T>(*reinterpret_cast<const uint4 *>(bs + (size_t)kk * L.b_stride + v * 16), bv);
+#pragma unroll
+                    for (int e = 0; e < VN; ++e) acc[kk] = fmaf(w[e], bv[e], acc[kk]);
+                }
+            }
+        }
+        float *lrow = lat + ((size_t)s * K + kp) * K;
+        int index = 0;
+        if (greedy) {
+            float best = 0.0f;
+#pragma unroll
+            for (int kk = 0; kk < KM; ++kk) {
+                if (kk < K) {
+                    const float e = acc[kk] + cu[s * K + kk];
+                    lrow[kk] = e;
+                    if (kk == 0 || e > best) {
+                        best = e;
+                        index = kk;
+                    }
+                }
+            }
+        } else {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int kk = 0; kk < KM; ++kk) {
+                if (kk < K) {
+                    const float e = acc[kk] + cu[s * K + kk];
+                    lrow[kk] = e;
+                    acc[kk] = e / temp;
+                    mx = fmaxf(mx, acc[kk]);
+                }
+            }
+            float total = 0.0f;
+#pragma unroll
+            for (int kk = 0; kk < KM; ++kk) {
+                if (kk < K) {
+                    acc[kk] = expf(acc[kk] - mx);
+                    total += acc[kk];
+                }
+            }
+            const float u = uni[s];
+            float cdf = 0.0f;
+            int count = 0;
+#pragma unroll
+            for (int kk = 0; kk < KM; ++kk) {
+                if (kk < K) {
+                    cdf += acc[kk] / total;
+                    count += (u >= cdf) ? 1 : 0;
+                }
+            }
+            index = count < K - 1 ? count : K - 1;
+            stat[(size_t)s * K + kp] = make_float2(mx, total);
+        }
+        nxt[(size_t)s * K + kp] = index;
+    }
+    __syncthreads();
+
+    // ---- the walk: follow the chosen index slot by slot
+    if (tid == 0) {
+        int prev = 0;
+        for (int s = 0; s < S; ++s) {
+            prev = nxt[(size_t)s * K + prev];
+            path[s] = prev;
+        }
+    }
+    __syncthreads();
+
+    // ---- outputs of the walked path
+    for (int t = tid; t < S * K; t += kLatThreads) {
+        const int s = t / K, kk = t - s * K;
+        const int kp = s == 0 ? 0 : path[s - 1];
+        const float e = lat[((size_t)s * K + kp) * K + kk];
+        float qv;
+        if (greedy) {
+            qv = kk == path[s] ? 1.0f : 0.0f;
+        } else {
+            const float2 st = stat[(size_t)s * K + kp];
+            qv = expf(e / temp - st.x) / st.y;
+        }
+        p.q[(row0 + s) * K + kk] = qv;
+        if (p.path_scores) p.path_scores[(row0 + s) * K + kk] = e;
+    }
+    for (int s = tid; s < S; s += kLatThreads) p.tokens[row0 + s] = ids[(size_t)s * K + path[s]];
+}
+
 // fp32 projection on CUDA cores: one CTA per row, one warp per output column.
 __global__ void __launch_bounds__(128)
     project_f32_kernel(const float *__restrict__ h, const float *__restrict__ proj, int hidden,
@@ -449,6 +685,10 @@ extern "C" dflash2_status dflash2_selector_walk(
         const int per = (num_kb + ksplits - 1) / ksplits;
         ksplits = (num_kb + per - 1) / per;  // the count the GEMM launcher keeps
     }
+    // Lattice mode: every slot's K x K edges and draws in parallel, one CTA
+    // per request, when the request's rows and lattice fit in shared memory.
+    const LatLayout LL = lat_layout(slots, top_k, rank, esz, ksplits);
+    const bool lattice = top_k <= 32 && LL.total <= kWalkSmemBytes;
     // One warp per request.  Among the shared-memory layouts that fit, take
     // the fewest waves of CTAs, then A-row prefetch, then the deepest
     // prefetch ring (every slot in flight at most).
@@ -477,9 +717,9 @@ extern "C" dflash2_status dflash2_selector_walk(
                 }
             }
         }
-        if (best_pa < 0) return DFLASH2_ERR_INVALID_ARG;  // one request's state exceeds shared memory
+        if (best_pa < 0 && !lattice) return DFLASH2_ERR_INVALID_ARG;  // one request's state exceeds shared memory
         // one mbarrier phase counts fewer than 2^20 transaction bytes
-        if ((int64_t)ksplits * slots * rank * 4 + (int64_t)slots * top_k * 12 >= (1 << 20))
+        if (!lattice && (int64_t)ksplits * slots * rank * 4 + (int64_t)slots * top_k * 12 >= (1 << 20))
             return DFLASH2_ERR_INVALID_ARG;
         prefetch_a = best_pa != 0;
     }
@@ -551,6 +791,14 @@ extern "C" dflash2_status dflash2_selector_walk(
         DFLASH2_WALK_ATTR(float, true, 4); DFLASH2_WALK_ATTR(float, false, 1);
         DFLASH2_WALK_ATTR(float, false, 2); DFLASH2_WALK_ATTR(float, false, 4);
 #undef DFLASH2_WALK_ATTR
+#define DFLASH2_LAT_ATTR(T_, KM_)                                                               \
+    if (e == cudaSuccess)                                                                      \
+        e = cudaFuncSetAttribute(walk_lattice_kernel<T_, KM_>,                                 \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
+        DFLASH2_LAT_ATTR(__nv_bfloat16, 8); DFLASH2_LAT_ATTR(__nv_bfloat16, 16);
+        DFLASH2_LAT_ATTR(__nv_bfloat16, 32); DFLASH2_LAT_ATTR(float, 8);
+        DFLASH2_LAT_ATTR(float, 16); DFLASH2_LAT_ATTR(float, 32);
+#undef DFLASH2_LAT_ATTR
         if (e != cudaSuccess) {
             cudaGetLastError();
             return DFLASH2_ERR_CUDA;
@@ -558,6 +806,22 @@ extern "C" dflash2_status dflash2_selector_walk(
         g_walk_attr[di.device] = true;
     }
     wp.batch = batch;
+    if (lattice) {
+        const int km = top_k <= 8 ? 8 : (top_k <= 16 ? 16 : 32);
+#define DFLASH2_LAT_LAUNCH(T_, KM_) \
+    walk_lattice_kernel<T_, KM_><<<(unsigned)batch, kLatThreads, LL.total, st>>>(wp, LL)
+        if (dtype == DFLASH2_BF16) {
+            if (km == 8) DFLASH2_LAT_LAUNCH(__nv_bfloat16, 8);
+            else if (km == 16) DFLASH2_LAT_LAUNCH(__nv_bfloat16, 16);
+            else DFLASH2_LAT_LAUNCH(__nv_bfloat16, 32);
+        } else {
+            if (km == 8) DFLASH2_LAT_LAUNCH(float, 8);
+            else if (km == 16) DFLASH2_LAT_LAUNCH(float, 16);
+            else DFLASH2_LAT_LAUNCH(float, 32);
+        }
+#undef DFLASH2_LAT_LAUNCH
+        return launch_status();
+    }
     wp.bulk_ids = ((int64_t)slots * top_k) % 4 == 0 && aligned16(cand_ids) && aligned16(cand_u);
     const unsigned grid = (unsigned)((batch + warps - 1) / warps);
     const size_t smem = L.total * warps;
