@@ -75,7 +75,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams &p, const float 
         }
     } else if (p.mode == kGemmPilot) {
         const bool valid = v < p.rows_w && v < p.target_vocab;
-        float *o = p.out + (int64_t)it.j * kGemmTileW + row_in_tile;
+        float *o = p.out + (int64_t)it.j * p.unit + row_in_tile;  // row_in_tile: offset in the unit
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const int m = m0 + i;
@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(192, 1)
             }
             if (!mbar_wait(&acc_full[a], ((uint32_t)t >> 1) & 1u, &abort_flag, p.err)) break;
             tc_fence_after();
-            const int64_t v = (int64_t)item.wt * kGemmTileW + row_in_tile;
+            const int64_t v = (int64_t)item.wt * p.unit + row_in_tile;
             const uint32_t tbase = tmem + (uint32_t)a * p.acc_cols + ((uint32_t)(quarter * 32) << 16);
             int nbuf = 0;
             for (int c0 = 0; c0 < p.bn; c0 += 32) {
@@ -326,20 +326,204 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// CTA-pair variant (pilot and filter modes): the two CTAs of a cluster run
+// one M = 256 MMA (tcgen05.mma.cta_group::2) over a 256-row weight unit.  Each
+// CTA stages its 128 weight rows and half of the token tile, so the shared-
+// memory traffic per SM for the token operand halves and more stages fit.
+// The leader (rank 0) issues the MMAs; both CTAs' TMA loads complete on the
+// leader's full barrier; the commits multicast to both CTAs' empty and
+// accumulator-full barriers; both CTAs' epilogues (each reading its own 128
+// TMEM lanes) arrive on the leader's accumulator-empty barrier.
+// ---------------------------------------------------------------------------
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+    gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_w,
+                        const __grid_constant__ CUtensorMap tm_h, const GemmParams p) {
+    extern __shared__ uint8_t dsmem[];
+    __shared__ uint64_t full_bar[kGemmMaxStages];
+    __shared__ uint64_t empty_bar[kGemmMaxStages];
+    __shared__ uint64_t acc_full[2];
+    __shared__ uint64_t acc_empty[2];
+    __shared__ uint64_t drain_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int half_bn = p.bn / 2;
+    const uint32_t h_bytes = (uint32_t)half_bn * kGemmTileK * 2;  // this CTA's half of the token tile
+    uint8_t *w_smem = smem;
+    uint8_t *h_smem = smem + (size_t)p.stages * kWTileBytes;
+    EpiScratch *epi = reinterpret_cast<EpiScratch *>(h_smem + (size_t)p.stages * h_bytes);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const uint32_t tmem_cols = 2 * p.acc_cols;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], 8);  // 4 epilogue warps in each CTA of the pair
+        }
+        mbar_init(&drain_bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc_pair(&tmem_slot, tmem_cols);
+        tmem_relinquish_pair();
+    }
+    if (warp == 1 && lane == 0) {
+        prefetch_tmap(&tm_w);
+        prefetch_tmap(&tm_h);
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the peer's barriers exist before anyone signals them
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const int total = p.pass_tiles * p.n_tok_tiles;
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int w = pair; w < total && ok; w += npairs) {
+                const Item item = decode(p, w);
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                    const int s = (int)(it % (uint32_t)p.stages);
+                    const uint32_t par = ((it / (uint32_t)p.stages) & 1u) ^ 1u;
+                    if (!mbar_wait(&empty_bar[s], par, &abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = mapa_shared(smem_u32(&full_bar[s]), 0);
+                    if (leader) mbar_arrive_expect_tx(&full_bar[s], 2 * (kWTileBytes + h_bytes));
+                    tma_load_2d_pair(w_smem + (size_t)s * kWTileBytes, &tm_w, fb, kb * kGemmTileK,
+                                     item.wt * p.unit + (int)rank * kGemmTileW);
+                    tma_load_2d_pair(h_smem + (size_t)s * h_bytes, &tm_h, fb, kb * kGemmTileK,
+                                     item.nt * p.bn + (int)rank * half_bn);
+                }
+            }
+            // the leader waits until the last loads of both CTAs have landed
+            if (leader) {
+                const uint32_t st = (uint32_t)p.stages;
+                for (uint32_t n = it > st ? it - st : 0; n < it; ++n)
+                    mbar_wait_drain(&full_bar[n % st], (n / st) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            const uint32_t idesc = idesc_bf16(2 * kGemmTileW, p.bn);
+            uint32_t it = 0;
+            int t = 0;
+            bool ok = true;
+            for (int w = pair; w < total; w += npairs, ++t) {
+                const int a = t & 1;
+                if (!mbar_wait(&acc_empty[a], (((uint32_t)t >> 1) & 1u) ^ 1u, &abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)a * p.acc_cols;
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                    const int s = (int)(it % (uint32_t)p.stages);
+                    if (!mbar_wait(&full_bar[s], (it / (uint32_t)p.stages) & 1u, &abort_flag,
+                                   p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t wa = smem_u32(w_smem + (size_t)s * kWTileBytes);
+                    const uint32_t ha = smem_u32(h_smem + (size_t)s * h_bytes);
+#pragma unroll
+                    for (int kk = 0; kk < kGemmTileK / 16; ++kk)
+                        tc_mma_bf16_pair(d_tmem, sw128_desc(wa + kk * 32), sw128_desc(ha + kk * 32),
+                                         idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit_pair_mc(&empty_bar[s], 0x3);
+                }
+                if (!ok) break;
+                tc_commit_pair_mc(&acc_full[a], 0x3);
+            }
+            if (!ok) {
+                tc_commit_pair(&drain_bar);
+                mbar_wait_drain(&drain_bar, 0);
+            }
+        }
+    } else {
+        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const int row_in_unit = (int)rank * kGemmTileW + quarter * 32 + lane;
+        EpiScratch &es = epi[warp - 2];
+        const uint32_t acc_empty_leader[2] = {mapa_shared(smem_u32(&acc_empty[0]), 0),
+                                              mapa_shared(smem_u32(&acc_empty[1]), 0)};
+        int t = 0;
+        for (int w = pair; w < total; w += npairs, ++t) {
+            const Item item = decode(p, w);
+            const int a = t & 1;
+            const int m_tile = item.nt * p.bn;
+            if (p.mode == kGemmFilter) {
+                for (int c = lane; c < 256; c += 32) {
+                    const int m = m_tile + c;
+                    const bool ok = c < p.bn && m < p.rows_h;
+                    es.pre[c] = ok ? p.theta_pre[m] : INFINITY;
+                    es.th[c] = ok ? p.theta[m] : ~0ull;
+                }
+                __syncwarp();
+            }
+            if (!mbar_wait(&acc_full[a], ((uint32_t)t >> 1) & 1u, &abort_flag, p.err)) break;
+            tc_fence_after();
+            const int64_t v = (int64_t)item.wt * p.unit + row_in_unit;
+            const uint32_t tbase = tmem + (uint32_t)a * p.acc_cols + ((uint32_t)(quarter * 32) << 16);
+            int nbuf = 0;
+            for (int c0 = 0; c0 < p.bn; c0 += 32) {
+                float z[32];
+                tmem_ld32_wait(tbase + (uint32_t)c0, z);
+                if (p.mode == kGemmFilter)
+                    filter_chunk(p, z, v, m_tile + c0, c0, tbase + (uint32_t)c0, es, nbuf, lane);
+                else
+                    epilogue_chunk(p, z, v, row_in_unit, m_tile + c0, min(32, p.bn - c0), item, lane);
+            }
+            tc_fence_before();
+            if (p.mode == kGemmFilter && nbuf > 0) flush_survivors(p, es, nbuf, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_empty_leader[a]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // no CTA leaves while its peer may still touch its shared memory
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, tmem_cols);
+    }
+}
+
 int g_smem_set[64];
 
 }  // namespace
 
 dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h, GemmParams p,
-                              cudaStream_t st) {
+                              cudaStream_t st, bool pair) {
     if (p.bn < 16 || p.bn > 256 || p.bn % 16 != 0 || p.k_splits < 1) return DFLASH2_ERR_INVALID_ARG;
     if (p.rows_h <= 0 || p.rows_w <= 0 || p.hidden <= 0) return DFLASH2_OK;
+    if (p.mode == kGemmStore) pair = false;  // the projection keeps one CTA per tile
+    if (pair && di.sm_count < 2) pair = false;
+    p.unit = pair ? 2 * kGemmTileW : kGemmTileW;
     p.n_tok_tiles = (p.rows_h + p.bn - 1) / p.bn;
     p.num_kb = (p.hidden + kGemmTileK - 1) / kGemmTileK;
     p.kb_per_split = (p.num_kb + p.k_splits - 1) / p.k_splits;
     p.k_splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;  // every split gets >= 1 block
-    p.n_wtiles = (p.rows_w + kGemmTileW - 1) / kGemmTileW;
-    pilot_layout(p.n_wtiles, &p.n_pilot, &p.pilot_stride);
+    p.n_wtiles = (p.rows_w + p.unit - 1) / p.unit;
+    pilot_layout(p.n_wtiles, &p.n_pilot, &p.pilot_stride, p.unit);
     if (p.mode == kGemmPilot)
         p.pass_tiles = p.n_pilot;
     else if (p.mode == kGemmFilter)
@@ -351,7 +535,8 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     uint32_t acc = 32;
     while (acc < (uint32_t)p.bn) acc <<= 1;
     p.acc_cols = acc;
-    const uint32_t stage_bytes = kWTileBytes + (uint32_t)p.bn * kGemmTileK * 2;
+    const uint32_t h_rows = pair ? (uint32_t)p.bn / 2 : (uint32_t)p.bn;
+    const uint32_t stage_bytes = kWTileBytes + h_rows * kGemmTileK * 2;
     const size_t epi_bytes = p.mode == kGemmFilter ? 4 * sizeof(EpiScratch) : 0;
     int stages = (int)((kGemmSmemBytes - 1024 - epi_bytes) / stage_bytes);
     if (stages > kGemmMaxStages) stages = kGemmMaxStages;
@@ -361,11 +546,13 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     CUtensorMap tm_w, tm_h;
     dflash2_status s = encode_tmap_bf16(&tm_w, w, (uint64_t)p.rows_w, (uint64_t)p.hidden, kGemmTileW);
     if (s != DFLASH2_OK) return s;
-    s = encode_tmap_bf16(&tm_h, h, (uint64_t)p.rows_h, (uint64_t)p.hidden, (uint32_t)p.bn);
+    s = encode_tmap_bf16(&tm_h, h, (uint64_t)p.rows_h, (uint64_t)p.hidden, h_rows);
     if (s != DFLASH2_OK) return s;
 
     if (di.device >= 0 && di.device < 64 && !g_smem_set[di.device]) {
         if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kGemmSmemBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(gemm_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kGemmSmemBytes) != cudaSuccess) {
             cudaGetLastError();
             return DFLASH2_ERR_CUDA;
@@ -373,8 +560,14 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
         g_smem_set[di.device] = 1;
     }
     const int64_t total = (int64_t)p.pass_tiles * p.n_tok_tiles * p.k_splits;
-    const int grid = (int)(total < di.sm_count ? total : di.sm_count);
-    gemm_tc_kernel<<<grid, 192, smem, st>>>(tm_w, tm_h, p);
+    if (pair) {
+        const int64_t pairs_max = di.sm_count / 2;
+        const int pairs = (int)(total < pairs_max ? total : pairs_max);
+        gemm_tc_pair_kernel<<<2 * pairs, 192, smem, st>>>(tm_w, tm_h, p);
+    } else {
+        const int grid = (int)(total < di.sm_count ? total : di.sm_count);
+        gemm_tc_kernel<<<grid, 192, smem, st>>>(tm_w, tm_h, p);
+    }
     return launch_status();
 }
 

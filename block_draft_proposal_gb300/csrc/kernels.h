@@ -36,6 +36,7 @@ struct GemmParams {
     int32_t n_pilot;
     int32_t pilot_stride;
     int32_t pass_tiles;
+    int32_t unit;     // weight rows per work unit: 128 (one CTA) or 256 (a CTA pair)
     int32_t stages;
     uint32_t acc_cols;
     // epilogue
@@ -53,16 +54,18 @@ struct GemmParams {
     int32_t *err;
 };
 
-// Pilot tiling of a weight matrix with n_wtiles tiles: n_pilot tiles spaced
-// pilot_stride apart, starting at tile 0.
-inline void pilot_layout(int64_t n_wtiles, int32_t *n_pilot, int32_t *stride) {
-    int64_t np = n_wtiles < kPilotTiles ? n_wtiles : kPilotTiles;
+// Pilot tiling of a weight matrix with n_wtiles units of unit_rows rows:
+// n_pilot units (4096 rows at most) spaced pilot_stride apart, from unit 0.
+inline void pilot_layout(int64_t n_wtiles, int32_t *n_pilot, int32_t *stride, int unit_rows = 128) {
+    const int64_t max_units = (int64_t)kPilotTiles * kGemmTileW / unit_rows;
+    int64_t np = n_wtiles < max_units ? n_wtiles : max_units;
     if (np < 1) np = 1;
     *n_pilot = (int32_t)np;
     *stride = (int32_t)(n_wtiles / np);
 }
 
+// pair: run the pilot / filter modes on CTA pairs (2-CTA MMA, 256-row units).
 dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h, GemmParams p,
-                              cudaStream_t st);
+                              cudaStream_t st, bool pair = false);
 
 }  // namespace dflash2

@@ -241,18 +241,18 @@ __global__ void __launch_bounds__(kSelThreads)
 // filter may skip the transform wherever fl(mult * z) < theta_pre.  With no
 // threshold, mult <= 0 or u_th <= 0, theta_pre is -inf (every entry checked).
 __global__ void __launch_bounds__(kSelThreads)
-    pilot_select_kernel(const float *__restrict__ pilot_u, int n_pilot, int pilot_stride, int k,
-                        float mult, uint64_t *theta, float *theta_pre, uint32_t *cnt,
+    pilot_select_kernel(const float *__restrict__ pilot_u, int n_pilot, int pilot_stride, int unit,
+                        int k, float mult, uint64_t *theta, float *theta_pre, uint32_t *cnt,
                         uint64_t *cand, int cand_cap) {
     __shared__ SelectShared sh;
     extern __shared__ __align__(16) uint8_t dyn[];
     uint64_t *keys = reinterpret_cast<uint64_t *>(dyn);
     const int64_t row = blockIdx.x;
-    const int n = n_pilot * kGemmTileW;
+    const int n = n_pilot * unit;
     const float *pu = pilot_u + row * n;
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
         const float u = pu[i];
-        const uint32_t v = (uint32_t)((i / kGemmTileW) * pilot_stride * kGemmTileW + (i % kGemmTileW));
+        const uint32_t v = (uint32_t)((i / unit) * pilot_stride * unit + (i % unit));
         keys[i] = (u == -INFINITY) ? 0ull : make_key(u, v);
     }
     __syncthreads();
@@ -311,15 +311,22 @@ struct TopkLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// The pilot and filter passes run on CTA pairs (2-CTA MMA over 256-row
+// weight units) when the token side spans at least 8 tiles; with fewer token
+// tiles one CTA per 128-row unit is faster.  Depends on the shape only.
+inline bool use_pairs(int64_t rows) { return (rows + 255) / 256 >= 8; }
+inline int unit_rows(int64_t rows) { return use_pairs(rows) ? 2 * kGemmTileW : kGemmTileW; }
+
 inline TopkLayout topk_layout(int64_t rows, int64_t draft_vocab) {
     TopkLayout L{};
-    L.n_wtiles = (int32_t)((draft_vocab + kGemmTileW - 1) / kGemmTileW);
-    pilot_layout(L.n_wtiles, &L.n_pilot, &L.pilot_stride);
+    const int unit = unit_rows(rows);
+    L.n_wtiles = (int32_t)((draft_vocab + unit - 1) / unit);
+    pilot_layout(L.n_wtiles, &L.n_pilot, &L.pilot_stride, unit);
     L.theta_off = 0;
     L.pre_off = align256(L.theta_off + (size_t)rows * 8);
     L.cnt_off = align256(L.pre_off + (size_t)rows * 4);
     L.pilot_off = align256(L.cnt_off + (size_t)rows * 4);
-    L.cand_off = align256(L.pilot_off + (size_t)rows * L.n_pilot * kGemmTileW * 4);
+    L.cand_off = align256(L.pilot_off + (size_t)rows * L.n_pilot * unit * 4);
     L.fixed_bytes = L.cand_off;
     return L;
 }
@@ -440,23 +447,26 @@ extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head,
 
     // The pilot covers at most 32 weight tiles: smaller token tiles spread
     // its work items over the SMs.
+    const bool pairs = use_pairs(rows);
+    const int unit = unit_rows(rows);
     p.mode = kGemmPilot;
     p.out = pilot_u;
-    p.ldo = (int64_t)L.n_pilot * kGemmTileW;
+    p.ldo = (int64_t)L.n_pilot * unit;
     {
-        int64_t want_tiles = di.sm_count / L.n_pilot;  // one wave of work items
+        int64_t want_tiles = (pairs ? di.sm_count / 2 : di.sm_count) / L.n_pilot;  // one wave
         if (want_tiles < 1) want_tiles = 1;
         int64_t per = (rows + want_tiles - 1) / want_tiles;
         per = (per + 15) / 16 * 16;
         p.bn = (int)(per < 16 ? 16 : (per > bn ? bn : per));
     }
-    s = launch_gemm_tc(di, lm_head, h, p, st);
+    s = launch_gemm_tc(di, lm_head, h, p, st, pairs);
     if (s != DFLASH2_OK) return s;
     p.bn = bn;
 
-    const size_t pilot_smem = (size_t)L.n_pilot * kGemmTileW * 8;
+    const size_t pilot_smem = (size_t)L.n_pilot * unit * 8;
     pilot_select_kernel<<<(unsigned)rows, kSelThreads, pilot_smem, st>>>(
-        pilot_u, L.n_pilot, L.pilot_stride, top_k, mult, theta, theta_pre, cnt, cand, (int)cap_keys);
+        pilot_u, L.n_pilot, L.pilot_stride, unit, top_k, mult, theta, theta_pre, cnt, cand,
+        (int)cap_keys);
     s = launch_status();
     if (s != DFLASH2_OK) return s;
 
@@ -467,7 +477,7 @@ extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head,
     p.cnt = cnt;
     p.cand = cand;
     p.cand_cap = (int32_t)cap_keys;
-    s = launch_gemm_tc(di, lm_head, h, p, st);
+    s = launch_gemm_tc(di, lm_head, h, p, st, pairs);
     if (s != DFLASH2_OK) return s;
 
     size_t fin_smem = (size_t)(cap_keys < kSmemKeys ? cap_keys : kSmemKeys) * 8;
