@@ -74,13 +74,13 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams &p, const float 
             }
         }
     } else if (p.mode == kGemmPilot) {
+        // raw logits; the pilot select applies the transform (-inf = padded / out of range)
         const bool valid = v < p.rows_w && v < p.target_vocab;
         float *o = p.out + (int64_t)it.j * p.unit + row_in_tile;  // row_in_tile: offset in the unit
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const int m = m0 + i;
-            if (i < ncols && m < p.rows_h)
-                o[(int64_t)m * p.ldo] = valid ? unary_transform(z[i], p.mult, p.cap) : -INFINITY;
+            if (i < ncols && m < p.rows_h) o[(int64_t)m * p.ldo] = valid ? z[i] : -INFINITY;
         }
     }
 }

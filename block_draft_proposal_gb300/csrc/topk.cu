@@ -3,9 +3,10 @@
 // _radix_topk; vLLM DSpark padded-vocab review: mask [target_vocab, draft_vocab)).
 //
 // bf16 pipeline (four launches, no full logit matrix in HBM):
-//   1. pilot GEMM: u for 32 weight tiles spread over the vocab (<= 4096 rows)
-//      is written to the workspace;
-//   2. pilot select: per row, the K-th best (u, id) key of the pilot is a
+//   1. pilot GEMM: the raw logits of weight units spread over the vocab
+//      (4096 rows at most) are written to the workspace;
+//   2. pilot select: per row, the pilot's keys are formed with the same
+//      transform as the filter epilogue; the K-th best (u, id) key is a
 //      lower bound of the row's true K-th best key (it is the K-th best of a
 //      subset), so it is a safe threshold; the pilot's own top K keys seed the
 //      row's candidate list;
@@ -241,19 +242,21 @@ __global__ void __launch_bounds__(kSelThreads)
 // filter may skip the transform wherever fl(mult * z) < theta_pre.  With no
 // threshold, mult <= 0 or u_th <= 0, theta_pre is -inf (every entry checked).
 __global__ void __launch_bounds__(kSelThreads)
-    pilot_select_kernel(const float *__restrict__ pilot_u, int n_pilot, int pilot_stride, int unit,
-                        int k, float mult, uint64_t *theta, float *theta_pre, uint32_t *cnt,
-                        uint64_t *cand, int cand_cap) {
+    pilot_select_kernel(const float *__restrict__ pilot_z, int n_pilot, int pilot_stride, int unit,
+                        int k, float mult, float cap, uint64_t *theta, float *theta_pre,
+                        uint32_t *cnt, uint64_t *cand, int cand_cap) {
     __shared__ SelectShared sh;
     extern __shared__ __align__(16) uint8_t dyn[];
     uint64_t *keys = reinterpret_cast<uint64_t *>(dyn);
     const int64_t row = blockIdx.x;
     const int n = n_pilot * unit;
-    const float *pu = pilot_u + row * n;
+    const float *pz = pilot_z + row * n;
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const float u = pu[i];
+        const float z = pz[i];
         const uint32_t v = (uint32_t)((i / unit) * pilot_stride * unit + (i % unit));
-        keys[i] = (u == -INFINITY) ? 0ull : make_key(u, v);
+        // the same transform the filter epilogue applies, so theta is the exact
+        // key of a real entry
+        keys[i] = (z == -INFINITY) ? 0ull : make_key(unary_transform(z, mult, cap), v);
     }
     __syncthreads();
     const uint64_t kth = block_kth_largest(keys, n, k, sh);
@@ -465,7 +468,7 @@ extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head,
 
     const size_t pilot_smem = (size_t)L.n_pilot * unit * 8;
     pilot_select_kernel<<<(unsigned)rows, kSelThreads, pilot_smem, st>>>(
-        pilot_u, L.n_pilot, L.pilot_stride, unit, top_k, mult, theta, theta_pre, cnt, cand,
+        pilot_u, L.n_pilot, L.pilot_stride, unit, top_k, mult, cap, theta, theta_pre, cnt, cand,
         (int)cap_keys);
     s = launch_status();
     if (s != DFLASH2_OK) return s;
