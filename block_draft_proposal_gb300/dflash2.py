@@ -36,8 +36,9 @@ EXPORTS = (
     "dflash2_status_string", "dflash2_abi_version", "dflash2_grouped_conv",
     "dflash2_unary_topk_workspace_size", "dflash2_unary_topk_workspace_min",
     "dflash2_unary_topk", "dflash2_selector_walk_workspace_size", "dflash2_selector_walk",
-    "dflash2_d2t_remap",
+    "dflash2_d2t_remap", "dflash2_selector_walk_noalloc",
 )
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class Dflash2Error(RuntimeError):
@@ -80,6 +81,9 @@ def library():
         lib.dflash2_selector_walk.restype = i32
         lib.dflash2_d2t_remap.argtypes = [P, P, i64, i64, i64, P, P, P]
         lib.dflash2_d2t_remap.restype = i32
+        lib.dflash2_selector_walk_noalloc.argtypes = [P, P, P, P, i64, P, P, P, P, P, P, i32, i32,
+                                                      i32, i32, i32, i32, P, P, P, P, P]
+        lib.dflash2_selector_walk_noalloc.restype = i32
         if lib.dflash2_abi_version() != ABI_VERSION:
             raise RuntimeError("libdflash2.so ABI version mismatch; rebuild it")
         _lib = lib
@@ -218,6 +222,39 @@ def selector_walk(h, proj, A, B, anchor_ids, cand_ids, cand_u, temperatures, gre
         _ptr(cand_u), _ptr(temperatures), _ptr(greedy), _ptr(uniforms), batch, slots, hidden,
         rank, top_k, code, _ptr(tokens), _ptr(q), _ptr(path_scores), _ptr(workspace),
         workspace.numel(), _ptr(err), _stream(stream)))
+    return tokens, q, path_scores, err
+
+
+def selector_walk_noalloc(h, proj, A, B, anchor_ids, cand_ids, cand_u, temperatures, greedy,
+                          uniforms, tokens=None, q=None, path_scores=None, err=None,
+                          with_path_scores: bool = False, stream=None):
+    """dflash2_selector_walk_noalloc: the selector walk with the library's own
+    fixed 4 MiB scratch instead of a workspace, for callers that cannot hand
+    over device memory at call time.  Calls that overlap on the GPU share that
+    scratch and race; shapes needing more scratch raise Dflash2Error."""
+    batch, slots, top_k = cand_ids.shape
+    for t, nm in ((h, "h"), (proj, "proj"), (A, "A"), (B, "B")):
+        _need(t, nm, h.dtype)
+    _need(anchor_ids, "anchor_ids", torch.int64, (batch,))
+    _need(cand_ids, "cand_ids", torch.int64)
+    _need(cand_u, "cand_u", torch.float32, (batch, slots, top_k))
+    _need(temperatures, "temperatures", torch.float32, (batch,))
+    _need(greedy, "greedy", torch.uint8, (batch,))
+    _need(uniforms, "uniforms", torch.float32, (batch, slots))
+    dev = h.device
+    if tokens is None:
+        tokens = torch.empty((batch, slots), dtype=torch.int64, device=dev)
+    if q is None:
+        q = torch.empty((batch, slots, top_k), dtype=torch.float32, device=dev)
+    if path_scores is None and with_path_scores:
+        path_scores = torch.empty((batch, slots, top_k), dtype=torch.float32, device=dev)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check("dflash2_selector_walk_noalloc", library().dflash2_selector_walk_noalloc(
+        _ptr(h), _ptr(proj), _ptr(A), _ptr(B), A.shape[0], _ptr(anchor_ids), _ptr(cand_ids),
+        _ptr(cand_u), _ptr(temperatures), _ptr(greedy), _ptr(uniforms), batch, slots,
+        h.shape[-1], proj.shape[0], top_k, _dtype_code(h), _ptr(tokens), _ptr(q),
+        _ptr(path_scores), _ptr(err), _stream(stream)))
     return tokens, q, path_scores, err
 
 

@@ -177,6 +177,38 @@ dflash2_status dflash2_selector_walk(const void *h, const void *proj, const void
                                      void *stream);
 
 /*
+ * Selector walk without a workspace argument.  The paper has no counterpart:
+ * this is a library convenience for callers that cannot provide device
+ * memory at call time, such as serving loops whose device memory belongs to
+ * another allocator (a caching allocator that reserved its pool up front and
+ * must not be bypassed), or latency-critical paths that must never call
+ * cudaMalloc / cudaFree, which can synchronise the whole device.
+ *
+ * Same arguments, meaning and result as dflash2_selector_walk, minus
+ * workspace and ws_bytes.  It allocates nothing: its scratch is a fixed
+ * 4 MiB (4194304-byte) array in the library's device memory, held by every
+ * GPU that loads the library until the process exits.
+ *   - A call whose scratch need (dflash2_selector_walk_workspace_size of its
+ *     shapes) exceeds 4 MiB returns DFLASH2_ERR_WORKSPACE and queues nothing.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call, on every stream, shares the one array and overwrites what
+ *     the previous call left there (nothing in it needs to start at zero).
+ *     Calls whose work overlaps on the GPU, on different streams or from
+ *     different threads, race on it: serialise them.
+ */
+dflash2_status dflash2_selector_walk_noalloc(const void *h, const void *proj, const void *A,
+                                             const void *B, int64_t table_rows,
+                                             const int64_t *anchor_ids, const int64_t *cand_ids,
+                                             const float *cand_u, const float *temperatures,
+                                             const uint8_t *greedy, const float *uniforms,
+                                             int32_t batch, int32_t slots, int32_t hidden,
+                                             int32_t rank, int32_t top_k, int32_t dtype,
+                                             int64_t *tokens, float *q, float *path_scores,
+                                             int32_t *err_word, void *stream);
+
+/*
  * Draft-to-target id remap.
  * vLLM Qwen3DSparkForCausalLM.map_draft_to_target: d2t holds offsets, so
  *   target_ids[i] = draft_ids[i] + d2t[draft_ids[i]];
