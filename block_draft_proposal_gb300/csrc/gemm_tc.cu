@@ -16,6 +16,13 @@
 // accumulators alternate so the epilogue of one tile overlaps the MMAs of
 // the next.  Every wait is bounded (common.cuh).
 //
+// A stage holds 128 hidden elements of both operands, as two 64-element
+// boxes (one 128-byte swizzle row each), so one wait and one commit cover 8
+// MMAs.  The issuing thread is the limit at these tile sizes: an MMA costs
+// it tens of cycles to issue, and each wait / fence / commit round a few
+// hundred, against 120 tensor cycles per MMA at N = 240.  Its loop therefore
+// keeps precomputed descriptors and an incremental stage / phase counter.
+//
 // Work items are ordered with the token tile fastest, so the CTAs that run
 // at the same time share weight tiles in L2 and the weight matrix streams
 // from HBM about once.
@@ -24,7 +31,8 @@
 namespace dflash2 {
 namespace {
 
-constexpr uint32_t kWTileBytes = kGemmTileW * kGemmTileK * 2;  // 16 KiB
+constexpr uint32_t kWTileBytes = kGemmTileW * kGemmTileK * 2;  // one weight box: 16 KiB
+constexpr uint32_t kWStageBytes = 2 * kWTileBytes;              // weight rows of one stage
 constexpr size_t kGemmSmemBytes = 220 * 1024;                   // dynamic shared memory cap
 
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
@@ -33,6 +41,41 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) 
         if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
     return true;
+}
+
+// The 8 MMAs (K = 16 each) of one stage.  wd / hd are the descriptors of the
+// stage's first weight / token box; +2 advances 32 bytes (16 elements) inside
+// the 128-byte swizzled row, +wsub / +hsub moves to the second box (all in the
+// descriptor's 16-byte address units).
+template <bool PAIR>
+__device__ __forceinline__ void mma_stage(uint32_t d, uint64_t wd, uint64_t hd, uint32_t wsub,
+                                          uint32_t hsub, uint32_t idesc, uint32_t acc0) {
+    if (PAIR) {
+        tc_mma_bf16_pair(d, wd, hd, idesc, acc0);
+        tc_mma_bf16_pair(d, wd + 2, hd + 2, idesc, 1u);
+        tc_mma_bf16_pair(d, wd + 4, hd + 4, idesc, 1u);
+        tc_mma_bf16_pair(d, wd + 6, hd + 6, idesc, 1u);
+        tc_mma_bf16_pair(d, wd + wsub, hd + hsub, idesc, 1u);
+        tc_mma_bf16_pair(d, wd + wsub + 2, hd + hsub + 2, idesc, 1u);
+        tc_mma_bf16_pair(d, wd + wsub + 4, hd + hsub + 4, idesc, 1u);
+        tc_mma_bf16_pair(d, wd + wsub + 6, hd + hsub + 6, idesc, 1u);
+    } else {
+        tc_mma_bf16(d, wd, hd, idesc, acc0);
+        tc_mma_bf16(d, wd + 2, hd + 2, idesc, 1u);
+        tc_mma_bf16(d, wd + 4, hd + 4, idesc, 1u);
+        tc_mma_bf16(d, wd + 6, hd + 6, idesc, 1u);
+        tc_mma_bf16(d, wd + wsub, hd + hsub, idesc, 1u);
+        tc_mma_bf16(d, wd + wsub + 2, hd + hsub + 2, idesc, 1u);
+        tc_mma_bf16(d, wd + wsub + 4, hd + hsub + 4, idesc, 1u);
+        tc_mma_bf16(d, wd + wsub + 6, hd + hsub + 6, idesc, 1u);
+    }
+}
+
+// Waits (bounded) until the last `stages` loads this producer issued have
+// landed, so no copy is still writing shared memory when the CTA leaves.
+__device__ __forceinline__ void drain_loads(uint64_t *full_bar, uint32_t issued, uint32_t stages) {
+    for (uint32_t n = issued > stages ? issued - stages : 0; n < issued; ++n)
+        mbar_wait_drain(&full_bar[n % stages], (n / stages) & 1u);
 }
 
 // Which weight tile the j-th tile of this launch's pass is.
@@ -174,10 +217,11 @@ __global__ void __launch_bounds__(192, 1)
 
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t h_bytes = (uint32_t)p.bn * kGemmTileK * 2;
+    const uint32_t h_sub = (uint32_t)p.bn * kGemmTileK * 2;  // one token box
+    const uint32_t h_stage = 2 * h_sub;
     uint8_t *w_smem = smem;
-    uint8_t *h_smem = smem + (size_t)p.stages * kWTileBytes;
-    EpiScratch *epi = reinterpret_cast<EpiScratch *>(h_smem + (size_t)p.stages * h_bytes);
+    uint8_t *h_smem = smem + (size_t)p.stages * kWStageBytes;
+    EpiScratch *epi = reinterpret_cast<EpiScratch *>(h_smem + (size_t)p.stages * h_stage);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -212,35 +256,43 @@ __global__ void __launch_bounds__(192, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            uint32_t it = 0;
+            uint32_t issued = 0, s = 0, ph = 1;  // the first pass finds every stage free
             bool ok = true;
             for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
                 const Item item = decode(p, w);
                 const int kb0 = item.ks * p.kb_per_split;
                 const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
-                for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                    const int s = (int)(it % (uint32_t)p.stages);
-                    const uint32_t par = ((it / (uint32_t)p.stages) & 1u) ^ 1u;
-                    if (!mbar_wait(&empty_bar[s], par, &abort_flag, p.err)) {
+                const int wrow = item.wt * kGemmTileW, hrow = item.nt * p.bn;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(&empty_bar[s], ph, &abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full_bar[s], kWTileBytes + h_bytes);
-                    tma_load_2d(w_smem + (size_t)s * kWTileBytes, &tm_w, &full_bar[s],
-                                kb * kGemmTileK, item.wt * kGemmTileW);
-                    tma_load_2d(h_smem + (size_t)s * h_bytes, &tm_h, &full_bar[s],
-                                kb * kGemmTileK, item.nt * p.bn);
+                    uint8_t *ws = w_smem + s * kWStageBytes;
+                    uint8_t *hs = h_smem + s * h_stage;
+                    const int k0 = kb * kGemmStageK;  // boxes past `hidden` read zeros
+                    mbar_arrive_expect_tx(&full_bar[s], kWStageBytes + h_stage);
+                    tma_load_2d(ws, &tm_w, &full_bar[s], k0, wrow);
+                    tma_load_2d(ws + kWTileBytes, &tm_w, &full_bar[s], k0 + kGemmTileK, wrow);
+                    tma_load_2d(hs, &tm_h, &full_bar[s], k0, hrow);
+                    tma_load_2d(hs + h_sub, &tm_h, &full_bar[s], k0 + kGemmTileK, hrow);
+                    ++issued;
+                    if (++s == (uint32_t)p.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
             // Never leave the CTA with copies still landing in its shared memory.
-            const uint32_t st = (uint32_t)p.stages;
-            for (uint32_t n = it > st ? it - st : 0; n < it; ++n)
-                mbar_wait_drain(&full_bar[n % st], (n / st) & 1u);
+            drain_loads(full_bar, issued, (uint32_t)p.stages);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16(kGemmTileW, p.bn);
-            uint32_t it = 0;
+            const uint64_t wd0 = sw128_desc(smem_u32(w_smem)), hd0 = sw128_desc(smem_u32(h_smem));
+            const uint32_t w_st = kWStageBytes >> 4, h_st = h_stage >> 4;  // descriptor units
+            const uint32_t w_sub = kWTileBytes >> 4, h_sb = h_sub >> 4;
+            uint32_t s = 0, ph = 0;
             int t = 0;
             bool ok = true;
             for (int w = blockIdx.x; w < total; w += gridDim.x, ++t) {
@@ -254,21 +306,19 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)a * p.acc_cols;
-                for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                    const int s = (int)(it % (uint32_t)p.stages);
-                    if (!mbar_wait(&full_bar[s], (it / (uint32_t)p.stages) & 1u, &abort_flag,
-                                   p.err)) {
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(&full_bar[s], ph, &abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t wa = smem_u32(w_smem + (size_t)s * kWTileBytes);
-                    const uint32_t ha = smem_u32(h_smem + (size_t)s * h_bytes);
-#pragma unroll
-                    for (int kk = 0; kk < kGemmTileK / 16; ++kk)
-                        tc_mma_bf16(d_tmem, sw128_desc(wa + kk * 32), sw128_desc(ha + kk * 32),
-                                    idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                    mma_stage<false>(d_tmem, wd0 + s * w_st, hd0 + s * h_st, w_sub, h_sb, idesc,
+                                     kb > kb0 ? 1u : 0u);
                     tc_commit(&empty_bar[s]);
+                    if (++s == (uint32_t)p.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
                 if (!ok) break;
                 tc_commit(&acc_full[a]);
@@ -352,10 +402,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~static_cast<uintptr_t>(1023));
     const int half_bn = p.bn / 2;
-    const uint32_t h_bytes = (uint32_t)half_bn * kGemmTileK * 2;  // this CTA's half of the token tile
+    const uint32_t h_sub = (uint32_t)half_bn * kGemmTileK * 2;  // one box of this CTA's half of the tokens
+    const uint32_t h_stage = 2 * h_sub;
     uint8_t *w_smem = smem;
-    uint8_t *h_smem = smem + (size_t)p.stages * kWTileBytes;
-    EpiScratch *epi = reinterpret_cast<EpiScratch *>(h_smem + (size_t)p.stages * h_bytes);
+    uint8_t *h_smem = smem + (size_t)p.stages * kWStageBytes;
+    EpiScratch *epi = reinterpret_cast<EpiScratch *>(h_smem + (size_t)p.stages * h_stage);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -394,36 +445,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            uint32_t it = 0;
+            uint32_t issued = 0, s = 0, ph = 1;  // the first pass finds every stage free
             bool ok = true;
             for (int w = pair; w < total && ok; w += npairs) {
                 const Item item = decode(p, w);
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                    const int s = (int)(it % (uint32_t)p.stages);
-                    const uint32_t par = ((it / (uint32_t)p.stages) & 1u) ^ 1u;
-                    if (!mbar_wait(&empty_bar[s], par, &abort_flag, p.err)) {
+                const int wrow = item.wt * p.unit + (int)rank * kGemmTileW;
+                const int hrow = item.nt * p.bn + (int)rank * half_bn;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait(&empty_bar[s], ph, &abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = mapa_shared(smem_u32(&full_bar[s]), 0);
-                    if (leader) mbar_arrive_expect_tx(&full_bar[s], 2 * (kWTileBytes + h_bytes));
-                    tma_load_2d_pair(w_smem + (size_t)s * kWTileBytes, &tm_w, fb, kb * kGemmTileK,
-                                     item.wt * p.unit + (int)rank * kGemmTileW);
-                    tma_load_2d_pair(h_smem + (size_t)s * h_bytes, &tm_h, fb, kb * kGemmTileK,
-                                     item.nt * p.bn + (int)rank * half_bn);
+                    if (leader) mbar_arrive_expect_tx(&full_bar[s], 2 * (kWStageBytes + h_stage));
+                    uint8_t *ws = w_smem + s * kWStageBytes;
+                    uint8_t *hs = h_smem + s * h_stage;
+                    const int k0 = kb * kGemmStageK;  // boxes past `hidden` read zeros
+                    tma_load_2d_pair(ws, &tm_w, fb, k0, wrow);
+                    tma_load_2d_pair(ws + kWTileBytes, &tm_w, fb, k0 + kGemmTileK, wrow);
+                    tma_load_2d_pair(hs, &tm_h, fb, k0, hrow);
+                    tma_load_2d_pair(hs + h_sub, &tm_h, fb, k0 + kGemmTileK, hrow);
+                    ++issued;
+                    if (++s == (uint32_t)p.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
             // the leader waits until the last loads of both CTAs have landed
-            if (leader) {
-                const uint32_t st = (uint32_t)p.stages;
-                for (uint32_t n = it > st ? it - st : 0; n < it; ++n)
-                    mbar_wait_drain(&full_bar[n % st], (n / st) & 1u);
-            }
+            if (leader) drain_loads(full_bar, issued, (uint32_t)p.stages);
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             const uint32_t idesc = idesc_bf16(2 * kGemmTileW, p.bn);
-            uint32_t it = 0;
+            const uint64_t wd0 = sw128_desc(smem_u32(w_smem)), hd0 = sw128_desc(smem_u32(h_smem));
+            const uint32_t w_st = kWStageBytes >> 4, h_st = h_stage >> 4;  // descriptor units
+            const uint32_t w_sub = kWTileBytes >> 4, h_sb = h_sub >> 4;
+            uint32_t s = 0, ph = 0;
             int t = 0;
             bool ok = true;
             for (int w = pair; w < total; w += npairs, ++t) {
@@ -434,21 +492,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)a * p.acc_cols;
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-                    const int s = (int)(it % (uint32_t)p.stages);
-                    if (!mbar_wait(&full_bar[s], (it / (uint32_t)p.stages) & 1u, &abort_flag,
-                                   p.err)) {
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait(&full_bar[s], ph, &abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t wa = smem_u32(w_smem + (size_t)s * kWTileBytes);
-                    const uint32_t ha = smem_u32(h_smem + (size_t)s * h_bytes);
-#pragma unroll
-                    for (int kk = 0; kk < kGemmTileK / 16; ++kk)
-                        tc_mma_bf16_pair(d_tmem, sw128_desc(wa + kk * 32), sw128_desc(ha + kk * 32),
-                                         idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                    mma_stage<true>(d_tmem, wd0 + s * w_st, hd0 + s * h_st, w_sub, h_sb, idesc,
+                                    kb > 0 ? 1u : 0u);
                     tc_commit_pair_mc(&empty_bar[s], 0x3);
+                    if (++s == (uint32_t)p.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
                 if (!ok) break;
                 tc_commit_pair_mc(&acc_full[a], 0x3);
@@ -516,10 +572,10 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     if (p.bn < 16 || p.bn > 256 || p.bn % 16 != 0 || p.k_splits < 1) return DFLASH2_ERR_INVALID_ARG;
     if (p.rows_h <= 0 || p.rows_w <= 0 || p.hidden <= 0) return DFLASH2_OK;
     if (p.mode == kGemmStore) pair = false;  // the projection keeps one CTA per tile
-    if (pair && di.sm_count < 2) pair = false;
+    if (pair && di.sm_count < 2) return DFLASH2_ERR_UNSUPPORTED_DEVICE;  // the caller's layout assumes pairs
     p.unit = pair ? 2 * kGemmTileW : kGemmTileW;
     p.n_tok_tiles = (p.rows_h + p.bn - 1) / p.bn;
-    p.num_kb = (p.hidden + kGemmTileK - 1) / kGemmTileK;
+    p.num_kb = (p.hidden + kGemmStageK - 1) / kGemmStageK;
     p.kb_per_split = (p.num_kb + p.k_splits - 1) / p.k_splits;
     p.k_splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;  // every split gets >= 1 block
     p.n_wtiles = (p.rows_w + p.unit - 1) / p.unit;
@@ -536,10 +592,11 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     while (acc < (uint32_t)p.bn) acc <<= 1;
     p.acc_cols = acc;
     const uint32_t h_rows = pair ? (uint32_t)p.bn / 2 : (uint32_t)p.bn;
-    const uint32_t stage_bytes = kWTileBytes + h_rows * kGemmTileK * 2;
+    const uint32_t stage_bytes = kWStageBytes + h_rows * kGemmStageK * 2;
     const size_t epi_bytes = p.mode == kGemmFilter ? 4 * sizeof(EpiScratch) : 0;
     int stages = (int)((kGemmSmemBytes - 1024 - epi_bytes) / stage_bytes);
     if (stages > kGemmMaxStages) stages = kGemmMaxStages;
+    if (stages < 2) return DFLASH2_ERR_INVALID_ARG;  // bn <= 256 always leaves room for two
     p.stages = stages;
     const size_t smem = (size_t)stages * stage_bytes + epi_bytes + 1024;
 

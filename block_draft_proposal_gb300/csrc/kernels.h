@@ -16,7 +16,8 @@ enum GemmMode : int32_t {
 };
 
 constexpr int kGemmTileW = 128;  // weight rows per tile (MMA M)
-constexpr int kGemmTileK = 64;   // hidden elements per pipeline stage (one 128-byte swizzle row)
+constexpr int kGemmTileK = 64;   // hidden elements per TMA box (one 128-byte swizzle row)
+constexpr int kGemmStageK = 128; // hidden elements per pipeline stage (two boxes per operand)
 constexpr int kGemmMaxStages = 8;
 constexpr int kPilotTiles = 32;  // pilot weight tiles sampled across the vocab
 
@@ -30,7 +31,7 @@ struct GemmParams {
     int32_t bn;       // token tile, multiple of 16 in [16, 256]
     int32_t k_splits; // store mode: number of hidden splits (>= 1)
     int32_t n_tok_tiles;
-    int32_t num_kb;
+    int32_t num_kb;       // pipeline stages (kGemmStageK hidden elements each) over hidden
     int32_t kb_per_split;
     int32_t n_wtiles;
     int32_t n_pilot;

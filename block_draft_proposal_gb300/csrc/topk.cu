@@ -315,14 +315,14 @@ struct TopkLayout {
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // The pilot and filter passes run on CTA pairs (2-CTA MMA over 256-row
-// weight units) when the token side spans at least 8 tiles; with fewer token
-// tiles one CTA per 128-row unit is faster.  Depends on the shape only.
-inline bool use_pairs(int64_t rows) { return (rows + 255) / 256 >= 8; }
-inline int unit_rows(int64_t rows) { return use_pairs(rows) ? 2 * kGemmTileW : kGemmTileW; }
+// weight units): each CTA of a pair stages only half of the token tile, so a
+// stage of 128 hidden elements is small enough for three stages in shared
+// memory, where one CTA per 128-row unit fits two.
+inline int unit_rows() { return 2 * kGemmTileW; }
 
 inline TopkLayout topk_layout(int64_t rows, int64_t draft_vocab) {
     TopkLayout L{};
-    const int unit = unit_rows(rows);
+    const int unit = unit_rows();
     L.n_wtiles = (int32_t)((draft_vocab + unit - 1) / unit);
     pilot_layout(L.n_wtiles, &L.n_pilot, &L.pilot_stride, unit);
     L.theta_off = 0;
@@ -450,8 +450,8 @@ extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head,
 
     // The pilot covers at most 32 weight tiles: smaller token tiles spread
     // its work items over the SMs.
-    const bool pairs = use_pairs(rows);
-    const int unit = unit_rows(rows);
+    const bool pairs = true;
+    const int unit = unit_rows();
     p.mode = kGemmPilot;
     p.out = pilot_u;
     p.ldo = (int64_t)L.n_pilot * unit;

@@ -628,7 +628,7 @@ __global__ void __launch_bounds__(128)
 inline void proj_tiling(int64_t rows, int hidden, int *bn, int *k_splits) {
     *bn = rows >= 4096 ? 64 : 16;
     const int64_t tiles = (rows + *bn - 1) / *bn;
-    const int num_kb = (hidden + kGemmTileK - 1) / kGemmTileK;
+    const int num_kb = (hidden + kGemmStageK - 1) / kGemmStageK;
     int64_t ks = (148 + tiles - 1) / tiles;
     if (ks > num_kb) ks = num_kb;
     if (ks > 8) ks = 8;
@@ -681,7 +681,7 @@ extern "C" dflash2_status dflash2_selector_walk(
     if (dtype == DFLASH2_BF16) {
         int bn_unused;
         proj_tiling((int64_t)batch * slots, hidden, &bn_unused, &ksplits);
-        const int num_kb = (hidden + kGemmTileK - 1) / kGemmTileK;
+        const int num_kb = (hidden + kGemmStageK - 1) / kGemmStageK;
         const int per = (num_kb + ksplits - 1) / ksplits;
         ksplits = (num_kb + per - 1) / per;  // the count the GEMM launcher keeps
     }
@@ -746,7 +746,7 @@ extern "C" dflash2_status dflash2_selector_walk(
         p.split_stride = rows * rank;
         p.err = err_word;
         // the launcher may trim k_splits; recompute the count it will use
-        const int num_kb = (hidden + kGemmTileK - 1) / kGemmTileK;
+        const int num_kb = (hidden + kGemmStageK - 1) / kGemmStageK;
         const int per = (num_kb + ks - 1) / ks;
         wp.k_splits = (num_kb + per - 1) / per;
         s = launch_gemm_tc(di, proj, h, p, st);

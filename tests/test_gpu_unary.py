@@ -54,10 +54,10 @@ SMALL = [
     (300, 264, 40000, 39990, 32, 1.0, 0.0, "bf16"),    # filter pass active, two token tiles
     (7, 512, 70000, 70000, 64, 1.0, 30.0, "bf16"),
     (513, 128, 9000, 8800, 8, 2.0, 0.0, "bf16"),       # three token tiles
-    (5, 96, 3000, 2999, 128, 1.0, 0.0, "bf16"),        # K at its maximum
+    (5, 96, 3000, 2999, 128, 1.0, 0.0, "bf16"),        # K at its maximum; hidden below one stage
     (9, 136, 1100, 1000, 16, 1.0, 10.0, "f32"),
-    (2100, 128, 9000, 8990, 24, 1.0, 30.0, "bf16"),   # >= 8 token tiles: CTA-pair (2-CTA MMA) path
-    (1800, 136, 4000, 4000, 8, 0.7, 0.0, "bf16"),     # pair path, pilot covers the vocab
+    (2100, 128, 9000, 8990, 24, 1.0, 30.0, "bf16"),   # nine token tiles over the CTA pairs
+    (1800, 136, 4000, 4000, 8, 0.7, 0.0, "bf16"),     # the pilot covers the whole vocab
 ]
 
 
