@@ -69,6 +69,11 @@ def _load():
             lib.oracle_walk.restype = None
             lib.oracle_d2t.argtypes = [P, P, i64, i64, i64, P]
             lib.oracle_d2t.restype = i64
+            u64 = ctypes.c_uint64
+            lib.oracle_philox4x64.argtypes = [P, P, P]
+            lib.oracle_philox4x64.restype = None
+            lib.oracle_philox_uniforms.argtypes = [u64, u64, i64, P]
+            lib.oracle_philox_uniforms.restype = None
             _lib = lib
     return _lib
 
@@ -210,3 +215,23 @@ def selector(h, proj, A, B, anchors, cand, cand_u, uniforms, temperatures, greed
     scores, errors = lattice(g, A, B, anchors, cand, cand_u)
     tokens, q, chosen = walk(scores, cand, uniforms, temperatures, greedy)
     return dict(g=g, scores=scores, errors=errors, tokens=tokens, q=q, chosen=chosen)
+
+
+def philox4x64(counter, key) -> np.ndarray:
+    """One Philox4x64-10 block: 4 counter words, 2 key words -> 4 uint64 words."""
+    c = np.ascontiguousarray(counter, dtype=np.uint64)
+    k = np.ascontiguousarray(key, dtype=np.uint64)
+    if c.shape != (4,) or k.shape != (2,):
+        raise ValueError("counter has 4 words, key 2")
+    out = np.zeros(4, dtype=np.uint64)
+    _load().oracle_philox4x64(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def philox_uniforms(seed: int, base: int, n: int) -> np.ndarray:
+    """n float32 uniforms in [0, 1): word i % 4 of the block at counter base + i // 4."""
+    out = np.zeros(int(n), dtype=np.float32)
+    if n:
+        _load().oracle_philox_uniforms(int(seed) & (2**64 - 1), int(base) & (2**64 - 1), int(n),
+                                       _ptr(out))
+    return out

@@ -391,3 +391,52 @@ int64_t oracle_d2t(const int64_t *draft_ids, const int64_t *d2t, int64_t n,
     }
     return errors;
 }
+
+/* ---- (9) counter-based uniforms --------------------------------------------
+ * The sglang DFlash2 sampler (_SelectorDraftSampler) draws the walk's
+ * uniforms inside the captured graph from a Philox generator whose state
+ * advances at every replay.  The generator here is Philox4x64 with 10 rounds
+ * as defined by Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
+ * easy as 1, 2, 3" (SC 2011): a 4-word counter and a 2-word key; a round
+ * multiplies words 0 and 2 by two fixed odd constants, the new words are
+ * (hi(M1*c2) ^ c1 ^ k0, lo(M1*c2), hi(M0*c0) ^ c3 ^ k1, lo(M0*c0)), and the
+ * key then advances by two fixed Weyl increments.
+ *
+ * Uniform i is word (i mod 4) of the block at counter (base + i / 4, 0, 0, 0)
+ * under key (seed, 0), mapped to [0, 1) as (word >> 40) * 2^-24 (exact in
+ * fp32).
+ */
+void oracle_philox4x64(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4])
+{
+    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+    uint64_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint64_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        unsigned __int128 p0 = (unsigned __int128)M0 * c0;
+        unsigned __int128 p1 = (unsigned __int128)M1 * c2;
+        uint64_t hi0 = (uint64_t)(p0 >> 64), lo0 = (uint64_t)p0;
+        uint64_t hi1 = (uint64_t)(p1 >> 64), lo1 = (uint64_t)p1;
+        c0 = hi1 ^ c1 ^ k0;
+        c1 = lo1;
+        c2 = hi0 ^ c3 ^ k1;
+        c3 = lo0;
+        k0 += W0;
+        k1 += W1;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+void oracle_philox_uniforms(uint64_t seed, uint64_t base, int64_t n, float *out)
+{
+    const uint64_t key[2] = {seed, 0};
+    for (int64_t i = 0; i < n; ++i) {
+        const uint64_t ctr[4] = {base + (uint64_t)(i / 4), 0, 0, 0};
+        uint64_t words[4];
+        oracle_philox4x64(ctr, key, words);
+        out[i] = (float)((double)(words[i % 4] >> 40) * 0x1p-24);
+    }
+}
