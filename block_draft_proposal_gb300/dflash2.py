@@ -36,7 +36,7 @@ EXPORTS = (
     "dflash2_status_string", "dflash2_abi_version", "dflash2_grouped_conv",
     "dflash2_unary_topk_workspace_size", "dflash2_unary_topk_workspace_min",
     "dflash2_unary_topk", "dflash2_selector_walk_workspace_size", "dflash2_selector_walk",
-    "dflash2_d2t_remap", "dflash2_selector_walk_noalloc",
+    "dflash2_d2t_remap", "dflash2_selector_walk_noalloc", "dflash2_philox_uniforms",
 )
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -84,6 +84,8 @@ def library():
         lib.dflash2_selector_walk_noalloc.argtypes = [P, P, P, P, i64, P, P, P, P, P, P, i32, i32,
                                                       i32, i32, i32, i32, P, P, P, P, P]
         lib.dflash2_selector_walk_noalloc.restype = i32
+        lib.dflash2_philox_uniforms.argtypes = [ctypes.c_uint64, ctypes.c_uint64, P, i64, P, P]
+        lib.dflash2_philox_uniforms.restype = i32
         if lib.dflash2_abi_version() != ABI_VERSION:
             raise RuntimeError("libdflash2.so ABI version mismatch; rebuild it")
         _lib = lib
@@ -274,6 +276,30 @@ def d2t_remap(draft_ids, d2t, draft_vocab: int, target_vocab: int, out=None, err
     return out, err
 
 
+def philox_uniforms(seed: int, n: int, out=None, offset: int = 0, counter=None, device=None,
+                    stream=None):
+    """dflash2_philox_uniforms: n float32 uniforms in [0, 1) from Philox4x64-10.
+
+    With ``counter`` (a 1-element int64 device tensor holding the uint64 bits),
+    the base is read and advanced on the device, so a captured graph draws a
+    fresh sequence at every replay."""
+    if counter is not None:
+        _need(counter, "counter", torch.int64, (1,))
+        device = counter.device
+    if out is None:
+        if device is None:
+            raise ValueError("philox_uniforms needs `out`, `counter` or `device`")
+        out = torch.empty(int(n), dtype=torch.float32, device=device)
+    else:
+        _need(out, "out", torch.float32)
+        if out.numel() < n:
+            raise ValueError("out holds fewer than n elements")
+    _check("dflash2_philox_uniforms", library().dflash2_philox_uniforms(
+        int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _ptr(counter), int(n), _ptr(out),
+        _stream(stream)))
+    return out
+
+
 # ---- host <-> device helpers (plumbing) ----------------------------------------------
 
 def to_device(a: np.ndarray, device) -> torch.Tensor:
@@ -303,6 +329,7 @@ class ProposalBuffers:
         self.tokens = torch.empty((w.batch, w.slots), dtype=torch.int64, device=device)
         self.q = torch.empty((w.batch, w.slots, w.top_k), dtype=torch.float32, device=device)
         self.target_ids = torch.empty((w.batch, w.slots), dtype=torch.int64, device=device)
+        self.uniforms = torch.empty((w.batch, w.slots), dtype=torch.float32, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         self.ws_topk = torch.empty(max(1, unary_topk_workspace_size(w.rows, w.draft_vocab, w.top_k, code)),
                                    dtype=torch.uint8, device=device)
@@ -310,14 +337,22 @@ class ProposalBuffers:
                                    dtype=torch.uint8, device=device)
 
 
-def proposal_step(w, t: dict, bufs: ProposalBuffers | None = None, stream=None) -> dict:
+def proposal_step(w, t: dict, bufs: ProposalBuffers | None = None, stream=None,
+                  rng=None) -> dict:
     """One pass of the hot path: conv, unary candidates, selector walk, d2t remap.
 
     `t` holds the device tensors of synth.make(w) (bf16 tensors as torch.bfloat16).
-    Returns the output tensors (no synchronisation)."""
+    With ``rng = (seed, counter)`` the walk's uniforms are drawn on the device
+    (dflash2_philox_uniforms, counter advanced on the device) instead of taken
+    from ``t["uniforms"]``.  Returns the output tensors (no synchronisation)."""
     dev = t["h"].device
     if bufs is None:
         bufs = ProposalBuffers(w, dev)
+    uniforms = t.get("uniforms")
+    if rng is not None:
+        seed, counter = rng
+        philox_uniforms(seed, w.rows, out=bufs.uniforms.view(-1), counter=counter, stream=stream)
+        uniforms = bufs.uniforms
     grouped_conv(t["x"], t["base"], t["delta"], w.block_size, w.group_size, w.taps,
                  out=bufs.conv_out, stream=stream)
     unary_topk(t["h"], t["lm_head"], w.target_vocab, w.mult, w.cap, w.top_k,
@@ -326,9 +361,10 @@ def proposal_step(w, t: dict, bufs: ProposalBuffers | None = None, stream=None) 
     selector_walk(t["h"], t["proj"], t["A"], t["B"], t["anchors"],
                   bufs.cand_ids.view(w.batch, w.slots, w.top_k),
                   bufs.cand_u.view(w.batch, w.slots, w.top_k), t["temperatures"], t["greedy"],
-                  t["uniforms"], tokens=bufs.tokens, q=bufs.q, workspace=bufs.ws_walk,
+                  uniforms, tokens=bufs.tokens, q=bufs.q, workspace=bufs.ws_walk,
                   err=bufs.err, stream=stream)
     d2t_remap(bufs.tokens, t.get("d2t"), w.draft_vocab, w.target_vocab, out=bufs.target_ids,
               err=bufs.err, stream=stream)
     return dict(conv_out=bufs.conv_out, cand_ids=bufs.cand_ids, cand_u=bufs.cand_u,
-                tokens=bufs.tokens, q=bufs.q, target_ids=bufs.target_ids, err=bufs.err)
+                tokens=bufs.tokens, q=bufs.q, target_ids=bufs.target_ids, err=bufs.err,
+                uniforms=uniforms)

@@ -209,6 +209,34 @@ dflash2_status dflash2_selector_walk_noalloc(const void *h, const void *proj, co
                                              int32_t *err_word, void *stream);
 
 /*
+ * Counter-based uniforms for the walk.
+ * sglang DFlash2 PR, _SelectorDraftSampler: the uniforms of the sampled rows
+ * are drawn inside the captured CUDA graph from a Philox generator whose state
+ * advances at every replay (and the PR's risk list warns that a replay reusing
+ * the sequence would break the sampling).  The generator is Philox4x64-10
+ * (Salmon et al., "Parallel random numbers: as easy as 1, 2, 3", SC 2011):
+ *
+ *   out[i] = (word[i % 4] >> 40) * 2^-24,
+ *   word = Philox4x64_10(counter = (base + i / 4, 0, 0, 0), key = (seed, 0)),
+ *
+ * so out[i] lies in [0, 1) on the 2^-24 grid.
+ *
+ * counter == NULL: base = offset; any n >= 0.
+ * counter != NULL: device uint64, read and advanced on the device:
+ *                  base = *counter + offset, then *counter += ceil(n / 4).
+ *                  A graph that captures the call draws a fresh sequence at
+ *                  every replay.  n <= 2^24.  Calls that share a counter must be
+ *                  ordered (one stream, or events).
+ * out:             device float32 [n], 4-byte aligned (16-byte aligned stores
+ *                  four at a time).
+ * Errors: n < 0, out == NULL, or n > 2^24 with a counter -> INVALID_ARG;
+ *         misaligned out or counter -> MISALIGNED.  n == 0 queues nothing and
+ *         leaves the counter as it is.
+ */
+dflash2_status dflash2_philox_uniforms(uint64_t seed, uint64_t offset, uint64_t *counter,
+                                       int64_t n, float *out, void *stream);
+
+/*
  * Draft-to-target id remap.
  * vLLM Qwen3DSparkForCausalLM.map_draft_to_target: d2t holds offsets, so
  *   target_ids[i] = draft_ids[i] + d2t[draft_ids[i]];
