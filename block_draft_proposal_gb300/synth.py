@@ -24,7 +24,7 @@ from dataclasses import dataclass, replace
 import numpy as np
 
 PARTS = ("x", "base", "delta", "h", "lm_head", "A", "B", "proj", "uniforms",
-         "d2t", "anchors")
+         "d2t", "anchors", "w_kp", "base2")
 
 
 @dataclass(frozen=True)
@@ -137,7 +137,10 @@ def d2t_table(w: Workload, seed: int | None = None):
     return (subset - np.arange(w.draft_vocab)).astype(np.int64)
 
 
-def make(w: Workload, parts=PARTS) -> dict:
+DEFAULT_PARTS = PARTS[:11]  # the proposal step's inputs; w_kp / base2 feed the conv prepare
+
+
+def make(w: Workload, parts=DEFAULT_PARTS) -> dict:
     """Draw the requested parts of a workload.  Floating parts are float32 for
     "f32" workloads and uint16 bf16 bits for "bf16" workloads."""
     s, dt = w.seed, w.dtype
@@ -161,6 +164,10 @@ def make(w: Workload, parts=PARTS) -> dict:
             out[p] = rng(s, p).random(size=(w.batch, w.slots), dtype=np.float32)
         elif p == "d2t":
             out[p] = d2t_table(w)
+        elif p == "w_kp":     # kernel_projection weight [2 * taps * groups, hidden]
+            out[p] = normal(s, p, (2 * w.taps * w.groups, w.hidden), w.w_std, dt)
+        elif p == "base2":    # base_kernel of both conv sides [2, taps, hidden]
+            out[p] = normal(s, p, (2, w.taps, w.hidden), w.w_std, dt)
         elif p == "anchors":
             hi = min(w.draft_vocab, w.target_vocab)
             out[p] = rng(s, p).integers(0, hi, size=w.batch, dtype=np.int64)

@@ -74,6 +74,8 @@ def _load():
             lib.oracle_philox4x64.restype = None
             lib.oracle_philox_uniforms.argtypes = [u64, u64, i64, P]
             lib.oracle_philox_uniforms.restype = None
+            lib.oracle_kernel_projection.argtypes = [P, P, i64, i32, i32, i32, P]
+            lib.oracle_kernel_projection.restype = None
             _lib = lib
     return _lib
 
@@ -235,3 +237,37 @@ def philox_uniforms(seed: int, base: int, n: int) -> np.ndarray:
         _load().oracle_philox_uniforms(int(seed) & (2**64 - 1), int(base) & (2**64 - 1), int(n),
                                        _ptr(out))
     return out
+
+
+def kernel_projection(x, w_kp) -> np.ndarray:
+    """coef[i, r] = sum_j x[i, j] w_kp[r, j], rounded once to x's dtype."""
+    x, code = _elem(x)
+    w_kp, _ = _elem(w_kp)
+    _same(code, w_kp)
+    n, hidden = x.shape
+    r, h2 = w_kp.shape
+    if h2 != hidden:
+        raise ValueError("w_kp must be [out_features, hidden]")
+    coef = np.empty((n, r), dtype=x.dtype)
+    _load().oracle_kernel_projection(_ptr(x), _ptr(w_kp), n, hidden, r, code, _ptr(coef))
+    return coef
+
+
+def conv_prepare(x, w_kp, base2, block_size: int, group_size: int, taps: int):
+    """DFlashGroupedConv.prepare: (conv of x with coefficient side 0, coef).
+
+    base2 is base_kernel [2, taps, hidden]; coef is [n, 2, taps, groups] flat
+    per token ([n, 2 * taps * groups])."""
+    coef = kernel_projection(x, w_kp)
+    groups = x.shape[1] // group_size
+    out = conv(x, np.ascontiguousarray(base2[0]), coef, block_size, group_size, taps,
+               delta_row_stride=2 * taps * groups)
+    return out, coef
+
+
+def conv_finish(y, coef, base2, block_size: int, group_size: int, taps: int):
+    """DFlashGroupedConv.finish: conv of y with coefficient side 1 and base side 1."""
+    groups = y.shape[1] // group_size
+    side1 = np.ascontiguousarray(coef.reshape(coef.shape[0], -1)[:, taps * groups:])
+    return conv(y, np.ascontiguousarray(base2[1]), side1, block_size, group_size, taps,
+                delta_row_stride=taps * groups)

@@ -440,3 +440,31 @@ void oracle_philox_uniforms(uint64_t seed, uint64_t base, int64_t n, float *out)
         out[i] = (float)((double)(words[i % 4] >> 40) * 0x1p-24);
     }
 }
+
+/* ---- (10) kernel projection of the grouped conv ---------------------------
+ * DFlashGroupedConv (sglang DFlash2 PR) derives the dynamic coefficients of
+ * both of its convolutions from one bias-free linear map of the input,
+ * nn.Linear(hidden, 2 * taps * groups), whose weight is
+ * w_kp[2 * taps * groups, hidden]:
+ *
+ *   coef[i, r] = sum_j x[i, j] * w_kp[r, j],   r = (side * taps + t) * groups + g
+ *
+ * stored in the layer's dtype, as the Linear's output is.  prepare() convolves
+ * the input with side 0 of coef and side 0 of base_kernel[2, taps, hidden];
+ * finish() convolves the sublayer's output with side 1 of both.  Both are
+ * oracle_conv with delta_row_stride = 2 * taps * groups (see oracle/__init__.py).
+ */
+void oracle_kernel_projection(const void *x, const void *w_kp, int64_t n, int32_t hidden,
+                              int32_t out_features, int32_t dtype, void *coef)
+{
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        for (int32_t r = 0; r < out_features; ++r) {
+            double acc = 0.0;
+            for (int32_t j = 0; j < hidden; ++j)
+                acc += load_elem(x, i * hidden + j, dtype) *
+                       load_elem(w_kp, (int64_t)r * hidden + j, dtype);
+            store_elem(coef, i * (int64_t)out_features + r, acc, dtype);
+        }
+    }
+}
