@@ -86,8 +86,10 @@ def algorithmic_work(w):
                   + w.rows * w.top_k * (4 + 8) + w.rows * 4
                   + w.rows * w.top_k * 4 + w.rows * 8)
     d2t_bytes = w.rows * (8 + 8 + (8 if w.uses_d2t else 0))
+    # conv prepare (beside the step): kernel projection n x hidden x 2*taps*groups
+    kproj_flops = 2 * n * hdim * (2 * w.taps * g)
     return dict(conv_bytes=conv_bytes, gemm_flops=gemm_flops, walk_bytes=walk_bytes,
-                d2t_bytes=d2t_bytes)
+                d2t_bytes=d2t_bytes, kproj_flops=kproj_flops)
 
 
 class ClockSampler:
@@ -382,6 +384,41 @@ def run_gpu(args, w):
                 e2e_ms.append(e0.elapsed_time(e1))
     e2e = statistics.mean(e2e_ms)
 
+    # NEXT-row kernels timed beside the step (not part of its value): the grouped
+    # conv's prepare (kernel projection GEMM + input-side conv), L2 flushed
+    next_rows = {}
+    if w.dtype == "bf16":
+        dk = synth.make(w, parts=("w_kp", "base2"))
+        t_wkp, t_base2 = dflash2.to_device(dk["w_kp"], dev), dflash2.to_device(dk["base2"], dev)
+        coef = torch.empty((w.n_tokens, 2, w.taps, w.groups), dtype=torch.bfloat16, device=dev)
+        p_out = torch.empty_like(t["x"])
+        p_err = torch.zeros(1, dtype=torch.int32, device=dev)
+        reps = max(1, min(args.steps, 200))
+        pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+
+        def prep():
+            dflash2.conv_prepare(t["x"], t_wkp, t_base2, w.block_size, w.group_size, w.taps,
+                                 out=p_out, coef=coef, err=p_err, stream=stream)
+
+        with torch.cuda.stream(stream):
+            prep()
+        stream.synchronize()
+        pgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(pgraph, stream=stream):
+            prep()
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + reps):
+                flush.zero_()
+                if i >= args.warmup:
+                    pev[i - args.warmup][0].record(stream)
+                pgraph.replay()
+                if i >= args.warmup:
+                    pev[i - args.warmup][1].record(stream)
+        torch.cuda.synchronize()
+        next_rows["conv_prepare"] = {"ms": statistics.mean(a.elapsed_time(b) for a, b in pev),
+                                     "calls": reps, "err": int(p_err.item())}
+
     # max over ranks
     if world > 1:
         ms, e2e = reduce_max_over_ranks([ms, e2e], device=dev)
@@ -416,6 +453,12 @@ def run_gpu(args, w):
                  "frac_hbm": work["walk_bytes"] / (walk_ms * 1e-3) / 1e9 / hbm},
         "d2t": {"ms": statistics.mean(stage_ms["d2t"])},
     }
+    if "conv_prepare" in next_rows:
+        cp = next_rows["conv_prepare"]
+        cp["TFLOP/s"] = work["kproj_flops"] / (cp["ms"] * 1e-3) / 1e12
+        cp["frac_bf16_burst"] = cp["TFLOP/s"] / tf_burst
+        cp["what"] = ("kernel projection x.W_kp^T (2*N*H*2*taps*G flops) + input-side conv, "
+                      "one captured call replayed, beside the step")
 
     # CPU baseline: the oracle as it stands on a bounded sample (rank 0, N = 1)
     cpu = None
@@ -438,6 +481,7 @@ def run_gpu(args, w):
                                "finalize), 2*M*V*H flops over the stage time",
                      "peak_kind": f"{peak_kind} bf16 burst"},
         "stages": stages,
+        "next_rows": next_rows,
         "cpu_baseline": cpu,
         "e2e": {"value": job_value(world, w.rows, e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

@@ -116,6 +116,15 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams &p, const float 
                 if (i < ncols && m < p.rows_h) o[(int64_t)m * p.ldo] = z[i];
             }
         }
+    } else if (p.mode == kGemmStoreBf16) {
+        if (v < p.rows_w) {
+            __nv_bfloat16 *o = p.out_bf16 + v;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int m = m0 + i;
+                if (i < ncols && m < p.rows_h) o[(int64_t)m * p.ldo] = __float2bfloat16_rn(z[i]);
+            }
+        }
     } else if (p.mode == kGemmPilot) {
         // raw logits; the pilot select applies the transform (-inf = padded / out of range)
         const bool valid = v < p.rows_w && v < p.target_vocab;

@@ -13,6 +13,7 @@ enum GemmMode : int32_t {
     kGemmStore = 0,   // write fp32 C (split-K partials) to out
     kGemmPilot = 1,   // write the transformed, masked u of the pilot tiles to out
     kGemmFilter = 2,  // append (u, id) keys that reach the row's threshold
+    kGemmStoreBf16 = 3,  // write C rounded to bf16 (nearest-even) to out_bf16, no split
 };
 
 constexpr int kGemmTileW = 128;  // weight rows per tile (MMA M)
@@ -45,6 +46,7 @@ struct GemmParams {
     float mult;
     float cap;
     float *out;            // store: [k_splits][rows_h][ldo]; pilot: [rows_h][ldo]
+    __nv_bfloat16 *out_bf16;  // store-bf16: [rows_h][ldo]
     int64_t ldo;
     int64_t split_stride;
     const uint64_t *theta; // filter: per-row threshold key

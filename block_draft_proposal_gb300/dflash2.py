@@ -37,6 +37,7 @@ EXPORTS = (
     "dflash2_unary_topk_workspace_size", "dflash2_unary_topk_workspace_min",
     "dflash2_unary_topk", "dflash2_selector_walk_workspace_size", "dflash2_selector_walk",
     "dflash2_d2t_remap", "dflash2_selector_walk_noalloc", "dflash2_philox_uniforms",
+    "dflash2_conv_prepare", "dflash2_conv_finish",
 )
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -86,6 +87,10 @@ def library():
         lib.dflash2_selector_walk_noalloc.restype = i32
         lib.dflash2_philox_uniforms.argtypes = [ctypes.c_uint64, ctypes.c_uint64, P, i64, P, P]
         lib.dflash2_philox_uniforms.restype = i32
+        lib.dflash2_conv_prepare.argtypes = [P, P, P, i64, i32, i32, i32, i32, i32, P, P, P, P]
+        lib.dflash2_conv_prepare.restype = i32
+        lib.dflash2_conv_finish.argtypes = [P, P, P, i64, i32, i32, i32, i32, i32, P, P]
+        lib.dflash2_conv_finish.restype = i32
         if lib.dflash2_abi_version() != ABI_VERSION:
             raise RuntimeError("libdflash2.so ABI version mismatch; rebuild it")
         _lib = lib
@@ -274,6 +279,45 @@ def d2t_remap(draft_ids, d2t, draft_vocab: int, target_vocab: int, out=None, err
         _ptr(draft_ids), _ptr(d2t), draft_ids.numel(), draft_vocab, target_vocab, _ptr(out),
         _ptr(err), _stream(stream)))
     return out, err
+
+
+def conv_prepare(x, w_kp, base2, block_size: int, group_size: int, taps: int, out=None,
+                 coef=None, err=None, stream=None):
+    """dflash2_conv_prepare: (conv of x with coefficient side 0, coef [n, 2, taps, groups])."""
+    n, hidden = x.shape
+    groups = hidden // group_size
+    code = _dtype_code(x)
+    _need(x, "x", x.dtype)
+    _need(w_kp, "w_kp", x.dtype, (2 * taps * groups, hidden))
+    _need(base2, "base2", x.dtype, (2, taps, hidden))
+    if out is None:
+        out = torch.empty_like(x)
+    if coef is None:
+        coef = torch.empty((n, 2, taps, groups), dtype=x.dtype, device=x.device)
+    _need(coef, "coef", x.dtype, (n, 2, taps, groups))
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=x.device)
+    _check("dflash2_conv_prepare", library().dflash2_conv_prepare(
+        _ptr(x), _ptr(w_kp), _ptr(base2), n, hidden, group_size, taps, block_size, code,
+        _ptr(out), _ptr(coef), _ptr(err), _stream(stream)))
+    return out, coef, err
+
+
+def conv_finish(y, coef, base2, block_size: int, group_size: int, taps: int, out=None,
+                stream=None):
+    """dflash2_conv_finish: conv of y with coefficient side 1 and base side 1."""
+    n, hidden = y.shape
+    groups = hidden // group_size
+    code = _dtype_code(y)
+    _need(y, "y", y.dtype)
+    _need(coef, "coef", y.dtype, (n, 2, taps, groups))
+    _need(base2, "base2", y.dtype, (2, taps, hidden))
+    if out is None:
+        out = torch.empty_like(y)
+    _check("dflash2_conv_finish", library().dflash2_conv_finish(
+        _ptr(y), _ptr(base2), _ptr(coef), n, hidden, group_size, taps, block_size, code,
+        _ptr(out), _stream(stream)))
+    return out
 
 
 def philox_uniforms(seed: int, n: int, out=None, offset: int = 0, counter=None, device=None,

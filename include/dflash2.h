@@ -209,6 +209,46 @@ dflash2_status dflash2_selector_walk_noalloc(const void *h, const void *proj, co
                                              int32_t *err_word, void *stream);
 
 /*
+ * Grouped-conv prepare: the kernel projection, then the input-side conv.
+ * sglang DFlash2 PR, DFlashGroupedConv.prepare: one bias-free linear map
+ * kernel_projection = Linear(hidden, 2 * taps * groups) gives each token the
+ * dynamic coefficients of both convolutions of a wrapped sublayer,
+ *
+ *   coef[i, r] = sum_j x[i, j] * w_kp[r, j],   r = (side * taps + t) * groups + g,
+ *
+ * stored in dtype (bf16: fp32 accumulation on the tensor cores, rounded to
+ * nearest-even once); then out = the grouped conv of x with base side 0 and
+ * coefficient side 0 (dflash2_grouped_conv, delta read in place with row
+ * stride 2 * taps * groups).  Side 1 stays in coef for dflash2_conv_finish.
+ *
+ * x, out   device, [n_tokens, hidden] as for dflash2_grouped_conv.
+ * w_kp     device, [2 * taps * groups, hidden] (nn.Linear weight layout).
+ * base2    device, base_kernel [2, taps, hidden].
+ * coef     device, [n_tokens, 2, taps, groups], written (caller-owned).
+ * err_word device int32 or NULL; a projection wait that gives up sets
+ *          DFLASH2_DEVERR_TIMEOUT.
+ * Errors:  as dflash2_grouped_conv; bf16 also needs hidden % 8 == 0 and x,
+ *          w_kp 16-byte aligned (tensor-memory-access copies) -> MISALIGNED.
+ *          n_tokens == 0 queues nothing.
+ */
+dflash2_status dflash2_conv_prepare(const void *x, const void *w_kp, const void *base2,
+                                    int64_t n_tokens, int32_t hidden, int32_t group_size,
+                                    int32_t taps, int32_t block_size, int32_t dtype, void *out,
+                                    void *coef, int32_t *err_word, void *stream);
+
+/*
+ * Grouped-conv finish: the output-side conv.
+ * sglang DFlash2 PR, DFlashGroupedConv.finish: the sublayer's output y is
+ * convolved with base side 1 and coefficient side 1 of the coef that
+ * dflash2_conv_prepare wrote for the same tokens.  Arguments and errors as for
+ * dflash2_grouped_conv; base2 and coef as for dflash2_conv_prepare.
+ */
+dflash2_status dflash2_conv_finish(const void *y, const void *base2, const void *coef,
+                                   int64_t n_tokens, int32_t hidden, int32_t group_size,
+                                   int32_t taps, int32_t block_size, int32_t dtype, void *out,
+                                   void *stream);
+
+/*
  * Counter-based uniforms for the walk.
  * sglang DFlash2 PR, _SelectorDraftSampler: the uniforms of the sampled rows
  * are drawn inside the captured CUDA graph from a Philox generator whose state
