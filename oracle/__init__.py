@@ -76,6 +76,8 @@ def _load():
             lib.oracle_philox_uniforms.restype = None
             lib.oracle_kernel_projection.argtypes = [P, P, i64, i32, i32, i32, P]
             lib.oracle_kernel_projection.restype = None
+            lib.oracle_verify.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i64, i32, P, P]
+            lib.oracle_verify.restype = i64
             _lib = lib
     return _lib
 
@@ -271,3 +273,29 @@ def conv_finish(y, coef, base2, block_size: int, group_size: int, taps: int):
     side1 = np.ascontiguousarray(coef.reshape(coef.shape[0], -1)[:, taps * groups:])
     return conv(y, np.ascontiguousarray(base2[1]), side1, block_size, group_size, taps,
                 delta_row_stride=taps * groups)
+
+
+def verify(logits, temperatures, greedy, draft, cand, q, r):
+    """Speculative-sampling verification of a proposed block.
+
+    logits [B, S+1, V] (float32 or bf16 bits); temperatures [B] f32; greedy [B] u8;
+    draft [B, S] and cand [B, S, K] target ids (int64); q [B, S, K] f32;
+    r [B, S+1] f32 (r[:, s] accepts slot s, r[:, S] draws the emitted token).
+    Returns (accept_len [B] int64, out_tokens [B, S+1] int64, errors)."""
+    logits, code = _elem(logits)
+    b, s1, vocab = logits.shape
+    slots = s1 - 1
+    draft = np.ascontiguousarray(draft, dtype=np.int64).reshape(b, slots)
+    cand = np.ascontiguousarray(cand, dtype=np.int64)
+    k = cand.shape[-1]
+    cand = cand.reshape(b, slots, k)
+    q = np.ascontiguousarray(q, dtype=np.float32).reshape(b, slots, k)
+    r = np.ascontiguousarray(r, dtype=np.float32).reshape(b, s1)
+    temperatures = np.ascontiguousarray(temperatures, dtype=np.float32)
+    greedy = np.ascontiguousarray(greedy, dtype=np.uint8)
+    acc = np.zeros(b, dtype=np.int64)
+    out = np.zeros((b, s1), dtype=np.int64)
+    errors = _load().oracle_verify(_ptr(logits), _ptr(temperatures), _ptr(greedy), _ptr(draft),
+                                   _ptr(cand), _ptr(q), _ptr(r), b, slots, k, vocab, code,
+                                   _ptr(acc), _ptr(out))
+    return acc, out, int(errors)

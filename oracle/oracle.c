@@ -468,3 +468,159 @@ void oracle_kernel_projection(const void *x, const void *w_kp, int64_t n, int32_
         }
     }
 }
+
+/* ---- (11) lossless verification of a proposed block ------------------------
+ * The consumer of the walk's q.  The pages do not print it; this is the
+ * standard speculative-sampling rule (Leviathan, Kalman and Matias, "Fast
+ * inference from transformers via speculative decoding", 2023; Chen et al.,
+ * "Accelerating large language model decoding with speculative sampling",
+ * 2023).  For request b with S drafted tokens and S + 1 target positions:
+ *
+ *   T' = max(T_b, 1e-5) (as the walk clamps), p_s = softmax(logits[b, s, :] / T')
+ *   for s = 0 .. S-1, in order:
+ *     x = draft[b, s] (a target id); k = the candidate with cand[b, s, k] == x
+ *     greedy row:  accept iff x == argmax_y logits[b, s, y] (smallest y on ties)
+ *     sampled row: accept iff r[b, s] * q[b, s, k] < p_s(x)
+ *                  (probability min(1, p_s(x) / q[b, s, k]))
+ *     on the first rejection emit one token and stop:
+ *       greedy:  argmax_y logits[b, s, y]
+ *       sampled: from res(y) = max(0, p_s(y) - qt(y)), where qt(y) = q[b, s, k]
+ *                if y = cand[b, s, k] and 0 elsewhere, by inverse CDF with
+ *                u = r[b, S]: y = min { y : sum_{y' <= y} res(y') > u * sum res }
+ *   if every slot is accepted, emit the bonus token from position S the same
+ *   way with res = p_S (greedy: argmax).
+ *
+ * Arithmetic in double from the exact logits (bf16 widened); the uniforms,
+ * q and T are the fp32 inputs.  Outputs: accept_len[b] = accepted drafts;
+ * out_tokens[b, 0 .. S] = the accepted drafts, then the emitted token, then -1.
+ * A draft that is not among its slot's candidates counts as an error and
+ * leaves that request's outputs at accept_len 0 and all -1.  Returns the
+ * number of errors.
+ */
+static int64_t argmax_row(const void *logits, int64_t off, int64_t vocab, int dtype)
+{
+    int64_t best = 0;
+    double bv = load_elem(logits, off, dtype);
+    for (int64_t y = 1; y < vocab; ++y) {
+        double v = load_elem(logits, off + y, dtype);
+        if (v > bv) {
+            bv = v;
+            best = y;
+        }
+    }
+    return best;
+}
+
+/* p_s(y) for every y of one position, in double */
+static void softmax_row(const void *logits, int64_t off, int64_t vocab, double temp, int dtype,
+                        double *p)
+{
+    double m = -INFINITY;
+    for (int64_t y = 0; y < vocab; ++y) {
+        double z = load_elem(logits, off + y, dtype) / temp;
+        if (z > m)
+            m = z;
+    }
+    double sum = 0.0;
+    for (int64_t y = 0; y < vocab; ++y) {
+        p[y] = exp(load_elem(logits, off + y, dtype) / temp - m);
+        sum += p[y];
+    }
+    for (int64_t y = 0; y < vocab; ++y)
+        p[y] /= sum;
+}
+
+/* inverse CDF over res[0, vocab) with threshold u * total */
+static int64_t inverse_cdf(const double *res, int64_t vocab, double u)
+{
+    double total = 0.0;
+    for (int64_t y = 0; y < vocab; ++y)
+        total += res[y];
+    const double target = u * total;
+    double c = 0.0;
+    int64_t last_pos = -1;
+    for (int64_t y = 0; y < vocab; ++y) {
+        if (res[y] > 0.0)
+            last_pos = y;
+        c += res[y];
+        if (c > target && res[y] > 0.0)
+            return y;
+    }
+    return last_pos; /* only reached through rounding at the very top */
+}
+
+int64_t oracle_verify(const void *logits, const float *temperatures, const uint8_t *greedy,
+                      const int64_t *draft, const int64_t *cand, const float *q,
+                      const float *r, int32_t batch, int32_t slots, int32_t top_k,
+                      int64_t vocab, int32_t dtype, int64_t *accept_len, int64_t *out_tokens)
+{
+    int64_t errors = 0;
+#pragma omp parallel for schedule(dynamic) reduction(+ : errors)
+    for (int32_t b = 0; b < batch; ++b) {
+        int64_t *out = out_tokens + (int64_t)b * (slots + 1);
+        for (int32_t s = 0; s <= slots; ++s)
+            out[s] = -1;
+        accept_len[b] = 0;
+        const double temp = (double)(temperatures[b] > 1e-5f ? temperatures[b] : 1e-5f);
+        double *p = (double *)malloc(sizeof(double) * (size_t)vocab);
+        int bad = 0, done = 0;
+        int32_t s = 0;
+        for (; s < slots && !done; ++s) {
+            const int64_t off = ((int64_t)b * (slots + 1) + s) * vocab;
+            const int64_t x = draft[(int64_t)b * slots + s];
+            const int64_t *cs = cand + ((int64_t)b * slots + s) * top_k;
+            const float *qs = q + ((int64_t)b * slots + s) * top_k;
+            int32_t k = -1;
+            for (int32_t j = 0; j < top_k; ++j)
+                if (cs[j] == x) {
+                    k = j;
+                    break;
+                }
+            if (k < 0 || x < 0 || x >= vocab) {
+                bad = 1;
+                break;
+            }
+            if (greedy[b]) {
+                const int64_t y = argmax_row(logits, off, vocab, dtype);
+                if (y == x) {
+                    out[s] = x;
+                    continue;
+                }
+                out[s] = y;
+                done = 1;
+                break;
+            }
+            softmax_row(logits, off, vocab, temp, dtype, p);
+            if ((double)r[(int64_t)b * (slots + 1) + s] * (double)qs[k] < p[x]) {
+                out[s] = x;
+                continue;
+            }
+            for (int32_t j = 0; j < top_k; ++j) { /* residual: subtract q on its candidates */
+                const int64_t y = cs[j];
+                if (y >= 0 && y < vocab)
+                    p[y] = p[y] - (double)qs[j] > 0.0 ? p[y] - (double)qs[j] : 0.0;
+            }
+            out[s] = inverse_cdf(p, vocab, (double)r[(int64_t)b * (slots + 1) + slots]);
+            done = 1;
+            break;
+        }
+        if (bad) {
+            for (int32_t j = 0; j <= slots; ++j)
+                out[j] = -1;
+            errors += 1;
+        } else {
+            accept_len[b] = s; /* s drafts accepted when the loop stopped at slot s */
+            if (!done) {       /* all accepted: the bonus token from position S */
+                const int64_t off = ((int64_t)b * (slots + 1) + slots) * vocab;
+                if (greedy[b]) {
+                    out[slots] = argmax_row(logits, off, vocab, dtype);
+                } else {
+                    softmax_row(logits, off, vocab, temp, dtype, p);
+                    out[slots] = inverse_cdf(p, vocab, (double)r[(int64_t)b * (slots + 1) + slots]);
+                }
+            }
+        }
+        free(p);
+    }
+    return errors;
+}
