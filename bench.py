@@ -88,8 +88,13 @@ def algorithmic_work(w):
     d2t_bytes = w.rows * (8 + 8 + (8 if w.uses_d2t else 0))
     # conv prepare (beside the step): kernel projection n x hidden x 2*taps*groups
     kproj_flops = 2 * n * hdim * (2 * w.taps * g)
+    # verify (beside the step): the target logits once, plus the per-chunk partials
+    # (32 x 16 B per position, written and read) and the small per-slot inputs
+    pos = w.batch * (w.slots + 1)
+    verify_bytes = (pos * w.target_vocab * e + 2 * pos * ((w.target_vocab + 4095) // 4096) * 16
+                    + w.rows * w.top_k * (8 + 4) + pos * (4 + 8))
     return dict(conv_bytes=conv_bytes, gemm_flops=gemm_flops, walk_bytes=walk_bytes,
-                d2t_bytes=d2t_bytes, kproj_flops=kproj_flops)
+                d2t_bytes=d2t_bytes, kproj_flops=kproj_flops, verify_bytes=verify_bytes)
 
 
 class ClockSampler:
@@ -419,6 +424,53 @@ def run_gpu(args, w):
         next_rows["conv_prepare"] = {"ms": statistics.mean(a.elapsed_time(b) for a, b in pev),
                                      "calls": reps, "err": int(p_err.item())}
 
+        # verification of the step's proposals against synthetic target logits
+        # [B, S+1, V_t] (seeded, on the device), uniforms from the device generator
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(w.seed)
+        tlog = torch.randn((w.batch, w.slots + 1, w.target_vocab), generator=gen, device=dev,
+                           dtype=torch.float32).to(torch.bfloat16)
+        v_unif = torch.empty((w.batch, w.slots + 1), dtype=torch.float32, device=dev)
+        v_counter = torch.full((1,), 1 << 40, dtype=torch.int64, device=dev)
+        tgt_cand = torch.empty_like(bufs.cand_ids)
+        v_acc = torch.empty(w.batch, dtype=torch.int64, device=dev)
+        v_out = torch.empty((w.batch, w.slots + 1), dtype=torch.int64, device=dev)
+        v_ws = torch.empty(dflash2.verify_workspace_size(w.batch, w.slots, w.target_vocab),
+                           dtype=torch.uint8, device=dev)
+        v_err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def ver():
+            dflash2.d2t_remap(bufs.cand_ids, t.get("d2t"), w.draft_vocab, w.target_vocab,
+                              out=tgt_cand, err=v_err, stream=stream)
+            dflash2.philox_uniforms(w.seed + 1, v_unif.numel(), out=v_unif.view(-1),
+                                    counter=v_counter, stream=stream)
+            dflash2.verify(tlog, t["temperatures"], t["greedy"], bufs.target_ids,
+                           tgt_cand.view(w.batch, w.slots, w.top_k), bufs.q, v_unif,
+                           accept_len=v_acc, out_tokens=v_out, workspace=v_ws, err=v_err,
+                           stream=stream)
+
+        with torch.cuda.stream(stream):
+            ver()
+        stream.synchronize()
+        vgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(vgraph, stream=stream):
+            ver()
+        vev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + reps):
+                flush.zero_()
+                if i >= args.warmup:
+                    vev[i - args.warmup][0].record(stream)
+                vgraph.replay()
+                if i >= args.warmup:
+                    vev[i - args.warmup][1].record(stream)
+        torch.cuda.synchronize()
+        next_rows["verify"] = {"ms": statistics.mean(a.elapsed_time(b) for a, b in vev),
+                               "calls": reps, "err": int(v_err.item()),
+                               "mean_accept_len": float(v_acc.double().mean().item())}
+        del tlog
+
     # max over ranks
     if world > 1:
         ms, e2e = reduce_max_over_ranks([ms, e2e], device=dev)
@@ -459,6 +511,13 @@ def run_gpu(args, w):
         cp["frac_bf16_burst"] = cp["TFLOP/s"] / tf_burst
         cp["what"] = ("kernel projection x.W_kp^T (2*N*H*2*taps*G flops) + input-side conv, "
                       "one captured call replayed, beside the step")
+    if "verify" in next_rows:
+        vr = next_rows["verify"]
+        vr["GB/s"] = work["verify_bytes"] / (vr["ms"] * 1e-3) / 1e9
+        vr["frac_hbm"] = vr["GB/s"] / hbm
+        vr["what"] = ("speculative-sampling verify of the step's proposals against synthetic "
+                      "bf16 target logits [B, S+1, V_t] (candidate remap + uniforms + 2 kernels), "
+                      "one captured call replayed; bytes = logits once + partials")
 
     # CPU baseline: the oracle as it stands on a bounded sample (rank 0, N = 1)
     cpu = None

@@ -37,7 +37,8 @@ EXPORTS = (
     "dflash2_unary_topk_workspace_size", "dflash2_unary_topk_workspace_min",
     "dflash2_unary_topk", "dflash2_selector_walk_workspace_size", "dflash2_selector_walk",
     "dflash2_d2t_remap", "dflash2_selector_walk_noalloc", "dflash2_philox_uniforms",
-    "dflash2_conv_prepare", "dflash2_conv_finish",
+    "dflash2_conv_prepare", "dflash2_conv_finish", "dflash2_verify_workspace_size",
+    "dflash2_verify",
 )
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -91,6 +92,11 @@ def library():
         lib.dflash2_conv_prepare.restype = i32
         lib.dflash2_conv_finish.argtypes = [P, P, P, i64, i32, i32, i32, i32, i32, P, P]
         lib.dflash2_conv_finish.restype = i32
+        lib.dflash2_verify_workspace_size.argtypes = [i32, i32, i64]
+        lib.dflash2_verify_workspace_size.restype = sz
+        lib.dflash2_verify.argtypes = [P, i64, P, P, P, P, P, P, i32, i32, i32, i32, P, P, P, sz,
+                                       P, P]
+        lib.dflash2_verify.restype = i32
         if lib.dflash2_abi_version() != ABI_VERSION:
             raise RuntimeError("libdflash2.so ABI version mismatch; rebuild it")
         _lib = lib
@@ -318,6 +324,43 @@ def conv_finish(y, coef, base2, block_size: int, group_size: int, taps: int, out
         _ptr(y), _ptr(base2), _ptr(coef), n, hidden, group_size, taps, block_size, code,
         _ptr(out), _stream(stream)))
     return out
+
+
+def verify(target_logits, temperatures, greedy, draft, cand, q, uniforms, accept_len=None,
+           out_tokens=None, workspace=None, err=None, stream=None):
+    """dflash2_verify: speculative-sampling verification of a proposed block.
+
+    target_logits [B, S+1, V]; draft [B, S] and cand [B, S, K] are target ids."""
+    b, s1, vocab = target_logits.shape
+    slots = s1 - 1
+    k = cand.shape[-1]
+    code = _dtype_code(target_logits)
+    _need(target_logits, "target_logits", target_logits.dtype)
+    _need(temperatures, "temperatures", torch.float32, (b,))
+    _need(greedy, "greedy", torch.uint8, (b,))
+    _need(draft, "draft", torch.int64, (b, slots))
+    _need(cand, "cand", torch.int64, (b, slots, k))
+    _need(q, "q", torch.float32, (b, slots, k))
+    _need(uniforms, "uniforms", torch.float32, (b, s1))
+    dev = target_logits.device
+    if accept_len is None:
+        accept_len = torch.empty(b, dtype=torch.int64, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((b, s1), dtype=torch.int64, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(1, verify_workspace_size(b, slots, vocab)),
+                                dtype=torch.uint8, device=dev)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check("dflash2_verify", library().dflash2_verify(
+        _ptr(target_logits), vocab, _ptr(temperatures), _ptr(greedy), _ptr(draft), _ptr(cand),
+        _ptr(q), _ptr(uniforms), b, slots, k, code, _ptr(accept_len), _ptr(out_tokens),
+        _ptr(workspace), workspace.numel(), _ptr(err), _stream(stream)))
+    return accept_len, out_tokens, err
+
+
+def verify_workspace_size(batch: int, slots: int, vocab: int) -> int:
+    return int(library().dflash2_verify_workspace_size(batch, slots, vocab))
 
 
 def philox_uniforms(seed: int, n: int, out=None, offset: int = 0, counter=None, device=None,

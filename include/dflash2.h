@@ -249,6 +249,52 @@ dflash2_status dflash2_conv_finish(const void *y, const void *base2, const void 
                                    void *stream);
 
 /*
+ * Lossless verification of a proposed block (speculative sampling).
+ * The consumer of the walk's q; the pages do not print it, so this is the
+ * standard rule of Leviathan et al. ("Fast inference from transformers via
+ * speculative decoding", 2023) and Chen et al. ("Accelerating large language
+ * model decoding with speculative sampling", 2023).  For request b, with
+ * T' = max(T_b, 1e-5) as the walk clamps and p_s = softmax(logits[b, s] / T'):
+ *
+ *   slots s = 0 .. slots-1 in order, x = draft[b, s], k its candidate index:
+ *     greedy row:  accept iff x == argmax_y logits[b, s, y] (smallest y on ties)
+ *     sampled row: accept iff uniforms[b, s] * q[b, s, k] < p_s(x)
+ *   first rejection at s: emit one token and stop;
+ *     greedy: the argmax; sampled: a draw from max(0, p_s - qt) (qt = q on the
+ *     slot's candidate ids, 0 elsewhere) by inverse CDF with u = uniforms[b, slots]
+ *   no rejection: the bonus token from position `slots` (argmax, or a draw from
+ *     p_slots with the same u).
+ *
+ * target_logits device, [batch, slots + 1, vocab] (dtype), the target model's
+ *               logits at the block's positions.
+ * draft, cand   device int64 [batch, slots] and [batch, slots, top_k]: TARGET ids
+ *               (map the walk's tokens and candidates with dflash2_d2t_remap).
+ * q             device f32 [batch, slots, top_k] (the walk's q).
+ * uniforms      device f32 [batch, slots + 1] in [0, 1).
+ * temperatures, greedy  as for dflash2_selector_walk.
+ * accept_len    device int64 [batch]: accepted drafts (0 .. slots).
+ * out_tokens    device int64 [batch, slots + 1]: the accepted drafts, the
+ *               emitted token, then -1.
+ * workspace     device, >= dflash2_verify_workspace_size(batch, slots, vocab)
+ *               bytes, 16-byte aligned (per-chunk softmax partials).
+ * Arithmetic: fp32; p = 2^(logit * log2(e) / T' - m) / Z with exp2f (the
+ *   scaling is exact in real arithmetic); fixed reduction orders, so results
+ *   are deterministic.
+ * Errors: slots > 64, top_k outside [1, 128], vocab outside [1, 2^20] ->
+ *   INVALID_ARG.  A draft that is not among its slot's candidates, or an id
+ *   outside [0, vocab), sets DFLASH2_DEVERR_ID_RANGE and leaves that request's
+ *   accept_len 0 and out_tokens -1.
+ */
+size_t dflash2_verify_workspace_size(int32_t batch, int32_t slots, int64_t vocab);
+dflash2_status dflash2_verify(const void *target_logits, int64_t vocab,
+                              const float *temperatures, const uint8_t *greedy,
+                              const int64_t *draft, const int64_t *cand, const float *q,
+                              const float *uniforms, int32_t batch, int32_t slots,
+                              int32_t top_k, int32_t dtype, int64_t *accept_len,
+                              int64_t *out_tokens, void *workspace, size_t ws_bytes,
+                              int32_t *err_word, void *stream);
+
+/*
  * Counter-based uniforms for the walk.
  * sglang DFlash2 PR, _SelectorDraftSampler: the uniforms of the sampled rows
  * are drawn inside the captured CUDA graph from a Philox generator whose state
