@@ -6,13 +6,15 @@
 //   1. pilot GEMM: the raw logits of weight units spread over the vocab
 //      (4096 rows at most) are written to the workspace;
 //   2. pilot select: per row, the pilot's keys are formed with the same
-//      transform as the filter epilogue; the K-th best (u, id) key is a
-//      lower bound of the row's true K-th best key (it is the K-th best of a
-//      subset), so it is a safe threshold; the pilot's own top K keys seed the
-//      row's candidate list;
+//      transform as the filter epilogue; the K-th largest of the per-thread
+//      maxima is at most the pilot's K-th best (u, id) key, itself at most the
+//      row's true K-th best key (the K-th best of a subset), so it is a safe
+//      threshold; every pilot key that reaches it seeds the candidate list;
 //   3. filter GEMM over the remaining tiles: the epilogue appends every key
 //      that reaches the threshold to the row's candidate list;
-//   4. finalize: exact radix select + sort of each row's candidates.  A row
+//   4. finalize: the same maxima threshold cuts each row's candidates to a
+//      few more than K, which are sorted exactly (the radix select remains
+//      for a row where more than kCollect keys reach it).  A row
 //      whose list overflowed is recomputed exactly on CUDA cores (rare: only
 //      adversarial weights defeat the pilot threshold).
 // fp32 pipeline: one CUDA-core kernel per row (the same exact routine as the
@@ -37,7 +39,118 @@ struct SelectShared {
     uint32_t bcast[4];
     uint32_t count;
     uint64_t top[kMaxTopK];
+    uint64_t sort[kSelThreads];   // per-thread maxima, sorted
 };
+
+constexpr int kCollect = 512;  // keys at or above the maxima threshold sorted in shared memory
+
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
+    const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, (uint32_t)v, m);
+    const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, (uint32_t)(v >> 32), m);
+    return ((uint64_t)hi << 32) | lo;
+}
+
+// Sorts the warp's 32 values (one per lane) descending by shuffles; lane i
+// ends with the i-th largest.
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v, int lane) {
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const uint64_t other = shfl_xor_u64(v, stride);
+            const bool desc = (lane & size) == 0 || size == 32;
+            const bool lower = (lane & stride) == 0;
+            v = (lower == desc) ? (v > other ? v : other) : (v < other ? v : other);
+        }
+    }
+    return v;
+}
+
+// The k-th largest (1 <= k <= kSelThreads) of one float per thread, by the
+// same bitonic scheme as block_kth_of_maxima (floats, no NaN).
+__device__ float block_kth_of_maxima_f(float tmax, int k, float *s) {
+    const int t = threadIdx.x;
+    float v = tmax;
+#pragma unroll 1
+    for (int size = 2; size <= kSelThreads; size <<= 1) {
+#pragma unroll 1
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            float other;
+            if (stride >= 32) {
+                s[t] = v;
+                __syncthreads();
+                other = s[t ^ stride];
+                __syncthreads();
+            } else {
+                other = __shfl_xor_sync(0xFFFFFFFFu, v, stride);
+            }
+            const bool desc = (t & size) == 0;
+            const bool lower = (t & stride) == 0;
+            v = (lower == desc) ? fmaxf(v, other) : fminf(v, other);
+        }
+    }
+    s[t] = v;
+    __syncthreads();
+    const float r = s[k - 1];
+    __syncthreads();
+    return r;
+}
+
+// The k-th largest (1 <= k <= kSelThreads) of the block's per-thread values
+// tmax (one per thread), by a bitonic sort of kSelThreads elements: warp
+// shuffles for strides below 32, shared memory for the others.  Every thread
+// gets the result.  Used as a threshold: when each thread's value is the
+// largest of the keys it holds, the k-th largest of these maxima is at most
+// the k-th largest key of the block (k distinct keys reach it), and with many
+// more threads than k it is rarely much lower.
+__device__ uint64_t block_kth_of_maxima(uint64_t tmax, int k, SelectShared &sh) {
+    const int t = threadIdx.x;
+    uint64_t v = tmax;
+#pragma unroll 1
+    for (int size = 2; size <= kSelThreads; size <<= 1) {
+#pragma unroll 1
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            uint64_t other;
+            if (stride >= 32) {
+                sh.sort[t] = v;
+                __syncthreads();
+                other = sh.sort[t ^ stride];
+                __syncthreads();
+            } else {
+                other = shfl_xor_u64(v, stride);
+            }
+            const bool desc = (t & size) == 0;   // this block of `size` sorts descending
+            const bool lower = (t & stride) == 0;
+            v = (lower == desc) ? (v > other ? v : other) : (v < other ? v : other);
+        }
+    }
+    sh.sort[t] = v;  // descending
+    __syncthreads();
+    const uint64_t r = sh.sort[k - 1];
+    __syncthreads();
+    return r;
+}
+
+// Sorts a[0, n) descending in place (n a power of two, at most 2 * kSelThreads
+// per pass of the threads); all threads call it.
+__device__ void block_sort_desc(uint64_t *a, int n) {
+    for (int size = 2; size <= n; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const uint64_t x = a[i], y = a[j];
+                    const bool desc = (i & size) == 0;
+                    if (desc ? (x < y) : (x > y)) {
+                        a[i] = y;
+                        a[j] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
 
 // Exact k-th largest of keys[0, n) (1 <= k <= n), by 8-bit radix passes from
 // the top byte.  All threads of the block call it; every thread gets the
@@ -246,28 +359,65 @@ __global__ void __launch_bounds__(kSelThreads)
                         int k, float mult, float cap, uint64_t *theta, float *theta_pre,
                         uint32_t *cnt, uint64_t *cand, int cand_cap) {
     __shared__ SelectShared sh;
-    extern __shared__ __align__(16) uint8_t dyn[];
-    uint64_t *keys = reinterpret_cast<uint64_t *>(dyn);
+    __shared__ float fsort[kSelThreads];
     const int64_t row = blockIdx.x;
-    const int n = n_pilot * unit;
+    const int n = n_pilot * unit;  // unit == kSelThreads: entry i = tid + 256 j is row tid of unit j
     const float *pz = pilot_z + row * n;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const float z = pz[i];
-        const uint32_t v = (uint32_t)((i / unit) * pilot_stride * unit + (i % unit));
-        // the same transform the filter epilogue applies, so theta is the exact
-        // key of a real entry
-        keys[i] = (z == -INFINITY) ? 0ull : make_key(unary_transform(z, mult, cap), v);
+    constexpr int kPer = kPilotTiles * kGemmTileW / kSelThreads;  // entries per thread, at most
+    const int t = threadIdx.x;
+    float z[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) z[j] = t + j * kSelThreads < n ? pz[t + j * kSelThreads] : -INFINITY;
+    const auto vocab_id = [&](int j) { return (uint32_t)(j * pilot_stride * unit + t); };
+    uint64_t th;
+    float pre;
+    if (mult > 0.0f) {
+        // the transform is non-decreasing in z: theta from the raw logits, the
+        // exact transform only where the pre-threshold lets a key reach theta.
+        // z* = the k-th largest per-thread maximum; u* = its transformed value.
+        // At least k entries have z >= z*, hence u >= u*, hence a key >= the
+        // smallest key with value u*, which is theta: a lower bound of the
+        // row's k-th best key.
+        float zm = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) zm = fmaxf(zm, z[j]);
+        const float zs = block_kth_of_maxima_f(zm, k, fsort);
+        if (zs == -INFINITY) {
+            th = 0;  // fewer than k threads hold a valid entry: all are candidates
+            pre = -INFINITY;
+        } else {
+            const float us = unary_transform(zs, mult, cap);
+            th = make_key(us, 0xFFFFFFFFu);  // the smallest key of value u*
+            pre = us > 0.0f ? us * (1.0f - 0x1p-18f) : -INFINITY;
+        }
+    } else {
+        // no monotone shortcut: every entry's exact key, theta from their maxima
+        uint64_t km = 0;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j)
+            if (z[j] != -INFINITY)
+                km = max(km, make_key(unary_transform(z[j], mult, cap), vocab_id(j)));
+        th = block_kth_of_maxima(km, k, sh);
+        pre = -INFINITY;
+    }
+    if (t == 0) sh.count = 0;
+    __syncthreads();
+    // every pilot key at or above theta seeds the candidate list
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        if (z[j] != -INFINITY && mult * z[j] >= pre) {
+            const uint64_t key = make_key(unary_transform(z[j], mult, cap), vocab_id(j));
+            if (key >= th) {
+                const uint32_t slot = atomicAdd(&sh.count, 1u);
+                if (slot < (uint32_t)cand_cap) cand[row * cand_cap + slot] = key;
+            }
+        }
     }
     __syncthreads();
-    const uint64_t kth = block_kth_largest(keys, n, k, sh);
-    const int got = block_collect_sorted(keys, n, kth, k, sh);
-    for (int i = threadIdx.x; i < got; i += blockDim.x) cand[row * cand_cap + i] = sh.top[i];
-    if (threadIdx.x == 0) {
-        theta[row] = kth;  // 0 when the pilot holds fewer than k valid entries
-        const float u_th = key_u(kth);
-        theta_pre[row] = (kth != 0 && mult > 0.0f && u_th > 0.0f) ? u_th * (1.0f - 0x1p-18f)
-                                                                  : -INFINITY;
-        cnt[row] = (uint32_t)got;
+    if (t == 0) {
+        theta[row] = th;
+        theta_pre[row] = pre;
+        cnt[row] = sh.count;  // more than cand_cap: finalize recomputes the row exactly
     }
 }
 
@@ -293,12 +443,53 @@ __global__ void __launch_bounds__(kSelThreads)
         return;
     }
     const uint64_t *src = cand + row * cand_cap;
-    const uint64_t *keys = src;
-    if (n <= (uint32_t)kSmemKeys) {
-        uint64_t *st = reinterpret_cast<uint64_t *>(dyn);
-        for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) st[i] = src[i];
+    // the keys staged in shared memory once (when they fit) while the
+    // per-thread maxima form the threshold; then an exact sort of the (few)
+    // keys at or above it.  The radix select remains for the rare row where
+    // more than kCollect keys reach the threshold.
+    const bool staged = n <= (uint32_t)kSmemKeys;
+    uint64_t *st = reinterpret_cast<uint64_t *>(dyn);
+    const uint64_t *keys = staged ? st : src;
+    uint64_t tmax = 0;
+    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
+        const uint64_t key = src[i];
+        if (staged) st[i] = key;
+        tmax = key > tmax ? key : tmax;
+    }
+    const uint64_t th = block_kth_of_maxima(tmax, k, sh);  // its barriers also publish st
+    uint64_t *col = reinterpret_cast<uint64_t *>(dyn) + (staged ? kSmemKeys : 0);  // kCollect keys
+    if (threadIdx.x == 0) sh.count = 0;
+    __syncthreads();
+    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
+        const uint64_t key = keys[i];
+        if (key != 0 && key >= th) {
+            const uint32_t slot = atomicAdd(&sh.count, 1u);
+            if (slot < (uint32_t)kCollect) col[slot] = key;
+        }
+    }
+    __syncthreads();
+    const int c = (int)sh.count;
+    if (c <= 32) {
+        if (threadIdx.x < 32) {
+            const uint64_t v = warp_sort_desc(threadIdx.x < c ? col[threadIdx.x] : 0, threadIdx.x);
+            if ((int)threadIdx.x < k) sh.top[threadIdx.x] = v;
+        }
+        for (int i = 32 + threadIdx.x; i < k; i += blockDim.x) sh.top[i] = 0;
         __syncthreads();
-        keys = st;
+        write_row(sh, c < k ? c : k, k, row, ids, vals, err);
+        return;
+    }
+    if (c <= kCollect) {
+        int np = 1;
+        while (np < c) np <<= 1;
+        for (int i = c + threadIdx.x; i < np; i += blockDim.x) col[i] = 0;
+        __syncthreads();
+        block_sort_desc(col, np);
+        const int got = c < k ? c : k;
+        for (int i = threadIdx.x; i < k; i += blockDim.x) sh.top[i] = i < got ? col[i] : 0;
+        __syncthreads();
+        write_row(sh, got, k, row, ids, vals, err);
+        return;
     }
     const int kk = (int)n < k ? (int)n : k;
     const uint64_t kth = kk > 0 ? block_kth_largest(keys, (int)n, kk, sh) : ~0ull;
@@ -466,8 +657,8 @@ extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head,
     if (s != DFLASH2_OK) return s;
     p.bn = bn;
 
-    const size_t pilot_smem = (size_t)L.n_pilot * unit * 8;
-    pilot_select_kernel<<<(unsigned)rows, kSelThreads, pilot_smem, st>>>(
+    static_assert(2 * kGemmTileW == kSelThreads, "pilot select maps one unit row per thread");
+    pilot_select_kernel<<<(unsigned)rows, kSelThreads, 0, st>>>(
         pilot_u, L.n_pilot, L.pilot_stride, unit, top_k, mult, cap, theta, theta_pre, cnt, cand,
         (int)cap_keys);
     s = launch_status();
@@ -483,7 +674,9 @@ extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head,
     s = launch_gemm_tc(di, lm_head, h, p, st, pairs);
     if (s != DFLASH2_OK) return s;
 
-    size_t fin_smem = (size_t)(cap_keys < kSmemKeys ? cap_keys : kSmemKeys) * 8;
+    // staged keys (a row with at most kSmemKeys candidates) followed by the
+    // collect buffer
+    size_t fin_smem = ((size_t)kSmemKeys + kCollect) * 8;
     if (fin_smem < dsm) fin_smem = dsm;
     finalize_kernel<<<(unsigned)rows, kSelThreads, fin_smem, st>>>(
         cnt, cand, (int)cap_keys, top_k, cand_ids, cand_u, err_word,
