@@ -173,13 +173,19 @@ __device__ __forceinline__ void filter_chunk(const GemmParams &p, const float (&
                                              int m0, int c0, uint32_t tcol, EpiScratch &es,
                                              int &nbuf, int lane) {
     const bool valid_v = v < p.rows_w && v < p.target_vocab;
-    const float pre_lane = es.pre[c0 + lane];
+    float pre[32];  // the 32 tokens' pre-thresholds: broadcast 16-byte shared loads
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 v4 = reinterpret_cast<const float4 *>(es.pre + c0)[q];
+        pre[4 * q] = v4.x;
+        pre[4 * q + 1] = v4.y;
+        pre[4 * q + 2] = v4.z;
+        pre[4 * q + 3] = v4.w;
+    }
     uint32_t hits = 0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const float pre = __shfl_sync(0xFFFFFFFFu, pre_lane, i);
-        hits |= (valid_v && p.mult * z[i] >= pre) ? (1u << i) : 0u;
-    }
+    for (int i = 0; i < 32; ++i) hits |= (p.mult * z[i] >= pre[i]) ? (1u << i) : 0u;
+    if (!valid_v) hits = 0;
     uint32_t cols = __reduce_or_sync(0xFFFFFFFFu, hits);
     if (cols == 0) return;
     const uint64_t th_lane = es.th[c0 + lane];
