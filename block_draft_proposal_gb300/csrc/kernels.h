@@ -20,7 +20,7 @@ constexpr int kGemmTileW = 128;  // weight rows per tile (MMA M)
 constexpr int kGemmTileK = 64;   // hidden elements per TMA box (one 128-byte swizzle row)
 constexpr int kGemmStageK = 128; // hidden elements per pipeline stage (two boxes per operand)
 constexpr int kGemmMaxStages = 8;
-constexpr int kPilotTiles = 32;  // pilot weight tiles sampled across the vocab
+constexpr int kPilotTiles = 64;  // pilot weight tiles (of 128 rows) sampled across the vocab, at most
 
 struct GemmParams {
     // problem
@@ -58,10 +58,17 @@ struct GemmParams {
 };
 
 // Pilot tiling of a weight matrix with n_wtiles units of unit_rows rows:
-// n_pilot units (4096 rows at most) spaced pilot_stride apart, from unit 0.
+// n_pilot units spaced pilot_stride apart, from unit 0.  A larger pilot gives
+// a tighter threshold (fewer filter survivors, about K * vocab / pilot rows
+// per token) at the cost of a larger one-wave pilot GEMM; measured on the
+// bf16 workloads, about a sixteenth of the vocab, between 8 units and 8192
+// rows, balances the two (every unit when the vocab has fewer than 8).
 inline void pilot_layout(int64_t n_wtiles, int32_t *n_pilot, int32_t *stride, int unit_rows = 128) {
     const int64_t max_units = (int64_t)kPilotTiles * kGemmTileW / unit_rows;
-    int64_t np = n_wtiles < max_units ? n_wtiles : max_units;
+    int64_t np = (n_wtiles + 15) / 16;
+    if (np < 8) np = 8;
+    if (np > max_units) np = max_units;
+    if (np > n_wtiles) np = n_wtiles;
     if (np < 1) np = 1;
     *n_pilot = (int32_t)np;
     *stride = (int32_t)(n_wtiles / np);

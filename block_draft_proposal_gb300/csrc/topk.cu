@@ -4,7 +4,8 @@
 //
 // bf16 pipeline (four launches, no full logit matrix in HBM):
 //   1. pilot GEMM: the raw logits of weight units spread over the vocab
-//      (4096 rows at most) are written to the workspace;
+//      (about a sixteenth of it, 8192 rows at most) are written to the
+//      workspace;
 //   2. pilot select: per row, the pilot's keys are formed with the same
 //      transform as the filter epilogue; the K-th largest of the per-thread
 //      maxima is at most the pilot's K-th best (u, id) key, itself at most the

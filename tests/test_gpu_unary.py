@@ -57,7 +57,8 @@ SMALL = [
     (5, 96, 3000, 2999, 128, 1.0, 0.0, "bf16"),        # K at its maximum; hidden below one stage
     (9, 136, 1100, 1000, 16, 1.0, 10.0, "f32"),
     (2100, 128, 9000, 8990, 24, 1.0, 30.0, "bf16"),   # nine token tiles over the CTA pairs
-    (1800, 136, 4000, 4000, 8, 0.7, 0.0, "bf16"),     # the pilot covers the whole vocab
+    (1800, 136, 4000, 4000, 8, 0.7, 0.0, "bf16"),     # pilot of 8 of 16 units
+    (300, 136, 1500, 1450, 16, 1.0, 30.0, "bf16"),    # under 8 units: the pilot covers the vocab
 ]
 
 
