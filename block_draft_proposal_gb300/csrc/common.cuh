@@ -17,6 +17,32 @@
 namespace dflash2 {
 
 // ---------------------------------------------------------------------------
+// Launches with programmatic stream serialization: a kernel of this library
+// may be scheduled while the kernel before it on the stream drains (its launch
+// latency and on-chip prologue overlap the previous kernel's tail).  Every
+// kernel therefore starts with grid_dep_wait() before it touches global
+// memory, which returns once the previous grid has completed and its writes
+// are visible; so the stream order of the data stays exactly as without it.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// ---------------------------------------------------------------------------
 // Host helpers (host_common.cu)
 // ---------------------------------------------------------------------------
 struct DeviceInfo {

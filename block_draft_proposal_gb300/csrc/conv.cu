@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kTileVecs *kTokenLanes)
     conv_vec_kernel(const T *__restrict__ x, const T *__restrict__ base,
                     const T *__restrict__ delta, int64_t dstride, T *__restrict__ out, int64_t n,
                     int hidden, int group_size, int taps, int bs, bool pow2) {
+    grid_dep_wait();
     using V = VecTraits<T>;
     constexpr int VN = V::N;
     extern __shared__ uint4 tile[];  // [kTileTokens + taps - 1][kTileVecs]
@@ -120,6 +121,7 @@ __global__ void conv_scalar_kernel(const T *__restrict__ x, const T *__restrict_
                                    const T *__restrict__ delta, int64_t dstride,
                                    T *__restrict__ out, int64_t n, int hidden, int group_size,
                                    int taps, int bs, bool pow2) {
+    grid_dep_wait();
     using V = VecTraits<T>;
     const int groups = hidden / group_size;
     const int64_t total = n * hidden;
@@ -154,16 +156,16 @@ dflash2_status run_conv(const DeviceInfo &di, const void *x, const void *base, c
                   (unsigned)((nvec + kTileVecs - 1) / kTileVecs));
         dim3 block(kTileVecs, kTokenLanes);
         const size_t smem = (size_t)(kTileTokens + taps_eff - 1) * kTileVecs * sizeof(uint4);
-        conv_vec_kernel<T><<<grid, block, smem, st>>>(
-            static_cast<const T *>(x), static_cast<const T *>(base), static_cast<const T *>(delta),
+        launch_k(conv_vec_kernel<T>, grid, block, smem, st, static_cast<const T *>(x),
+            static_cast<const T *>(base), static_cast<const T *>(delta),
             dstride, static_cast<T *>(out), n, hidden, gs, taps_eff, bs, pow2);
     } else {
         const int64_t total = n * hidden;
         int64_t blocks = (total + 255) / 256;
         const int64_t cap = (int64_t)di.sm_count * 16;
         if (blocks > cap) blocks = cap;
-        conv_scalar_kernel<T><<<(unsigned)blocks, 256, 0, st>>>(
-            static_cast<const T *>(x), static_cast<const T *>(base), static_cast<const T *>(delta),
+        launch_k(conv_scalar_kernel<T>, (unsigned)blocks, 256, 0, st, static_cast<const T *>(x),
+            static_cast<const T *>(base), static_cast<const T *>(delta),
             dstride, static_cast<T *>(out), n, hidden, gs, taps_eff, bs, pow2);
     }
     return launch_status();

@@ -22,6 +22,7 @@ namespace {
 __global__ void __launch_bounds__(256)
     kproj_f32_kernel(const float *__restrict__ x, const float *__restrict__ w, int hidden,
                      int out_features, float *coef) {
+    grid_dep_wait();
     const int64_t i = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float *xr = x + i * hidden;
@@ -84,8 +85,8 @@ extern "C" dflash2_status dflash2_conv_prepare(const void *x, const void *w_kp, 
         if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w_kp) |
              reinterpret_cast<uintptr_t>(coef)) % 4 != 0)
             return DFLASH2_ERR_MISALIGNED;
-        kproj_f32_kernel<<<(unsigned)n_tokens, 256, 0, st>>>(
-            static_cast<const float *>(x), static_cast<const float *>(w_kp), hidden,
+        launch_k(kproj_f32_kernel, (unsigned)n_tokens, 256, 0, st, static_cast<const float *>(x),
+            static_cast<const float *>(w_kp), hidden,
             (int)out_features, static_cast<float *>(coef));
         s = launch_status();
     } else {

@@ -8,6 +8,7 @@ namespace {
 __global__ void d2t_kernel(const int64_t *__restrict__ ids, const int64_t *__restrict__ d2t,
                            int64_t n, int64_t draft_vocab, int64_t target_vocab,
                            int64_t *target_ids, int32_t *err) {
+    grid_dep_wait();
     bool bad_any = false;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -46,7 +47,7 @@ extern "C" dflash2_status dflash2_d2t_remap(const int64_t *draft_ids, const int6
     int64_t blocks = (n + 255) / 256;
     const int64_t cap = (int64_t)di.sm_count * 8;
     if (blocks > cap) blocks = cap;
-    d2t_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        draft_ids, d2t, n, draft_vocab, target_vocab, target_ids, err_word);
+    launch_k(d2t_kernel, (unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream), draft_ids,
+        d2t, n, draft_vocab, target_vocab, target_ids, err_word);
     return launch_status();
 }

@@ -266,6 +266,7 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    grid_dep_wait();  // barriers and TMEM are set up; now the inputs
     const uint32_t tmem = tmem_slot;
     const int total = p.pass_tiles * p.n_tok_tiles * p.k_splits;
 
@@ -454,6 +455,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     __syncthreads();
     cluster_sync();  // the peer's barriers exist before anyone signals them
     tc_fence_after();
+    grid_dep_wait();  // barriers and TMEM are set up; now the inputs
     const uint32_t tmem = tmem_slot;
     const int total = p.pass_tiles * p.n_tok_tiles;
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
@@ -635,10 +637,10 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     if (pair) {
         const int64_t pairs_max = di.sm_count / 2;
         const int pairs = (int)(total < pairs_max ? total : pairs_max);
-        gemm_tc_pair_kernel<<<2 * pairs, 192, smem, st>>>(tm_w, tm_h, p);
+        launch_k(gemm_tc_pair_kernel, 2 * pairs, 192, smem, st, tm_w, tm_h, p);
     } else {
         const int grid = (int)(total < di.sm_count ? total : di.sm_count);
-        gemm_tc_kernel<<<grid, 192, smem, st>>>(tm_w, tm_h, p);
+        launch_k(gemm_tc_kernel, grid, 192, smem, st, tm_w, tm_h, p);
     }
     return launch_status();
 }

@@ -61,6 +61,7 @@ __device__ __forceinline__ void write_block(float *out, int64_t n, int64_t j, ui
 }
 
 __global__ void philox_kernel(uint64_t seed, uint64_t base, int64_t n, float *out) {
+    grid_dep_wait();
     const bool vec = (reinterpret_cast<uintptr_t>(out) & 15) == 0;
     const int64_t nb = (n + 3) / 4;
     for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < nb;
@@ -73,6 +74,7 @@ __global__ void philox_kernel(uint64_t seed, uint64_t base, int64_t n, float *ou
 // the counter, so its read precedes its write.
 __global__ void philox_counter_kernel(uint64_t seed, uint64_t offset, uint64_t *counter, int64_t n,
                                       float *out) {
+    grid_dep_wait();
     __shared__ uint64_t base_s;
     const int64_t nb = (n + 3) / 4;
     if (threadIdx.x == 0) {
@@ -103,12 +105,12 @@ extern "C" dflash2_status dflash2_philox_uniforms(uint64_t seed, uint64_t offset
     if (s != DFLASH2_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (counter) {
-        philox_counter_kernel<<<1, 256, 0, st>>>(seed, offset, counter, n, out);
+        launch_k(philox_counter_kernel, 1, 256, 0, st, seed, offset, counter, n, out);
     } else {
         int64_t blocks = ((n + 3) / 4 + 255) / 256;
         const int64_t cap = (int64_t)di.sm_count * 4;
         if (blocks > cap) blocks = cap;
-        philox_kernel<<<(unsigned)blocks, 256, 0, st>>>(seed, offset, n, out);
+        launch_k(philox_kernel, (unsigned)blocks, 256, 0, st, seed, offset, n, out);
     }
     return launch_status();
 }

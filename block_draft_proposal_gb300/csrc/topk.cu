@@ -336,6 +336,7 @@ __global__ void __launch_bounds__(kSelThreads)
     direct_topk_kernel(const T *__restrict__ h, const T *__restrict__ w, int hidden,
                        int64_t draft_vocab, int64_t target_vocab, float mult, float cap, int k,
                        int64_t *ids, float *vals, int32_t *err) {
+    grid_dep_wait();
     __shared__ SelectShared sh;
     extern __shared__ __align__(16) uint8_t dyn[];
     float *hs = reinterpret_cast<float *>(dyn);
@@ -359,6 +360,7 @@ __global__ void __launch_bounds__(kSelThreads)
     pilot_select_kernel(const float *__restrict__ pilot_z, int n_pilot, int pilot_stride, int unit,
                         int k, float mult, float cap, uint64_t *theta, float *theta_pre,
                         uint32_t *cnt, uint64_t *cand, int cand_cap) {
+    grid_dep_wait();
     __shared__ SelectShared sh;
     __shared__ float fsort[kSelThreads];
     const int64_t row = blockIdx.x;
@@ -429,6 +431,7 @@ __global__ void __launch_bounds__(kSelThreads)
                     int cand_cap, int k, int64_t *ids, float *vals, int32_t *err,
                     const __nv_bfloat16 *__restrict__ h, const __nv_bfloat16 *__restrict__ w,
                     int hidden, int64_t draft_vocab, int64_t target_vocab, float mult, float cap) {
+    grid_dep_wait();
     __shared__ SelectShared sh;
     extern __shared__ __align__(16) uint8_t dyn[];
     const int64_t row = blockIdx.x;
@@ -605,8 +608,9 @@ extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head,
     if (dtype == DFLASH2_F32) {
         if ((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(lm_head)) % 4 != 0)
             return DFLASH2_ERR_MISALIGNED;
-        direct_topk_kernel<float><<<(unsigned)rows, kSelThreads, dsm, st>>>(
+        launch_k(direct_topk_kernel<float>, (unsigned)rows, kSelThreads, dsm, st,
             static_cast<const float *>(h), static_cast<const float *>(lm_head), hidden, draft_vocab,
+
             target_vocab, mult, cap, top_k, cand_ids, cand_u, err_word);
         return launch_status();
     }
@@ -659,8 +663,8 @@ extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head,
     p.bn = bn;
 
     static_assert(2 * kGemmTileW == kSelThreads, "pilot select maps one unit row per thread");
-    pilot_select_kernel<<<(unsigned)rows, kSelThreads, 0, st>>>(
-        pilot_u, L.n_pilot, L.pilot_stride, unit, top_k, mult, cap, theta, theta_pre, cnt, cand,
+    launch_k(pilot_select_kernel, (unsigned)rows, kSelThreads, 0, st, pilot_u, L.n_pilot,
+        L.pilot_stride, unit, top_k, mult, cap, theta, theta_pre, cnt, cand,
         (int)cap_keys);
     s = launch_status();
     if (s != DFLASH2_OK) return s;
@@ -679,8 +683,8 @@ extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head,
     // collect buffer
     size_t fin_smem = ((size_t)kSmemKeys + kCollect) * 8;
     if (fin_smem < dsm) fin_smem = dsm;
-    finalize_kernel<<<(unsigned)rows, kSelThreads, fin_smem, st>>>(
-        cnt, cand, (int)cap_keys, top_k, cand_ids, cand_u, err_word,
+    launch_k(finalize_kernel, (unsigned)rows, kSelThreads, fin_smem, st, cnt, cand, (int)cap_keys,
+        top_k, cand_ids, cand_u, err_word,
         static_cast<const __nv_bfloat16 *>(h), static_cast<const __nv_bfloat16 *>(lm_head), hidden,
         draft_vocab, target_vocab, mult, cap);
     return launch_status();

@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(kVThreads)
     verify_stats_kernel(const T *__restrict__ logits, int64_t vocab, int32_t n_chunks,
                         int32_t slots1, const float *__restrict__ temperatures,
                         const uint8_t *__restrict__ greedy, bool vec, ChunkStat *stats) {
+    grid_dep_wait();
     const int64_t row = blockIdx.x;  // one target position; blockIdx.y splits its chunks
     const int b = (int)(row / slots1);
     const bool is_greedy = greedy[b] != 0;
@@ -263,6 +264,7 @@ __global__ void __launch_bounds__(kVThreads)
                          const int64_t *__restrict__ draft, const int64_t *__restrict__ cand,
                          const float *__restrict__ q, const float *__restrict__ r,
                          int64_t *accept_len, int64_t *out_tokens, int32_t *err) {
+    grid_dep_wait();
     __shared__ DecideShared sh;
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
@@ -576,17 +578,17 @@ extern "C" dflash2_status dflash2_verify(const void *target_logits, int64_t voca
     }
     if (dtype == DFLASH2_BF16) {
         const auto *lg = static_cast<const __nv_bfloat16 *>(target_logits);
-        verify_stats_kernel<__nv_bfloat16><<<sgrid, kVThreads, 0, st>>>(
-            lg, vocab, n_chunks, slots + 1, temperatures, greedy, vec, stats);
-        verify_decide_kernel<__nv_bfloat16><<<(unsigned)batch, kVThreads, dsm, st>>>(
-            lg, vocab, n_chunks, slots, top_k, stats, temperatures, greedy, draft, cand, q,
+        launch_k(verify_stats_kernel<__nv_bfloat16>, sgrid, kVThreads, 0, st, lg, vocab, n_chunks,
+            slots + 1, temperatures, greedy, vec, stats);
+        launch_k(verify_decide_kernel<__nv_bfloat16>, (unsigned)batch, kVThreads, dsm, st, lg,
+            vocab, n_chunks, slots, top_k, stats, temperatures, greedy, draft, cand, q,
             uniforms, accept_len, out_tokens, err_word);
     } else {
         const auto *lg = static_cast<const float *>(target_logits);
-        verify_stats_kernel<float><<<sgrid, kVThreads, 0, st>>>(
-            lg, vocab, n_chunks, slots + 1, temperatures, greedy, vec, stats);
-        verify_decide_kernel<float><<<(unsigned)batch, kVThreads, dsm, st>>>(
-            lg, vocab, n_chunks, slots, top_k, stats, temperatures, greedy, draft, cand, q,
+        launch_k(verify_stats_kernel<float>, sgrid, kVThreads, 0, st, lg, vocab, n_chunks,
+            slots + 1, temperatures, greedy, vec, stats);
+        launch_k(verify_decide_kernel<float>, (unsigned)batch, kVThreads, dsm, st, lg, vocab,
+            n_chunks, slots, top_k, stats, temperatures, greedy, draft, cand, q,
             uniforms, accept_len, out_tokens, err_word);
     }
     return launch_status();

@@ -187,6 +187,7 @@ __device__ __forceinline__ void issue_group(const WalkParams &p, const WalkLayou
 template <typename T, bool PA, int E>
 __global__ void __launch_bounds__(kMaxWarpsPerCta * 32)
     walk_kernel(const WalkParams p, int warps_per_cta, WalkLayout L) {
+    grid_dep_wait();
     extern __shared__ __align__(16) uint8_t dyn[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x * warps_per_cta + warp;
@@ -425,6 +426,7 @@ __device__ __forceinline__ int lat_arow(int s, int kp, int K) { return s == 0 ? 
 
 template <typename T, int KM>
 __global__ void __launch_bounds__(kLatThreads) walk_lattice_kernel(const WalkParams p, LatLayout L) {
+    grid_dep_wait();
     extern __shared__ __align__(16) uint8_t dyn[];
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
@@ -609,6 +611,7 @@ __global__ void __launch_bounds__(kLatThreads) walk_lattice_kernel(const WalkPar
 __global__ void __launch_bounds__(128)
     project_f32_kernel(const float *__restrict__ h, const float *__restrict__ proj, int hidden,
                        int rank, float *g) {
+    grid_dep_wait();
     const int64_t m = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float *hr = h + m * hidden;
@@ -755,7 +758,7 @@ extern "C" dflash2_status dflash2_selector_walk(
         if ((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(proj)) % 4 != 0)
             return DFLASH2_ERR_MISALIGNED;
         wp.k_splits = 1;
-        project_f32_kernel<<<(unsigned)rows, 128, 0, st>>>(static_cast<const float *>(h),
+        launch_k(project_f32_kernel, (unsigned)rows, 128, 0, st, static_cast<const float *>(h),
                                                            static_cast<const float *>(proj), hidden,
                                                            rank, g);
         s = launch_status();
@@ -809,7 +812,7 @@ extern "C" dflash2_status dflash2_selector_walk(
     if (lattice) {
         const int km = top_k <= 8 ? 8 : (top_k <= 16 ? 16 : 32);
 #define DFLASH2_LAT_LAUNCH(T_, KM_) \
-    walk_lattice_kernel<T_, KM_><<<(unsigned)batch, kLatThreads, LL.total, st>>>(wp, LL)
+    launch_k(walk_lattice_kernel<T_, KM_>, (unsigned)batch, kLatThreads, LL.total, st, wp, LL)
         if (dtype == DFLASH2_BF16) {
             if (km == 8) DFLASH2_LAT_LAUNCH(__nv_bfloat16, 8);
             else if (km == 16) DFLASH2_LAT_LAUNCH(__nv_bfloat16, 16);
@@ -827,7 +830,7 @@ extern "C" dflash2_status dflash2_selector_walk(
     const size_t smem = L.total * warps;
     const int threads = 32 * warps;
 #define DFLASH2_WALK_LAUNCH(T_, PA_, E_) \
-    walk_kernel<T_, PA_, E_><<<grid, threads, smem, st>>>(wp, warps, L)
+    launch_k(walk_kernel<T_, PA_, E_>, grid, threads, smem, st, wp, warps, L)
     const int E = top_k <= 32 ? 1 : (top_k <= 64 ? 2 : 4);
     if (dtype == DFLASH2_BF16) {
         if (prefetch_a) {
