@@ -116,10 +116,17 @@ dflash2_status dflash2_grouped_conv(const void *x, const void *base, const void 
  * Arithmetic: bf16 -> tcgen05 tensor-core GEMM with fp32 accumulation; fp32 ->
  *             fp32 FMA on CUDA cores (no TF32).  The transform runs in fp32
  *             (tanhf), and selection compares the fp32 u.
- * Errors:     rows < 0, hidden < 1, top_k < 1, top_k > 128, top_k > target_vocab,
- *             target_vocab > draft_vocab ... see validation: INVALID_ARG;
- *             bf16 needs hidden % 8 == 0 and 16-byte aligned h and lm_head
- *             (MISALIGNED).  rows == 0 queues nothing.
+ * Errors:     INVALID_ARG for rows outside [0, 2^31), hidden outside [1, 32768],
+ *             draft_vocab outside [1, 2^31), target_vocab < 1, top_k outside
+ *             [1, 128] or above either vocab size, cap negative or NaN, or a null
+ *             pointer; UNSUPPORTED_DTYPE for a dtype other than f32 / bf16;
+ *             MISALIGNED for cand_ids not 8-byte or cand_u not 4-byte aligned, and
+ *             for bf16 when hidden % 8 != 0, h or lm_head is not 16-byte aligned
+ *             or the workspace is not 256-byte aligned; WORKSPACE for a bf16
+ *             workspace below the minimum.  rows == 0 queues nothing.
+ * Device:     a row whose candidate list outgrows the workspace is recomputed
+ *             exactly on CUDA cores and flagged DFLASH2_DEVINFO_TOPK_FALLBACK (not
+ *             an error); fewer than top_k valid entries set DFLASH2_DEVERR_SHORT.
  */
 size_t dflash2_unary_topk_workspace_size(int64_t rows, int64_t draft_vocab, int32_t top_k,
                                          int32_t dtype);
