@@ -59,6 +59,8 @@ SMALL = [
     (2100, 128, 9000, 8990, 24, 1.0, 30.0, "bf16"),   # nine token tiles over the CTA pairs
     (1800, 136, 4000, 4000, 8, 0.7, 0.0, "bf16"),     # pilot of 8 of 16 units
     (300, 136, 1500, 1450, 16, 1.0, 30.0, "bf16"),    # under 8 units: the pilot covers the vocab
+    (96, 256, 20000, 19990, 16, -0.5, 0.0, "bf16"),   # negative multiplier: order reversed
+    (40, 128, 12000, 12000, 8, -1.0, 30.0, "bf16"),   # negative multiplier with the soft cap
 ]
 
 
