@@ -383,82 +383,107 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32)
 }
 
 // ---------------------------------------------------------------------------
-// Lattice mode (top_k <= 32): one CTA per request.  Slot s's possible
-// predecessors are exactly slot s-1's candidates (the anchor at slot 0), so
-// every slot's K x K edges and the draw from every lattice row can be formed
-// in parallel before the walk; the walk itself is then a chase through the
-// per-row choices.  Each (slot, predecessor) row is reduced by one thread in
-// candidate order, as the sequential sums of the walk's definition.
+// Lattice mode (top_k <= 32), two kernels.  Slot s's possible predecessors are
+// exactly slot s-1's candidates (the anchor at slot 0), so every slot's K x K
+// edges and the draw from every (slot, predecessor) row can be formed in
+// parallel before the walk; the walk itself is then a chase through the
+// per-row draws.
+//   walk_rows_kernel, grid (batch, parts): a CTA forms the rows of a range of
+//     slots of one request and writes their edges, softmax statistics and
+//     draws to the workspace.  Parts spread a request over several SMs: one
+//     SM per request was bound by its instruction issue.  A row is formed by
+//     kLatGroup adjacent lanes (K / kLatGroup consecutive candidates each),
+//     and its sums run in candidate order, as the sequential sums of the
+//     walk's definition: the running value passes from lane to lane by
+//     shuffles.
+//   walk_chase_kernel, one CTA per request: follows the draws slot by slot
+//     and writes the walked path's tokens, q and edges.
 // ---------------------------------------------------------------------------
-constexpr int kLatThreads = 256;
+constexpr int kLatticeMaxK = 32;
+constexpr int kRowThreads = 256;
+constexpr int kLatGroup = 4;
+constexpr int kChaseThreads = 256;
 
-struct LatLayout {
+struct RowsLayout {
     int a_stride;   // bytes per staged A row (rank * esz + 16)
     int b_stride;   // bytes per staged B row (rank * esz + 16)
     int b_slot;     // bytes per slot of B rows (k * b_stride + 16)
-    size_t ids, cu, uni, gs, brow, arow, lat, stat, nxt, path, scratch_bytes, total;
+    size_t ids, cu, uni, gs, brow, arow, total;
 };
 
-__host__ __device__ inline LatLayout lat_layout(int slots, int k, int rank, int esz, int k_splits) {
-    LatLayout L;
+// Shared memory of a CTA covering spp slots: the ids of those slots and of the
+// slot before them, their unary values, uniforms, projections, and the staged
+// B (candidate) and A (predecessor) rows.
+__host__ __device__ inline RowsLayout rows_layout(int spp, int k, int rank, int esz) {
+    RowsLayout L;
     L.a_stride = rank * esz + 16;
     L.b_stride = rank * esz + 16;
     L.b_slot = k * L.b_stride + 16;
     L.ids = 0;
-    L.cu = L.ids + pad16((size_t)slots * k * 8);
-    L.uni = L.cu + pad16((size_t)slots * k * 4);
-    L.gs = L.uni + pad16((size_t)slots * 4);
-    L.brow = L.gs + pad16((size_t)slots * rank * 4);
-    L.arow = L.brow + (size_t)slots * L.b_slot;
-    L.lat = L.arow + pad16((size_t)(1 + (slots - 1) * k) * L.a_stride);
-    L.stat = L.lat + pad16((size_t)slots * k * k * 4);
-    L.nxt = L.stat + pad16((size_t)slots * k * 8);
-    L.path = L.nxt + pad16((size_t)slots * k * 4);
-    L.total = L.path + pad16((size_t)slots * 4);
-    L.scratch_bytes = 0;
-    (void)k_splits;
+    L.cu = L.ids + pad16((size_t)(spp + 1) * k * 8);
+    L.uni = L.cu + pad16((size_t)spp * k * 4);
+    L.gs = L.uni + pad16((size_t)spp * 4);
+    L.brow = L.gs + pad16((size_t)spp * rank * 4);
+    L.arow = L.brow + (size_t)spp * L.b_slot;
+    L.total = L.arow + pad16((size_t)spp * k * L.a_stride);
     return L;
 }
 
-// Row staged for predecessor kp of slot s: the anchor (row 0) at slot 0,
-// else slot s-1's candidate kp.
-__device__ __forceinline__ int lat_arow(int s, int kp, int K) { return s == 0 ? 0 : 1 + (s - 1) * K + kp; }
+// The lattice of every request in the workspace.
+struct LatticeWs {
+    float *lat;    // [batch][slots][K][K] edges, row (slot, predecessor)
+    float2 *stat;  // [batch][slots][K] (max of e / T, sum of exp) of sampled rows
+    int32_t *nxt;  // [batch][slots][K] the candidate drawn from each row
+};
+
+inline size_t align256w(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workspace offsets of the lattice buffers (after the projection partials).
+inline void lattice_ws_layout(int64_t rows, int k, size_t base, size_t *lat, size_t *stat,
+                              size_t *nxt, size_t *end) {
+    *lat = align256w(base);
+    *stat = align256w(*lat + (size_t)rows * k * k * 4);
+    *nxt = align256w(*stat + (size_t)rows * k * 8);
+    *end = align256w(*nxt + (size_t)rows * k * 4);
+}
 
 template <typename T, int KM>
-__global__ void __launch_bounds__(kLatThreads) walk_lattice_kernel(const WalkParams p, LatLayout L) {
+__global__ void __launch_bounds__(kRowThreads)
+    walk_rows_kernel(const WalkParams p, RowsLayout L, int spp, LatticeWs ws) {
     grid_dep_wait();
     extern __shared__ __align__(16) uint8_t dyn[];
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
     const int S = p.slots, K = p.k, R = p.rank;
-    int64_t *ids = reinterpret_cast<int64_t *>(dyn + L.ids);
-    float *cu = reinterpret_cast<float *>(dyn + L.cu);
+    const int s0 = blockIdx.y * spp;
+    if (s0 >= S) return;
+    const int s1 = min(S, s0 + spp), ns = s1 - s0;
+    const int sf = s0 > 0 ? s0 - 1 : 0;  // first slot whose ids are staged
+    const int nid = s1 - sf;
+    int64_t *ids = reinterpret_cast<int64_t *>(dyn + L.ids);  // [nid][K]: slot sf + i
+    float *cu = reinterpret_cast<float *>(dyn + L.cu);        // [ns][K]: slot s0 + i
     float *uni = reinterpret_cast<float *>(dyn + L.uni);
     float *gs = reinterpret_cast<float *>(dyn + L.gs);
     uint8_t *brow = dyn + L.brow;
     uint8_t *arow = dyn + L.arow;
-    float *lat = reinterpret_cast<float *>(dyn + L.lat);
-    float2 *stat = reinterpret_cast<float2 *>(dyn + L.stat);   // (max of e/T, sum of exp) per row
-    int32_t *nxt = reinterpret_cast<int32_t *>(dyn + L.nxt);
-    int32_t *path = reinterpret_cast<int32_t *>(dyn + L.path);
     const int64_t row0 = (int64_t)b * S;
     const T *A = static_cast<const T *>(p.A);
     const T *B = static_cast<const T *>(p.B);
 
     // ---- prologue
     bool bad = false;
-    for (int t = tid; t < S * K; t += kLatThreads) {
-        const int64_t c = p.cand[row0 * K + t];
+    for (int t = tid; t < nid * K; t += kRowThreads) {
+        const int64_t c = p.cand[(row0 + sf) * K + t];
         bad |= !id_ok(c, p.table_rows);
         ids[t] = c;
-        cu[t] = p.cand_u[row0 * K + t];
     }
-    for (int t = tid; t < S; t += kLatThreads) uni[t] = p.uniforms[row0 + t];
+    for (int t = tid; t < ns * K; t += kRowThreads) cu[t] = p.cand_u[(row0 + s0) * K + t];
+    for (int t = tid; t < ns; t += kRowThreads) uni[t] = p.uniforms[row0 + s0 + t];
     {
-        const float4 *g4 = reinterpret_cast<const float4 *>(p.g + row0 * R);
+        const float4 *g4 = reinterpret_cast<const float4 *>(p.g + (row0 + s0) * R);
         const int64_t stride4 = p.split_stride / 4;
         float4 *gs4 = reinterpret_cast<float4 *>(gs);
-        for (int t = tid; t < S * R / 4; t += kLatThreads) {
+        for (int t = tid; t < ns * R / 4; t += kRowThreads) {
             float4 acc = g4[t];
             for (int ks = 1; ks < p.k_splits; ++ks) {
                 const float4 v = g4[ks * stride4 + t];
@@ -474,21 +499,25 @@ __global__ void __launch_bounds__(kLatThreads) walk_lattice_kernel(const WalkPar
     bad |= !id_ok(anchor, p.table_rows);
     if (__syncthreads_or(bad) && tid == 0 && p.err) atomicOr(p.err, DFLASH2_DEVERR_ID_RANGE);
 
-    // ---- gather the rows of the whole request (16-byte copies, zero rows for bad ids)
+    // ---- gather the rows of the range (16-byte copies, zero rows for bad ids):
+    // B row (ls, kk) = candidate kk of slot s0 + ls; A row (ls, kp) = predecessor
+    // kp of that slot (slot 0: the anchor, as row (0, 0))
     const int chunks = R * (int)sizeof(T) / 16;
-    const int n_b = S * K, n_a = 1 + (S - 1) * K;
-    for (int t = tid; t < (n_b + n_a) * chunks; t += kLatThreads) {
+    const int n_rows = ns * K;
+    for (int t = tid; t < 2 * n_rows * chunks; t += kRowThreads) {
         const int r = t / chunks;
         const int ch = t - r * chunks;
-        if (r < n_b) {
-            const int s = r / K, kk = r - s * K;
-            const int64_t c = ids[r];
+        if (r < n_rows) {
+            const int ls = r / K, kk = r - ls * K;
+            const int64_t c = ids[(s0 + ls - sf) * K + kk];
             const bool ok = id_ok(c, p.table_rows);
-            cp_async16(brow + (size_t)s * L.b_slot + (size_t)kk * L.b_stride + ch * 16,
+            cp_async16(brow + (size_t)ls * L.b_slot + (size_t)kk * L.b_stride + ch * 16,
                        reinterpret_cast<const uint8_t *>(ok ? B + c * R : B) + ch * 16, ok);
         } else {
-            const int ar = r - n_b;
-            const int64_t c = ar == 0 ? anchor : ids[ar - 1];  // row 1 + (s-1)K + kp = ids[(s-1)K + kp]
+            const int ar = r - n_rows;
+            const int ls = ar / K, kp = ar - ls * K;
+            const int s = s0 + ls;
+            const int64_t c = s == 0 ? (kp == 0 ? anchor : -1) : ids[(s - 1 - sf) * K + kp];
             const bool ok = id_ok(c, p.table_rows);
             cp_async16(arow + (size_t)ar * L.a_stride + ch * 16,
                        reinterpret_cast<const uint8_t *>(ok ? A + c * R : A) + ch * 16, ok);
@@ -498,116 +527,172 @@ __global__ void __launch_bounds__(kLatThreads) walk_lattice_kernel(const WalkPar
     cp_async_wait<0>();
     __syncthreads();
 
-    // ---- every lattice row: K edges, then the row's draw
+    // ---- every lattice row of the range: K edges, then the row's draw.  The
+    // kLatGroup lanes of a row hold candidates kk = g * KPT + q (q < KPT).
     const bool greedy = p.greedy[b] != 0;
     float temp = p.temps[b];
     if (!(temp >= 1e-5f)) temp = 1e-5f;
     constexpr int VN = 16 / sizeof(T);
-    const int n_rows = 1 + (S - 1) * K;  // slot 0 has the anchor row only
-    for (int pr = tid; pr < n_rows; pr += kLatThreads) {
-        const int s = pr == 0 ? 0 : 1 + (pr - 1) / K;
-        const int kp = pr == 0 ? 0 : (pr - 1) - (s - 1) * K;
-        const uint8_t *ar = arow + (size_t)lat_arow(s, kp, K) * L.a_stride;
-        const uint8_t *bs = brow + (size_t)s * L.b_slot;
-        const float *gsl = gs + (size_t)s * R;
-        float acc[KM];
+    constexpr int KPT = KM / kLatGroup;
+    const int g = tid & (kLatGroup - 1);
+    const int gbase = (tid & 31) & ~(kLatGroup - 1);  // lane of the row's first member
+    for (int base = 0; base < n_rows; base += kRowThreads / kLatGroup) {  // uniform trip count
+        const int r = base + tid / kLatGroup;
+        const int ls = r / K, kp = r - (r / K) * K;
+        const int s = s0 + ls;
+        // slot 0 has the anchor row only
+        const bool active = r < n_rows && !(s == 0 && kp > 0);
+        float acc[KPT];
 #pragma unroll
-        for (int kk = 0; kk < KM; ++kk) acc[kk] = 0.0f;
-        for (int v = 0; v < R / VN; ++v) {
-            float av[VN], w[VN];
-            unpack16<T>(*reinterpret_cast<const uint4 *>(ar + v * 16), av);
+        for (int q = 0; q < KPT; ++q) acc[q] = 0.0f;
+        if (active) {
+            const uint8_t *ar = arow + (size_t)r * L.a_stride;
+            const uint8_t *bs = brow + (size_t)ls * L.b_slot;
+            const float *gsl = gs + (size_t)ls * R;
+            for (int v = 0; v < R / VN; ++v) {
+                float av[VN], w[VN];
+                unpack16<T>(*reinterpret_cast<const uint4 *>(ar + v * 16), av);
 #pragma unroll
-            for (int e = 0; e < VN; ++e) w[e] = av[e] * gsl[v * VN + e];
+                for (int e = 0; e < VN; ++e) w[e] = av[e] * gsl[v * VN + e];
 #pragma unroll
-            for (int kk = 0; kk < KM; ++kk) {
-                if (kk < K) {
-                    float bv[VN];
-                    unpack16<T>(*reinterpret_cast<const uint4 *>(bs + (size_t)kk * L.b_stride + v * 16), bv);
+                for (int q = 0; q < KPT; ++q) {
+                    const int kk = g * KPT + q;
+                    if (kk < K) {
+                        float bv[VN];
+                        unpack16<T>(*reinterpret_cast<const uint4 *>(bs + (size_t)kk * L.b_stride + v * 16), bv);
 #pragma unroll
-                    for (int e = 0; e < VN; ++e) acc[kk] = fmaf(w[e], bv[e], acc[kk]);
-                }
-            }
-        }
-        float *lrow = lat + ((size_t)s * K + kp) * K;
-        int index = 0;
-        if (greedy) {
-            float best = 0.0f;
-#pragma unroll
-            for (int kk = 0; kk < KM; ++kk) {
-                if (kk < K) {
-                    const float e = acc[kk] + cu[s * K + kk];
-                    lrow[kk] = e;
-                    if (kk == 0 || e > best) {
-                        best = e;
-                        index = kk;
+                        for (int e = 0; e < VN; ++e) acc[q] = fmaf(w[e], bv[e], acc[q]);
                     }
                 }
             }
+        }
+        const int64_t lrow_i = ((row0 + s) * K + kp);  // this row's index in the workspace
+        float ev[KPT];
+#pragma unroll
+        for (int q = 0; q < KPT; ++q) {
+            const int kk = g * KPT + q;
+            ev[q] = (active && kk < K) ? acc[q] + cu[ls * K + kk] : -INFINITY;
+            if (active && kk < K) ws.lat[lrow_i * K + kk] = ev[q];
+        }
+        int index = 0;
+        if (greedy) {
+            // first maximum in candidate order: per lane, then across the row's lanes
+            float best = -INFINITY;
+            int bi = K;
+#pragma unroll
+            for (int q = 0; q < KPT; ++q) {
+                const int kk = g * KPT + q;
+                if (kk < K && (bi == K || ev[q] > best)) {
+                    best = ev[q];
+                    bi = kk;
+                }
+            }
+#pragma unroll
+            for (int o = 1; o < kLatGroup; o <<= 1) {
+                const float b2 = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+                const int i2 = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+                if (i2 < K && (bi == K || b2 > best || (b2 == best && i2 < bi))) {
+                    best = b2;
+                    bi = i2;
+                }
+            }
+            index = bi;
         } else {
+            float x[KPT];
             float mx = -INFINITY;
 #pragma unroll
-            for (int kk = 0; kk < KM; ++kk) {
-                if (kk < K) {
-                    const float e = acc[kk] + cu[s * K + kk];
-                    lrow[kk] = e;
-                    acc[kk] = e / temp;
-                    mx = fmaxf(mx, acc[kk]);
-                }
+            for (int q = 0; q < KPT; ++q) {
+                const int kk = g * KPT + q;
+                x[q] = kk < K ? ev[q] / temp : -INFINITY;
+                mx = fmaxf(mx, x[q]);
             }
-            float total = 0.0f;
 #pragma unroll
-            for (int kk = 0; kk < KM; ++kk) {
-                if (kk < K) {
-                    acc[kk] = expf(acc[kk] - mx);
-                    total += acc[kk];
+            for (int o = 1; o < kLatGroup; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+#pragma unroll
+            for (int q = 0; q < KPT; ++q) x[q] = g * KPT + q < K ? expf(x[q] - mx) : 0.0f;
+            // total = the K terms summed in candidate order, lane after lane
+            float run = 0.0f, prev = 0.0f;
+#pragma unroll
+            for (int h = 0; h < kLatGroup; ++h) {
+                if (g == h) {
+                    run = prev;
+#pragma unroll
+                    for (int q = 0; q < KPT; ++q)
+                        if (g * KPT + q < K) run += x[q];
                 }
+                prev = __shfl_sync(0xFFFFFFFFu, run, gbase + h);
             }
-            const float u = uni[s];
+            const float total = prev;
+            const float u = uni[ls < ns ? ls : 0];
+            // cdf_k = sequential prefix of x_k / total; count of u >= cdf_k
             float cdf = 0.0f;
             int count = 0;
+            prev = 0.0f;
 #pragma unroll
-            for (int kk = 0; kk < KM; ++kk) {
-                if (kk < K) {
-                    cdf += acc[kk] / total;
-                    count += (u >= cdf) ? 1 : 0;
+            for (int h = 0; h < kLatGroup; ++h) {
+                if (g == h) {
+                    cdf = prev;
+#pragma unroll
+                    for (int q = 0; q < KPT; ++q) {
+                        if (g * KPT + q < K) {
+                            cdf += x[q] / total;
+                            count += (u >= cdf) ? 1 : 0;
+                        }
+                    }
                 }
+                prev = __shfl_sync(0xFFFFFFFFu, cdf, gbase + h);
             }
+#pragma unroll
+            for (int o = 1; o < kLatGroup; o <<= 1) count += __shfl_xor_sync(0xFFFFFFFFu, count, o);
             index = count < K - 1 ? count : K - 1;
-            stat[(size_t)s * K + kp] = make_float2(mx, total);
+            if (active && g == 0) ws.stat[lrow_i] = make_float2(mx, total);
         }
-        nxt[(size_t)s * K + kp] = index;
+        if (active && g == 0) ws.nxt[lrow_i] = index;
     }
-    __syncthreads();
+}
 
-    // ---- the walk: follow the chosen index slot by slot
+__global__ void __launch_bounds__(kChaseThreads)
+    walk_chase_kernel(const WalkParams p, LatticeWs ws) {
+    grid_dep_wait();
+    extern __shared__ __align__(16) int32_t chase_smem[];
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int S = p.slots, K = p.k;
+    int32_t *nxt = chase_smem;       // [S][K]
+    int32_t *path = chase_smem + S * K;
+    const int64_t row0 = (int64_t)b * S;
+    for (int t = tid; t < S * K; t += kChaseThreads) nxt[t] = ws.nxt[row0 * K + t];
+    __syncthreads();
+    // the walk: follow the drawn index slot by slot (slot 0 from the anchor row)
     if (tid == 0) {
         int prev = 0;
         for (int s = 0; s < S; ++s) {
-            prev = nxt[(size_t)s * K + prev];
+            prev = nxt[s * K + prev];
             path[s] = prev;
         }
     }
     __syncthreads();
-
-    // ---- outputs of the walked path
-    for (int t = tid; t < S * K; t += kLatThreads) {
+    const bool greedy = p.greedy[b] != 0;
+    float temp = p.temps[b];
+    if (!(temp >= 1e-5f)) temp = 1e-5f;
+    for (int t = tid; t < S * K; t += kChaseThreads) {
         const int s = t / K, kk = t - s * K;
         const int kp = s == 0 ? 0 : path[s - 1];
-        const float e = lat[((size_t)s * K + kp) * K + kk];
+        const int64_t lrow_i = (row0 + s) * K + kp;
+        const float e = ws.lat[lrow_i * K + kk];
         float qv;
         if (greedy) {
             qv = kk == path[s] ? 1.0f : 0.0f;
         } else {
-            const float2 st = stat[(size_t)s * K + kp];
+            const float2 st = ws.stat[lrow_i];
             qv = expf(e / temp - st.x) / st.y;
         }
         p.q[(row0 + s) * K + kk] = qv;
         if (p.path_scores) p.path_scores[(row0 + s) * K + kk] = e;
     }
-    for (int s = tid; s < S; s += kLatThreads) p.tokens[row0 + s] = ids[(size_t)s * K + path[s]];
+    for (int s = tid; s < S; s += kChaseThreads) p.tokens[row0 + s] = p.cand[(row0 + s) * K + path[s]];
 }
 
-// fp32 projection on CUDA cores: one CTA per row, one warp per output column.
 __global__ void __launch_bounds__(128)
     project_f32_kernel(const float *__restrict__ h, const float *__restrict__ proj, int hidden,
                        int rank, float *g) {
@@ -639,6 +724,14 @@ inline void proj_tiling(int64_t rows, int hidden, int *bn, int *k_splits) {
     *k_splits = (int)ks;
 }
 
+// Projection partials the workspace reserves (the tiling's split count before
+// the GEMM launcher trims it; 1 for fp32).
+inline int ksplits_ws(int64_t rows, int hidden, int32_t dtype) {
+    int bn = 32, ks = 1;
+    if (dtype == DFLASH2_BF16) proj_tiling(rows, hidden, &bn, &ks);
+    return ks;
+}
+
 bool g_walk_attr[64];
 
 }  // namespace
@@ -647,12 +740,14 @@ bool g_walk_attr[64];
 using namespace dflash2;
 
 extern "C" size_t dflash2_selector_walk_workspace_size(int32_t batch, int32_t slots, int32_t hidden,
-                                                       int32_t rank, int32_t dtype) {
-    if (batch <= 0 || slots <= 0 || hidden <= 0 || rank <= 0) return 0;
+                                                       int32_t rank, int32_t top_k, int32_t dtype) {
+    if (batch <= 0 || slots <= 0 || hidden <= 0 || rank <= 0 || top_k <= 0) return 0;
     const int64_t rows = (int64_t)batch * slots;
-    int bn = 32, ks = 1;
-    if (dtype == DFLASH2_BF16) proj_tiling(rows, hidden, &bn, &ks);
-    return (size_t)ks * rows * rank * sizeof(float);
+    const size_t partials = (size_t)ksplits_ws(rows, hidden, dtype) * rows * rank * sizeof(float);
+    if (top_k > kLatticeMaxK) return partials;
+    size_t o_lat, o_stat, o_nxt, o_end;
+    lattice_ws_layout(rows, top_k, partials, &o_lat, &o_stat, &o_nxt, &o_end);
+    return o_end;
 }
 
 extern "C" dflash2_status dflash2_selector_walk(
@@ -672,7 +767,8 @@ extern "C" dflash2_status dflash2_selector_walk(
     if (!h || !proj || !A || !B || !anchor_ids || !cand_ids || !cand_u || !temperatures || !greedy ||
         !uniforms || !tokens || !q)
         return DFLASH2_ERR_INVALID_ARG;
-    const size_t need = dflash2_selector_walk_workspace_size(batch, slots, hidden, rank, dtype);
+    const size_t need =
+        dflash2_selector_walk_workspace_size(batch, slots, hidden, rank, top_k, dtype);
     if (!workspace || ws_bytes < need) return DFLASH2_ERR_WORKSPACE;
     if (!aligned16(A) || !aligned16(B) || reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
         return DFLASH2_ERR_MISALIGNED;
@@ -688,10 +784,16 @@ extern "C" dflash2_status dflash2_selector_walk(
         const int per = (num_kb + ksplits - 1) / ksplits;
         ksplits = (num_kb + per - 1) / per;  // the count the GEMM launcher keeps
     }
-    // Lattice mode: every slot's K x K edges and draws in parallel, one CTA
-    // per request, when the request's rows and lattice fit in shared memory.
-    const LatLayout LL = lat_layout(slots, top_k, rank, esz, ksplits);
-    const bool lattice = top_k <= 32 && LL.total <= kWalkSmemBytes;
+    // Lattice mode (top_k <= 32): the request's slots in parts of spp slots,
+    // enough parts that the batch covers the SMs, when a part's rows fit in
+    // shared memory; the lattice itself lives in the workspace.
+    int parts = (int)((di.sm_count + batch - 1) / batch);
+    if (parts > slots) parts = slots;
+    if (parts < 1) parts = 1;
+    const int spp = (slots + parts - 1) / parts;
+    parts = (slots + spp - 1) / spp;
+    const RowsLayout RL = rows_layout(spp, top_k, rank, esz);
+    const bool lattice = top_k <= kLatticeMaxK && RL.total <= kWalkSmemBytes;
     // One warp per request.  Among the shared-memory layouts that fit, take
     // the fewest waves of CTAs, then A-row prefetch, then the deepest
     // prefetch ring (every slot in flight at most).
@@ -796,7 +898,7 @@ extern "C" dflash2_status dflash2_selector_walk(
 #undef DFLASH2_WALK_ATTR
 #define DFLASH2_LAT_ATTR(T_, KM_)                                                               \
     if (e == cudaSuccess)                                                                      \
-        e = cudaFuncSetAttribute(walk_lattice_kernel<T_, KM_>,                                 \
+        e = cudaFuncSetAttribute(walk_rows_kernel<T_, KM_>,                                    \
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
         DFLASH2_LAT_ATTR(__nv_bfloat16, 8); DFLASH2_LAT_ATTR(__nv_bfloat16, 16);
         DFLASH2_LAT_ATTR(__nv_bfloat16, 32); DFLASH2_LAT_ATTR(float, 8);
@@ -810,9 +912,18 @@ extern "C" dflash2_status dflash2_selector_walk(
     }
     wp.batch = batch;
     if (lattice) {
+        LatticeWs lw;
+        size_t o_lat, o_stat, o_nxt, o_end;
+        lattice_ws_layout(rows, top_k, (size_t)ksplits_ws(rows, hidden, dtype) * rows * rank * 4,
+                          &o_lat, &o_stat, &o_nxt, &o_end);
+        uint8_t *wsb = static_cast<uint8_t *>(workspace);
+        lw.lat = reinterpret_cast<float *>(wsb + o_lat);
+        lw.stat = reinterpret_cast<float2 *>(wsb + o_stat);
+        lw.nxt = reinterpret_cast<int32_t *>(wsb + o_nxt);
         const int km = top_k <= 8 ? 8 : (top_k <= 16 ? 16 : 32);
+        const dim3 rgrid((unsigned)batch, (unsigned)parts);
 #define DFLASH2_LAT_LAUNCH(T_, KM_) \
-    launch_k(walk_lattice_kernel<T_, KM_>, (unsigned)batch, kLatThreads, LL.total, st, wp, LL)
+    launch_k(walk_rows_kernel<T_, KM_>, rgrid, kRowThreads, RL.total, st, wp, RL, spp, lw)
         if (dtype == DFLASH2_BF16) {
             if (km == 8) DFLASH2_LAT_LAUNCH(__nv_bfloat16, 8);
             else if (km == 16) DFLASH2_LAT_LAUNCH(__nv_bfloat16, 16);
@@ -823,6 +934,10 @@ extern "C" dflash2_status dflash2_selector_walk(
             else DFLASH2_LAT_LAUNCH(float, 32);
         }
 #undef DFLASH2_LAT_LAUNCH
+        s = launch_status();
+        if (s != DFLASH2_OK) return s;
+        launch_k(walk_chase_kernel, (unsigned)batch, kChaseThreads,
+                 (size_t)(slots * top_k + slots) * sizeof(int32_t), st, wp, lw);
         return launch_status();
     }
     wp.bulk_ids = ((int64_t)slots * top_k) % 4 == 0 && aligned16(cand_ids) && aligned16(cand_u);

@@ -19,9 +19,9 @@ namespace dflash2 {
 namespace {
 
 // Upper bound of the scratch this entry point can use.  The walk's scratch
-// holds the hidden-split partial projections, k_splits x rows x rank fp32
-// values; 4 MiB covers, for example, 480 rows at rank 64 with five splits
-// (0.6 MiB) or 1408 rows at rank 64 with two splits (0.7 MiB).
+// holds the hidden-split partial projections (k_splits x rows x rank fp32)
+// and, for top_k <= 32, the lattice (rows x top_k x (top_k + 3) x 4 bytes);
+// 4 MiB covers, for example, 480 rows at rank 64 and top_k 16 (1.2 MiB).
 constexpr size_t kNoAllocScratchBytes = 4u << 20;
 
 static __device__ __align__(256) unsigned char g_walk_scratch[kNoAllocScratchBytes];
@@ -64,7 +64,8 @@ extern "C" dflash2_status dflash2_selector_walk_noalloc(
     using namespace dflash2;
     // The shapes decide how much scratch the walk needs; reject what does not
     // fit before touching the device.
-    const size_t need = dflash2_selector_walk_workspace_size(batch, slots, hidden, rank, dtype);
+    const size_t need =
+        dflash2_selector_walk_workspace_size(batch, slots, hidden, rank, top_k, dtype);
     if (need > kNoAllocScratchBytes) return DFLASH2_ERR_WORKSPACE;
     void *scratch = nullptr;
     const dflash2_status s = scratch_address(&scratch);

@@ -29,7 +29,7 @@ DEVERR_ID_RANGE = 0x1
 DEVERR_TIMEOUT = 0x2
 DEVERR_SHORT = 0x4
 DEVINFO_TOPK_FALLBACK = 0x100
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 # Every symbol include/dflash2.h declares.
 EXPORTS = (
@@ -76,7 +76,7 @@ def library():
         lib.dflash2_unary_topk.argtypes = [P, P, i64, i32, i64, i64, f32, f32, i32, i32, P, P, P,
                                            sz, P, P]
         lib.dflash2_unary_topk.restype = i32
-        lib.dflash2_selector_walk_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        lib.dflash2_selector_walk_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.dflash2_selector_walk_workspace_size.restype = sz
         lib.dflash2_selector_walk.argtypes = [P, P, P, P, i64, P, P, P, P, P, P, i32, i32, i32,
                                               i32, i32, i32, P, P, P, P, sz, P, P]
@@ -194,9 +194,9 @@ def unary_topk(h, lm_head, target_vocab: int, mult: float, cap: float, top_k: in
     return cand_ids, cand_u, err
 
 
-def selector_walk_workspace_size(batch: int, slots: int, hidden: int, rank: int,
+def selector_walk_workspace_size(batch: int, slots: int, hidden: int, rank: int, top_k: int,
                                  dtype_code: int) -> int:
-    return int(library().dflash2_selector_walk_workspace_size(batch, slots, hidden, rank,
+    return int(library().dflash2_selector_walk_workspace_size(batch, slots, hidden, rank, top_k,
                                                               dtype_code))
 
 
@@ -226,8 +226,9 @@ def selector_walk(h, proj, A, B, anchor_ids, cand_ids, cand_u, temperatures, gre
     if path_scores is None and with_path_scores:
         path_scores = torch.empty((batch, slots, top_k), dtype=torch.float32, device=dev)
     if workspace is None:
-        workspace = torch.empty(max(1, selector_walk_workspace_size(batch, slots, hidden, rank, code)),
-                                dtype=torch.uint8, device=dev)
+        workspace = torch.empty(
+            max(1, selector_walk_workspace_size(batch, slots, hidden, rank, top_k, code)),
+            dtype=torch.uint8, device=dev)
     if err is None:
         err = torch.zeros(1, dtype=torch.int32, device=dev)
     _check("dflash2_selector_walk", library().dflash2_selector_walk(
@@ -420,7 +421,8 @@ class ProposalBuffers:
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         self.ws_topk = torch.empty(max(1, unary_topk_workspace_size(w.rows, w.draft_vocab, w.top_k, code)),
                                    dtype=torch.uint8, device=device)
-        self.ws_walk = torch.empty(max(1, selector_walk_workspace_size(w.batch, w.slots, w.hidden, w.rank, code)),
+        self.ws_walk = torch.empty(max(1, selector_walk_workspace_size(w.batch, w.slots, w.hidden,
+                                                                       w.rank, w.top_k, code)),
                                    dtype=torch.uint8, device=device)
 
 

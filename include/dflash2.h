@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define DFLASH2_ABI_VERSION 1
+#define DFLASH2_ABI_VERSION 2
 
 typedef enum {
     DFLASH2_OK = 0,
@@ -162,7 +162,10 @@ dflash2_status dflash2_unary_topk(const void *h, const void *lm_head, int64_t ro
  * tokens        device int64 [batch, slots]; q device float [batch, slots, top_k].
  * path_scores   device float [batch, slots, top_k] or NULL: the edges e[k] of the
  *               lattice row the walk actually read at each slot.
- * workspace     device, ws_bytes >= dflash2_selector_walk_workspace_size(...).
+ * workspace     device, 16-byte aligned, ws_bytes >=
+ *               dflash2_selector_walk_workspace_size(batch, slots, hidden, rank,
+ *               top_k, dtype): the projection partials and, for top_k <= 32, the
+ *               lattice of every request (edges, row statistics, draws).
  * Arithmetic: g in fp32 (bf16: tcgen05 GEMM; fp32: CUDA-core FMA), edges,
  *             softmax (expf) and the running sum in fp32.
  * Errors:     top_k < 1 or > 128, rank < 1 or > 256, rank % 8 != 0 (bf16) or
@@ -171,7 +174,7 @@ dflash2_status dflash2_unary_topk(const void *h, const void *lm_head, int64_t ro
  *             and uses a zero table row.
  */
 size_t dflash2_selector_walk_workspace_size(int32_t batch, int32_t slots, int32_t hidden,
-                                            int32_t rank, int32_t dtype);
+                                            int32_t rank, int32_t top_k, int32_t dtype);
 dflash2_status dflash2_selector_walk(const void *h, const void *proj, const void *A,
                                      const void *B, int64_t table_rows,
                                      const int64_t *anchor_ids, const int64_t *cand_ids,

@@ -52,8 +52,8 @@ def test_noalloc_walk_matches_the_workspace_walk_twice(name, scale):
 
 def test_noalloc_walk_refuses_shapes_beyond_its_scratch():
     dev = torch.device("cuda:0")
-    # 1024 requests x 15 slots x rank 256 in bf16 need more than 4 MiB of partials
-    need = dflash2.selector_walk_workspace_size(1024, 15, 4096, 256, dflash2.BF16)
+    # 1024 requests x 15 slots x rank 256 in bf16 need more than 4 MiB of scratch
+    need = dflash2.selector_walk_workspace_size(1024, 15, 4096, 256, 16, dflash2.BF16)
     assert need > dflash2.NOALLOC_SCRATCH_BYTES
     lib = dflash2.library()
     status = lib.dflash2_selector_walk_noalloc(
