@@ -511,12 +511,15 @@ def run_gpu(args, w):
         ms, e2e = reduce_max_over_ranks([ms, e2e], device=dev)
 
     # conv, unary (pilot GEMM, pilot select, filter GEMM, finalize), uniforms,
-    # walk (projection + walk), d2t
-    launches_per_step = 1 + 4 + 1 + 2 + 1
+    # walk (projection, then rows + chase in lattice mode, top_k <= 32, or the
+    # path-mode walk), d2t
+    walk_launches = 3 if w.top_k <= 32 else 2
+    unary_launches = 4
     if w.dtype == "f32":
-        launches_per_step = 1 + 1 + 1 + 2 + 1
-    elif (w.draft_vocab + 255) // 256 <= 16:  # the pilot covers the vocab: no filter pass
-        launches_per_step = 1 + 3 + 1 + 2 + 1
+        unary_launches = 1
+    elif (w.draft_vocab + 255) // 256 <= 8:  # the pilot covers the vocab: no filter pass
+        unary_launches = 3
+    launches_per_step = 1 + unary_launches + 1 + walk_launches + 1
 
     if rank != 0:
         if world > 1:
