@@ -2,8 +2,9 @@
 
 One step = one pass of the whole hot path over one batch of synthetic input:
 grouped conv, unary candidates (lm_head GEMM + transform + padded mask +
-top-K), selector walk (projection + edges + walk) and d2t remap, all through
-the C ABI on one stream, replayed from one captured CUDA graph.
+top-K), selector walk (projection + edges + walk) and d2t remap, through the
+C ABI (dflash2.proposal_step, the input-only work on a second stream beside
+the top-K), replayed from one captured CUDA graph.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                     [--workload NAME]
@@ -285,29 +286,31 @@ def run_gpu(args, w):
     uniforms = t["uniforms"].view(-1)
 
     def step(record: bool, t=t):
-        if record:
-            ev[0].record(stream)
+        if not record:
+            # the timed step: the public API, the input-only work (uniforms,
+            # conv, selector projection) on a second stream beside the top-K
+            dflash2.proposal_step(w, t, bufs, stream=stream, rng=(w.seed, rng_counter))
+            return
+        # the staged step: the same launches on one stream, with events
+        # between the stages
+        ev[0].record(stream)
         dflash2.grouped_conv(t["x"], t["base"], t["delta"], w.block_size, w.group_size, w.taps,
                              out=bufs.conv_out, stream=stream)
-        if record:
-            ev[1].record(stream)
+        ev[1].record(stream)
         dflash2.unary_topk(t["h"], t["lm_head"], w.target_vocab, w.mult, w.cap, w.top_k,
                            cand_ids=bufs.cand_ids, cand_u=bufs.cand_u, workspace=bufs.ws_topk,
                            err=bufs.err, stream=stream)
-        if record:
-            ev[2].record(stream)
+        ev[2].record(stream)
         dflash2.philox_uniforms(w.seed, w.rows, out=uniforms, counter=rng_counter, stream=stream)
         dflash2.selector_walk(t["h"], t["proj"], t["A"], t["B"], t["anchors"],
                               bufs.cand_ids.view(w.batch, w.slots, w.top_k),
                               bufs.cand_u.view(w.batch, w.slots, w.top_k), t["temperatures"],
                               t["greedy"], t["uniforms"], tokens=bufs.tokens, q=bufs.q,
                               workspace=bufs.ws_walk, err=bufs.err, stream=stream)
-        if record:
-            ev[3].record(stream)
+        ev[3].record(stream)
         dflash2.d2t_remap(bufs.tokens, t.get("d2t"), w.draft_vocab, w.target_vocab,
                           out=bufs.target_ids, err=bufs.err, stream=stream)
-        if record:
-            ev[4].record(stream)
+        ev[4].record(stream)
 
     # capture one step into a graph (stage events cannot be timed inside a graph)
     with torch.cuda.stream(stream):

@@ -20,11 +20,21 @@ namespace dflash2 {
 // Launches with programmatic stream serialization: a kernel of this library
 // may be scheduled while the kernel before it on the stream drains (its launch
 // latency and on-chip prologue overlap the previous kernel's tail).  Every
-// kernel therefore starts with grid_dep_wait() before it touches global
-// memory, which returns once the previous grid has completed and its writes
-// are visible; so the stream order of the data stays exactly as without it.
+// kernel therefore calls grid_dep_wait() before it touches global memory that
+// an earlier kernel may write, which returns once the previous grid has
+// completed and its writes are visible; so the stream order of the data stays
+// exactly as without it.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel on the stream be scheduled before this one ends: it may
+// start once every CTA of this grid has executed this or exited.  It makes
+// nothing visible to that kernel (whose grid_dep_wait() still waits for this
+// grid to complete), so before its own grid_dep_wait() the next kernel may
+// read only data that was complete before this kernel started.
+__device__ __forceinline__ void grid_dep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,

@@ -455,7 +455,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     __syncthreads();
     cluster_sync();  // the peer's barriers exist before anyone signals them
     tc_fence_after();
-    grid_dep_wait();  // barriers and TMEM are set up; now the inputs
+    // Barriers and TMEM are set up; now the inputs.  The filter pass follows
+    // the pilot select, which lets it start while the select runs: its loads
+    // and MMAs read only the weights and the tokens, complete before the pilot
+    // pass (and so the select) began, so only its epilogue (thresholds in,
+    // candidates out) waits for the select.  (Letting the select, and so the
+    // filter, start during the pilot pass was slower: the early filter CTAs
+    // took bandwidth from the pilot.)
+    if (p.mode != kGemmFilter || warp >= 2) grid_dep_wait();
     const uint32_t tmem = tmem_slot;
     const int total = p.pass_tiles * p.n_tok_tiles;
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;

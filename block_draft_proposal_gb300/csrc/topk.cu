@@ -360,6 +360,10 @@ __global__ void __launch_bounds__(kSelThreads)
     pilot_select_kernel(const float *__restrict__ pilot_z, int n_pilot, int pilot_stride, int unit,
                         int k, float mult, float cap, uint64_t *theta, float *theta_pre,
                         uint32_t *cnt, uint64_t *cand, int cand_cap) {
+    // The filter pass after this kernel reads only its inputs until its
+    // epilogue waits for this grid, so it may start now (this kernel starts
+    // only once the pilot pass, which waited for the inputs, has ended).
+    grid_dep_launch();
     grid_dep_wait();
     __shared__ SelectShared sh;
     __shared__ float fsort[kSelThreads];

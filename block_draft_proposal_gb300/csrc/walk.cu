@@ -750,40 +750,96 @@ extern "C" size_t dflash2_selector_walk_workspace_size(int32_t batch, int32_t sl
     return o_end;
 }
 
-extern "C" dflash2_status dflash2_selector_walk(
-    const void *h, const void *proj, const void *A, const void *B, int64_t table_rows,
-    const int64_t *anchor_ids, const int64_t *cand_ids, const float *cand_u,
-    const float *temperatures, const uint8_t *greedy, const float *uniforms, int32_t batch,
-    int32_t slots, int32_t hidden, int32_t rank, int32_t top_k, int32_t dtype, int64_t *tokens,
-    float *q, float *path_scores, void *workspace, size_t ws_bytes, int32_t *err_word,
-    void *stream) {
+namespace {
+
+// Checks shared by the walk entry points, before any pointer is looked at.
+dflash2_status check_walk_shape(int32_t batch, int32_t slots, int32_t hidden, int32_t rank,
+                                int32_t top_k, int32_t dtype) {
     if (dtype != DFLASH2_F32 && dtype != DFLASH2_BF16) return DFLASH2_ERR_UNSUPPORTED_DTYPE;
     const int rank_mult = dtype == DFLASH2_BF16 ? 8 : 4;
     if (batch < 0 || slots < 0 || hidden <= 0 || rank <= 0 || rank > kMaxRank ||
-        rank % rank_mult != 0 || top_k <= 0 || top_k > kMaxK || table_rows <= 0)
+        rank % rank_mult != 0 || top_k <= 0 || top_k > kMaxK)
         return DFLASH2_ERR_INVALID_ARG;
-    const int esz = dtype == DFLASH2_BF16 ? 2 : 4;
-    if (batch == 0 || slots == 0) return DFLASH2_OK;
-    if (!h || !proj || !A || !B || !anchor_ids || !cand_ids || !cand_u || !temperatures || !greedy ||
-        !uniforms || !tokens || !q)
-        return DFLASH2_ERR_INVALID_ARG;
-    const size_t need =
-        dflash2_selector_walk_workspace_size(batch, slots, hidden, rank, top_k, dtype);
-    if (!workspace || ws_bytes < need) return DFLASH2_ERR_WORKSPACE;
-    if (!aligned16(A) || !aligned16(B) || reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
-        return DFLASH2_ERR_MISALIGNED;
-    DeviceInfo di;
-    dflash2_status s = current_device(&di);
-    if (s != DFLASH2_OK) return s;
-    // projection tiling decides how many partials the walk sums
-    int ksplits = 1;
+    return DFLASH2_OK;
+}
+
+// Projection partials the walk sums: the tiling's split count as the GEMM
+// launcher trims it (every split gets at least one pipeline stage).
+int kept_ksplits(int64_t rows, int hidden, int32_t dtype) {
+    if (dtype != DFLASH2_BF16) return 1;
+    int bn_unused, ks;
+    proj_tiling(rows, hidden, &bn_unused, &ks);
+    const int num_kb = (hidden + kGemmStageK - 1) / kGemmStageK;
+    const int per = (num_kb + ks - 1) / ks;
+    return (num_kb + per - 1) / per;
+}
+
+// Step a5: g = h . proj^T as k-split fp32 partials at the start of the workspace.
+dflash2_status run_projection(const DeviceInfo &di, const void *h, const void *proj, int64_t rows,
+                              int32_t hidden, int32_t rank, int32_t dtype, float *g,
+                              int32_t *err_word, cudaStream_t st) {
     if (dtype == DFLASH2_BF16) {
-        int bn_unused;
-        proj_tiling((int64_t)batch * slots, hidden, &bn_unused, &ksplits);
-        const int num_kb = (hidden + kGemmStageK - 1) / kGemmStageK;
-        const int per = (num_kb + ksplits - 1) / ksplits;
-        ksplits = (num_kb + per - 1) / per;  // the count the GEMM launcher keeps
+        if (hidden % 8 != 0 || !aligned16(h) || !aligned16(proj)) return DFLASH2_ERR_MISALIGNED;
+        int bn, ks;
+        proj_tiling(rows, hidden, &bn, &ks);
+        GemmParams p{};
+        p.rows_w = rank;
+        p.rows_h = (int32_t)rows;
+        p.hidden = hidden;
+        p.mode = kGemmStore;
+        p.bn = bn;
+        p.k_splits = ks;
+        p.out = g;
+        p.ldo = rank;
+        p.split_stride = rows * rank;
+        p.err = err_word;
+        return launch_gemm_tc(di, proj, h, p, st);
     }
+    if ((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(proj)) % 4 != 0)
+        return DFLASH2_ERR_MISALIGNED;
+    launch_k(project_f32_kernel, (unsigned)rows, 128, 0, st, static_cast<const float *>(h),
+             static_cast<const float *>(proj), hidden, rank, g);
+    return launch_status();
+}
+
+dflash2_status set_walk_attributes(const DeviceInfo &di) {
+    if (di.device < 0 || di.device >= 64 || g_walk_attr[di.device]) return DFLASH2_OK;
+    const int bytes = (int)kWalkSmemBytes;
+    cudaError_t e = cudaSuccess;
+#define DFLASH2_WALK_ATTR(T_, PA_, E_)                                                          \
+    if (e == cudaSuccess)                                                                      \
+        e = cudaFuncSetAttribute(walk_kernel<T_, PA_, E_>,                                     \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
+    DFLASH2_WALK_ATTR(__nv_bfloat16, true, 1); DFLASH2_WALK_ATTR(__nv_bfloat16, true, 2);
+    DFLASH2_WALK_ATTR(__nv_bfloat16, true, 4); DFLASH2_WALK_ATTR(__nv_bfloat16, false, 1);
+    DFLASH2_WALK_ATTR(__nv_bfloat16, false, 2); DFLASH2_WALK_ATTR(__nv_bfloat16, false, 4);
+    DFLASH2_WALK_ATTR(float, true, 1); DFLASH2_WALK_ATTR(float, true, 2);
+    DFLASH2_WALK_ATTR(float, true, 4); DFLASH2_WALK_ATTR(float, false, 1);
+    DFLASH2_WALK_ATTR(float, false, 2); DFLASH2_WALK_ATTR(float, false, 4);
+#undef DFLASH2_WALK_ATTR
+#define DFLASH2_LAT_ATTR(T_, KM_)                                                               \
+    if (e == cudaSuccess)                                                                      \
+        e = cudaFuncSetAttribute(walk_rows_kernel<T_, KM_>,                                    \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
+    DFLASH2_LAT_ATTR(__nv_bfloat16, 8); DFLASH2_LAT_ATTR(__nv_bfloat16, 16);
+    DFLASH2_LAT_ATTR(__nv_bfloat16, 32); DFLASH2_LAT_ATTR(float, 8);
+    DFLASH2_LAT_ATTR(float, 16); DFLASH2_LAT_ATTR(float, 32);
+#undef DFLASH2_LAT_ATTR
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return DFLASH2_ERR_CUDA;
+    }
+    g_walk_attr[di.device] = true;
+    return DFLASH2_OK;
+}
+
+// Steps a6-a7 from the projection partials at the start of the workspace.
+dflash2_status run_walk(const DeviceInfo &di, WalkParams wp, int32_t hidden, int32_t dtype,
+                        void *workspace, cudaStream_t st) {
+    const int batch = wp.batch, slots = wp.slots, rank = wp.rank, top_k = wp.k;
+    const int esz = dtype == DFLASH2_BF16 ? 2 : 4;
+    const int64_t rows = (int64_t)batch * slots;
+    const int ksplits = kept_ksplits(rows, hidden, dtype);
     // Lattice mode (top_k <= 32): the request's slots in parts of spp slots,
     // enough parts that the batch covers the SMs, when a part's rows fit in
     // shared memory; the lattice itself lives in the workspace.
@@ -828,89 +884,11 @@ extern "C" dflash2_status dflash2_selector_walk(
             return DFLASH2_ERR_INVALID_ARG;
         prefetch_a = best_pa != 0;
     }
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int64_t rows = (int64_t)batch * slots;
-    float *g = static_cast<float *>(workspace);
-
-    WalkParams wp{};
-    wp.g = g;
+    wp.g = static_cast<const float *>(workspace);
     wp.split_stride = rows * rank;
-    if (dtype == DFLASH2_BF16) {
-        if (hidden % 8 != 0 || !aligned16(h) || !aligned16(proj)) return DFLASH2_ERR_MISALIGNED;
-        int bn, ks;
-        proj_tiling(rows, hidden, &bn, &ks);
-        GemmParams p{};
-        p.rows_w = rank;
-        p.rows_h = (int32_t)rows;
-        p.hidden = hidden;
-        p.mode = kGemmStore;
-        p.bn = bn;
-        p.k_splits = ks;
-        p.out = g;
-        p.ldo = rank;
-        p.split_stride = rows * rank;
-        p.err = err_word;
-        // the launcher may trim k_splits; recompute the count it will use
-        const int num_kb = (hidden + kGemmStageK - 1) / kGemmStageK;
-        const int per = (num_kb + ks - 1) / ks;
-        wp.k_splits = (num_kb + per - 1) / per;
-        s = launch_gemm_tc(di, proj, h, p, st);
-        if (s != DFLASH2_OK) return s;
-    } else {
-        if ((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(proj)) % 4 != 0)
-            return DFLASH2_ERR_MISALIGNED;
-        wp.k_splits = 1;
-        launch_k(project_f32_kernel, (unsigned)rows, 128, 0, st, static_cast<const float *>(h),
-                                                           static_cast<const float *>(proj), hidden,
-                                                           rank, g);
-        s = launch_status();
-        if (s != DFLASH2_OK) return s;
-    }
-    wp.A = A;
-    wp.B = B;
-    wp.table_rows = table_rows;
-    wp.anchors = anchor_ids;
-    wp.cand = cand_ids;
-    wp.cand_u = cand_u;
-    wp.temps = temperatures;
-    wp.greedy = greedy;
-    wp.uniforms = uniforms;
-    wp.slots = slots;
-    wp.rank = rank;
-    wp.k = top_k;
-    wp.tokens = tokens;
-    wp.q = q;
-    wp.path_scores = path_scores;
-    wp.err = err_word;
-    if (di.device >= 0 && di.device < 64 && !g_walk_attr[di.device]) {
-        const int bytes = (int)kWalkSmemBytes;
-        cudaError_t e = cudaSuccess;
-#define DFLASH2_WALK_ATTR(T_, PA_, E_)                                                          \
-    if (e == cudaSuccess)                                                                      \
-        e = cudaFuncSetAttribute(walk_kernel<T_, PA_, E_>,                                     \
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
-        DFLASH2_WALK_ATTR(__nv_bfloat16, true, 1); DFLASH2_WALK_ATTR(__nv_bfloat16, true, 2);
-        DFLASH2_WALK_ATTR(__nv_bfloat16, true, 4); DFLASH2_WALK_ATTR(__nv_bfloat16, false, 1);
-        DFLASH2_WALK_ATTR(__nv_bfloat16, false, 2); DFLASH2_WALK_ATTR(__nv_bfloat16, false, 4);
-        DFLASH2_WALK_ATTR(float, true, 1); DFLASH2_WALK_ATTR(float, true, 2);
-        DFLASH2_WALK_ATTR(float, true, 4); DFLASH2_WALK_ATTR(float, false, 1);
-        DFLASH2_WALK_ATTR(float, false, 2); DFLASH2_WALK_ATTR(float, false, 4);
-#undef DFLASH2_WALK_ATTR
-#define DFLASH2_LAT_ATTR(T_, KM_)                                                               \
-    if (e == cudaSuccess)                                                                      \
-        e = cudaFuncSetAttribute(walk_rows_kernel<T_, KM_>,                                    \
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
-        DFLASH2_LAT_ATTR(__nv_bfloat16, 8); DFLASH2_LAT_ATTR(__nv_bfloat16, 16);
-        DFLASH2_LAT_ATTR(__nv_bfloat16, 32); DFLASH2_LAT_ATTR(float, 8);
-        DFLASH2_LAT_ATTR(float, 16); DFLASH2_LAT_ATTR(float, 32);
-#undef DFLASH2_LAT_ATTR
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            return DFLASH2_ERR_CUDA;
-        }
-        g_walk_attr[di.device] = true;
-    }
-    wp.batch = batch;
+    wp.k_splits = ksplits;
+    dflash2_status s = set_walk_attributes(di);
+    if (s != DFLASH2_OK) return s;
     if (lattice) {
         LatticeWs lw;
         size_t o_lat, o_stat, o_nxt, o_end;
@@ -940,7 +918,7 @@ extern "C" dflash2_status dflash2_selector_walk(
                  (size_t)(slots * top_k + slots) * sizeof(int32_t), st, wp, lw);
         return launch_status();
     }
-    wp.bulk_ids = ((int64_t)slots * top_k) % 4 == 0 && aligned16(cand_ids) && aligned16(cand_u);
+    wp.bulk_ids = ((int64_t)slots * top_k) % 4 == 0 && aligned16(wp.cand) && aligned16(wp.cand_u);
     const unsigned grid = (unsigned)((batch + warps - 1) / warps);
     const size_t smem = L.total * warps;
     const int threads = 32 * warps;
@@ -970,4 +948,116 @@ extern "C" dflash2_status dflash2_selector_walk(
     }
 #undef DFLASH2_WALK_LAUNCH
     return launch_status();
+}
+
+// The walk's parameters from the entry-point arguments (g and the split
+// count are filled by run_walk).
+WalkParams walk_params(const void *A, const void *B, int64_t table_rows, const int64_t *anchor_ids,
+                       const int64_t *cand_ids, const float *cand_u, const float *temperatures,
+                       const uint8_t *greedy, const float *uniforms, int32_t batch, int32_t slots,
+                       int32_t rank, int32_t top_k, int64_t *tokens, float *q, float *path_scores,
+                       int32_t *err_word) {
+    WalkParams wp{};
+    wp.A = A;
+    wp.B = B;
+    wp.table_rows = table_rows;
+    wp.anchors = anchor_ids;
+    wp.cand = cand_ids;
+    wp.cand_u = cand_u;
+    wp.temps = temperatures;
+    wp.greedy = greedy;
+    wp.uniforms = uniforms;
+    wp.batch = batch;
+    wp.slots = slots;
+    wp.rank = rank;
+    wp.k = top_k;
+    wp.tokens = tokens;
+    wp.q = q;
+    wp.path_scores = path_scores;
+    wp.err = err_word;
+    return wp;
+}
+
+}  // namespace
+
+extern "C" dflash2_status dflash2_selector_walk(
+    const void *h, const void *proj, const void *A, const void *B, int64_t table_rows,
+    const int64_t *anchor_ids, const int64_t *cand_ids, const float *cand_u,
+    const float *temperatures, const uint8_t *greedy, const float *uniforms, int32_t batch,
+    int32_t slots, int32_t hidden, int32_t rank, int32_t top_k, int32_t dtype, int64_t *tokens,
+    float *q, float *path_scores, void *workspace, size_t ws_bytes, int32_t *err_word,
+    void *stream) {
+    dflash2_status s = check_walk_shape(batch, slots, hidden, rank, top_k, dtype);
+    if (s != DFLASH2_OK) return s;
+    if (table_rows <= 0) return DFLASH2_ERR_INVALID_ARG;
+    if (batch == 0 || slots == 0) return DFLASH2_OK;
+    if (!h || !proj || !A || !B || !anchor_ids || !cand_ids || !cand_u || !temperatures || !greedy ||
+        !uniforms || !tokens || !q)
+        return DFLASH2_ERR_INVALID_ARG;
+    const size_t need =
+        dflash2_selector_walk_workspace_size(batch, slots, hidden, rank, top_k, dtype);
+    if (!workspace || ws_bytes < need) return DFLASH2_ERR_WORKSPACE;
+    if (!aligned16(A) || !aligned16(B) || reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+        return DFLASH2_ERR_MISALIGNED;
+    DeviceInfo di;
+    s = current_device(&di);
+    if (s != DFLASH2_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    s = run_projection(di, h, proj, (int64_t)batch * slots, hidden, rank, dtype,
+                       static_cast<float *>(workspace), err_word, st);
+    if (s != DFLASH2_OK) return s;
+    return run_walk(di,
+                    walk_params(A, B, table_rows, anchor_ids, cand_ids, cand_u, temperatures,
+                                greedy, uniforms, batch, slots, rank, top_k, tokens, q,
+                                path_scores, err_word),
+                    hidden, dtype, workspace, st);
+}
+
+extern "C" dflash2_status dflash2_selector_project(const void *h, const void *proj, int32_t batch,
+                                                   int32_t slots, int32_t hidden, int32_t rank,
+                                                   int32_t top_k, int32_t dtype, void *workspace,
+                                                   size_t ws_bytes, int32_t *err_word,
+                                                   void *stream) {
+    dflash2_status s = check_walk_shape(batch, slots, hidden, rank, top_k, dtype);
+    if (s != DFLASH2_OK) return s;
+    if (batch == 0 || slots == 0) return DFLASH2_OK;
+    if (!h || !proj) return DFLASH2_ERR_INVALID_ARG;
+    const size_t need =
+        dflash2_selector_walk_workspace_size(batch, slots, hidden, rank, top_k, dtype);
+    if (!workspace || ws_bytes < need) return DFLASH2_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return DFLASH2_ERR_MISALIGNED;
+    DeviceInfo di;
+    s = current_device(&di);
+    if (s != DFLASH2_OK) return s;
+    return run_projection(di, h, proj, (int64_t)batch * slots, hidden, rank, dtype,
+                          static_cast<float *>(workspace), err_word,
+                          static_cast<cudaStream_t>(stream));
+}
+
+extern "C" dflash2_status dflash2_selector_walk_projected(
+    const void *A, const void *B, int64_t table_rows, const int64_t *anchor_ids,
+    const int64_t *cand_ids, const float *cand_u, const float *temperatures, const uint8_t *greedy,
+    const float *uniforms, int32_t batch, int32_t slots, int32_t hidden, int32_t rank,
+    int32_t top_k, int32_t dtype, int64_t *tokens, float *q, float *path_scores, void *workspace,
+    size_t ws_bytes, int32_t *err_word, void *stream) {
+    dflash2_status s = check_walk_shape(batch, slots, hidden, rank, top_k, dtype);
+    if (s != DFLASH2_OK) return s;
+    if (table_rows <= 0) return DFLASH2_ERR_INVALID_ARG;
+    if (batch == 0 || slots == 0) return DFLASH2_OK;
+    if (!A || !B || !anchor_ids || !cand_ids || !cand_u || !temperatures || !greedy || !uniforms ||
+        !tokens || !q)
+        return DFLASH2_ERR_INVALID_ARG;
+    const size_t need =
+        dflash2_selector_walk_workspace_size(batch, slots, hidden, rank, top_k, dtype);
+    if (!workspace || ws_bytes < need) return DFLASH2_ERR_WORKSPACE;
+    if (!aligned16(A) || !aligned16(B) || reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+        return DFLASH2_ERR_MISALIGNED;
+    DeviceInfo di;
+    s = current_device(&di);
+    if (s != DFLASH2_OK) return s;
+    return run_walk(di,
+                    walk_params(A, B, table_rows, anchor_ids, cand_ids, cand_u, temperatures,
+                                greedy, uniforms, batch, slots, rank, top_k, tokens, q,
+                                path_scores, err_word),
+                    hidden, dtype, workspace, static_cast<cudaStream_t>(stream));
 }

@@ -29,7 +29,7 @@ DEVERR_ID_RANGE = 0x1
 DEVERR_TIMEOUT = 0x2
 DEVERR_SHORT = 0x4
 DEVINFO_TOPK_FALLBACK = 0x100
-ABI_VERSION = 2
+ABI_VERSION = 3
 
 # Every symbol include/dflash2.h declares.
 EXPORTS = (
@@ -38,7 +38,7 @@ EXPORTS = (
     "dflash2_unary_topk", "dflash2_selector_walk_workspace_size", "dflash2_selector_walk",
     "dflash2_d2t_remap", "dflash2_selector_walk_noalloc", "dflash2_philox_uniforms",
     "dflash2_conv_prepare", "dflash2_conv_finish", "dflash2_verify_workspace_size",
-    "dflash2_verify",
+    "dflash2_verify", "dflash2_selector_project", "dflash2_selector_walk_projected",
 )
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -97,6 +97,11 @@ def library():
         lib.dflash2_verify.argtypes = [P, i64, P, P, P, P, P, P, i32, i32, i32, i32, P, P, P, sz,
                                        P, P]
         lib.dflash2_verify.restype = i32
+        lib.dflash2_selector_project.argtypes = [P, P, i32, i32, i32, i32, i32, i32, P, sz, P, P]
+        lib.dflash2_selector_project.restype = i32
+        lib.dflash2_selector_walk_projected.argtypes = [P, P, i64, P, P, P, P, P, P, i32, i32, i32,
+                                                        i32, i32, i32, P, P, P, P, sz, P, P]
+        lib.dflash2_selector_walk_projected.restype = i32
         if lib.dflash2_abi_version() != ABI_VERSION:
             raise RuntimeError("libdflash2.so ABI version mismatch; rebuild it")
         _lib = lib
@@ -236,6 +241,61 @@ def selector_walk(h, proj, A, B, anchor_ids, cand_ids, cand_u, temperatures, gre
         _ptr(cand_u), _ptr(temperatures), _ptr(greedy), _ptr(uniforms), batch, slots, hidden,
         rank, top_k, code, _ptr(tokens), _ptr(q), _ptr(path_scores), _ptr(workspace),
         workspace.numel(), _ptr(err), _stream(stream)))
+    return tokens, q, path_scores, err
+
+
+def selector_project(h, proj, batch: int, slots: int, top_k: int, workspace, err=None,
+                     stream=None):
+    """dflash2_selector_project: the projection partials of g = h . proj^T into
+    `workspace` (a selector_walk workspace for the same shapes), for a later
+    selector_walk_projected call ordered after it."""
+    hidden = h.shape[-1]
+    rank = proj.shape[0]
+    code = _dtype_code(h)
+    for t, nm in ((h, "h"), (proj, "proj")):
+        _need(t, nm, h.dtype)
+    if h.numel() != batch * slots * hidden:
+        raise ValueError("h must hold batch * slots rows of hidden")
+    _need(workspace, "workspace", torch.uint8)
+    _check("dflash2_selector_project", library().dflash2_selector_project(
+        _ptr(h), _ptr(proj), batch, slots, hidden, rank, top_k, code, _ptr(workspace),
+        workspace.numel(), _ptr(err), _stream(stream)))
+    return workspace
+
+
+def selector_walk_projected(A, B, anchor_ids, cand_ids, cand_u, temperatures, greedy, uniforms,
+                            hidden: int, workspace, tokens=None, q=None, path_scores=None,
+                            err=None, with_path_scores: bool = False, stream=None):
+    """dflash2_selector_walk_projected: the edges and the walk from the
+    projection a selector_project call left in `workspace`."""
+    batch, slots, top_k = cand_ids.shape
+    rank = A.shape[1]
+    code = _dtype_code(A)
+    dev = A.device
+    _need(A, "A")
+    _need(B, "B", A.dtype)
+    _need(anchor_ids, "anchor_ids", torch.int64, (batch,))
+    _need(cand_ids, "cand_ids", torch.int64)
+    _need(cand_u, "cand_u", torch.float32, (batch, slots, top_k))
+    _need(temperatures, "temperatures", torch.float32, (batch,))
+    _need(greedy, "greedy", torch.uint8, (batch,))
+    _need(uniforms, "uniforms", torch.float32, (batch, slots))
+    _need(workspace, "workspace", torch.uint8)
+    if A.shape != B.shape:
+        raise ValueError("A and B must both be [table_rows, rank]")
+    if tokens is None:
+        tokens = torch.empty((batch, slots), dtype=torch.int64, device=dev)
+    if q is None:
+        q = torch.empty((batch, slots, top_k), dtype=torch.float32, device=dev)
+    if path_scores is None and with_path_scores:
+        path_scores = torch.empty((batch, slots, top_k), dtype=torch.float32, device=dev)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check("dflash2_selector_walk_projected", library().dflash2_selector_walk_projected(
+        _ptr(A), _ptr(B), A.shape[0], _ptr(anchor_ids), _ptr(cand_ids), _ptr(cand_u),
+        _ptr(temperatures), _ptr(greedy), _ptr(uniforms), batch, slots, hidden, rank, top_k, code,
+        _ptr(tokens), _ptr(q), _ptr(path_scores), _ptr(workspace), workspace.numel(), _ptr(err),
+        _stream(stream)))
     return tokens, q, path_scores, err
 
 
@@ -424,36 +484,58 @@ class ProposalBuffers:
         self.ws_walk = torch.empty(max(1, selector_walk_workspace_size(w.batch, w.slots, w.hidden,
                                                                        w.rank, w.top_k, code)),
                                    dtype=torch.uint8, device=device)
+        # the second stream of an overlapped step and the events that fork it
+        # from, and join it back into, the caller's stream
+        self.side_stream = torch.cuda.Stream(device=device)
+        self.fork = torch.cuda.Event()
+        self.join = torch.cuda.Event()
 
 
 def proposal_step(w, t: dict, bufs: ProposalBuffers | None = None, stream=None,
-                  rng=None) -> dict:
+                  rng=None, overlap: bool = True) -> dict:
     """One pass of the hot path: conv, unary candidates, selector walk, d2t remap.
 
     `t` holds the device tensors of synth.make(w) (bf16 tensors as torch.bfloat16).
     With ``rng = (seed, counter)`` the walk's uniforms are drawn on the device
     (dflash2_philox_uniforms, counter advanced on the device) instead of taken
-    from ``t["uniforms"]``.  Returns the output tensors (no synchronisation)."""
+    from ``t["uniforms"]``.  Returns the output tensors (no synchronisation).
+
+    With ``overlap`` the work that needs only the step's inputs (the uniforms,
+    the grouped conv and the selector projection) runs on a second stream,
+    forked from and joined back into `stream` by events, beside the unary
+    top-K; the walk waits for both.  The results are the same either way; the
+    fork and join are captured into a CUDA graph like the launches."""
     dev = t["h"].device
     if bufs is None:
         bufs = ProposalBuffers(w, dev)
+    main = torch.cuda.current_stream(dev) if stream is None else stream
+    side = main
+    if overlap:
+        side = bufs.side_stream
+        bufs.fork.record(main)
+        side.wait_event(bufs.fork)
     uniforms = t.get("uniforms")
     if rng is not None:
         seed, counter = rng
-        philox_uniforms(seed, w.rows, out=bufs.uniforms.view(-1), counter=counter, stream=stream)
+        philox_uniforms(seed, w.rows, out=bufs.uniforms.view(-1), counter=counter, stream=side)
         uniforms = bufs.uniforms
     grouped_conv(t["x"], t["base"], t["delta"], w.block_size, w.group_size, w.taps,
-                 out=bufs.conv_out, stream=stream)
+                 out=bufs.conv_out, stream=side)
+    selector_project(t["h"], t["proj"], w.batch, w.slots, w.top_k, bufs.ws_walk, err=bufs.err,
+                     stream=side)
     unary_topk(t["h"], t["lm_head"], w.target_vocab, w.mult, w.cap, w.top_k,
                cand_ids=bufs.cand_ids, cand_u=bufs.cand_u, workspace=bufs.ws_topk, err=bufs.err,
-               stream=stream)
-    selector_walk(t["h"], t["proj"], t["A"], t["B"], t["anchors"],
-                  bufs.cand_ids.view(w.batch, w.slots, w.top_k),
-                  bufs.cand_u.view(w.batch, w.slots, w.top_k), t["temperatures"], t["greedy"],
-                  uniforms, tokens=bufs.tokens, q=bufs.q, workspace=bufs.ws_walk,
-                  err=bufs.err, stream=stream)
+               stream=main)
+    if overlap:
+        bufs.join.record(side)
+        main.wait_event(bufs.join)
+    selector_walk_projected(t["A"], t["B"], t["anchors"],
+                            bufs.cand_ids.view(w.batch, w.slots, w.top_k),
+                            bufs.cand_u.view(w.batch, w.slots, w.top_k), t["temperatures"],
+                            t["greedy"], uniforms, w.hidden, bufs.ws_walk, tokens=bufs.tokens,
+                            q=bufs.q, err=bufs.err, stream=main)
     d2t_remap(bufs.tokens, t.get("d2t"), w.draft_vocab, w.target_vocab, out=bufs.target_ids,
-              err=bufs.err, stream=stream)
+              err=bufs.err, stream=main)
     return dict(conv_out=bufs.conv_out, cand_ids=bufs.cand_ids, cand_u=bufs.cand_u,
                 tokens=bufs.tokens, q=bufs.q, target_ids=bufs.target_ids, err=bufs.err,
                 uniforms=uniforms)

@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define DFLASH2_ABI_VERSION 2
+#define DFLASH2_ABI_VERSION 3
 
 typedef enum {
     DFLASH2_OK = 0,
@@ -185,6 +185,42 @@ dflash2_status dflash2_selector_walk(const void *h, const void *proj, const void
                                      int64_t *tokens, float *q, float *path_scores,
                                      void *workspace, size_t ws_bytes, int32_t *err_word,
                                      void *stream);
+
+/*
+ * The selector walk in two calls, so that the projection (which needs only h)
+ * can run on another stream while the unary candidates are computed.  The
+ * paper computes project(h) inside build_lattice; splitting it changes no
+ * arithmetic: the two calls together give exactly what dflash2_selector_walk
+ * gives for the same arguments.
+ *
+ * dflash2_selector_project  step a5 alone: writes the fp32 partials of
+ *   g = h . proj^T to the start of `workspace` (the same bytes
+ *   dflash2_selector_walk uses for them).  h, proj, batch, slots, hidden,
+ *   rank, dtype as for dflash2_selector_walk; top_k only sizes the workspace.
+ * dflash2_selector_walk_projected  the edges and the walk from the partials
+ *   a dflash2_selector_project call with the same batch, slots, hidden, rank,
+ *   top_k and dtype left in `workspace`; the other arguments as for
+ *   dflash2_selector_walk.  The caller orders the two calls (same stream, or
+ *   an event); nothing checks that the partials are there.
+ * Both: workspace device, 16-byte aligned, ws_bytes >=
+ *   dflash2_selector_walk_workspace_size(batch, slots, hidden, rank, top_k,
+ *   dtype); the same errors as dflash2_selector_walk for the arguments they
+ *   take.
+ */
+dflash2_status dflash2_selector_project(const void *h, const void *proj, int32_t batch,
+                                        int32_t slots, int32_t hidden, int32_t rank,
+                                        int32_t top_k, int32_t dtype, void *workspace,
+                                        size_t ws_bytes, int32_t *err_word, void *stream);
+dflash2_status dflash2_selector_walk_projected(const void *A, const void *B, int64_t table_rows,
+                                               const int64_t *anchor_ids,
+                                               const int64_t *cand_ids, const float *cand_u,
+                                               const float *temperatures, const uint8_t *greedy,
+                                               const float *uniforms, int32_t batch,
+                                               int32_t slots, int32_t hidden, int32_t rank,
+                                               int32_t top_k, int32_t dtype, int64_t *tokens,
+                                               float *q, float *path_scores, void *workspace,
+                                               size_t ws_bytes, int32_t *err_word,
+                                               void *stream);
 
 /*
  * Selector walk without a workspace argument.  The paper has no counterpart:

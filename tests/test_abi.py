@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.dflash2_abi_version() == 2
+    assert lib.dflash2_abi_version() == 3
     assert lib.dflash2_status_string(0) == b"ok"
     for s in range(1, 7):
         assert lib.dflash2_status_string(s) not in (b"ok", b"unknown status")
@@ -71,6 +71,19 @@ def test_host_validation_rejects_before_any_launch(lib):
                                      null, 0, null, null) == 1
     assert lib.dflash2_selector_walk(*w, 10, *(null,) * 6, 2, 3, 64, 16, 200, 1, null, null, null,
                                      null, 0, null, null) == 1
+    # the split walk: the same shape checks, and a missing workspace, before any launch
+    assert lib.dflash2_selector_project(null, null, 2, 3, 64, 12, 8, 1, null, 0, null,
+                                        null) == 1
+    assert lib.dflash2_selector_project(null, null, 2, 3, 64, 16, 8, 4, null, 0, null,
+                                        null) == 2
+    assert lib.dflash2_selector_project(ctypes.c_void_p(256), ctypes.c_void_p(256), 2, 3, 64, 16,
+                                        8, 1, null, 0, null, null) == 4
+    assert lib.dflash2_selector_project(null, null, 0, 3, 64, 16, 8, 1, null, 0, null,
+                                        null) == 0
+    assert lib.dflash2_selector_walk_projected(null, null, 10, *(null,) * 6, 2, 3, 64, 16, 200, 1,
+                                               null, null, null, null, 0, null, null) == 1
+    assert lib.dflash2_selector_walk_projected(null, null, 0, *(null,) * 6, 2, 3, 64, 16, 8, 1,
+                                               null, null, null, null, 0, null, null) == 1
     # d2t: a table exists exactly when the draft vocab is smaller than the target
     assert lib.dflash2_d2t_remap(null, null, 4, 100, 200, null, null, null) == 1
     assert lib.dflash2_d2t_remap(null, ctypes.c_void_p(64), 4, 200, 100, null, null, null) == 1

@@ -96,3 +96,24 @@ def test_captured_graph_replays_the_eager_step(cuda):
     torch.cuda.synchronize()
     for key in ("cand_ids", "cand_u", "tokens", "q", "target_ids", "conv_out"):
         assert torch.equal(getattr(bufs, key), eager[key]), key
+
+
+@pytest.mark.parametrize("name,scale", [("qwen3-8b-bf16", dict(batch=6, draft_vocab=30000,
+                                                               target_vocab=30000)),
+                                        ("tiny-fp32", {})])
+def test_overlapped_step_equals_the_one_stream_step(cuda, name, scale):
+    """The conv, the uniforms and the selector projection on a second stream
+    beside the top-K change no result: every output equals the one-stream
+    step's, bit for bit (the same Philox counter draws the same uniforms)."""
+    w = synth.BY_NAME[name].scaled(**scale)
+    inp = synth.make(w)
+    t = {k: dflash2.to_device(v, cuda) for k, v in inp.items() if v is not None}
+    outs = []
+    for overlap in (False, True):
+        bufs = dflash2.ProposalBuffers(w, cuda)
+        counter = torch.zeros(1, dtype=torch.int64, device=cuda)
+        out = dflash2.proposal_step(w, t, bufs, rng=(w.seed, counter), overlap=overlap)
+        torch.cuda.synchronize()
+        outs.append({k: v.clone() for k, v in out.items()})
+    for key in ("conv_out", "cand_ids", "cand_u", "tokens", "q", "target_ids", "uniforms", "err"):
+        assert torch.equal(outs[0][key], outs[1][key]), key

@@ -183,3 +183,35 @@ def test_greedy_rows_do_not_depend_on_other_rows(cuda):
     g = inp["greedy"] == 1
     np.testing.assert_array_equal(t1[g], t2[g])
     np.testing.assert_array_equal(q1[g], q2[g])
+
+
+@pytest.mark.parametrize("case", [WALK_CASES[0], WALK_CASES[2], WALK_CASES[3]],
+                         ids=lambda c: f"r{c['rank']}-k{c['top_k']}-{c['dtype']}")
+def test_projection_then_walk_equals_the_one_call_walk(cuda, case):
+    """dflash2_selector_project on one stream, then dflash2_selector_walk_projected
+    on another (ordered by an event), give exactly what dflash2_selector_walk gives."""
+    w = synth.CONFIGS[0].scaled(draft_vocab=3000, target_vocab=3000, seed=97, **case)
+    inp, cand, cand_u = _random_candidates(w, 98, scale_ab=20.0)
+    tokens, q, ps, err = _run_walk(cuda, inp, cand, cand_u)
+    t = {k: dflash2.to_device(v, cuda) for k, v in inp.items() if v is not None}
+    tc = torch.from_numpy(np.ascontiguousarray(cand)).to(cuda)
+    tu = torch.from_numpy(np.ascontiguousarray(cand_u)).to(cuda)
+    code = dflash2.BF16 if w.dtype == "bf16" else dflash2.F32
+    ws = torch.full((dflash2.selector_walk_workspace_size(w.batch, w.slots, w.hidden, w.rank,
+                                                          w.top_k, code),), 0xA5,
+                    dtype=torch.uint8, device=cuda)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    dflash2.selector_project(t["h"], t["proj"], w.batch, w.slots, w.top_k, ws, stream=s1)
+    done = torch.cuda.Event()
+    done.record(s1)
+    s2.wait_event(done)
+    tok2, q2, ps2, err2 = dflash2.selector_walk_projected(
+        t["A"], t["B"], t["anchors"], tc, tu, t["temperatures"], t["greedy"], t["uniforms"],
+        w.hidden, ws, with_path_scores=True, stream=s2)
+    torch.cuda.synchronize()
+    assert int(err2.item()) == err == 0
+    np.testing.assert_array_equal(tok2.cpu().numpy(), tokens)
+    np.testing.assert_array_equal(q2.cpu().numpy(), q)
+    np.testing.assert_array_equal(ps2.cpu().numpy(), ps)
