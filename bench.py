@@ -152,7 +152,7 @@ class ClockSampler:
 
 
 def _profile_traffic(kernel_sources):
-    """DRAM bytes (read + write) of one unary_topk stage (its four launches)
+    """DRAM bytes (read + write) of one unary_topk stage (all its launches)
     from the committed ncu summary, or None when the kernel sources changed
     since the capture."""
     import hashlib
@@ -379,7 +379,7 @@ def run_gpu(args, w):
     host_in = {k: torch.from_numpy(inp[k].view(np.int16) if inp[k].dtype == np.uint16 else inp[k])
                .pin_memory() for k in in_keys}
     t_b = dict(t)
-    t_b.update({k: torch.empty_like(t[k]) for k in in_keys})
+    t_b.update({k: t[k].clone() for k in in_keys})  # valid inputs for the warm-up before capture
     sets = [t, t_b]
     graphs = [graph, None]
     if use_graph:
@@ -513,15 +513,12 @@ def run_gpu(args, w):
     if world > 1:
         ms, e2e = reduce_max_over_ranks([ms, e2e], device=dev)
 
-    # conv, unary (pilot GEMM, pilot select, filter GEMM, finalize), uniforms,
+    # conv, unary (as the library reports for this device and shape), uniforms,
     # walk (projection, then rows + chase in lattice mode, top_k <= 32, or the
     # path-mode walk), d2t
     walk_launches = 3 if w.top_k <= 32 else 2
-    unary_launches = 4
-    if w.dtype == "f32":
-        unary_launches = 1
-    elif (w.draft_vocab + 255) // 256 <= 8:  # the pilot covers the vocab: no filter pass
-        unary_launches = 3
+    unary_launches = dflash2.library().dflash2_unary_topk_launches(
+        w.rows, w.draft_vocab, w.mult, dflash2.BF16 if w.dtype == "bf16" else dflash2.F32)
     launches_per_step = 1 + unary_launches + 1 + walk_launches + 1
 
     if rank != 0:
@@ -577,7 +574,7 @@ def run_gpu(args, w):
         "activations N(0,1); walk uniforms drawn on the device by Philox4x64-10)", "config": _config(w),
         "roofline": {"bound": "tensor", "achieved": achieved_tf, "peak": tf_burst,
                      "unit": "TFLOP/s", "frac": achieved_tf / tf_burst, "traffic": traffic,
-                     "kernel": "unary_topk stage (pilot GEMM + pilot select + filter GEMM + "
+                     "kernel": "unary_topk stage (fused pilot + select + filter GEMM, then "
                                "finalize), 2*M*V*H flops over the stage time",
                      "peak_kind": f"{peak_kind} bf16 burst"},
         "stages": stages,

@@ -201,6 +201,44 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// Grid-wide counters of a cooperative launch (every CTA resident at once).
+// A warp publishes what its lanes wrote with counter_arrive (all lanes call
+// it); a waiter polls with acquire loads, bounded like mbar_wait, and reads
+// the published data through L2 (__ldcg) afterwards.
+__device__ __forceinline__ void counter_arrive(uint32_t *ctr, int lane) {
+    __syncwarp();
+    if (lane == 0) {
+        __threadfence();
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+    }
+    __syncwarp();
+}
+__device__ __forceinline__ bool counter_wait(const uint32_t *ctr, uint32_t target,
+                                             volatile int *abort_flag, int32_t *err, int lane) {
+    int ok = 1;
+    if (lane == 0) {
+        const uint64_t t0 = global_timer_ns();
+        for (;;) {
+            uint32_t v;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+            if (v >= target) break;
+            if (*abort_flag) {
+                ok = 0;
+                break;
+            }
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                if (err) atomicOr(err, DFLASH2_DEVERR_TIMEOUT);
+                ok = 0;
+                break;
+            }
+            __nanosleep(128);
+        }
+        __threadfence();
+    }
+    return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+
 // 2-D tiled TMA load into this CTA's shared memory; completion is signalled
 // on `bar` as transaction bytes.  c0 is the column (inner) coordinate.
 __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, uint64_t *bar,

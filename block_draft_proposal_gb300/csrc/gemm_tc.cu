@@ -81,7 +81,11 @@ __device__ __forceinline__ void drain_loads(uint64_t *full_bar, uint32_t issued,
 // Which weight tile the j-th tile of this launch's pass is.
 __device__ __forceinline__ int pass_tile(const GemmParams &p, int j) {
     if (p.mode == kGemmPilot) return j * p.pilot_stride;
-    if (p.mode == kGemmFilter) {
+    if (p.mode == kGemmFused) {  // the pilot tiles first, then the filter's order
+        if (j < p.n_pilot) return j * p.pilot_stride;
+        j -= p.n_pilot;
+    }
+    if (p.mode == kGemmFilter || p.mode == kGemmFused) {
         const int per = p.pilot_stride - 1;  // non-pilot tiles between two pilot tiles
         const int in_blocks = p.n_pilot * per;
         if (per > 0 && j < in_blocks) return (j / per) * p.pilot_stride + 1 + (j % per);
@@ -92,6 +96,8 @@ __device__ __forceinline__ int pass_tile(const GemmParams &p, int j) {
 
 struct Item {
     int wt, nt, ks, j;
+    bool pilot;   // a pilot tile: raw logits to out
+    bool filter;  // a filter tile: candidates against the row thresholds
 };
 __device__ __forceinline__ Item decode(const GemmParams &p, int w) {
     Item it;
@@ -100,6 +106,8 @@ __device__ __forceinline__ Item decode(const GemmParams &p, int w) {
     it.nt = rest % p.n_tok_tiles;
     it.j = rest / p.n_tok_tiles;
     it.wt = pass_tile(p, it.j);
+    it.pilot = p.mode == kGemmPilot || (p.mode == kGemmFused && it.j < p.n_pilot);
+    it.filter = p.mode == kGemmFilter || (p.mode == kGemmFused && it.j >= p.n_pilot);
     return it;
 }
 
@@ -125,7 +133,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams &p, const float 
                 if (i < ncols && m < p.rows_h) o[(int64_t)m * p.ldo] = __float2bfloat16_rn(z[i]);
             }
         }
-    } else if (p.mode == kGemmPilot) {
+    } else if (it.pilot) {
         // raw logits; the pilot select applies the transform (-inf = padded / out of range)
         const bool valid = v < p.rows_w && v < p.target_vocab;
         float *o = p.out + (int64_t)it.j * p.unit + row_in_tile;  // row_in_tile: offset in the unit
@@ -135,6 +143,22 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams &p, const float 
             if (i < ncols && m < p.rows_h) o[(int64_t)m * p.ldo] = valid ? z[i] : -INFINITY;
         }
     }
+}
+
+// Fused pilot tile: the warp's 32 vocab rows form group g; lane i stores the
+// order bits of the group's largest logit for token m0 + i (NaN and invalid
+// rows count as -inf).
+__device__ __forceinline__ void group_max_chunk(const GemmParams &p, const float (&z)[32],
+                                                bool valid, int m0, int ncols, int g, int lane) {
+    uint32_t mine = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float zi = valid && z[i] == z[i] ? z[i] : -INFINITY;
+        const uint32_t r = __reduce_max_sync(0xFFFFFFFFu, order_bits(zi));
+        if (lane == i) mine = r;
+    }
+    const int m = m0 + lane;
+    if (lane < ncols && m < p.rows_h) p.pmax[(int64_t)m * p.ld_pmax + g] = mine;
 }
 
 // Per-epilogue-warp shared scratch of the filter mode: the thresholds of the
@@ -216,6 +240,72 @@ __device__ __forceinline__ void filter_chunk(const GemmParams &p, const float (&
             nbuf += __popc(b);
         }
     }
+}
+
+// ---- fused mode: the row thresholds on the epilogue warps -------------------
+// One row's pilot select on one warp.  The groups are the 32-row slices of
+// the pilot units (lane l holds unit l's 8 group maxima, written by the pilot
+// tiles' epilogues).  z* = the k-th largest group maximum, found by a bitwise
+// search over their order bits in registers: at least k entries have
+// z >= z*, hence u >= u* = the transform of z*, hence a key at or above the
+// smallest key of value u*, which is theta (a lower bound of the row's k-th
+// best key; the pre-threshold follows from u* as in pilot_select_kernel in
+// topk.cu).  The pilot tiles' own candidates are then taken from their
+// accumulators like any filter tile's, so the select writes only theta, the
+// pre-threshold and a zero count.  It keeps off shared memory and nearly off
+// the load path, which are busy feeding the tensor cores while it runs.
+// Used only with mult > 0 (a non-decreasing transform).
+__device__ __noinline__ void fused_select_row(const GemmParams &p, int64_t row, int lane) {
+    const int k = p.top_k;
+    const uint32_t kNegInf = order_bits(-INFINITY);
+    uint32_t ob[8];
+    if (lane < p.n_pilot) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.pmax + row * p.ld_pmax + 8 * lane);
+        const uint4 a = __ldcg(src), b = __ldcg(src + 1);
+        ob[0] = a.x; ob[1] = a.y; ob[2] = a.z; ob[3] = a.w;
+        ob[4] = b.x; ob[5] = b.y; ob[6] = b.z; ob[7] = b.w;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ob[i] = kNegInf;
+    }
+    // the largest T with at least k maxima >= T is the k-th largest maximum
+    uint32_t T = 0;
+    for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t c = T | (1u << bit);
+        uint32_t n = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) n += ob[i] >= c ? 1u : 0u;
+        if (__reduce_add_sync(0xFFFFFFFFu, n) >= (uint32_t)k) T = c;
+    }
+    const float zs = order_to_float(T);
+    uint64_t th;
+    float pre;
+    if (zs == -INFINITY) {
+        th = 0;  // fewer than k groups hold a valid entry: all are candidates
+        pre = -INFINITY;
+    } else {
+        const float us = unary_transform(zs, p.mult, p.cap);
+        th = make_key(us, 0xFFFFFFFFu);  // the smallest key of value u*
+        pre = us > 0.0f ? us * (1.0f - 0x1p-18f) : -INFINITY;
+    }
+    if (lane == 0) {
+        const_cast<uint64_t *>(p.theta)[row] = th;
+        const_cast<float *>(p.theta_pre)[row] = pre;
+        p.cnt[row] = 0;
+    }
+}
+
+// Every epilogue warp of the launch (4 per CTA) waits for the pilot tiles'
+// group maxima, selects rows gw, gw + nw, ... and publishes; false when a
+// bounded wait gave up.
+__device__ bool fused_select(const GemmParams &p, volatile int *abort_flag, int lane) {
+    const int nw = (int)gridDim.x * 4;
+    const int gw = (int)blockIdx.x * 4 + ((int)(threadIdx.x >> 5) - 2);
+    const uint32_t pilot_warps = (uint32_t)p.n_pilot * (uint32_t)p.n_tok_tiles * 8u;
+    if (!counter_wait(p.sync, pilot_warps, abort_flag, p.err, lane)) return false;
+    for (int64_t row = gw; row < p.rows_h; row += nw) fused_select_row(p, row, lane);
+    counter_arrive(p.sync + 1, lane);
+    return true;
 }
 
 __global__ void __launch_bounds__(192, 1)
@@ -544,35 +634,91 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         EpiScratch &es = epi[warp - 2];
         const uint32_t acc_empty_leader[2] = {mapa_shared(smem_u32(&acc_empty[0]), 0),
                                               mapa_shared(smem_u32(&acc_empty[1]), 0)};
-        int t = 0;
-        for (int w = pair; w < total; w += npairs, ++t) {
-            const Item item = decode(p, w);
-            const int a = t & 1;
+        // The candidates of one filter-style tile whose accumulator is full:
+        // its tokens' thresholds, the chunks, then the buffer goes back.
+        const auto load_thresholds = [&](const Item &item) {
             const int m_tile = item.nt * p.bn;
-            if (p.mode == kGemmFilter) {
-                for (int c = lane; c < 256; c += 32) {
-                    const int m = m_tile + c;
-                    const bool ok = c < p.bn && m < p.rows_h;
-                    es.pre[c] = ok ? p.theta_pre[m] : INFINITY;
-                    es.th[c] = ok ? p.theta[m] : ~0ull;
-                }
-                __syncwarp();
+            for (int c = lane; c < 256; c += 32) {
+                const int m = m_tile + c;
+                const bool ok = c < p.bn && m < p.rows_h;
+                es.pre[c] = ok ? __ldcg(p.theta_pre + m) : INFINITY;
+                es.th[c] = ok ? __ldcg(p.theta + m) : ~0ull;
             }
-            if (!mbar_wait(&acc_full[a], ((uint32_t)t >> 1) & 1u, &abort_flag, p.err)) break;
-            tc_fence_after();
+            __syncwarp();
+        };
+        const auto filter_tile = [&](const Item &item, int a) {
+            const int m_tile = item.nt * p.bn;
             const int64_t v = (int64_t)item.wt * p.unit + row_in_unit;
             const uint32_t tbase = tmem + (uint32_t)a * p.acc_cols + ((uint32_t)(quarter * 32) << 16);
             int nbuf = 0;
             for (int c0 = 0; c0 < p.bn; c0 += 32) {
                 float z[32];
                 tmem_ld32_wait(tbase + (uint32_t)c0, z);
-                if (p.mode == kGemmFilter)
-                    filter_chunk(p, z, v, m_tile + c0, c0, tbase + (uint32_t)c0, es, nbuf, lane);
-                else
-                    epilogue_chunk(p, z, v, row_in_unit, m_tile + c0, min(32, p.bn - c0), item, lane);
+                filter_chunk(p, z, v, m_tile + c0, c0, tbase + (uint32_t)c0, es, nbuf, lane);
             }
             tc_fence_before();
-            if (p.mode == kGemmFilter && nbuf > 0) flush_survivors(p, es, nbuf, lane);
+            if (nbuf > 0) flush_survivors(p, es, nbuf, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_empty_leader[a]);
+        };
+        int t = 0;
+        int w = pair;
+        if (p.mode == kGemmFused) {
+            // Phase A: the group maxima of this pair's pilot tiles (the first
+            // in its order, at most two), whose accumulators stay in TMEM.
+            int np = 0;
+            bool ok = true;
+            for (; w < total; w += npairs, ++t) {
+                const Item item = decode(p, w);
+                if (!item.pilot) break;
+                const int a = t & 1;
+                if (!mbar_wait(&acc_full[a], ((uint32_t)t >> 1) & 1u, &abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int64_t v = (int64_t)item.wt * p.unit + row_in_unit;
+                const bool valid = v < p.rows_w && v < p.target_vocab;
+                const uint32_t tbase =
+                    tmem + (uint32_t)a * p.acc_cols + ((uint32_t)(quarter * 32) << 16);
+                const int g = item.j * (p.unit / 32) + row_in_unit / 32;
+                for (int c0 = 0; c0 < p.bn; c0 += 32) {
+                    float z[32];
+                    tmem_ld32_wait(tbase + (uint32_t)c0, z);
+                    group_max_chunk(p, z, valid, item.nt * p.bn + c0, min(32, p.bn - c0), g, lane);
+                }
+                counter_arrive(p.sync, lane);
+                ++np;
+            }
+            // the thresholds of every row, then the pilot tiles' candidates
+            ok = ok && fused_select(p, &abort_flag, lane) &&
+                 counter_wait(p.sync + 1, gridDim.x * 4, &abort_flag, p.err, lane);
+            for (int i = 0; ok && i < np; ++i) {
+                const Item item = decode(p, pair + i * npairs);
+                load_thresholds(item);
+                filter_tile(item, i & 1);
+            }
+            if (!ok) w = total;
+        }
+        for (; w < total; w += npairs, ++t) {
+            const Item item = decode(p, w);
+            const int a = t & 1;
+            if (item.filter) load_thresholds(item);  // while the MMAs finish
+            if (!mbar_wait(&acc_full[a], ((uint32_t)t >> 1) & 1u, &abort_flag, p.err)) break;
+            tc_fence_after();
+            if (item.filter) {
+                filter_tile(item, a);
+                continue;
+            }
+            const int m_tile = item.nt * p.bn;
+            const int64_t v = (int64_t)item.wt * p.unit + row_in_unit;
+            const uint32_t tbase = tmem + (uint32_t)a * p.acc_cols + ((uint32_t)(quarter * 32) << 16);
+            for (int c0 = 0; c0 < p.bn; c0 += 32) {
+                float z[32];
+                tmem_ld32_wait(tbase + (uint32_t)c0, z);
+                epilogue_chunk(p, z, v, row_in_unit, m_tile + c0, min(32, p.bn - c0), item, lane);
+            }
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(acc_empty_leader[a]);
         }
@@ -588,8 +734,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 }
 
 int g_smem_set[64];
+int g_fused_pairs[64];  // 0: not yet asked; -1: none
+
+dflash2_status set_gemm_attrs(const DeviceInfo &di) {
+    if (di.device < 0 || di.device >= 64) return DFLASH2_ERR_CUDA;
+    if (g_smem_set[di.device]) return DFLASH2_OK;
+    if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kGemmSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kGemmSmemBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return DFLASH2_ERR_CUDA;
+    }
+    g_smem_set[di.device] = 1;
+    return DFLASH2_OK;
+}
+
+// CTA pairs of the pair kernel the device holds at once (its full shared
+// memory, so one CTA per SM), or 0.
+int fused_pairs(const DeviceInfo &di) {
+    if (di.device < 0 || di.device >= 64) return 0;
+    if (g_fused_pairs[di.device] == 0) {
+        int n = 0;
+        if (set_gemm_attrs(di) == DFLASH2_OK) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(di.sm_count / 2 * 2));
+            cfg.blockDim = dim3(192);
+            cfg.dynamicSmemBytes = kGemmSmemBytes;
+            if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_pair_kernel, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                n = 0;
+            }
+        }
+        g_fused_pairs[di.device] = n > 0 ? n : -1;
+    }
+    return g_fused_pairs[di.device] > 0 ? g_fused_pairs[di.device] : 0;
+}
 
 }  // namespace
+
+int fused_epilogue_warps(const DeviceInfo &di) { return fused_pairs(di) * 2 * 4; }
 
 dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h, GemmParams p,
                               cudaStream_t st, bool pair) {
@@ -617,7 +801,10 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     p.acc_cols = acc;
     const uint32_t h_rows = pair ? (uint32_t)p.bn / 2 : (uint32_t)p.bn;
     const uint32_t stage_bytes = kWStageBytes + h_rows * kGemmStageK * 2;
-    const size_t epi_bytes = p.mode == kGemmFilter ? 4 * sizeof(EpiScratch) : 0;
+    const bool fused = p.mode == kGemmFused;
+    if (fused && !pair) return DFLASH2_ERR_INVALID_ARG;
+    const size_t epi_bytes =
+        p.mode == kGemmFilter || fused ? 4 * sizeof(EpiScratch) : 0;
     int stages = (int)((kGemmSmemBytes - 1024 - epi_bytes) / stage_bytes);
     if (stages > kGemmMaxStages) stages = kGemmMaxStages;
     if (stages < 2) return DFLASH2_ERR_INVALID_ARG;  // bn <= 256 always leaves room for two
@@ -630,17 +817,32 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     s = encode_tmap_bf16(&tm_h, h, (uint64_t)p.rows_h, (uint64_t)p.hidden, h_rows);
     if (s != DFLASH2_OK) return s;
 
-    if (di.device >= 0 && di.device < 64 && !g_smem_set[di.device]) {
-        if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kGemmSmemBytes) != cudaSuccess ||
-            cudaFuncSetAttribute(gemm_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kGemmSmemBytes) != cudaSuccess) {
-            cudaGetLastError();
-            return DFLASH2_ERR_CUDA;
-        }
-        g_smem_set[di.device] = 1;
-    }
+    s = set_gemm_attrs(di);
+    if (s != DFLASH2_OK) return s;
     const int64_t total = (int64_t)p.pass_tiles * p.n_tok_tiles * p.k_splits;
+    if (fused) {
+        // every CTA resident at once (its warps wait on one another): a
+        // cooperative launch of at most the pairs the device holds together
+        const int64_t pairs_max = fused_pairs(di);
+        if (pairs_max < 1) return DFLASH2_ERR_UNSUPPORTED_DEVICE;
+        const int pairs = (int)(total < pairs_max ? total : pairs_max);
+        // a pair keeps its pilot accumulators until the select: two at most
+        if ((int64_t)p.n_pilot * p.n_tok_tiles > 2LL * pairs) return DFLASH2_ERR_INVALID_ARG;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(2 * pairs));
+        cfg.blockDim = dim3(192);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeCooperative;
+        attr[1].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel, tm_w, tm_h, p);
+        return launch_status();
+    }
     if (pair) {
         const int64_t pairs_max = di.sm_count / 2;
         const int pairs = (int)(total < pairs_max ? total : pairs_max);

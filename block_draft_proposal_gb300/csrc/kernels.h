@@ -14,6 +14,12 @@ enum GemmMode : int32_t {
     kGemmPilot = 1,   // write the transformed, masked u of the pilot tiles to out
     kGemmFilter = 2,  // append (u, id) keys that reach the row's threshold
     kGemmStoreBf16 = 3,  // write C rounded to bf16 (nearest-even) to out_bf16, no split
+    // pilot, select and filter in one cooperative launch: the pilot tiles come
+    // first (at most two per CTA pair) and their epilogues write group maxima,
+    // the epilogue warps then derive every row's threshold while the MMAs run
+    // on, and every tile's candidates (the pilot tiles' from the accumulators
+    // they kept) are taken against the thresholds
+    kGemmFused = 4,
 };
 
 constexpr int kGemmTileW = 128;  // weight rows per tile (MMA M)
@@ -55,6 +61,14 @@ struct GemmParams {
     uint64_t *cand;        // filter: [rows_h][cand_cap] keys
     int32_t cand_cap;
     int32_t *err;
+    // fused: the pilot tiles' group maxima (order bits of the largest logit
+    // of each 32 consecutive vocab rows of a pilot unit) [rows_h][ld_pmax];
+    // top_k; two grid counters (pilot warps done, select warps done), zero at
+    // launch
+    uint32_t *pmax;
+    int64_t ld_pmax;
+    int32_t top_k;
+    uint32_t *sync;
 };
 
 // Pilot tiling of a weight matrix with n_wtiles units of unit_rows rows:
@@ -74,8 +88,12 @@ inline void pilot_layout(int64_t n_wtiles, int32_t *n_pilot, int32_t *stride, in
     *stride = (int32_t)(n_wtiles / np);
 }
 
-// pair: run the pilot / filter modes on CTA pairs (2-CTA MMA, 256-row units).
+// pair: run the pilot / filter / fused modes on CTA pairs (2-CTA MMA, 256-row units).
 dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h, GemmParams p,
                               cudaStream_t st, bool pair = false);
+
+// Epilogue warps of one fused launch (4 per CTA, every CTA resident at once),
+// or 0 when the device cannot hold such a launch.  Host-side, cached per device.
+int fused_epilogue_warps(const DeviceInfo &di);
 
 }  // namespace dflash2

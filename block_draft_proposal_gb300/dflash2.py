@@ -29,7 +29,7 @@ DEVERR_ID_RANGE = 0x1
 DEVERR_TIMEOUT = 0x2
 DEVERR_SHORT = 0x4
 DEVINFO_TOPK_FALLBACK = 0x100
-ABI_VERSION = 3
+ABI_VERSION = 4
 
 # Every symbol include/dflash2.h declares.
 EXPORTS = (
@@ -39,6 +39,7 @@ EXPORTS = (
     "dflash2_d2t_remap", "dflash2_selector_walk_noalloc", "dflash2_philox_uniforms",
     "dflash2_conv_prepare", "dflash2_conv_finish", "dflash2_verify_workspace_size",
     "dflash2_verify", "dflash2_selector_project", "dflash2_selector_walk_projected",
+    "dflash2_unary_topk_launches",
 )
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -102,6 +103,8 @@ def library():
         lib.dflash2_selector_walk_projected.argtypes = [P, P, i64, P, P, P, P, P, P, i32, i32, i32,
                                                         i32, i32, i32, P, P, P, P, sz, P, P]
         lib.dflash2_selector_walk_projected.restype = i32
+        lib.dflash2_unary_topk_launches.argtypes = [i64, i64, f32, i32]
+        lib.dflash2_unary_topk_launches.restype = i32
         if lib.dflash2_abi_version() != ABI_VERSION:
             raise RuntimeError("libdflash2.so ABI version mismatch; rebuild it")
         _lib = lib
