@@ -29,7 +29,7 @@ DEVERR_ID_RANGE = 0x1
 DEVERR_TIMEOUT = 0x2
 DEVERR_SHORT = 0x4
 DEVINFO_TOPK_FALLBACK = 0x100
-ABI_VERSION = 4
+ABI_VERSION = 5
 
 # Every symbol include/dflash2.h declares.
 EXPORTS = (
@@ -39,7 +39,7 @@ EXPORTS = (
     "dflash2_d2t_remap", "dflash2_selector_walk_noalloc", "dflash2_philox_uniforms",
     "dflash2_conv_prepare", "dflash2_conv_finish", "dflash2_verify_workspace_size",
     "dflash2_verify", "dflash2_selector_project", "dflash2_selector_walk_projected",
-    "dflash2_unary_topk_launches",
+    "dflash2_unary_topk_launches", "dflash2_topk_merge",
 )
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -103,6 +103,8 @@ def library():
         lib.dflash2_selector_walk_projected.argtypes = [P, P, i64, P, P, P, P, P, P, i32, i32, i32,
                                                         i32, i32, i32, P, P, P, P, sz, P, P]
         lib.dflash2_selector_walk_projected.restype = i32
+        lib.dflash2_topk_merge.argtypes = [P, P, P, i32, i64, i32, i32, P, P, P, P]
+        lib.dflash2_topk_merge.restype = i32
         lib.dflash2_unary_topk_launches.argtypes = [i64, i64, f32, i32]
         lib.dflash2_unary_topk_launches.restype = i32
         if lib.dflash2_abi_version() != ABI_VERSION:
@@ -200,6 +202,98 @@ def unary_topk(h, lm_head, target_vocab: int, mult: float, cap: float, top_k: in
         float(cap), top_k, code, _ptr(cand_ids), _ptr(cand_u), _ptr(workspace),
         workspace.numel(), _ptr(err), _stream(stream)))
     return cand_ids, cand_u, err
+
+
+def topk_merge(ids, u, id_offsets, k_out: int, out_ids=None, out_u=None, err=None, stream=None):
+    """dflash2_topk_merge: the k_out best (u, global id) per row over shard
+    lists ids / u [shards, rows, k_in] (shard-local ids; u = -inf absent)."""
+    shards, rows, k_in = ids.shape
+    _need(ids, "ids", torch.int64)
+    _need(u, "u", torch.float32, tuple(ids.shape))
+    offs = [int(o) for o in id_offsets]
+    if len(offs) != shards:
+        raise ValueError("one id offset per shard")
+    dev = ids.device
+    if out_ids is None:
+        out_ids = torch.empty((rows, k_out), dtype=torch.int64, device=dev)
+    if out_u is None:
+        out_u = torch.empty((rows, k_out), dtype=torch.float32, device=dev)
+    _need(out_ids, "out_ids", torch.int64, (rows, k_out))
+    _need(out_u, "out_u", torch.float32, (rows, k_out))
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    host_offs = (ctypes.c_int64 * shards)(*offs)
+    _check("dflash2_topk_merge", library().dflash2_topk_merge(
+        _ptr(ids), _ptr(u), ctypes.cast(host_offs, ctypes.c_void_p), shards, rows, k_in, k_out,
+        _ptr(out_ids), _ptr(out_u), _ptr(err), _stream(stream)))
+    return out_ids, out_u, err
+
+
+def vocab_shard(draft_vocab: int, target_vocab: int, shards: int, s: int):
+    """Shard s of `shards` near-equal slices of the lm_head rows: (first id,
+    rows in the slice, ids of the slice below target_vocab)."""
+    if not 0 <= s < shards:
+        raise ValueError("shard index out of range")
+    per = -(-draft_vocab // shards)
+    first = min(s * per, draft_vocab)
+    n = min(per, draft_vocab - first)
+    return first, n, max(0, min(n, target_vocab - first))
+
+
+def shard_topk(h, lm_head_slice, first: int, target_vocab: int, mult: float, cap: float,
+               top_k: int, workspace=None, err=None, stream=None):
+    """This shard's part of a vocab-sharded unary top-K: dflash2_unary_topk over
+    its lm_head rows, as a [rows, top_k] list with shard-local ids.  A slice
+    with fewer than top_k ids below target_vocab pads its list with u = -inf
+    (absent for the merge)."""
+    rows = h.shape[0]
+    n = lm_head_slice.shape[0]
+    local_target = max(0, min(n, target_vocab - first))
+    k_here = min(top_k, local_target)
+    if k_here == top_k:
+        ids, u, _ = unary_topk(h, lm_head_slice, local_target, mult, cap, top_k,
+                               workspace=workspace, err=err, stream=stream)
+        return ids, u
+    s = torch.cuda.current_stream(h.device) if stream is None else stream
+    with torch.cuda.stream(s):
+        ids = torch.zeros((rows, top_k), dtype=torch.int64, device=h.device)
+        u = torch.full((rows, top_k), float("-inf"), dtype=torch.float32, device=h.device)
+        if k_here > 0 and rows > 0:
+            i2, u2, _ = unary_topk(h, lm_head_slice, local_target, mult, cap, k_here,
+                                   workspace=workspace, err=err, stream=s)
+            ids[:, :k_here] = i2
+            u[:, :k_here] = u2
+    return ids, u
+
+
+def gather_shard_lists(ids, u, group=None):
+    """The exchange of a vocab-sharded top-K: every rank's [rows, K] list,
+    all-gathered into [world, rows, K] (rank order = shard order)."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    all_ids = [torch.empty_like(ids) for _ in range(world)]
+    all_u = [torch.empty_like(u) for _ in range(world)]
+    dist.all_gather(all_ids, ids.contiguous(), group=group)
+    dist.all_gather(all_u, u.contiguous(), group=group)
+    return torch.stack(all_ids), torch.stack(all_u)
+
+
+def unary_topk_vocab_sharded(h, lm_head_slice, draft_vocab: int, target_vocab: int, mult: float,
+                             cap: float, top_k: int, group=None, err=None, stream=None):
+    """Vocab-sharded unary top-K over a process group: this rank holds lm_head
+    rows vocab_shard(draft_vocab, target_vocab, world, rank); the shard's
+    list, one all-gather and dflash2_topk_merge give every rank the unsharded
+    result (the same ids and u as dflash2_unary_topk over the whole lm_head)."""
+    import torch.distributed as dist
+    world, rank = dist.get_world_size(group), dist.get_rank(group)
+    first, n, _ = vocab_shard(draft_vocab, target_vocab, world, rank)
+    if lm_head_slice.shape[0] != n:
+        raise ValueError(f"rank {rank} holds {lm_head_slice.shape[0]} lm_head rows, expected {n}")
+    ids, u = shard_topk(h, lm_head_slice, first, target_vocab, mult, cap, top_k, err=err,
+                        stream=stream)
+    all_ids, all_u = gather_shard_lists(ids, u, group)
+    offsets = [vocab_shard(draft_vocab, target_vocab, world, s)[0] for s in range(world)]
+    return topk_merge(all_ids, all_u, offsets, top_k, err=err, stream=stream)
 
 
 def selector_walk_workspace_size(batch: int, slots: int, hidden: int, rank: int, top_k: int,

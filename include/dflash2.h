@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define DFLASH2_ABI_VERSION 4
+#define DFLASH2_ABI_VERSION 5
 
 typedef enum {
     DFLASH2_OK = 0,
@@ -378,6 +378,38 @@ dflash2_status dflash2_verify(const void *target_logits, int64_t vocab,
  */
 dflash2_status dflash2_philox_uniforms(uint64_t seed, uint64_t offset, uint64_t *counter,
                                        int64_t n, float *out, void *stream);
+
+/*
+ * Exact merge of vocab-sharded top-K lists (the one exchange of a
+ * vocab-sharded unary top-K: each GPU runs dflash2_unary_topk over its slice
+ * of lm_head rows, the [rows, k_in] lists are all-gathered, and every rank
+ * merges them).  The sglang DFlash2 PR computes the candidates over the whole
+ * vocab on one GPU; this splits the same computation.  The logits of a vocab
+ * row do not depend on the slice that computes them, so the merge gives
+ * exactly the unsharded dflash2_unary_topk result:
+ *
+ *   out[r, :] = the k_out largest (u, id_offsets[s] + ids[s, r, j]) over all
+ *               shards s and j, ordered by u descending, equal u by smaller id
+ *
+ * ids         device int64 [shards, rows, k_in]: shard-local vocab ids.
+ * u           device float [shards, rows, k_in]; u = -inf or NaN marks an
+ *             absent entry (a shard with fewer than k_in selectable ids pads
+ *             its list so, as dflash2_unary_topk does).  No order is assumed.
+ * id_offsets  HOST int64 [shards]: the first global vocab id of each shard,
+ *             in [0, 2^31).
+ * out_ids     device int64 [rows, k_out]; out_u device float [rows, k_out].
+ * Errors:     shards outside [1, 64], k_in < 1, k_out outside [1, 128],
+ *             shards * k_in > 4096, rows outside [0, 2^31), an offset out of
+ *             range or a null pointer -> INVALID_ARG; ids not 8-byte or u not
+ *             4-byte aligned -> MISALIGNED.  rows == 0 queues nothing.
+ * Device:     fewer than k_out present entries fill the rest with id 0 and
+ *             -inf and set DFLASH2_DEVERR_SHORT; a global id outside
+ *             [0, 2^32 - 1) is dropped and sets DFLASH2_DEVERR_ID_RANGE.
+ */
+dflash2_status dflash2_topk_merge(const int64_t *ids, const float *u, const int64_t *id_offsets,
+                                  int32_t shards, int64_t rows, int32_t k_in, int32_t k_out,
+                                  int64_t *out_ids, float *out_u, int32_t *err_word,
+                                  void *stream);
 
 /*
  * Draft-to-target id remap.

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.dflash2_abi_version() == 4
+    assert lib.dflash2_abi_version() == 5
     assert lib.dflash2_status_string(0) == b"ok"
     for s in range(1, 7):
         assert lib.dflash2_status_string(s) not in (b"ok", b"unknown status")
@@ -84,6 +84,16 @@ def test_host_validation_rejects_before_any_launch(lib):
                                                null, null, null, null, 0, null, null) == 1
     assert lib.dflash2_selector_walk_projected(null, null, 0, *(null,) * 6, 2, 3, 64, 16, 8, 1,
                                                null, null, null, null, 0, null, null) == 1
+    # top-K merge: shard count, list sizes and offsets are checked before any launch
+    offs = (ctypes.c_int64 * 2)(0, 100)
+    assert lib.dflash2_topk_merge(null, null, offs, 0, 4, 8, 8, null, null, null, null) == 1
+    assert lib.dflash2_topk_merge(null, null, offs, 2, 4, 2049, 8, null, null, null, null) == 1
+    assert lib.dflash2_topk_merge(null, null, offs, 2, 4, 8, 129, null, null, null, null) == 1
+    assert lib.dflash2_topk_merge(null, null, offs, 2, 0, 8, 8, null, null, null, null) == 0
+    assert lib.dflash2_topk_merge(null, null, offs, 2, 4, 8, 8, null, null, null, null) == 1
+    bad = (ctypes.c_int64 * 2)(0, -1)
+    p8 = ctypes.c_void_p(64)
+    assert lib.dflash2_topk_merge(p8, p8, bad, 2, 4, 8, 8, p8, p8, null, null) == 1
     # d2t: a table exists exactly when the draft vocab is smaller than the target
     assert lib.dflash2_d2t_remap(null, null, 4, 100, 200, null, null, null) == 1
     assert lib.dflash2_d2t_remap(null, ctypes.c_void_p(64), 4, 200, 100, null, null, null) == 1
