@@ -249,8 +249,9 @@ def _config(w):
             "l2": "value: flushed before every timed step (256 MiB write, outside the timed events); "
                   "e2e: a pipelined loop without flush, inputs larger than L2 (the lm_head streams "
                   "from HBM at every step)",
-            "e2e": "double-buffered device inputs: the next step's H2D copy overlaps this step's "
-                   "compute; timed from the first copy to the last D2H read-back",
+            "e2e": "double-buffered device inputs and outputs: the next step's H2D copy and the "
+                   "previous step's D2H read-back overlap this step's compute; timed from the "
+                   "first copy to the last D2H read-back",
             "graph": "one CUDA graph per step (replayed)"}
 
 
@@ -285,11 +286,11 @@ def run_gpu(args, w):
     rng_counter = torch.zeros(1, dtype=torch.int64, device=dev)
     uniforms = t["uniforms"].view(-1)
 
-    def step(record: bool, t=t):
+    def step(record: bool, t=t, b=bufs):
         if not record:
             # the timed step: the public API, the input-only work (uniforms,
             # conv, selector projection) on a second stream beside the top-K
-            dflash2.proposal_step(w, t, bufs, stream=stream, rng=(w.seed, rng_counter))
+            dflash2.proposal_step(w, t, b, stream=stream, rng=(w.seed, rng_counter))
             return
         # the staged step: the same launches on one stream, with events
         # between the stages
@@ -371,31 +372,36 @@ def run_gpu(args, w):
     # end to end through the public API, as a serving loop runs it: every step
     # copies its inputs from pinned host memory into one of two device input
     # sets on a copy stream (overlapping the previous step's compute), replays
-    # the captured step on that set, and reads its tokens and q back into
-    # pinned host memory.  Timed from the first copy to the last read-back over
-    # K steps; the 1.24 GB lm_head streams from HBM at every step (inputs
-    # larger than L2), so this loop runs without the flush.
+    # the captured step on that set (each set has its own outputs), and reads
+    # its tokens and q back into pinned host memory on a third stream, so the
+    # next step's compute does not wait for the read-back.  Timed from the
+    # first copy to the last read-back over K steps; the 1.24 GB lm_head
+    # streams from HBM at every step (inputs larger than L2), so this loop runs
+    # without the flush.
     in_keys = ("x", "delta", "h", "temperatures", "greedy", "anchors")
     host_in = {k: torch.from_numpy(inp[k].view(np.int16) if inp[k].dtype == np.uint16 else inp[k])
                .pin_memory() for k in in_keys}
     t_b = dict(t)
     t_b.update({k: t[k].clone() for k in in_keys})  # valid inputs for the warm-up before capture
     sets = [t, t_b]
+    outs = [bufs, dflash2.ProposalBuffers(w, dev)]
     graphs = [graph, None]
     if use_graph:
         with torch.cuda.stream(stream):
-            step(False, t=t_b)
+            step(False, t=t_b, b=outs[1])
         stream.synchronize()
         graphs[1] = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graphs[1], stream=stream):
-            step(False, t=t_b)
+            step(False, t=t_b, b=outs[1])
     host_tok = [torch.empty(bufs.target_ids.shape, dtype=torch.int64).pin_memory() for _ in range(2)]
     host_q = [torch.empty(bufs.q.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = host_tok[0].numel() * 8 + host_q[0].numel() * 4
     copy_stream = torch.cuda.Stream(device=dev)
-    ev_copied = [torch.cuda.Event() for _ in range(2)]
-    ev_free = [torch.cuda.Event() for _ in range(2)]
+    d2h_stream = torch.cuda.Stream(device=dev)
+    ev_copied = [torch.cuda.Event() for _ in range(2)]   # set j's inputs are on the device
+    ev_free = [torch.cuda.Event() for _ in range(2)]     # set j's step is done with its inputs
+    ev_read = [torch.cuda.Event() for _ in range(2)]     # set j's outputs are on the host
 
     def e2e_steps(n):
         for i in range(n):
@@ -409,21 +415,25 @@ def run_gpu(args, w):
                     dv.copy_(hv, non_blocking=True)
                 ev_copied[j].record(copy_stream)
             stream.wait_event(ev_copied[j])
+            stream.wait_event(ev_read[j])  # the step two back has been read back
             with torch.cuda.stream(stream):
                 if use_graph:
                     graphs[j].replay()
                 else:
-                    step(False, t=sets[j])
-                host_tok[j].copy_(bufs.target_ids, non_blocking=True)
-                host_q[j].copy_(bufs.q, non_blocking=True)
+                    step(False, t=sets[j], b=outs[j])
                 ev_free[j].record(stream)
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(ev_free[j])
+                host_tok[j].copy_(outs[j].target_ids, non_blocking=True)
+                host_q[j].copy_(outs[j].q, non_blocking=True)
+                ev_read[j].record(d2h_stream)
 
     e2e_steps(args.warmup)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(copy_stream)
     e2e_steps(args.steps)
-    e1.record(stream)
+    e1.record(d2h_stream)
     torch.cuda.synchronize()
     e2e = e0.elapsed_time(e1) / args.steps
 
@@ -518,7 +528,7 @@ def run_gpu(args, w):
     # path-mode walk), d2t
     walk_launches = 3 if w.top_k <= 32 else 2
     unary_launches = dflash2.library().dflash2_unary_topk_launches(
-        w.rows, w.draft_vocab, w.mult, dflash2.BF16 if w.dtype == "bf16" else dflash2.F32)
+        w.rows, w.draft_vocab, w.top_k, w.mult, dflash2.BF16 if w.dtype == "bf16" else dflash2.F32)
     launches_per_step = 1 + unary_launches + 1 + walk_launches + 1
 
     if rank != 0:

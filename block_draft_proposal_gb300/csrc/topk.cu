@@ -556,6 +556,7 @@ inline int token_tile(int64_t rows) {
 // filter tiles) replaces the pilot pass, the select kernel and the filter
 // pass when
 //   - mult > 0 (its select relies on the monotone transform),
+//   - the pilot has at least 4 K groups of 32 rows (8 per unit),
 //   - each epilogue warp selects at most two rows and each CTA pair keeps at
 //     most two pilot accumulators, so the thresholds are ready while the
 //     first filter tiles are still in the tensor cores, and
@@ -563,9 +564,13 @@ inline int token_tile(int64_t rows) {
 //     alone.  The pilot pass and the select it saves cost about 1.3 rounds at
 //     the bf16 workloads (measured on GB300: 7 us faster with one extra
 //     round, 11 us slower with two).
-bool use_fused(const DeviceInfo &di, const TopkLayout &L, int64_t rows, int bn, float mult) {
+bool use_fused(const DeviceInfo &di, const TopkLayout &L, int64_t rows, int bn, float mult,
+               int top_k) {
     const int fused_warps = fused_epilogue_warps(di);
     if (!(mult > 0.0f) || fused_warps <= 0 || rows > 2LL * fused_warps) return false;
+    // its groups are 32-row slices of the pilot units; with fewer than 4 K of
+    // them the threshold is loose and candidate lists overflow
+    if ((int64_t)L.n_pilot * (unit_rows() / 32) < 4LL * top_k) return false;
     const int64_t tok_tiles = (rows + bn - 1) / bn;
     const int64_t all_tiles = (int64_t)L.n_wtiles * tok_tiles;
     const int64_t filter_tiles = (int64_t)(L.n_wtiles - L.n_pilot) * tok_tiles;
@@ -621,16 +626,18 @@ extern "C" size_t dflash2_unary_topk_workspace_min(int64_t rows, int64_t draft_v
     return L.fixed_bytes + (size_t)rows * top_k * 8;
 }
 
-extern "C" int32_t dflash2_unary_topk_launches(int64_t rows, int64_t draft_vocab, float mult,
-                                               int32_t dtype) {
+extern "C" int32_t dflash2_unary_topk_launches(int64_t rows, int64_t draft_vocab, int32_t top_k,
+                                               float mult, int32_t dtype) {
     if (dtype != DFLASH2_F32 && dtype != DFLASH2_BF16) return -1;
-    if (rows < 0 || rows > INT32_MAX || draft_vocab <= 0 || draft_vocab > INT32_MAX) return -1;
+    if (rows < 0 || rows > INT32_MAX || draft_vocab <= 0 || draft_vocab > INT32_MAX ||
+        top_k <= 0 || top_k > kMaxTopK || top_k > draft_vocab)
+        return -1;
     if (rows == 0) return 0;
     if (dtype == DFLASH2_F32) return 1;
     DeviceInfo di;
     if (current_device(&di) != DFLASH2_OK) return -1;
     const TopkLayout L = topk_layout(rows, draft_vocab);
-    if (use_fused(di, L, rows, token_tile(rows), mult)) return 2;  // fused GEMM, finalize
+    if (use_fused(di, L, rows, token_tile(rows), mult, top_k)) return 2;  // fused GEMM, finalize
     return L.n_wtiles > L.n_pilot ? 4 : 3;  // pilot, select, (filter), finalize
 }
 
@@ -701,7 +708,7 @@ extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head,
     if (fin_smem < dsm) fin_smem = dsm;
 
     // the pilot pass, select and filter pass in one cooperative launch?
-    if (use_fused(di, L, rows, bn, mult)) {
+    if (use_fused(di, L, rows, bn, mult, top_k)) {
         if (cudaMemsetAsync(sync, 0, 2 * sizeof(uint32_t), st) != cudaSuccess) {
             cudaGetLastError();
             return DFLASH2_ERR_CUDA;

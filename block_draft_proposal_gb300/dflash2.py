@@ -29,7 +29,7 @@ DEVERR_ID_RANGE = 0x1
 DEVERR_TIMEOUT = 0x2
 DEVERR_SHORT = 0x4
 DEVINFO_TOPK_FALLBACK = 0x100
-ABI_VERSION = 5
+ABI_VERSION = 6
 
 # Every symbol include/dflash2.h declares.
 EXPORTS = (
@@ -105,7 +105,7 @@ def library():
         lib.dflash2_selector_walk_projected.restype = i32
         lib.dflash2_topk_merge.argtypes = [P, P, P, i32, i64, i32, i32, P, P, P, P]
         lib.dflash2_topk_merge.restype = i32
-        lib.dflash2_unary_topk_launches.argtypes = [i64, i64, f32, i32]
+        lib.dflash2_unary_topk_launches.argtypes = [i64, i64, i32, f32, i32]
         lib.dflash2_unary_topk_launches.restype = i32
         if lib.dflash2_abi_version() != ABI_VERSION:
             raise RuntimeError("libdflash2.so ABI version mismatch; rebuild it")

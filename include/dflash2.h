@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define DFLASH2_ABI_VERSION 5
+#define DFLASH2_ABI_VERSION 6
 
 typedef enum {
     DFLASH2_OK = 0,
@@ -138,11 +138,12 @@ size_t dflash2_unary_topk_workspace_min(int64_t rows, int64_t draft_vocab, int32
  * tiles, the thresholds and the filter tiles, then the final top-K) or 3 / 4
  * (pilot pass, pilot select, filter pass unless the pilot covers the vocab,
  * final top-K); 0 for rows == 0.  Host arithmetic only, nothing is queued;
- * -1 for a dtype, rows or draft_vocab that dflash2_unary_topk rejects, or
+ * -1 for a dtype, rows, draft_vocab or top_k that dflash2_unary_topk rejects, or
  * when no device is usable.  (dflash2_unary_topk also queues a memset of
  * 8 bytes before the cooperative launch.)
  */
-int32_t dflash2_unary_topk_launches(int64_t rows, int64_t draft_vocab, float mult, int32_t dtype);
+int32_t dflash2_unary_topk_launches(int64_t rows, int64_t draft_vocab, int32_t top_k, float mult,
+                                    int32_t dtype);
 dflash2_status dflash2_unary_topk(const void *h, const void *lm_head, int64_t rows,
                                   int32_t hidden, int64_t draft_vocab, int64_t target_vocab,
                                   float mult, float cap, int32_t top_k, int32_t dtype,

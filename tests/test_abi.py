@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.dflash2_abi_version() == 5
+    assert lib.dflash2_abi_version() == 6
     assert lib.dflash2_status_string(0) == b"ok"
     for s in range(1, 7):
         assert lib.dflash2_status_string(s) not in (b"ok", b"unknown status")
@@ -107,9 +107,10 @@ def test_workspace_sizes_are_host_arithmetic(lib):
     assert lib.dflash2_unary_topk_workspace_size(7, 4096, 8, 0) == 0   # fp32 path needs none
     # launch counts: fp32 is one kernel on any device, zero rows queue nothing,
     # a rejected dtype answers -1 (bf16 needs the device's SM count)
-    assert lib.dflash2_unary_topk_launches(7, 4096, ctypes.c_float(1.0), 0) == 1
-    assert lib.dflash2_unary_topk_launches(0, 4096, ctypes.c_float(1.0), 1) == 0
-    assert lib.dflash2_unary_topk_launches(7, 4096, ctypes.c_float(1.0), 3) == -1
+    assert lib.dflash2_unary_topk_launches(7, 4096, 8, ctypes.c_float(1.0), 0) == 1
+    assert lib.dflash2_unary_topk_launches(0, 4096, 8, ctypes.c_float(1.0), 1) == 0
+    assert lib.dflash2_unary_topk_launches(7, 4096, 8, ctypes.c_float(1.0), 3) == -1
+    assert lib.dflash2_unary_topk_launches(7, 4096, 129, ctypes.c_float(1.0), 0) == -1
     walk = lib.dflash2_selector_walk_workspace_size(32, 15, 4096, 64, 16, 1)
     assert walk >= 32 * 15 * 64 * 4 + 32 * 15 * 16 * (16 + 3) * 4   # partials + the lattice
     # top_k above the lattice mode's 32 needs the partials only

@@ -163,3 +163,21 @@ def test_zero_rows_is_a_no_op(cuda):
     W = torch.zeros((256, 64), dtype=torch.bfloat16, device=cuda)
     ids, vals, err = dflash2.unary_topk(h, W, 256, 1.0, 0.0, 8)
     assert ids.shape == (0, 8)
+
+
+def test_launch_plan_of_the_named_workloads(cuda):
+    """Which bf16 path each workload takes on a 152-SM GB300, so that both
+    the fused launch and the split passes stay covered by the parity tests
+    above: the Qwen3-8B-shaped workload is fused; the padded vocab (two more
+    tile rounds) and the stress size (16 rows per epilogue warp) are split."""
+    lib = dflash2.library()
+    plan = {c.name: lib.dflash2_unary_topk_launches(c.rows, c.draft_vocab, c.top_k, c.mult,
+                                                    dflash2.BF16 if c.dtype == "bf16"
+                                                    else dflash2.F32)
+            for c in synth.CONFIGS}
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the plan depends on the SM count")
+    assert plan["qwen3-8b-bf16"] == 2
+    assert plan["padded-vocab-bf16"] == 4
+    assert plan["stress-bf16"] == 4
+    assert plan["tiny-fp32"] == 1
