@@ -60,7 +60,17 @@ __device__ __forceinline__ int64_t in_block_pos(int64_t i, int bs, bool pow2) {
     return pow2 ? (i & (int64_t)(bs - 1)) : (i % bs);
 }
 
-template <typename T>
+// Tokens each thread covers (kTileTokens / kTokenLanes) and the largest tap
+// count whose loads are issued together up front.
+constexpr int kTokPerThread = kTileTokens / kTokenLanes;
+constexpr int kRegTaps = 8;
+
+// KT = 0: any tap count up to kMaxVecTaps, one tap's loads at a time.
+// KT > 0: at most KT taps; the tile's base coefficients are loaded once into
+// registers and every delta the thread needs is loaded before the first
+// multiply-add, so a thread waits for memory about once instead of once per
+// tap and token.  The arithmetic (order of taps, fp32 fma) is the same.
+template <typename T, int KT>
 __global__ void __launch_bounds__(kTileVecs *kTokenLanes)
     conv_vec_kernel(const T *__restrict__ x, const T *__restrict__ base,
                     const T *__restrict__ delta, int64_t dstride, T *__restrict__ out, int64_t n,
@@ -70,8 +80,11 @@ __global__ void __launch_bounds__(kTileVecs *kTokenLanes)
     constexpr int VN = V::N;
     extern __shared__ uint4 tile[];  // [kTileTokens + taps - 1][kTileVecs]
     const int nvec = hidden / VN;
-    const int64_t i0 = (int64_t)blockIdx.x * kTileTokens;
-    const int v0 = blockIdx.y * kTileVecs;
+    // one-dimensional grid, token tiles fastest (at 8192 tokens x 7168 channels
+    // 113 us against 128 us with vector tiles fastest, measured on GB300)
+    const int n_ttiles = (int)((n + kTileTokens - 1) / kTileTokens);
+    const int64_t i0 = (int64_t)(blockIdx.x % n_ttiles) * kTileTokens;
+    const int v0 = (int)(blockIdx.x / n_ttiles) * kTileVecs;
     const int halo = taps - 1;
     const int rows = kTileTokens + halo;
     const int tid = threadIdx.y * kTileVecs + threadIdx.x;
@@ -86,32 +99,74 @@ __global__ void __launch_bounds__(kTileVecs *kTokenLanes)
             val = __ldg(reinterpret_cast<const uint4 *>(x + gi * hidden) + gv);
         tile[idx] = val;
     }
-    __syncthreads();
 
     const int v = v0 + threadIdx.x;
-    if (v >= nvec) return;
+    const bool active = v < nvec;
     const int groups = hidden / group_size;
-    const int g = (v * VN) / group_size;
+    const int g = active ? (v * VN) / group_size : 0;
     const uint4 *base_v = reinterpret_cast<const uint4 *>(base) + v;
 
-    for (int tt = threadIdx.y; tt < kTileTokens; tt += kTokenLanes) {
-        const int64_t i = i0 + tt;
-        if (i >= n) break;
-        const int64_t pos = in_block_pos(i, bs, pow2);
-        const int tmax = (int)min((int64_t)(taps - 1), pos);
-        const T *drow = delta + i * dstride + g;
-        float acc[VN];
+    if constexpr (KT > 0) {
+        // loads first: the tile's base rows and every delta of this thread
+        uint4 bq[KT];
+        float d[kTokPerThread][KT];
 #pragma unroll
-        for (int e = 0; e < VN; ++e) acc[e] = 0.0f;
-        for (int t = 0; t <= tmax; ++t) {
-            const float d = V::scalar(drow[(int64_t)t * groups]);
-            float bf[VN], xf[VN];
-            V::unpack(__ldg(base_v + (int64_t)t * nvec), bf);
-            V::unpack(tile[(tt + halo - t) * kTileVecs + threadIdx.x], xf);
+        for (int t = 0; t < KT; ++t)
+            bq[t] = active && t < taps ? __ldg(base_v + (int64_t)t * nvec) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-            for (int e = 0; e < VN; ++e) acc[e] = fmaf(bf[e] + d, xf[e], acc[e]);
+        for (int j = 0; j < kTokPerThread; ++j) {
+            const int64_t i = i0 + threadIdx.y + j * kTokenLanes;
+            const int64_t pos = i < n ? in_block_pos(i, bs, pow2) : -1;
+            const T *drow = delta + i * dstride + g;
+#pragma unroll
+            for (int t = 0; t < KT; ++t)
+                d[j][t] = active && t <= pos && t < taps ? V::scalar(drow[(int64_t)t * groups]) : 0.0f;
         }
-        reinterpret_cast<uint4 *>(out + i * hidden)[v] = V::pack(acc);
+        __syncthreads();
+        if (!active) return;
+#pragma unroll
+        for (int j = 0; j < kTokPerThread; ++j) {
+            const int tt = threadIdx.y + j * kTokenLanes;
+            const int64_t i = i0 + tt;
+            if (i >= n) break;
+            const int64_t pos = in_block_pos(i, bs, pow2);
+            float acc[VN];
+#pragma unroll
+            for (int e = 0; e < VN; ++e) acc[e] = 0.0f;
+#pragma unroll
+            for (int t = 0; t < KT; ++t) {
+                if (t < taps && t <= pos) {
+                    float bf[VN], xf[VN];
+                    V::unpack(bq[t], bf);
+                    V::unpack(tile[(tt + halo - t) * kTileVecs + threadIdx.x], xf);
+#pragma unroll
+                    for (int e = 0; e < VN; ++e) acc[e] = fmaf(bf[e] + d[j][t], xf[e], acc[e]);
+                }
+            }
+            reinterpret_cast<uint4 *>(out + i * hidden)[v] = V::pack(acc);
+        }
+    } else {
+        __syncthreads();
+        if (!active) return;
+        for (int tt = threadIdx.y; tt < kTileTokens; tt += kTokenLanes) {
+            const int64_t i = i0 + tt;
+            if (i >= n) break;
+            const int64_t pos = in_block_pos(i, bs, pow2);
+            const int tmax = (int)min((int64_t)(taps - 1), pos);
+            const T *drow = delta + i * dstride + g;
+            float acc[VN];
+#pragma unroll
+            for (int e = 0; e < VN; ++e) acc[e] = 0.0f;
+            for (int t = 0; t <= tmax; ++t) {
+                const float dt = V::scalar(drow[(int64_t)t * groups]);
+                float bf[VN], xf[VN];
+                V::unpack(__ldg(base_v + (int64_t)t * nvec), bf);
+                V::unpack(tile[(tt + halo - t) * kTileVecs + threadIdx.x], xf);
+#pragma unroll
+                for (int e = 0; e < VN; ++e) acc[e] = fmaf(bf[e] + dt, xf[e], acc[e]);
+            }
+            reinterpret_cast<uint4 *>(out + i * hidden)[v] = V::pack(acc);
+        }
     }
 }
 
@@ -152,13 +207,24 @@ dflash2_status run_conv(const DeviceInfo &di, const void *x, const void *base, c
                         taps_eff <= kMaxVecTaps;
     if (vec_ok) {
         const int nvec = hidden / VN;
-        dim3 grid((unsigned)((n + kTileTokens - 1) / kTileTokens),
-                  (unsigned)((nvec + kTileVecs - 1) / kTileVecs));
+        const int64_t ctas = (int64_t)((nvec + kTileVecs - 1) / kTileVecs) *
+                             ((n + kTileTokens - 1) / kTileTokens);
+        if (ctas > INT32_MAX) return DFLASH2_ERR_INVALID_ARG;
+        const dim3 grid((unsigned)ctas);
         dim3 block(kTileVecs, kTokenLanes);
         const size_t smem = (size_t)(kTileTokens + taps_eff - 1) * kTileVecs * sizeof(uint4);
-        launch_k(conv_vec_kernel<T>, grid, block, smem, st, static_cast<const T *>(x),
-            static_cast<const T *>(base), static_cast<const T *>(delta),
-            dstride, static_cast<T *>(out), n, hidden, gs, taps_eff, bs, pow2);
+        const T *xp = static_cast<const T *>(x), *bp = static_cast<const T *>(base),
+                *dp = static_cast<const T *>(delta);
+        T *op = static_cast<T *>(out);
+        if (taps_eff <= 4)
+            launch_k(conv_vec_kernel<T, 4>, grid, block, smem, st, xp, bp, dp, dstride, op, n,
+                     hidden, gs, taps_eff, bs, pow2);
+        else if (taps_eff <= kRegTaps)
+            launch_k(conv_vec_kernel<T, kRegTaps>, grid, block, smem, st, xp, bp, dp, dstride, op,
+                     n, hidden, gs, taps_eff, bs, pow2);
+        else
+            launch_k(conv_vec_kernel<T, 0>, grid, block, smem, st, xp, bp, dp, dstride, op, n,
+                     hidden, gs, taps_eff, bs, pow2);
     } else {
         const int64_t total = n * hidden;
         int64_t blocks = (total + 255) / 256;
