@@ -24,7 +24,7 @@ from dataclasses import dataclass, replace
 import numpy as np
 
 PARTS = ("x", "base", "delta", "h", "lm_head", "A", "B", "proj", "uniforms",
-         "d2t", "anchors", "w_kp", "base2")
+         "d2t", "anchors", "w_kp", "base2", "lm_head_fp8", "w_scale")
 
 
 @dataclass(frozen=True)
@@ -102,6 +102,13 @@ def to_bf16_bits(a: np.ndarray) -> np.ndarray:
     return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
+def fp8_codes(a: np.ndarray) -> np.ndarray:
+    """E4M3 (float8_e4m3fn) codes of float32 values within +-448, as uint8."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    return t.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (b.astype(np.uint32) << 16).view(np.float32)
 
@@ -137,7 +144,8 @@ def d2t_table(w: Workload, seed: int | None = None):
     return (subset - np.arange(w.draft_vocab)).astype(np.int64)
 
 
-DEFAULT_PARTS = PARTS[:11]  # the proposal step's inputs; w_kp / base2 feed the conv prepare
+DEFAULT_PARTS = PARTS[:11]  # the proposal step's inputs; w_kp / base2 feed the conv prepare,
+                            # lm_head_fp8 / w_scale the FP8 head
 
 
 def make(w: Workload, parts=DEFAULT_PARTS) -> dict:
@@ -168,6 +176,15 @@ def make(w: Workload, parts=DEFAULT_PARTS) -> dict:
             out[p] = normal(s, p, (2 * w.taps * w.groups, w.hidden), w.w_std, dt)
         elif p == "base2":    # base_kernel of both conv sides [2, taps, hidden]
             out[p] = normal(s, p, (2, w.taps, w.hidden), w.w_std, dt)
+        elif p == "lm_head_fp8":
+            # an FP8 (E4M3) checkpoint of the head: codes of N(0, 64^2) draws
+            # (torch's float8_e4m3fn conversion), about 3 sigma inside +-448
+            out[p] = fp8_codes(rng(s, p).standard_normal(size=(w.draft_vocab, w.hidden),
+                                                         dtype=np.float32) * np.float32(64.0))
+        elif p == "w_scale":
+            # per-row dequantization scales: scale * code ~ N(0, w_std^2)
+            out[p] = (rng(s, p).uniform(0.5, 1.5, size=w.draft_vocab)
+                      * (w.w_std / 64.0)).astype(np.float32)
         elif p == "anchors":
             hi = min(w.draft_vocab, w.target_vocab)
             out[p] = rng(s, p).integers(0, hi, size=w.batch, dtype=np.int64)

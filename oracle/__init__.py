@@ -78,6 +78,14 @@ def _load():
             lib.oracle_kernel_projection.restype = None
             lib.oracle_verify.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i64, i32, P, P]
             lib.oracle_verify.restype = i64
+            lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_decode.restype = f64
+            lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+            lib.oracle_quantize_rows_e4m3.argtypes = [P, i64, i32, i32, P, P]
+            lib.oracle_quantize_rows_e4m3.restype = None
+            lib.oracle_unary_rows_fp8.argtypes = [P, P, P, P, P, i64, i32, i64, i64, f64, f64, P]
+            lib.oracle_unary_rows_fp8.restype = None
             _lib = lib
     return _lib
 
@@ -299,3 +307,50 @@ def verify(logits, temperatures, greedy, draft, cand, q, r):
                                    _ptr(cand), _ptr(q), _ptr(r), b, slots, k, vocab, code,
                                    _ptr(acc), _ptr(out))
     return acc, out, int(errors)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values (double) of E4M3 codes (uint8 array)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    lib = _load()
+    return np.array([lib.oracle_e4m3_decode(int(b)) for b in c.reshape(-1)],
+                    dtype=np.float64).reshape(c.shape)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """E4M3 codes (round to nearest even, saturating) of float32 values."""
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    lib = _load()
+    return np.array([lib.oracle_e4m3_encode(float(v)) for v in a.reshape(-1)],
+                    dtype=np.uint8).reshape(a.shape)
+
+
+def quantize_rows_e4m3(h):
+    """Per-row E4M3 codes and dequantization scales (uint8 [rows, hidden],
+    float32 [rows]) of a float32 or bf16-bits matrix."""
+    h, code = _elem(h)
+    rows, hidden = h.shape
+    q = np.empty((rows, hidden), dtype=np.uint8)
+    d = np.empty(rows, dtype=np.float32)
+    _load().oracle_quantize_rows_e4m3(_ptr(h), rows, hidden, code, _ptr(q), _ptr(d))
+    return q, d
+
+
+def unary_rows_fp8(qh, dh, qw, sw, target_vocab: int, mult: float, cap: float,
+                   rows=None) -> np.ndarray:
+    """u (double) of the W8A8 logits for the selected rows over the whole vocab."""
+    qh = np.ascontiguousarray(qh, dtype=np.uint8)
+    qw = np.ascontiguousarray(qw, dtype=np.uint8)
+    dh = np.ascontiguousarray(dh, dtype=np.float32)
+    sw = np.ascontiguousarray(sw, dtype=np.float32)
+    hidden = qh.shape[1]
+    vd = qw.shape[0]
+    if rows is None:
+        sel, n_sel = None, qh.shape[0]
+    else:
+        sel = np.ascontiguousarray(rows, dtype=np.int64)
+        n_sel = sel.shape[0]
+    u = np.empty((n_sel, vd), dtype=np.float64)
+    _load().oracle_unary_rows_fp8(_ptr(qh), _ptr(dh), _ptr(qw), _ptr(sw), _ptr(sel), n_sel,
+                                  hidden, vd, target_vocab, float(mult), float(cap), _ptr(u))
+    return u

@@ -624,3 +624,104 @@ int64_t oracle_verify(const void *logits, const float *temperatures, const uint8
     }
     return errors;
 }
+
+/* ---- (10) FP8 lm_head: E4M3 codes and W8A8 logits -------------------------
+ * The quantized-head path asked for beside the pages' method (sglang DFlash2
+ * PR: a quantized lm_head makes the selector fall back; the vLLM DSpark
+ * review's drafts ship NVFP4 heads).  Plain definitions:
+ *   - E4M3 ("e4m3fn" of the OCP 8-bit floating point formats): sign bit,
+ *     4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 holds
+ *     the subnormals m * 2^-9 (m = 0..7); no infinities; codes 0x7F / 0xFF are
+ *     NaN; the largest finite value is 448.  Encoding rounds to nearest, ties
+ *     to the even code, and saturates at +-448.
+ *   - Per-row activation quantization (W8A8 with dynamic per-token scales):
+ *     amax = max_j |h[m, j]| in fp32, inv = 448 / amax and d = amax / 448 in
+ *     fp32 (amax == 0: every code 0, d = 1), q[m, j] = E4M3(h[m, j] * inv)
+ *     with the product rounded to fp32 first.  These decide integer codes, so
+ *     they run in fp32, the precision of the kernel.
+ *   - Logits: z[m, v] = d[m] * s_w[v] * sum_j dec(q_h[m, j]) * dec(q_w[v, j]),
+ *     the sum in double (exact: each product has at most 8 significant bits
+ *     within 2^-18 .. 2^17), then the transform and mask of (3).
+ */
+double oracle_e4m3_decode(uint8_t c)
+{
+    const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    const double v = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+uint8_t oracle_e4m3_encode(float x)
+{
+    if (x != x)
+        return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    if (a >= 464.0) /* at or past the midpoint above 448: saturate */
+        return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) { /* subnormal: steps of 2^-9; m = 8 is the smallest normal */
+        const double m = nearbyint(ldexp(a, 9));
+        return sign | (uint8_t)m;
+    }
+    int e;
+    (void)frexp(a, &e); /* a = f * 2^e with f in [0.5, 1): unbiased exponent e - 1 */
+    e -= 1;
+    double m = nearbyint(ldexp(a, 3 - e)); /* in [8, 16] */
+    if (m == 16.0) {
+        m = 8.0;
+        e += 1;
+    }
+    const int code = ((e + 7) << 3) | ((int)m - 8);
+    return sign | (uint8_t)(code > 0x7E ? 0x7E : code);
+}
+
+void oracle_quantize_rows_e4m3(const void *h, int64_t rows, int32_t hidden, int32_t dtype,
+                               uint8_t *q, float *d)
+{
+    for (int64_t m = 0; m < rows; ++m) {
+        float amax = 0.0f;
+        for (int32_t j = 0; j < hidden; ++j) {
+            const float a = fabsf((float)load_elem(h, m * hidden + j, dtype));
+            if (a > amax)
+                amax = a;
+        }
+        if (amax == 0.0f) {
+            memset(q + m * hidden, 0, (size_t)hidden);
+            d[m] = 1.0f;
+            continue;
+        }
+        const float inv = 448.0f / amax; /* fp32 division, rounded once */
+        const float dm = amax / 448.0f;
+        d[m] = dm;
+        for (int32_t j = 0; j < hidden; ++j) {
+            const float x = (float)load_elem(h, m * hidden + j, dtype) * inv;
+            q[m * hidden + j] = oracle_e4m3_encode(x);
+        }
+    }
+}
+
+void oracle_unary_rows_fp8(const uint8_t *qh, const float *dh, const uint8_t *qw,
+                           const float *sw, const int64_t *rows, int64_t n_sel, int32_t hidden,
+                           int64_t draft_vocab, int64_t target_vocab, double mult, double cap,
+                           double *u_out)
+{
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t r = 0; r < n_sel; ++r) {
+        for (int64_t v = 0; v < draft_vocab; ++v) {
+            const int64_t m = rows ? rows[r] : r;
+            double u;
+            if (v >= target_vocab) {
+                u = -INFINITY;
+            } else {
+                double acc = 0.0;
+                for (int32_t j = 0; j < hidden; ++j)
+                    acc += oracle_e4m3_decode(qh[m * hidden + j]) *
+                           oracle_e4m3_decode(qw[v * hidden + j]);
+                const double z = (double)dh[m] * (double)sw[v] * acc;
+                u = cap > 0.0 ? cap * tanh(mult * z / cap) : mult * z;
+            }
+            u_out[r * draft_vocab + v] = u;
+        }
+    }
+}
