@@ -8,6 +8,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -69,6 +70,10 @@ dflash2_status current_device(DeviceInfo *info);
 // {64 columns, box_rows rows} box, 128-byte swizzle, zero fill out of bounds.
 dflash2_status encode_tmap_bf16(CUtensorMap *map, const void *base, uint64_t rows,
                                 uint64_t cols, uint32_t box_rows);
+// The same for 1-byte (elem_bytes = 1, uint8 codes) or bf16 (2) elements: the
+// box is one 128-byte swizzle row wide (128 / elem_bytes columns).
+dflash2_status encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                              uint32_t box_rows, uint32_t elem_bytes);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
@@ -383,6 +388,17 @@ __device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t a_des
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// The same for 8-bit operands (kind::f8f6f4: K = 32 elements = 32 bytes per MMA,
+// so the shared-memory descriptors advance exactly as for bf16).
+__device__ __forceinline__ void tc_mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Arrive once on the mbarrier at this shared offset in every CTA of `mask`
 // when the pair's tcgen05 operations issued so far complete.
 __device__ __forceinline__ void tc_commit_pair_mc(uint64_t *bar, uint16_t mask) {
@@ -416,6 +432,15 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
 
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 x bf16 -> fp32,
 // both operands K-major, tile M x N.
+// Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format code 0 for
+// both), fp32 accumulator, K-major operands.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n) {
+    return (1u << 4)                      // accumulator format fp32
+           | (0u << 7)                    // A format E4M3
+           | (0u << 10)                   // B format E4M3
+           | ((uint32_t)(n >> 3) << 17)   // N / 8
+           | ((uint32_t)(m >> 4) << 24);  // M / 16
+}
 __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
     return (1u << 4)                      // accumulator format fp32
            | (1u << 7)                    // A format bf16

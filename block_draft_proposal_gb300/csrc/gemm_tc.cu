@@ -71,6 +71,21 @@ __device__ __forceinline__ void mma_stage(uint32_t d, uint64_t wd, uint64_t hd, 
     }
 }
 
+// The 8 MMAs of one stage for 8-bit operands on a CTA pair (K = 32 elements,
+// still 32 bytes per MMA: the same descriptor steps, twice the hidden span).
+__device__ __forceinline__ void mma_stage_f8_pair(uint32_t d, uint64_t wd, uint64_t hd,
+                                                  uint32_t wsub, uint32_t hsub, uint32_t idesc,
+                                                  uint32_t acc0) {
+    tc_mma_f8_pair(d, wd, hd, idesc, acc0);
+    tc_mma_f8_pair(d, wd + 2, hd + 2, idesc, 1u);
+    tc_mma_f8_pair(d, wd + 4, hd + 4, idesc, 1u);
+    tc_mma_f8_pair(d, wd + 6, hd + 6, idesc, 1u);
+    tc_mma_f8_pair(d, wd + wsub, hd + hsub, idesc, 1u);
+    tc_mma_f8_pair(d, wd + wsub + 2, hd + hsub + 2, idesc, 1u);
+    tc_mma_f8_pair(d, wd + wsub + 4, hd + hsub + 4, idesc, 1u);
+    tc_mma_f8_pair(d, wd + wsub + 6, hd + hsub + 6, idesc, 1u);
+}
+
 // Waits (bounded) until the last `stages` loads this producer issued have
 // landed, so no copy is still writing shared memory when the CTA leaves.
 __device__ __forceinline__ void drain_loads(uint64_t *full_bar, uint32_t issued, uint32_t stages) {
@@ -161,6 +176,19 @@ __device__ __forceinline__ void group_max_chunk(const GemmParams &p, const float
     if (lane < ncols && m < p.rows_h) p.pmax[(int64_t)m * p.ld_pmax + g] = mine;
 }
 
+// fp8: C = acc * (a_scale[m] * w_scale[v]) for a chunk of 32 tokens m0 ..
+// m0 + 31 (lane i loads a_scale[m0 + i], zero past the last token; wsv is the
+// thread's w_scale[v]).  Returns the lane's a_scale, with which a single
+// column re-read later is scaled by the same expression.
+__device__ __forceinline__ float fp8_scale_chunk(const GemmParams &p, float (&z)[32], int m0,
+                                                 float wsv, int lane) {
+    const int m = m0 + lane;
+    const float a = m < p.rows_h ? __ldg(p.a_scale + m) : 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] *= __shfl_sync(0xFFFFFFFFu, a, i) * wsv;
+    return a;
+}
+
 // Per-epilogue-warp shared scratch of the filter mode: the thresholds of the
 // current tile's tokens and a buffer of survivors waiting for their global
 // slots.
@@ -195,7 +223,8 @@ __device__ __noinline__ void flush_survivors(const GemmParams &p, EpiScratch &es
 // nbuf counts them (warp-uniform).
 __device__ __forceinline__ void filter_chunk(const GemmParams &p, const float (&z)[32], int64_t v,
                                              int m0, int c0, uint32_t tcol, EpiScratch &es,
-                                             int &nbuf, int lane) {
+                                             int &nbuf, int lane, float asc = 1.0f,
+                                             float wsv = 1.0f) {
     const bool valid_v = v < p.rows_w && v < p.target_vocab;
     float pre[32];  // the 32 tokens' pre-thresholds: broadcast 16-byte shared loads
 #pragma unroll
@@ -218,7 +247,8 @@ __device__ __forceinline__ void filter_chunk(const GemmParams &p, const float (&
     while (cols) {  // warp-uniform
         const int i = __ffs(cols) - 1;
         cols &= cols - 1;
-        const float zi = tmem_ld1_wait(tcol + (uint32_t)i);
+        float zi = tmem_ld1_wait(tcol + (uint32_t)i);
+        if (p.fp8) zi *= __shfl_sync(0xFFFFFFFFu, asc, i) * wsv;  // as fp8_scale_chunk
         const uint64_t th = shfl_u64(th_lane, i);
         bool pass = false;
         uint64_t key = 0;
@@ -574,11 +604,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     if (leader) mbar_arrive_expect_tx(&full_bar[s], 2 * (kWStageBytes + h_stage));
                     uint8_t *ws = w_smem + s * kWStageBytes;
                     uint8_t *hs = h_smem + s * h_stage;
-                    const int k0 = kb * kGemmStageK;  // boxes past `hidden` read zeros
+                    const int k0 = kb * 2 * p.box_k;  // boxes past `hidden` read zeros
                     tma_load_2d_pair(ws, &tm_w, fb, k0, wrow);
-                    tma_load_2d_pair(ws + kWTileBytes, &tm_w, fb, k0 + kGemmTileK, wrow);
+                    tma_load_2d_pair(ws + kWTileBytes, &tm_w, fb, k0 + p.box_k, wrow);
                     tma_load_2d_pair(hs, &tm_h, fb, k0, hrow);
-                    tma_load_2d_pair(hs + h_sub, &tm_h, fb, k0 + kGemmTileK, hrow);
+                    tma_load_2d_pair(hs + h_sub, &tm_h, fb, k0 + p.box_k, hrow);
                     ++issued;
                     if (++s == (uint32_t)p.stages) {
                         s = 0;
@@ -591,7 +621,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
-            const uint32_t idesc = idesc_bf16(2 * kGemmTileW, p.bn);
+            const uint32_t idesc =
+                p.fp8 ? idesc_e4m3(2 * kGemmTileW, p.bn) : idesc_bf16(2 * kGemmTileW, p.bn);
             const uint64_t wd0 = sw128_desc(smem_u32(w_smem)), hd0 = sw128_desc(smem_u32(h_smem));
             const uint32_t w_st = kWStageBytes >> 4, h_st = h_stage >> 4;  // descriptor units
             const uint32_t w_sub = kWTileBytes >> 4, h_sb = h_sub >> 4;
@@ -612,8 +643,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                         break;
                     }
                     tc_fence_after();
-                    mma_stage<true>(d_tmem, wd0 + s * w_st, hd0 + s * h_st, w_sub, h_sb, idesc,
-                                    kb > 0 ? 1u : 0u);
+                    if (p.fp8)
+                        mma_stage_f8_pair(d_tmem, wd0 + s * w_st, hd0 + s * h_st, w_sub, h_sb,
+                                          idesc, kb > 0 ? 1u : 0u);
+                    else
+                        mma_stage<true>(d_tmem, wd0 + s * w_st, hd0 + s * h_st, w_sub, h_sb,
+                                        idesc, kb > 0 ? 1u : 0u);
                     tc_commit_pair_mc(&empty_bar[s], 0x3);
                     if (++s == (uint32_t)p.stages) {
                         s = 0;
@@ -646,15 +681,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             }
             __syncwarp();
         };
+        // fp8: this thread's weight-row scale
+        const auto row_scale = [&](int64_t v) {
+            return p.fp8 ? (v < p.rows_w ? __ldg(p.w_scale + v) : 0.0f) : 1.0f;
+        };
         const auto filter_tile = [&](const Item &item, int a) {
             const int m_tile = item.nt * p.bn;
             const int64_t v = (int64_t)item.wt * p.unit + row_in_unit;
+            const float wsv = row_scale(v);
             const uint32_t tbase = tmem + (uint32_t)a * p.acc_cols + ((uint32_t)(quarter * 32) << 16);
             int nbuf = 0;
             for (int c0 = 0; c0 < p.bn; c0 += 32) {
                 float z[32];
                 tmem_ld32_wait(tbase + (uint32_t)c0, z);
-                filter_chunk(p, z, v, m_tile + c0, c0, tbase + (uint32_t)c0, es, nbuf, lane);
+                const float asc = p.fp8 ? fp8_scale_chunk(p, z, m_tile + c0, wsv, lane) : 1.0f;
+                filter_chunk(p, z, v, m_tile + c0, c0, tbase + (uint32_t)c0, es, nbuf, lane, asc,
+                             wsv);
             }
             tc_fence_before();
             if (nbuf > 0) flush_survivors(p, es, nbuf, lane);
@@ -682,9 +724,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 const uint32_t tbase =
                     tmem + (uint32_t)a * p.acc_cols + ((uint32_t)(quarter * 32) << 16);
                 const int g = item.j * (p.unit / 32) + row_in_unit / 32;
+                const float wsv = row_scale(v);
                 for (int c0 = 0; c0 < p.bn; c0 += 32) {
                     float z[32];
                     tmem_ld32_wait(tbase + (uint32_t)c0, z);
+                    if (p.fp8) fp8_scale_chunk(p, z, item.nt * p.bn + c0, wsv, lane);
                     group_max_chunk(p, z, valid, item.nt * p.bn + c0, min(32, p.bn - c0), g, lane);
                 }
                 counter_arrive(p.sync, lane);
@@ -712,10 +756,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             }
             const int m_tile = item.nt * p.bn;
             const int64_t v = (int64_t)item.wt * p.unit + row_in_unit;
+            const float wsv = row_scale(v);
             const uint32_t tbase = tmem + (uint32_t)a * p.acc_cols + ((uint32_t)(quarter * 32) << 16);
             for (int c0 = 0; c0 < p.bn; c0 += 32) {
                 float z[32];
                 tmem_ld32_wait(tbase + (uint32_t)c0, z);
+                if (p.fp8) fp8_scale_chunk(p, z, m_tile + c0, wsv, lane);
                 epilogue_chunk(p, z, v, row_in_unit, m_tile + c0, min(32, p.bn - c0), item, lane);
             }
             tc_fence_before();
@@ -781,9 +827,11 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     if (p.rows_h <= 0 || p.rows_w <= 0 || p.hidden <= 0) return DFLASH2_OK;
     if (p.mode == kGemmStore) pair = false;  // the projection keeps one CTA per tile
     if (pair && di.sm_count < 2) return DFLASH2_ERR_UNSUPPORTED_DEVICE;  // the caller's layout assumes pairs
+    if (p.fp8 && (!pair || p.hidden % 16 != 0)) return DFLASH2_ERR_INVALID_ARG;
     p.unit = pair ? 2 * kGemmTileW : kGemmTileW;
     p.n_tok_tiles = (p.rows_h + p.bn - 1) / p.bn;
-    p.num_kb = (p.hidden + kGemmStageK - 1) / kGemmStageK;
+    p.box_k = p.fp8 ? 2 * kGemmTileK : kGemmTileK;  // one 128-byte row: 128 codes or 64 bf16
+    p.num_kb = (p.hidden + 2 * p.box_k - 1) / (2 * p.box_k);
     p.kb_per_split = (p.num_kb + p.k_splits - 1) / p.k_splits;
     p.k_splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;  // every split gets >= 1 block
     p.n_wtiles = (p.rows_w + p.unit - 1) / p.unit;
@@ -800,7 +848,7 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     while (acc < (uint32_t)p.bn) acc <<= 1;
     p.acc_cols = acc;
     const uint32_t h_rows = pair ? (uint32_t)p.bn / 2 : (uint32_t)p.bn;
-    const uint32_t stage_bytes = kWStageBytes + h_rows * kGemmStageK * 2;
+    const uint32_t stage_bytes = kWStageBytes + h_rows * kGemmStageK * 2;  // same bytes for fp8
     const bool fused = p.mode == kGemmFused;
     if (fused && !pair) return DFLASH2_ERR_INVALID_ARG;
     const size_t epi_bytes =
@@ -812,9 +860,11 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     const size_t smem = (size_t)stages * stage_bytes + epi_bytes + 1024;
 
     CUtensorMap tm_w, tm_h;
-    dflash2_status s = encode_tmap_bf16(&tm_w, w, (uint64_t)p.rows_w, (uint64_t)p.hidden, kGemmTileW);
+    const uint32_t eb = p.fp8 ? 1 : 2;
+    dflash2_status s =
+        encode_tmap_2d(&tm_w, w, (uint64_t)p.rows_w, (uint64_t)p.hidden, kGemmTileW, eb);
     if (s != DFLASH2_OK) return s;
-    s = encode_tmap_bf16(&tm_h, h, (uint64_t)p.rows_h, (uint64_t)p.hidden, h_rows);
+    s = encode_tmap_2d(&tm_h, h, (uint64_t)p.rows_h, (uint64_t)p.hidden, h_rows, eb);
     if (s != DFLASH2_OK) return s;
 
     s = set_gemm_attrs(di);

@@ -47,6 +47,11 @@ dflash2_status current_device(DeviceInfo *info) {
 
 dflash2_status encode_tmap_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                                 uint32_t box_rows) {
+    return encode_tmap_2d(map, base, rows, cols, box_rows, 2);
+}
+
+dflash2_status encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                              uint32_t box_rows, uint32_t elem_bytes) {
     {
         std::lock_guard<std::mutex> lock(g_mu);
         if (!g_encode) {
@@ -62,10 +67,12 @@ dflash2_status encode_tmap_bf16(CUtensorMap *map, const void *base, uint64_t row
         }
     }
     cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {64, box_rows};
+    cuuint64_t strides[1] = {cols * elem_bytes};
+    cuuint32_t box[2] = {128 / elem_bytes, box_rows};  // one 128-byte swizzle row wide
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+    const CUtensorMapDataType type =
+        elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUresult r = g_encode(map, type, 2, const_cast<void *>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

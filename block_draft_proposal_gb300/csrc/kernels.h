@@ -69,6 +69,12 @@ struct GemmParams {
     int64_t ld_pmax;
     int32_t top_k;
     uint32_t *sync;
+    // fp8: E4M3 operands (kind::f8f6f4; a box covers 128 hidden elements, a
+    // stage 256); C = acc * (a_scale[m] * w_scale[v]) before the epilogue
+    int32_t fp8;
+    int32_t box_k;  // hidden elements per TMA box (filled by launch_gemm_tc)
+    const float *a_scale;
+    const float *w_scale;
 };
 
 // Pilot tiling of a weight matrix with n_wtiles units of unit_rows rows:
@@ -91,6 +97,10 @@ inline void pilot_layout(int64_t n_wtiles, int32_t *n_pilot, int32_t *stride, in
 // pair: run the pilot / filter / fused modes on CTA pairs (2-CTA MMA, 256-row units).
 dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h, GemmParams p,
                               cudaStream_t st, bool pair = false);
+
+// Per-row E4M3 quantization (quant.cu): q [rows, cols] codes, d [rows] scales.
+dflash2_status launch_quant_rows_e4m3(const void *x, int32_t dtype, int64_t rows, int32_t cols,
+                                      uint8_t *q, float *d, cudaStream_t st);
 
 // Epilogue warps of one fused launch (4 per CTA, every CTA resident at once),
 // or 0 when the device cannot hold such a launch.  Host-side, cached per device.

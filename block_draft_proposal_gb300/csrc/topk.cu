@@ -26,6 +26,7 @@
 #include "kernels.h"
 
 #include <algorithm>
+#include <type_traits>
 
 namespace dflash2 {
 namespace {
@@ -276,16 +277,23 @@ template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
 template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) {
     return __bfloat162float(v);
 }
+template <> __device__ __forceinline__ float to_f<__nv_fp8_e4m3>(__nv_fp8_e4m3 v) {
+    return static_cast<float>(v);
+}
 
 // Exact top-k of one row on CUDA cores: every vocab row's u is computed in
 // fp32 (lane-strided FMA over hidden, then a warp tree sum), keys that reach
 // the running threshold are buffered in shared memory, and a full buffer is
 // cut back to its k best (whose k-th key becomes the new threshold).  Leaves
 // the sorted result in sh.top and returns how many keys it holds.
+// With w_scale (fp8 codes), the dot product is scaled by a_scale * w_scale[v],
+// the expression the tensor-core epilogue uses.
 template <typename T>
 __device__ int direct_row_topk(const T *__restrict__ hrow, const T *__restrict__ w, int hidden,
                                int64_t draft_vocab, int64_t target_vocab, float mult, float cap,
-                               int k, float *hs, uint64_t *buf, SelectShared &sh) {
+                               int k, float *hs, uint64_t *buf, SelectShared &sh,
+                               const float *__restrict__ w_scale = nullptr,
+                               float a_scale = 1.0f) {
     for (int j = threadIdx.x; j < hidden; j += blockDim.x) hs[j] = to_f(hrow[j]);
     if (threadIdx.x == 0) sh.count = 0;
     __syncthreads();
@@ -301,6 +309,7 @@ __device__ int direct_row_topk(const T *__restrict__ hrow, const T *__restrict__
             float acc = 0.0f;
             for (int j = lane; j < hidden; j += 32) acc = fmaf(hs[j], to_f(wr[j]), acc);
             acc = warp_sum(acc);
+            if (w_scale) acc *= a_scale * __ldg(w_scale + v);
             if (lane == 0) {
                 const uint64_t key = make_key(unary_transform(acc, mult, cap), (uint32_t)v);
                 if (key >= theta) {
@@ -431,12 +440,15 @@ __global__ void __launch_bounds__(kSelThreads)
 }
 
 // Final exact top-k of each row's candidate list (or the exact CUDA-core
-// recomputation of the row when its list overflowed).
+// recomputation of the row when its list overflowed; T = the operands' type,
+// with the fp8 scales when T is the E4M3 code).
+template <typename T>
 __global__ void __launch_bounds__(kSelThreads)
     finalize_kernel(const uint32_t *__restrict__ cnt, const uint64_t *__restrict__ cand,
                     int cand_cap, int k, int64_t *ids, float *vals, int32_t *err,
-                    const __nv_bfloat16 *__restrict__ h, const __nv_bfloat16 *__restrict__ w,
-                    int hidden, int64_t draft_vocab, int64_t target_vocab, float mult, float cap) {
+                    const T *__restrict__ h, const T *__restrict__ w, int hidden,
+                    int64_t draft_vocab, int64_t target_vocab, float mult, float cap,
+                    const float *__restrict__ a_scale, const float *__restrict__ w_scale) {
     grid_dep_wait();
     __shared__ SelectShared sh;
     extern __shared__ __align__(16) uint8_t dyn[];
@@ -446,8 +458,9 @@ __global__ void __launch_bounds__(kSelThreads)
         float *hs = reinterpret_cast<float *>(dyn);
         uint64_t *buf =
             reinterpret_cast<uint64_t *>(dyn + (((size_t)hidden * 4 + 15) & ~(size_t)15));
-        const int got = direct_row_topk<__nv_bfloat16>(h + row * hidden, w, hidden, draft_vocab,
-                                                       target_vocab, mult, cap, k, hs, buf, sh);
+        const int got = direct_row_topk<T>(h + row * hidden, w, hidden, draft_vocab, target_vocab,
+                                           mult, cap, k, hs, buf, sh, w_scale,
+                                           a_scale ? a_scale[row] : 1.0f);
         write_row(sh, got, k, row, ids, vals, err);
         if (threadIdx.x == 0 && err) atomicOr(err, DFLASH2_DEVINFO_TOPK_FALLBACK);
         return;
@@ -588,8 +601,10 @@ dflash2_status set_select_attrs(int device) {
     if (device < 0 || device >= 64) return DFLASH2_ERR_CUDA;
     if (g_topk_attr[device]) return DFLASH2_OK;
     const int bytes = 160 * 1024;
-    if (cudaFuncSetAttribute(finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
-            cudaSuccess ||
+    if (cudaFuncSetAttribute(finalize_kernel<__nv_bfloat16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(finalize_kernel<__nv_fp8_e4m3>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
         cudaFuncSetAttribute(pilot_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              bytes) != cudaSuccess ||
         cudaFuncSetAttribute(direct_topk_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -605,76 +620,18 @@ dflash2_status set_select_attrs(int device) {
 
 constexpr int kMaxHidden = 32768;  // the exact path stages one h row as fp32 in shared memory
 
-}  // namespace
-}  // namespace dflash2
-
-using namespace dflash2;
-
-extern "C" size_t dflash2_unary_topk_workspace_size(int64_t rows, int64_t draft_vocab, int32_t top_k,
-                                                    int32_t dtype) {
-    if (rows <= 0 || draft_vocab <= 0 || top_k <= 0) return 0;
-    if (dtype == DFLASH2_F32) return 0;
-    const TopkLayout L = topk_layout(rows, draft_vocab);
-    return L.fixed_bytes + (size_t)rows * recommended_cap(L, top_k) * 8;
-}
-
-extern "C" size_t dflash2_unary_topk_workspace_min(int64_t rows, int64_t draft_vocab, int32_t top_k,
-                                                   int32_t dtype) {
-    if (rows <= 0 || draft_vocab <= 0 || top_k <= 0) return 0;
-    if (dtype == DFLASH2_F32) return 0;
-    const TopkLayout L = topk_layout(rows, draft_vocab);
-    return L.fixed_bytes + (size_t)rows * top_k * 8;
-}
-
-extern "C" int32_t dflash2_unary_topk_launches(int64_t rows, int64_t draft_vocab, int32_t top_k,
-                                               float mult, int32_t dtype) {
-    if (dtype != DFLASH2_F32 && dtype != DFLASH2_BF16) return -1;
-    if (rows < 0 || rows > INT32_MAX || draft_vocab <= 0 || draft_vocab > INT32_MAX ||
-        top_k <= 0 || top_k > kMaxTopK || top_k > draft_vocab)
-        return -1;
-    if (rows == 0) return 0;
-    if (dtype == DFLASH2_F32) return 1;
-    DeviceInfo di;
-    if (current_device(&di) != DFLASH2_OK) return -1;
-    const TopkLayout L = topk_layout(rows, draft_vocab);
-    if (use_fused(di, L, rows, token_tile(rows), mult, top_k)) return 2;  // fused GEMM, finalize
-    return L.n_wtiles > L.n_pilot ? 4 : 3;  // pilot, select, (filter), finalize
-}
-
-extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head, int64_t rows,
-                                             int32_t hidden, int64_t draft_vocab,
-                                             int64_t target_vocab, float mult, float cap,
-                                             int32_t top_k, int32_t dtype, int64_t *cand_ids,
-                                             float *cand_u, void *workspace, size_t ws_bytes,
-                                             int32_t *err_word, void *stream) {
-    if (dtype != DFLASH2_F32 && dtype != DFLASH2_BF16) return DFLASH2_ERR_UNSUPPORTED_DTYPE;
-    if (rows < 0 || rows > INT32_MAX || hidden <= 0 || hidden > kMaxHidden || draft_vocab <= 0 ||
-        draft_vocab > INT32_MAX || target_vocab <= 0 || top_k <= 0 || top_k > kMaxTopK ||
-        top_k > target_vocab || top_k > draft_vocab || !(cap >= 0.0f))
-        return DFLASH2_ERR_INVALID_ARG;
-    if (rows == 0) return DFLASH2_OK;
-    if (!h || !lm_head || !cand_ids || !cand_u) return DFLASH2_ERR_INVALID_ARG;
-    if (reinterpret_cast<uintptr_t>(cand_ids) % 8 != 0 || reinterpret_cast<uintptr_t>(cand_u) % 4 != 0)
-        return DFLASH2_ERR_MISALIGNED;
-    DeviceInfo di;
-    dflash2_status s = current_device(&di);
-    if (s != DFLASH2_OK) return s;
-    s = set_select_attrs(di.device);
-    if (s != DFLASH2_OK) return s;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+// The tensor-core top-K (T = __nv_bfloat16, or __nv_fp8_e4m3 codes with the
+// per-row scales a_scale [rows] and w_scale [draft_vocab]): the pilot pass,
+// select and filter pass (or their fused launch), then the final top-K.  The
+// arguments are checked by the caller.
+template <typename T>
+dflash2_status run_tc_topk(const DeviceInfo &di, const void *h, const void *lm_head,
+                           const float *a_scale, const float *w_scale, int64_t rows, int hidden,
+                           int64_t draft_vocab, int64_t target_vocab, float mult, float cap,
+                           int top_k, int64_t *cand_ids, float *cand_u, void *workspace,
+                           size_t ws_bytes, int32_t *err_word, cudaStream_t st) {
+    dflash2_status s = DFLASH2_OK;
     const size_t dsm = direct_smem_bytes(hidden);
-
-    if (dtype == DFLASH2_F32) {
-        if ((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(lm_head)) % 4 != 0)
-            return DFLASH2_ERR_MISALIGNED;
-        launch_k(direct_topk_kernel<float>, (unsigned)rows, kSelThreads, dsm, st,
-            static_cast<const float *>(h), static_cast<const float *>(lm_head), hidden, draft_vocab,
-
-            target_vocab, mult, cap, top_k, cand_ids, cand_u, err_word);
-        return launch_status();
-    }
-
-    if (hidden % 8 != 0 || !aligned16(h) || !aligned16(lm_head)) return DFLASH2_ERR_MISALIGNED;
     const TopkLayout L = topk_layout(rows, draft_vocab);
     if (!workspace || ws_bytes < L.fixed_bytes + (size_t)rows * top_k * 8)
         return DFLASH2_ERR_WORKSPACE;
@@ -700,6 +657,9 @@ extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head,
     p.mult = mult;
     p.cap = cap;
     p.err = err_word;
+    p.fp8 = std::is_same<T, __nv_fp8_e4m3>::value ? 1 : 0;
+    p.a_scale = a_scale;
+    p.w_scale = w_scale;
 
     const bool pairs = true;
     const int unit = unit_rows();
@@ -727,10 +687,10 @@ extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head,
         p.ld_pmax = (int64_t)L.n_pilot * (unit / 32);
         s = launch_gemm_tc(di, lm_head, h, p, st, pairs);
         if (s != DFLASH2_OK) return s;
-        launch_k(finalize_kernel, (unsigned)rows, kSelThreads, fin_smem, st, cnt, cand,
-                 (int)cap_keys, top_k, cand_ids, cand_u, err_word,
-                 static_cast<const __nv_bfloat16 *>(h), static_cast<const __nv_bfloat16 *>(lm_head),
-                 hidden, draft_vocab, target_vocab, mult, cap);
+        launch_k(finalize_kernel<T>, (unsigned)rows, kSelThreads, fin_smem, st, cnt, cand,
+                 (int)cap_keys, top_k, cand_ids, cand_u, err_word, static_cast<const T *>(h),
+                 static_cast<const T *>(lm_head), hidden, draft_vocab, target_vocab, mult, cap,
+                 a_scale, w_scale);
         return launch_status();
     }
 
@@ -769,9 +729,137 @@ extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head,
 
     // staged keys (a row with at most kSmemKeys candidates) followed by the
     // collect buffer
-    launch_k(finalize_kernel, (unsigned)rows, kSelThreads, fin_smem, st, cnt, cand, (int)cap_keys,
-        top_k, cand_ids, cand_u, err_word,
-        static_cast<const __nv_bfloat16 *>(h), static_cast<const __nv_bfloat16 *>(lm_head), hidden,
-        draft_vocab, target_vocab, mult, cap);
+    launch_k(finalize_kernel<T>, (unsigned)rows, kSelThreads, fin_smem, st, cnt, cand,
+             (int)cap_keys, top_k, cand_ids, cand_u, err_word, static_cast<const T *>(h),
+             static_cast<const T *>(lm_head), hidden, draft_vocab, target_vocab, mult, cap,
+             a_scale, w_scale);
     return launch_status();
+}
+
+}  // namespace
+}  // namespace dflash2
+
+using namespace dflash2;
+
+extern "C" size_t dflash2_unary_topk_workspace_size(int64_t rows, int64_t draft_vocab, int32_t top_k,
+                                                    int32_t dtype) {
+    if (rows <= 0 || draft_vocab <= 0 || top_k <= 0) return 0;
+    if (dtype == DFLASH2_F32) return 0;
+    const TopkLayout L = topk_layout(rows, draft_vocab);
+    return L.fixed_bytes + (size_t)rows * recommended_cap(L, top_k) * 8;
+}
+
+extern "C" size_t dflash2_unary_topk_workspace_min(int64_t rows, int64_t draft_vocab, int32_t top_k,
+                                                   int32_t dtype) {
+    if (rows <= 0 || draft_vocab <= 0 || top_k <= 0) return 0;
+    if (dtype == DFLASH2_F32) return 0;
+    const TopkLayout L = topk_layout(rows, draft_vocab);
+    return L.fixed_bytes + (size_t)rows * top_k * 8;
+}
+
+extern "C" int32_t dflash2_unary_topk_launches(int64_t rows, int64_t draft_vocab, int32_t top_k,
+                                               float mult, int32_t dtype) {
+    if (dtype != DFLASH2_F32 && dtype != DFLASH2_BF16) return -1;
+    if (rows < 0 || rows > INT32_MAX || draft_vocab <= 0 || draft_vocab > INT32_MAX ||
+        top_k <= 0 || top_k > kMaxTopK || top_k > draft_vocab)
+        return -1;
+    if (rows == 0) return 0;
+    if (dtype == DFLASH2_F32) return 1;
+    DeviceInfo di;
+    if (current_device(&di) != DFLASH2_OK) return -1;
+    const TopkLayout L = topk_layout(rows, draft_vocab);
+    if (use_fused(di, L, rows, token_tile(rows), mult, top_k)) return 2;  // fused GEMM, finalize
+    return L.n_wtiles > L.n_pilot ? 4 : 3;  // pilot, select, (filter), finalize
+}
+
+namespace {
+inline size_t fp8_ws_prefix(int64_t rows, int32_t hidden) {
+    return align256((size_t)rows * hidden) + align256((size_t)rows * 4);
+}
+}  // namespace
+
+extern "C" size_t dflash2_unary_topk_fp8_workspace_size(int64_t rows, int32_t hidden,
+                                                        int64_t draft_vocab, int32_t top_k) {
+    if (rows <= 0 || hidden <= 0 || draft_vocab <= 0 || top_k <= 0) return 0;
+    return fp8_ws_prefix(rows, hidden) +
+           dflash2_unary_topk_workspace_size(rows, draft_vocab, top_k, DFLASH2_BF16);
+}
+
+extern "C" dflash2_status dflash2_unary_topk_fp8(const void *h, int32_t h_dtype,
+                                                 const uint8_t *lm_head_q, const float *w_scale,
+                                                 int64_t rows, int32_t hidden, int64_t draft_vocab,
+                                                 int64_t target_vocab, float mult, float cap,
+                                                 int32_t top_k, int64_t *cand_ids, float *cand_u,
+                                                 void *workspace, size_t ws_bytes,
+                                                 int32_t *err_word, void *stream) {
+    if (h_dtype != DFLASH2_F32 && h_dtype != DFLASH2_BF16) return DFLASH2_ERR_UNSUPPORTED_DTYPE;
+    if (rows < 0 || rows > INT32_MAX || hidden <= 0 || hidden > kMaxHidden || draft_vocab <= 0 ||
+        draft_vocab > INT32_MAX || target_vocab <= 0 || top_k <= 0 || top_k > kMaxTopK ||
+        top_k > target_vocab || top_k > draft_vocab || !(cap >= 0.0f))
+        return DFLASH2_ERR_INVALID_ARG;
+    if (rows == 0) return DFLASH2_OK;
+    if (!h || !lm_head_q || !w_scale || !cand_ids || !cand_u) return DFLASH2_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(cand_ids) % 8 != 0 ||
+        reinterpret_cast<uintptr_t>(cand_u) % 4 != 0 ||
+        reinterpret_cast<uintptr_t>(w_scale) % 4 != 0 ||
+        reinterpret_cast<uintptr_t>(h) % (h_dtype == DFLASH2_BF16 ? 2 : 4) != 0)
+        return DFLASH2_ERR_MISALIGNED;
+    // TMA rows of codes: a 16-byte row stride and base
+    if (hidden % 16 != 0 || !aligned16(lm_head_q)) return DFLASH2_ERR_MISALIGNED;
+    const size_t prefix = fp8_ws_prefix(rows, hidden);
+    if (!workspace || ws_bytes < prefix) return DFLASH2_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return DFLASH2_ERR_MISALIGNED;
+    DeviceInfo di;
+    dflash2_status s = current_device(&di);
+    if (s != DFLASH2_OK) return s;
+    s = set_select_attrs(di.device);
+    if (s != DFLASH2_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint8_t *qh = ws;
+    float *dh = reinterpret_cast<float *>(ws + align256((size_t)rows * hidden));
+    s = launch_quant_rows_e4m3(h, h_dtype, rows, hidden, qh, dh, st);
+    if (s != DFLASH2_OK) return s;
+    return run_tc_topk<__nv_fp8_e4m3>(di, qh, lm_head_q, dh, w_scale, rows, hidden, draft_vocab,
+                                      target_vocab, mult, cap, top_k, cand_ids, cand_u,
+                                      ws + prefix, ws_bytes - prefix, err_word, st);
+}
+
+extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head, int64_t rows,
+                                             int32_t hidden, int64_t draft_vocab,
+                                             int64_t target_vocab, float mult, float cap,
+                                             int32_t top_k, int32_t dtype, int64_t *cand_ids,
+                                             float *cand_u, void *workspace, size_t ws_bytes,
+                                             int32_t *err_word, void *stream) {
+    if (dtype != DFLASH2_F32 && dtype != DFLASH2_BF16) return DFLASH2_ERR_UNSUPPORTED_DTYPE;
+    if (rows < 0 || rows > INT32_MAX || hidden <= 0 || hidden > kMaxHidden || draft_vocab <= 0 ||
+        draft_vocab > INT32_MAX || target_vocab <= 0 || top_k <= 0 || top_k > kMaxTopK ||
+        top_k > target_vocab || top_k > draft_vocab || !(cap >= 0.0f))
+        return DFLASH2_ERR_INVALID_ARG;
+    if (rows == 0) return DFLASH2_OK;
+    if (!h || !lm_head || !cand_ids || !cand_u) return DFLASH2_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(cand_ids) % 8 != 0 || reinterpret_cast<uintptr_t>(cand_u) % 4 != 0)
+        return DFLASH2_ERR_MISALIGNED;
+    DeviceInfo di;
+    dflash2_status s = current_device(&di);
+    if (s != DFLASH2_OK) return s;
+    s = set_select_attrs(di.device);
+    if (s != DFLASH2_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t dsm = direct_smem_bytes(hidden);
+
+    if (dtype == DFLASH2_F32) {
+        if ((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(lm_head)) % 4 != 0)
+            return DFLASH2_ERR_MISALIGNED;
+        launch_k(direct_topk_kernel<float>, (unsigned)rows, kSelThreads, dsm, st,
+            static_cast<const float *>(h), static_cast<const float *>(lm_head), hidden, draft_vocab,
+
+            target_vocab, mult, cap, top_k, cand_ids, cand_u, err_word);
+        return launch_status();
+    }
+
+    if (hidden % 8 != 0 || !aligned16(h) || !aligned16(lm_head)) return DFLASH2_ERR_MISALIGNED;
+    return run_tc_topk<__nv_bfloat16>(di, h, lm_head, nullptr, nullptr, rows, hidden, draft_vocab,
+                                      target_vocab, mult, cap, top_k, cand_ids, cand_u,
+                                      workspace, ws_bytes, err_word, st);
 }

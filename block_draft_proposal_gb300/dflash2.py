@@ -29,7 +29,7 @@ DEVERR_ID_RANGE = 0x1
 DEVERR_TIMEOUT = 0x2
 DEVERR_SHORT = 0x4
 DEVINFO_TOPK_FALLBACK = 0x100
-ABI_VERSION = 6
+ABI_VERSION = 7
 
 # Every symbol include/dflash2.h declares.
 EXPORTS = (
@@ -39,7 +39,8 @@ EXPORTS = (
     "dflash2_d2t_remap", "dflash2_selector_walk_noalloc", "dflash2_philox_uniforms",
     "dflash2_conv_prepare", "dflash2_conv_finish", "dflash2_verify_workspace_size",
     "dflash2_verify", "dflash2_selector_project", "dflash2_selector_walk_projected",
-    "dflash2_unary_topk_launches", "dflash2_topk_merge",
+    "dflash2_unary_topk_launches", "dflash2_topk_merge", "dflash2_quantize_rows_e4m3",
+    "dflash2_unary_topk_fp8_workspace_size", "dflash2_unary_topk_fp8",
 )
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -103,6 +104,13 @@ def library():
         lib.dflash2_selector_walk_projected.argtypes = [P, P, i64, P, P, P, P, P, P, i32, i32, i32,
                                                         i32, i32, i32, P, P, P, P, sz, P, P]
         lib.dflash2_selector_walk_projected.restype = i32
+        lib.dflash2_quantize_rows_e4m3.argtypes = [P, i64, i32, i32, P, P, P]
+        lib.dflash2_quantize_rows_e4m3.restype = i32
+        lib.dflash2_unary_topk_fp8_workspace_size.argtypes = [i64, i32, i64, i32]
+        lib.dflash2_unary_topk_fp8_workspace_size.restype = sz
+        lib.dflash2_unary_topk_fp8.argtypes = [P, i32, P, P, i64, i32, i64, i64, f32, f32, i32, P,
+                                               P, P, sz, P, P]
+        lib.dflash2_unary_topk_fp8.restype = i32
         lib.dflash2_topk_merge.argtypes = [P, P, P, i32, i64, i32, i32, P, P, P, P]
         lib.dflash2_topk_merge.restype = i32
         lib.dflash2_unary_topk_launches.argtypes = [i64, i64, i32, f32, i32]
@@ -201,6 +209,50 @@ def unary_topk(h, lm_head, target_vocab: int, mult: float, cap: float, top_k: in
         _ptr(h), _ptr(lm_head), rows, hidden, draft_vocab, target_vocab, float(mult),
         float(cap), top_k, code, _ptr(cand_ids), _ptr(cand_u), _ptr(workspace),
         workspace.numel(), _ptr(err), _stream(stream)))
+    return cand_ids, cand_u, err
+
+
+def quantize_rows_e4m3(x, q=None, scale=None, stream=None):
+    """dflash2_quantize_rows_e4m3: per-row E4M3 codes (uint8) and scales of x."""
+    rows, cols = x.shape
+    _need(x, "x")
+    if q is None:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _check("dflash2_quantize_rows_e4m3", library().dflash2_quantize_rows_e4m3(
+        _ptr(x), rows, cols, _dtype_code(x), _ptr(q), _ptr(scale), _stream(stream)))
+    return q, scale
+
+
+def unary_topk_fp8_workspace_size(rows: int, hidden: int, draft_vocab: int, top_k: int) -> int:
+    return int(library().dflash2_unary_topk_fp8_workspace_size(rows, hidden, draft_vocab, top_k))
+
+
+def unary_topk_fp8(h, lm_head_q, w_scale, target_vocab: int, mult: float, cap: float, top_k: int,
+                   cand_ids=None, cand_u=None, workspace=None, err=None, stream=None):
+    """dflash2_unary_topk_fp8: top_k (ids, u) per row of h against an E4M3 head
+    (lm_head_q uint8 codes [draft_vocab, hidden], w_scale float [draft_vocab])."""
+    rows, hidden = h.shape
+    draft_vocab = lm_head_q.shape[0]
+    _need(h, "h")
+    _need(lm_head_q, "lm_head_q", torch.uint8, (draft_vocab, hidden))
+    _need(w_scale, "w_scale", torch.float32, (draft_vocab,))
+    dev = h.device
+    if cand_ids is None:
+        cand_ids = torch.empty((rows, top_k), dtype=torch.int64, device=dev)
+    if cand_u is None:
+        cand_u = torch.empty((rows, top_k), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(1, unary_topk_fp8_workspace_size(rows, hidden, draft_vocab,
+                                                                     top_k)),
+                                dtype=torch.uint8, device=dev)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check("dflash2_unary_topk_fp8", library().dflash2_unary_topk_fp8(
+        _ptr(h), _dtype_code(h), _ptr(lm_head_q), _ptr(w_scale), rows, hidden, draft_vocab,
+        target_vocab, float(mult), float(cap), top_k, _ptr(cand_ids), _ptr(cand_u),
+        _ptr(workspace), workspace.numel(), _ptr(err), _stream(stream)))
     return cand_ids, cand_u, err
 
 

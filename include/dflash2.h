@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define DFLASH2_ABI_VERSION 6
+#define DFLASH2_ABI_VERSION 7
 
 typedef enum {
     DFLASH2_OK = 0,
@@ -149,6 +149,52 @@ dflash2_status dflash2_unary_topk(const void *h, const void *lm_head, int64_t ro
                                   float mult, float cap, int32_t top_k, int32_t dtype,
                                   int64_t *cand_ids, float *cand_u, void *workspace,
                                   size_t ws_bytes, int32_t *err_word, void *stream);
+
+/*
+ * FP8 (E4M3) lm_head: the unary candidates of an FP8 head checkpoint.  The
+ * sglang DFlash2 PR lets a quantized lm_head fall back to its eager path;
+ * this computes the same candidates from the quantized head on the tensor
+ * cores (tcgen05.mma kind::f8f6f4).  W8A8 with per-row scales:
+ *
+ *   activation codes, per row m of h (dflash2_quantize_rows_e4m3):
+ *     amax = max_j |h[m, j]|, inv = 448 / amax, d[m] = amax / 448 (fp32),
+ *     q_h[m, j] = E4M3(h[m, j] * inv)   (fp32 product, round to nearest even,
+ *     saturating at +-448; a row of zeros: codes 0, d = 1)
+ *   z[m, v] = d[m] * w_scale[v] * sum_j dec(q_h[m, j]) * dec(lm_head_q[v, j])
+ *   then the transform, the padded-vocab mask and the top-K of
+ *   dflash2_unary_topk.
+ *
+ * E4M3 is the OCP 8-bit "e4m3fn" format (bias 7, 3 mantissa bits, max 448,
+ * no infinities, 0x7F / 0xFF NaN).
+ *
+ * dflash2_quantize_rows_e4m3: x device [rows, cols] (dtype f32 or bf16) ->
+ *   q device uint8 [rows, cols], scale device float [rows].
+ *   Errors: dtype -> UNSUPPORTED_DTYPE; rows outside [0, 2^31), cols < 1 or a
+ *   null pointer -> INVALID_ARG; x or scale misaligned for its type ->
+ *   MISALIGNED.  rows == 0 queues nothing.
+ * dflash2_unary_topk_fp8: h device [rows, hidden] (h_dtype f32 or bf16);
+ *   lm_head_q device uint8 [draft_vocab, hidden] E4M3 codes, 16-byte aligned;
+ *   w_scale device float [draft_vocab]; the other arguments as for
+ *   dflash2_unary_topk.  hidden % 16 == 0 (the codes' rows are TMA rows).
+ *   workspace device, 256-byte aligned, ws_bytes >=
+ *   dflash2_unary_topk_fp8_workspace_size(rows, hidden, draft_vocab, top_k):
+ *   the activation codes and scales, then a dflash2_unary_topk workspace.
+ *   Queues the quantization kernel and then what dflash2_unary_topk_launches
+ *   reports for bf16.  Errors as for dflash2_unary_topk, plus MISALIGNED for
+ *   hidden % 16 != 0 or lm_head_q not 16-byte aligned.
+ * Arithmetic: exact products of codes summed in fp32 in the tensor cores,
+ *   then z = acc * (d[m] * w_scale[v]) in fp32.
+ */
+dflash2_status dflash2_quantize_rows_e4m3(const void *x, int64_t rows, int32_t cols, int32_t dtype,
+                                          uint8_t *q, float *scale, void *stream);
+size_t dflash2_unary_topk_fp8_workspace_size(int64_t rows, int32_t hidden, int64_t draft_vocab,
+                                             int32_t top_k);
+dflash2_status dflash2_unary_topk_fp8(const void *h, int32_t h_dtype, const uint8_t *lm_head_q,
+                                      const float *w_scale, int64_t rows, int32_t hidden,
+                                      int64_t draft_vocab, int64_t target_vocab, float mult,
+                                      float cap, int32_t top_k, int64_t *cand_ids, float *cand_u,
+                                      void *workspace, size_t ws_bytes, int32_t *err_word,
+                                      void *stream);
 
 /*
  * Selector lattice and walk.

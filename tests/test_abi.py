@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.dflash2_abi_version() == 6
+    assert lib.dflash2_abi_version() == 7
     assert lib.dflash2_status_string(0) == b"ok"
     for s in range(1, 7):
         assert lib.dflash2_status_string(s) not in (b"ok", b"unknown status")
@@ -84,6 +84,27 @@ def test_host_validation_rejects_before_any_launch(lib):
                                                null, null, null, null, 0, null, null) == 1
     assert lib.dflash2_selector_walk_projected(null, null, 0, *(null,) * 6, 2, 3, 64, 16, 8, 1,
                                                null, null, null, null, 0, null, null) == 1
+    # FP8 head: dtype, shapes, hidden % 16 and the workspace are checked before any launch
+    p16 = ctypes.c_void_p(256)
+    fp8 = (p16, 1, p16, p16)
+    assert lib.dflash2_unary_topk_fp8(p16, 3, p16, p16, 7, 256, 4096, 4096, ctypes.c_float(1.0),
+                                      ctypes.c_float(0.0), 8, p16, p16, p16, 1 << 30, null,
+                                      null) == 2
+    assert lib.dflash2_unary_topk_fp8(*fp8, 7, 256, 4096, 4096, ctypes.c_float(1.0),
+                                      ctypes.c_float(0.0), 129, p16, p16, p16, 1 << 30, null,
+                                      null) == 1
+    assert lib.dflash2_unary_topk_fp8(*fp8, 7, 264, 4096, 4096, ctypes.c_float(1.0),
+                                      ctypes.c_float(0.0), 8, p16, p16, p16, 1 << 30, null,
+                                      null) == 3
+    assert lib.dflash2_unary_topk_fp8(*fp8, 7, 256, 4096, 4096, ctypes.c_float(1.0),
+                                      ctypes.c_float(0.0), 8, p16, p16, null, 0, null, null) == 4
+    assert lib.dflash2_unary_topk_fp8(*fp8, 0, 256, 4096, 4096, ctypes.c_float(1.0),
+                                      ctypes.c_float(0.0), 8, p16, p16, null, 0, null, null) == 0
+    assert lib.dflash2_quantize_rows_e4m3(p16, 4, 64, 5, p16, p16, null) == 2
+    assert lib.dflash2_quantize_rows_e4m3(p16, 4, 0, 1, p16, p16, null) == 1
+    assert lib.dflash2_quantize_rows_e4m3(null, 0, 64, 1, null, null, null) == 0
+    assert lib.dflash2_unary_topk_fp8_workspace_size(480, 4096, 151936, 16) > \
+        lib.dflash2_unary_topk_workspace_size(480, 151936, 16, 1) + 480 * 4096
     # top-K merge: shard count, list sizes and offsets are checked before any launch
     offs = (ctypes.c_int64 * 2)(0, 100)
     assert lib.dflash2_topk_merge(null, null, offs, 0, 4, 8, 8, null, null, null, null) == 1
