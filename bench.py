@@ -519,6 +519,44 @@ def run_gpu(args, w):
                                "mean_accept_len": float(v_acc.double().mean().item())}
         del tlog
 
+        # the FP8 (E4M3) head: the same candidates from a W8A8 head (activation
+        # quantization + kind::f8f6f4 top-K), one captured call replayed
+        fq = synth.make(w, parts=("lm_head_fp8", "w_scale"))
+        t_q8, t_sw = dflash2.to_device(fq["lm_head_fp8"], dev), dflash2.to_device(fq["w_scale"], dev)
+        del fq
+        f_ids = torch.empty_like(bufs.cand_ids)
+        f_u = torch.empty_like(bufs.cand_u)
+        f_ws = torch.empty(dflash2.unary_topk_fp8_workspace_size(w.rows, w.hidden, w.draft_vocab,
+                                                                 w.top_k),
+                           dtype=torch.uint8, device=dev)
+        f_err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def fp8():
+            dflash2.unary_topk_fp8(t["h"], t_q8, t_sw, w.target_vocab, w.mult, w.cap, w.top_k,
+                                   cand_ids=f_ids, cand_u=f_u, workspace=f_ws, err=f_err,
+                                   stream=stream)
+
+        with torch.cuda.stream(stream):
+            fp8()
+        stream.synchronize()
+        fgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(fgraph, stream=stream):
+            fp8()
+        fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + reps):
+                flush.zero_()
+                if i >= args.warmup:
+                    fev[i - args.warmup][0].record(stream)
+                fgraph.replay()
+                if i >= args.warmup:
+                    fev[i - args.warmup][1].record(stream)
+        torch.cuda.synchronize()
+        next_rows["unary_topk_fp8"] = {"ms": statistics.mean(a.elapsed_time(b) for a, b in fev),
+                                       "calls": reps, "err": int(f_err.item())}
+        del t_q8
+
     # max over ranks
     if world > 1:
         ms, e2e = reduce_max_over_ranks([ms, e2e], device=dev)
@@ -566,6 +604,17 @@ def run_gpu(args, w):
         vr["what"] = ("speculative-sampling verify of the step's proposals against synthetic "
                       "bf16 target logits [B, S+1, V_t] (candidate remap + uniforms + 2 kernels), "
                       "one captured call replayed; bytes = logits once + partials")
+
+    if "unary_topk_fp8" in next_rows:
+        f8 = next_rows["unary_topk_fp8"]
+        f8["TFLOP/s"] = work["gemm_flops"] / (f8["ms"] * 1e-3) / 1e12
+        # fp8 peak: the measured bf16 peak times the nominal fp8 / bf16 ratio (2)
+        f8["frac_fp8_burst"] = f8["TFLOP/s"] / (2 * tf_burst)
+        f8["frac_fp8_sustained"] = f8["TFLOP/s"] / (2 * tf_sust)
+        f8["speedup_vs_bf16_stage"] = unary_ms / f8["ms"]
+        f8["what"] = ("unary top-K from an E4M3 head with per-row scales: activation "
+                      "quantization + tcgen05 kind::f8f6f4 GEMM + top-K, one captured call "
+                      "replayed; 2*M*V*H flops; peak = measured bf16 x 2 (nominal ratio)")
 
     # CPU baseline: the oracle as it stands on a bounded sample (rank 0, N = 1)
     cpu = None
