@@ -358,6 +358,43 @@ __global__ void __launch_bounds__(kSelThreads)
     write_row(sh, got, k, row, ids, vals, err);
 }
 
+// fp32 with a workspace: the vocab split into chunks of chunk_len rows, one
+// CTA per (row, chunk) running the exact routine on its chunk; the lists
+// ([chunks][rows][k], chunk-local ids, u = -inf where a chunk holds fewer than
+// k entries) are merged by dflash2_topk_merge.
+constexpr int kFp32ChunkMin = 256;   // vocab rows per chunk, at least
+constexpr int kFp32MaxChunks = 32;
+
+inline int fp32_chunks(int64_t rows, int64_t vmax, int k) {
+    int64_t c = (304 + rows - 1) / rows;  // about two CTAs per SM of a 152-SM GPU
+    const int64_t by_len = vmax / std::max<int64_t>(kFp32ChunkMin, k);
+    if (c > by_len) c = by_len;
+    if (c > kFp32MaxChunks) c = kFp32MaxChunks;
+    if ((int64_t)c * k > 4096) c = 4096 / k;  // the merge's key budget
+    return c < 1 ? 1 : (int)c;
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+    direct_chunk_kernel(const float *__restrict__ h, const float *__restrict__ w, int hidden,
+                        int64_t vmax, int64_t chunk_len, float mult, float cap, int k,
+                        int64_t *ids, float *vals) {
+    grid_dep_wait();
+    __shared__ SelectShared sh;
+    extern __shared__ __align__(16) uint8_t dyn[];
+    float *hs = reinterpret_cast<float *>(dyn);
+    uint64_t *buf = reinterpret_cast<uint64_t *>(dyn + (((size_t)hidden * 4 + 15) & ~(size_t)15));
+    const int64_t row = blockIdx.x, rows = gridDim.x;
+    const int64_t c0 = (int64_t)blockIdx.y * chunk_len;
+    const int64_t len = min(chunk_len, vmax - c0);
+    const int got = direct_row_topk<float>(h + row * hidden, w + c0 * hidden, hidden, len, len,
+                                           mult, cap, k, hs, buf, sh);
+    const int64_t base = ((int64_t)blockIdx.y * rows + row) * k;
+    for (int i = threadIdx.x; i < k; i += blockDim.x) {
+        ids[base + i] = i < got ? (int64_t)key_id(sh.top[i]) : 0;
+        vals[base + i] = i < got ? key_u(sh.top[i]) : -INFINITY;  // absent for the merge
+    }
+}
+
 // Pilot select: threshold and seed candidates of each row from its pilot u.
 //
 // theta_pre: for mult > 0 and a positive threshold u_th, the transform obeys
@@ -607,6 +644,8 @@ dflash2_status set_select_attrs(int device) {
                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
         cudaFuncSetAttribute(pilot_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(direct_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes) != cudaSuccess ||
         cudaFuncSetAttribute(direct_topk_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              bytes) != cudaSuccess ||
         cudaFuncSetAttribute(direct_topk_kernel<__nv_bfloat16>,
@@ -744,7 +783,11 @@ using namespace dflash2;
 extern "C" size_t dflash2_unary_topk_workspace_size(int64_t rows, int64_t draft_vocab, int32_t top_k,
                                                     int32_t dtype) {
     if (rows <= 0 || draft_vocab <= 0 || top_k <= 0) return 0;
-    if (dtype == DFLASH2_F32) return 0;
+    if (dtype == DFLASH2_F32) {
+        // the chunked exact path's lists (none when one chunk covers the vocab)
+        const int c = fp32_chunks(rows, draft_vocab, top_k);
+        return c > 1 ? (size_t)c * rows * top_k * 12 : 0;
+    }
     const TopkLayout L = topk_layout(rows, draft_vocab);
     return L.fixed_bytes + (size_t)rows * recommended_cap(L, top_k) * 8;
 }
@@ -764,7 +807,7 @@ extern "C" int32_t dflash2_unary_topk_launches(int64_t rows, int64_t draft_vocab
         top_k <= 0 || top_k > kMaxTopK || top_k > draft_vocab)
         return -1;
     if (rows == 0) return 0;
-    if (dtype == DFLASH2_F32) return 1;
+    if (dtype == DFLASH2_F32) return fp32_chunks(rows, draft_vocab, top_k) > 1 ? 2 : 1;
     DeviceInfo di;
     if (current_device(&di) != DFLASH2_OK) return -1;
     const TopkLayout L = topk_layout(rows, draft_vocab);
@@ -851,6 +894,27 @@ extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head,
     if (dtype == DFLASH2_F32) {
         if ((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(lm_head)) % 4 != 0)
             return DFLASH2_ERR_MISALIGNED;
+        // chunks over the candidate vocab: the workspace size uses the draft
+        // vocab (the host knows no target bound there), which only over-counts
+        const int64_t vmax = std::min<int64_t>(draft_vocab, target_vocab);
+        const int chunks = fp32_chunks(rows, vmax, top_k);
+        const size_t need = (size_t)chunks * rows * top_k * 12;
+        if (chunks > 1 && workspace && ws_bytes >= need &&
+            reinterpret_cast<uintptr_t>(workspace) % 8 == 0) {
+            const int64_t chunk_len = (vmax + chunks - 1) / chunks;
+            const int n_chunks = (int)((vmax + chunk_len - 1) / chunk_len);
+            int64_t *lid = static_cast<int64_t *>(workspace);
+            float *lu = reinterpret_cast<float *>(lid + (size_t)n_chunks * rows * top_k);
+            launch_k(direct_chunk_kernel, dim3((unsigned)rows, (unsigned)n_chunks), kSelThreads,
+                     dsm, st, static_cast<const float *>(h), static_cast<const float *>(lm_head),
+                     hidden, vmax, chunk_len, mult, cap, top_k, lid, lu);
+            s = launch_status();
+            if (s != DFLASH2_OK) return s;
+            int64_t offs[kFp32MaxChunks];
+            for (int c = 0; c < n_chunks; ++c) offs[c] = (int64_t)c * chunk_len;
+            return dflash2_topk_merge(lid, lu, offs, n_chunks, rows, top_k, top_k, cand_ids,
+                                      cand_u, err_word, stream);
+        }
         launch_k(direct_topk_kernel<float>, (unsigned)rows, kSelThreads, dsm, st,
             static_cast<const float *>(h), static_cast<const float *>(lm_head), hidden, draft_vocab,
 

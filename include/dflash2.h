@@ -111,7 +111,9 @@ dflash2_status dflash2_grouped_conv(const void *x, const void *base, const void 
  * cand_ids    device int64 [rows, top_k];  cand_u device float [rows, top_k].
  * workspace   device, ws_bytes >= dflash2_unary_topk_workspace_min(...);
  *             dflash2_unary_topk_workspace_size(...) is the recommended size.
- *             Its contents need no initialisation and are clobbered.
+ *             Its contents need no initialisation and are clobbered.  fp32 needs
+ *             none (min 0); with the recommended size (8-byte aligned) a few
+ *             rows' vocab is split over CTAs and the lists merged exactly.
  * err_word    device int32, may be NULL.
  * Arithmetic: bf16 -> tcgen05 tensor-core GEMM with fp32 accumulation; fp32 ->
  *             fp32 FMA on CUDA cores (no TF32).  The transform runs in fp32
@@ -134,7 +136,9 @@ size_t dflash2_unary_topk_workspace_min(int64_t rows, int64_t draft_vocab, int32
                                         int32_t dtype);
 /*
  * Kernels one dflash2_unary_topk call with these shapes queues on the current
- * device: 1 for fp32; for bf16 either 2 (one cooperative launch of the pilot
+ * device: for fp32 1, or 2 when the recommended workspace splits the vocab
+ * over CTAs (chunks, then dflash2_topk_merge; counted for target_vocab >=
+ * draft_vocab); for bf16 either 2 (one cooperative launch of the pilot
  * tiles, the thresholds and the filter tiles, then the final top-K) or 3 / 4
  * (pilot pass, pilot select, filter pass unless the pilot covers the vocab,
  * final top-K); 0 for rows == 0.  Host arithmetic only, nothing is queued;

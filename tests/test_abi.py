@@ -125,10 +125,14 @@ def test_workspace_sizes_are_host_arithmetic(lib):
     rec = lib.dflash2_unary_topk_workspace_size(480, 151936, 16, 1)
     mn = lib.dflash2_unary_topk_workspace_min(480, 151936, 16, 1)
     assert rec > mn > 0
-    assert lib.dflash2_unary_topk_workspace_size(7, 4096, 8, 0) == 0   # fp32 path needs none
+    # fp32: no workspace needed; the recommended one splits the vocab over CTAs
+    assert lib.dflash2_unary_topk_workspace_min(7, 4096, 8, 0) == 0
+    assert lib.dflash2_unary_topk_workspace_size(7, 4096, 8, 0) == 16 * 7 * 8 * 12
+    assert lib.dflash2_unary_topk_workspace_size(480, 4096, 8, 0) == 0  # one chunk per row
     # launch counts: fp32 is one kernel on any device, zero rows queue nothing,
     # a rejected dtype answers -1 (bf16 needs the device's SM count)
-    assert lib.dflash2_unary_topk_launches(7, 4096, 8, ctypes.c_float(1.0), 0) == 1
+    assert lib.dflash2_unary_topk_launches(7, 4096, 8, ctypes.c_float(1.0), 0) == 2  # chunks
+    assert lib.dflash2_unary_topk_launches(480, 4096, 8, ctypes.c_float(1.0), 0) == 1
     assert lib.dflash2_unary_topk_launches(0, 4096, 8, ctypes.c_float(1.0), 1) == 0
     assert lib.dflash2_unary_topk_launches(7, 4096, 8, ctypes.c_float(1.0), 3) == -1
     assert lib.dflash2_unary_topk_launches(7, 4096, 129, ctypes.c_float(1.0), 0) == -1
