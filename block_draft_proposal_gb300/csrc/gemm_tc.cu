@@ -1,6 +1,8 @@
-// Persistent warp-specialised bf16 GEMM on the 5th-generation tensor cores.
+// Persistent warp-specialised GEMM on the 5th-generation tensor cores, bf16
+// (kind::f16) or, on CTA pairs, E4M3 codes with per-row scales (kind::f8f6f4).
 //
 //   C[m, v] = sum_j h[m, j] * w[v, j]      (w: lm_head or selector projection)
+//   fp8:   C[m, v] = a_scale[m] * w_scale[v] * sum_j h[m, j] * w[v, j]
 //
 // Swap-AB: the weight rows are the MMA's M side (128-row tiles) and the
 // tokens its N side (bn-column tiles, bn <= 256), so the fp32 accumulator of
@@ -23,9 +25,15 @@
 // hundred, against 120 tensor cycles per MMA at N = 240.  Its loop therefore
 // keeps precomputed descriptors and an incremental stage / phase counter.
 //
+// An E4M3 box holds 128 codes in the same 128-byte row, so a stage of the
+// same bytes covers 256 hidden elements and the same descriptor steps (32
+// bytes per MMA, K = 32 codes) serve both kinds.
+//
 // Work items are ordered with the token tile fastest, so the CTAs that run
 // at the same time share weight tiles in L2 and the weight matrix streams
-// from HBM about once.
+// from HBM about once.  Modes: store (split-K fp32 partials), store-bf16, the
+// top-K's pilot and filter passes, and their fused cooperative launch (the
+// CTA-pair variant below).
 #include "kernels.h"
 
 namespace dflash2 {

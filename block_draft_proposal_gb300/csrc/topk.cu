@@ -18,8 +18,17 @@
 //      for a row where more than kCollect keys reach it).  A row
 //      whose list overflowed is recomputed exactly on CUDA cores (rare: only
 //      adversarial weights defeat the pilot threshold).
-// fp32 pipeline: one CUDA-core kernel per row (the same exact routine as the
-// overflow path), fp32 FMA accumulation.
+// Steps 1-3 also run as one cooperative launch (gemm_tc.cu, fused mode) where
+// the host's rule (use_fused) expects it to be faster: the pilot tiles come
+// first, their epilogues write 32-row group maxima, the epilogue warps then
+// take each row's threshold from those maxima, and the pilot tiles' own
+// candidates come from the accumulators they kept.
+// FP8 head (dflash2_unary_topk_fp8): the tokens' E4M3 codes and scales
+// (quant.cu), then the same pipeline on kind::f8f6f4 MMAs with the logits
+// scaled in the epilogue.
+// fp32 pipeline: the same exact CUDA-core routine as the overflow path, one
+// CTA per row, or per (row, vocab chunk) with the chunk lists merged exactly
+// (merge.cu) when the caller passes the recommended workspace.
 //
 // Keys order (u descending, id ascending) as one uint64 (common.cuh), so the
 // selection is a plain "K largest keys" problem with no ties.
