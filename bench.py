@@ -621,9 +621,20 @@ def run_gpu(args, w):
     if world == 1 and not args.no_cpu_baseline:
         n_req = max(1, min(w.batch, 20))   # about 10-30 s of CPU work on 16 cores
         tc = oracle_sample_time(w, inp, n_req)
-        cpu = {"value": n_req * w.slots / tc, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+        import oracle
+        threads = oracle.set_threads(0)
+        # the same chain on one core, over one request
+        oracle.set_threads(1)
+        try:
+            t1 = oracle_sample_time(w, inp, 1)
+        finally:
+            oracle.set_threads(threads)
+        cpu = {"value": n_req * w.slots / tc, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{n_req} requests ({n_req * w.slots} proposal rows) of {w.name}: the "
-                         f"whole oracle chain, {tc:.1f} s"}
+                         f"whole oracle chain, {tc:.1f} s on {threads} OpenMP threads "
+                         f"({_cores()} cores available)",
+               "value_single_thread": w.slots / t1,
+               "sample_single_thread": f"1 request ({w.slots} rows), one thread, {t1:.1f} s"}
 
     value = job_value(world, w.rows, ms)
     line = {

@@ -78,6 +78,8 @@ def _load():
             lib.oracle_kernel_projection.restype = None
             lib.oracle_verify.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i64, i32, P, P]
             lib.oracle_verify.restype = i64
+            lib.oracle_set_threads.argtypes = [i32]
+            lib.oracle_set_threads.restype = i32
             lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
             lib.oracle_e4m3_decode.restype = f64
             lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
@@ -354,3 +356,8 @@ def unary_rows_fp8(qh, dh, qw, sw, target_vocab: int, mult: float, cap: float,
     _load().oracle_unary_rows_fp8(_ptr(qh), _ptr(dh), _ptr(qw), _ptr(sw), _ptr(sel), n_sel,
                                   hidden, vd, target_vocab, float(mult), float(cap), _ptr(u))
     return u
+
+
+def set_threads(n: int = 0) -> int:
+    """Set (n > 0) or ask (n <= 0) the oracle's OpenMP thread count; returns it."""
+    return int(_load().oracle_set_threads(int(n)))

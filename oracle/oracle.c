@@ -24,6 +24,9 @@
  */
 #include <math.h>
 #include <stdint.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <stdlib.h>
 #include <string.h>
 
@@ -724,4 +727,18 @@ void oracle_unary_rows_fp8(const uint8_t *qh, const float *dh, const uint8_t *qw
             u_out[r * draft_vocab + v] = u;
         }
     }
+}
+
+/* Threads the OpenMP loops above use: n > 0 sets them, n <= 0 only asks.
+ * Returns the count now in force (1 without OpenMP).  Timing aid only. */
+int oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
 }

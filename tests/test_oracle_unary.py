@@ -120,3 +120,22 @@ def test_high_padded_logits_never_chosen(ora):
     # K equal to the logical vocab returns every valid id and no padded one
     ids_all, _ = ora.topk(u, vt)
     assert sorted(ids_all[0].tolist()) == list(range(vt))
+
+
+def test_oracle_results_do_not_depend_on_the_thread_count():
+    """The OpenMP loops split independent rows only: one thread and all give
+    the same bits (the CPU baseline times both)."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(77)
+    h = rng.normal(0, 1, (9, 64)).astype(np.float32)
+    w = rng.normal(0, 0.1, (300, 64)).astype(np.float32)
+    threads = oracle.set_threads(0)
+    try:
+        oracle.set_threads(1)
+        one = oracle.unary_rows(h, w, 290, 1.0, 30.0)
+        oracle.set_threads(max(2, threads))
+        many = oracle.unary_rows(h, w, 290, 1.0, 30.0)
+    finally:
+        oracle.set_threads(threads)
+    assert np.array_equal(one, many)
