@@ -127,3 +127,20 @@ def test_fp8_matches_bf16_candidates_closely(cuda):
     overlap = np.mean([len(set(a) & set(b)) / k for a, b in zip(i8.cpu().numpy(),
                                                                 i16.cpu().numpy())])
     assert overlap > 0.6
+
+
+@pytest.mark.parametrize("case", [(1, 16, 300, 300, 8, 1.0, 0.0, "bf16"),
+                                  (2, 32, 200, 150, 4, 1.0, 30.0, "f32"),
+                                  (3, 4096, 257, 257, 16, 1.0, 0.0, "bf16")],
+                         ids=lambda c: f"r{c[0]}-h{c[1]}-v{c[2]}")
+def test_fp8_topk_minimum_sizes(cuda, case):
+    """One or two rows, hidden of one 16-code row, a vocab inside one unit or
+    one row past it."""
+    rows, hidden, vd, vt, k, mult, cap, h_dtype = case
+    hin, qw, sw = _case(rows, hidden, vd, 500 + hidden, h_dtype)
+    ids, vals, err = dflash2.unary_topk_fp8(_dev(hin, cuda), _dev(qw, cuda), _dev(sw, cuda), vt,
+                                            mult, cap, k)
+    torch.cuda.synchronize()
+    assert int(err.item()) & ~dflash2.DEVINFO_TOPK_FALLBACK == 0
+    _check_fp8(hin, qw, sw, vt, mult, cap, k, ids.cpu().numpy(), vals.cpu().numpy(),
+               np.arange(rows))

@@ -100,3 +100,45 @@ def test_merge_drops_an_id_past_the_largest_vocab(cuda):
     torch.cuda.synchronize()
     assert out_ids.tolist() == [[5, 2, 2**31 + 2]]
     assert int(err.item()) & dflash2.DEVERR_ID_RANGE
+
+
+def test_sharded_helper_through_a_process_group(cuda):
+    """unary_topk_vocab_sharded end to end on a one-rank NCCL group: the shard
+    is the whole head, the all-gather and the merge still run."""
+    import os
+    import socket
+    import torch.distributed as dist
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("nccl", rank=0, world_size=1, device_id=cuda)
+    try:
+        w = synth.BY_NAME["qwen3-8b-bf16"].scaled(batch=4, draft_vocab=12000, target_vocab=11000)
+        inp = synth.make(w, parts=("h", "lm_head"))
+        t = {k: dflash2.to_device(v, cuda) for k, v in inp.items() if v is not None}
+        ref_ids, ref_u, _ = dflash2.unary_topk(t["h"], t["lm_head"], w.target_vocab, w.mult,
+                                               w.cap, w.top_k)
+        ids, u, err = dflash2.unary_topk_vocab_sharded(t["h"], t["lm_head"], w.draft_vocab,
+                                                       w.target_vocab, w.mult, w.cap, w.top_k)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert torch.equal(ids, ref_ids) and torch.equal(u, ref_u)
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("shards,rows,k_in,k_out", [(64, 1, 1, 64), (64, 3, 64, 128),
+                                                    (3, 1, 1, 1)])
+def test_merge_edge_shapes(cuda, shards, rows, k_in, k_out):
+    rng = np.random.default_rng(2000 + shards + k_in)
+    offsets = np.arange(shards) * 1000
+    ids = rng.integers(0, 1000, (shards, rows, k_in)).astype(np.int64)
+    u = rng.normal(0, 1, (shards, rows, k_in)).astype(np.float32)
+    out_ids, out_u, err = dflash2.topk_merge(torch.from_numpy(ids).to(cuda),
+                                             torch.from_numpy(u).to(cuda), offsets.tolist(), k_out)
+    torch.cuda.synchronize()
+    ref_ids, ref_u = _lexsort_merge(ids, u, offsets, k_out)
+    np.testing.assert_array_equal(out_ids.cpu().numpy(), ref_ids)
+    np.testing.assert_array_equal(out_u.cpu().numpy(), ref_u)
+    assert bool(int(err.item()) & dflash2.DEVERR_SHORT) == (shards * k_in < k_out)
