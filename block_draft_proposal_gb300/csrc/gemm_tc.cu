@@ -36,6 +36,8 @@
 // CTA-pair variant below).
 #include "kernels.h"
 
+#include <atomic>
+
 namespace dflash2 {
 namespace {
 
@@ -787,8 +789,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     }
 }
 
-int g_smem_set[64];
-int g_fused_pairs[64];  // 0: not yet asked; -1: none
+// Per-device caches; several host threads may fill them at once (the guarded
+// calls are idempotent).
+std::atomic<int> g_smem_set[64];
+std::atomic<int> g_fused_pairs[64];  // 0: not yet asked; -1: none
 
 dflash2_status set_gemm_attrs(const DeviceInfo &di) {
     if (di.device < 0 || di.device >= 64) return DFLASH2_ERR_CUDA;
@@ -822,7 +826,8 @@ int fused_pairs(const DeviceInfo &di) {
         }
         g_fused_pairs[di.device] = n > 0 ? n : -1;
     }
-    return g_fused_pairs[di.device] > 0 ? g_fused_pairs[di.device] : 0;
+    const int n = g_fused_pairs[di.device];
+    return n > 0 ? n : 0;
 }
 
 }  // namespace

@@ -34,6 +34,8 @@
 // selection is a plain "K largest keys" problem with no ties.
 #include "kernels.h"
 
+#include <atomic>
+
 #include <algorithm>
 #include <type_traits>
 
@@ -641,7 +643,7 @@ bool use_fused(const DeviceInfo &di, const TopkLayout &L, int64_t rows, int bn, 
            (filter_tiles + filter_pairs - 1) / filter_pairs + 1;
 }
 
-bool g_topk_attr[64];
+std::atomic<bool> g_topk_attr[64];  // per device; the attribute calls are idempotent
 
 dflash2_status set_select_attrs(int device) {
     if (device < 0 || device >= 64) return DFLASH2_ERR_CUDA;

@@ -18,6 +18,8 @@
 // serial chain of a slot then touches shared memory and registers only.
 #include "kernels.h"
 
+#include <atomic>
+
 namespace dflash2 {
 namespace {
 
@@ -732,7 +734,7 @@ inline int ksplits_ws(int64_t rows, int hidden, int32_t dtype) {
     return ks;
 }
 
-bool g_walk_attr[64];
+std::atomic<bool> g_walk_attr[64];  // per device; the attribute calls are idempotent
 
 }  // namespace
 }  // namespace dflash2
