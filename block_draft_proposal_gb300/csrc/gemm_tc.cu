@@ -203,16 +203,23 @@ __device__ __forceinline__ float fp8_scale_chunk(const GemmParams &p, float (&z)
 // current tile's tokens and a buffer of survivors waiting for their global
 // slots.
 constexpr int kEpiBuf = 128;
-struct EpiScratch {
-    float pre[256];
-    uint64_t th[256];
+template <int COLS>
+struct EpiScratchT {
+    float pre[COLS];
+    uint64_t th[COLS];
     uint64_t key[kEpiBuf];
     int32_t row[kEpiBuf];
 };
+using EpiScratch = EpiScratchT<256>;      // one CTA: a warp covers every column of a tile
+constexpr int kPairEpiWarps = 8;          // CTA pairs: two warps per TMEM lane quarter,
+constexpr int kPairEpiCols = 128;         // each on half of the tile's columns
+using EpiScratchPair = EpiScratchT<kPairEpiCols>;
+constexpr int kPairThreads = 64 + 32 * kPairEpiWarps;  // producer, MMA issuer, epilogue
 
 // Moves the buffered survivors to their rows' candidate lists: one global
 // atomic per survivor, issued by all lanes together.
-__device__ __noinline__ void flush_survivors(const GemmParams &p, EpiScratch &es, int n, int lane) {
+template <typename S>
+__device__ __noinline__ void flush_survivors(const GemmParams &p, S &es, int n, int lane) {
     __syncwarp();
 #pragma unroll 4
     for (int e = lane; e < n; e += 32) {
@@ -223,7 +230,8 @@ __device__ __noinline__ void flush_survivors(const GemmParams &p, EpiScratch &es
     __syncwarp();
 }
 
-// Filter epilogue of 32 columns (tokens m0 .. m0+31, tile columns c0 ..).
+// Filter epilogue of 32 columns (tokens m0 .. m0+31; c0 indexes them in the
+// warp's scratch, tcol in TMEM).
 // fl(mult * z), the first rounding step of the transform, is compared with
 // the token's pre-threshold; only where some lane passes is the exact key
 // formed and compared with the threshold key (pilot_select_kernel shows the
@@ -231,8 +239,9 @@ __device__ __noinline__ void flush_survivors(const GemmParams &p, EpiScratch &es
 // hit are visited in a compact loop that re-reads the one column from TMEM,
 // which keeps the code small.  Keys that pass are buffered in shared memory;
 // nbuf counts them (warp-uniform).
+template <typename S>
 __device__ __forceinline__ void filter_chunk(const GemmParams &p, const float (&z)[32], int64_t v,
-                                             int m0, int c0, uint32_t tcol, EpiScratch &es,
+                                             int m0, int c0, uint32_t tcol, S &es,
                                              int &nbuf, int lane, float asc = 1.0f,
                                              float wsv = 1.0f) {
     const bool valid_v = v < p.rows_w && v < p.target_vocab;
@@ -335,13 +344,15 @@ __device__ __noinline__ void fused_select_row(const GemmParams &p, int64_t row, 
     }
 }
 
-// Every epilogue warp of the launch (4 per CTA) waits for the pilot tiles'
+// Every epilogue warp of the launch (kPairEpiWarps per CTA) waits for the pilot tiles'
 // group maxima, selects rows gw, gw + nw, ... and publishes; false when a
 // bounded wait gave up.
 __device__ bool fused_select(const GemmParams &p, volatile int *abort_flag, int lane) {
-    const int nw = (int)gridDim.x * 4;
-    const int gw = (int)blockIdx.x * 4 + ((int)(threadIdx.x >> 5) - 2);
-    const uint32_t pilot_warps = (uint32_t)p.n_pilot * (uint32_t)p.n_tok_tiles * 8u;
+    const int nw = (int)gridDim.x * kPairEpiWarps;
+    const int gw = (int)blockIdx.x * kPairEpiWarps + ((int)(threadIdx.x >> 5) - 2);
+    // every epilogue warp of both CTAs arrives once per pilot tile
+    const uint32_t pilot_warps =
+        (uint32_t)p.n_pilot * (uint32_t)p.n_tok_tiles * (2u * kPairEpiWarps);
     if (!counter_wait(p.sync, pilot_warps, abort_flag, p.err, lane)) return false;
     for (int64_t row = gw; row < p.rows_h; row += nw) fused_select_row(p, row, lane);
     counter_arrive(p.sync + 1, lane);
@@ -533,7 +544,7 @@ __global__ void __launch_bounds__(192, 1)
 // accumulator-full barriers; both CTAs' epilogues (each reading its own 128
 // TMEM lanes) arrive on the leader's accumulator-empty barrier.
 // ---------------------------------------------------------------------------
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kPairEpiWarps, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_w,
                         const __grid_constant__ CUtensorMap tm_h, const GemmParams p) {
     extern __shared__ uint8_t dsmem[];
@@ -552,7 +563,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     const uint32_t h_stage = 2 * h_sub;
     uint8_t *w_smem = smem;
     uint8_t *h_smem = smem + (size_t)p.stages * kWStageBytes;
-    EpiScratch *epi = reinterpret_cast<EpiScratch *>(h_smem + (size_t)p.stages * h_stage);
+    EpiScratchPair *epi =
+        reinterpret_cast<EpiScratchPair *>(h_smem + (size_t)p.stages * h_stage);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -567,7 +579,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], 8);  // 4 epilogue warps in each CTA of the pair
+            mbar_init(&acc_empty[a], 2 * kPairEpiWarps);  // every epilogue warp of the pair
         }
         mbar_init(&drain_bar, 1);
         abort_flag = 0;
@@ -676,16 +688,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     } else {
         const int quarter = warp & 3;  // TMEM lanes this warp may access
         const int row_in_unit = (int)rank * kGemmTileW + quarter * 32 + lane;
-        EpiScratch &es = epi[warp - 2];
+        // the tile columns this warp takes: one half of them
+        const int cb = ((warp - 2) / 4) * kPairEpiCols;
+        const int ce = min(p.bn, cb + kPairEpiCols);
+        EpiScratchPair &es = epi[warp - 2];
         const uint32_t acc_empty_leader[2] = {mapa_shared(smem_u32(&acc_empty[0]), 0),
                                               mapa_shared(smem_u32(&acc_empty[1]), 0)};
         // The candidates of one filter-style tile whose accumulator is full:
         // its tokens' thresholds, the chunks, then the buffer goes back.
         const auto load_thresholds = [&](const Item &item) {
             const int m_tile = item.nt * p.bn;
-            for (int c = lane; c < 256; c += 32) {
-                const int m = m_tile + c;
-                const bool ok = c < p.bn && m < p.rows_h;
+            for (int c = lane; c < kPairEpiCols; c += 32) {
+                const int cc = cb + c;
+                const int m = m_tile + cc;
+                const bool ok = cc < p.bn && m < p.rows_h;
                 es.pre[c] = ok ? __ldcg(p.theta_pre + m) : INFINITY;
                 es.th[c] = ok ? __ldcg(p.theta + m) : ~0ull;
             }
@@ -701,12 +717,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             const float wsv = row_scale(v);
             const uint32_t tbase = tmem + (uint32_t)a * p.acc_cols + ((uint32_t)(quarter * 32) << 16);
             int nbuf = 0;
-            for (int c0 = 0; c0 < p.bn; c0 += 32) {
+            for (int c0 = cb; c0 < ce; c0 += 32) {
                 float z[32];
                 tmem_ld32_wait(tbase + (uint32_t)c0, z);
                 const float asc = p.fp8 ? fp8_scale_chunk(p, z, m_tile + c0, wsv, lane) : 1.0f;
-                filter_chunk(p, z, v, m_tile + c0, c0, tbase + (uint32_t)c0, es, nbuf, lane, asc,
-                             wsv);
+                filter_chunk(p, z, v, m_tile + c0, c0 - cb, tbase + (uint32_t)c0, es, nbuf, lane,
+                             asc, wsv);
             }
             tc_fence_before();
             if (nbuf > 0) flush_survivors(p, es, nbuf, lane);
@@ -735,7 +751,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     tmem + (uint32_t)a * p.acc_cols + ((uint32_t)(quarter * 32) << 16);
                 const int g = item.j * (p.unit / 32) + row_in_unit / 32;
                 const float wsv = row_scale(v);
-                for (int c0 = 0; c0 < p.bn; c0 += 32) {
+                for (int c0 = cb; c0 < ce; c0 += 32) {
                     float z[32];
                     tmem_ld32_wait(tbase + (uint32_t)c0, z);
                     if (p.fp8) fp8_scale_chunk(p, z, item.nt * p.bn + c0, wsv, lane);
@@ -746,7 +762,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             }
             // the thresholds of every row, then the pilot tiles' candidates
             ok = ok && fused_select(p, &abort_flag, lane) &&
-                 counter_wait(p.sync + 1, gridDim.x * 4, &abort_flag, p.err, lane);
+                 counter_wait(p.sync + 1, gridDim.x * kPairEpiWarps, &abort_flag, p.err, lane);
             for (int i = 0; ok && i < np; ++i) {
                 const Item item = decode(p, pair + i * npairs);
                 load_thresholds(item);
@@ -768,7 +784,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             const int64_t v = (int64_t)item.wt * p.unit + row_in_unit;
             const float wsv = row_scale(v);
             const uint32_t tbase = tmem + (uint32_t)a * p.acc_cols + ((uint32_t)(quarter * 32) << 16);
-            for (int c0 = 0; c0 < p.bn; c0 += 32) {
+            for (int c0 = cb; c0 < ce; c0 += 32) {
                 float z[32];
                 tmem_ld32_wait(tbase + (uint32_t)c0, z);
                 if (p.fp8) fp8_scale_chunk(p, z, m_tile + c0, wsv, lane);
@@ -817,7 +833,7 @@ int fused_pairs(const DeviceInfo &di) {
         if (set_gemm_attrs(di) == DFLASH2_OK) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)(di.sm_count / 2 * 2));
-            cfg.blockDim = dim3(192);
+            cfg.blockDim = dim3(kPairThreads);
             cfg.dynamicSmemBytes = kGemmSmemBytes;
             if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_pair_kernel, &cfg) != cudaSuccess) {
                 cudaGetLastError();
@@ -832,7 +848,8 @@ int fused_pairs(const DeviceInfo &di) {
 
 }  // namespace
 
-int fused_epilogue_warps(const DeviceInfo &di) { return fused_pairs(di) * 2 * 4; }
+int fused_pair_count(const DeviceInfo &di) { return fused_pairs(di); }
+int fused_epilogue_warps(const DeviceInfo &di) { return fused_pairs(di) * 2 * kPairEpiWarps; }
 
 dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h, GemmParams p,
                               cudaStream_t st, bool pair) {
@@ -864,8 +881,10 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     const uint32_t stage_bytes = kWStageBytes + h_rows * kGemmStageK * 2;  // same bytes for fp8
     const bool fused = p.mode == kGemmFused;
     if (fused && !pair) return DFLASH2_ERR_INVALID_ARG;
-    const size_t epi_bytes =
-        p.mode == kGemmFilter || fused ? 4 * sizeof(EpiScratch) : 0;
+    const size_t epi_bytes = p.mode == kGemmFilter || fused
+                                 ? (pair ? kPairEpiWarps * sizeof(EpiScratchPair)
+                                         : 4 * sizeof(EpiScratch))
+                                 : 0;
     int stages = (int)((kGemmSmemBytes - 1024 - epi_bytes) / stage_bytes);
     if (stages > kGemmMaxStages) stages = kGemmMaxStages;
     if (stages < 2) return DFLASH2_ERR_INVALID_ARG;  // bn <= 256 always leaves room for two
@@ -893,7 +912,7 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
         if ((int64_t)p.n_pilot * p.n_tok_tiles > 2LL * pairs) return DFLASH2_ERR_INVALID_ARG;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(2 * pairs));
-        cfg.blockDim = dim3(192);
+        cfg.blockDim = dim3(kPairThreads);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = st;
         cudaLaunchAttribute attr[2];
@@ -909,7 +928,7 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     if (pair) {
         const int64_t pairs_max = di.sm_count / 2;
         const int pairs = (int)(total < pairs_max ? total : pairs_max);
-        launch_k(gemm_tc_pair_kernel, 2 * pairs, 192, smem, st, tm_w, tm_h, p);
+        launch_k(gemm_tc_pair_kernel, 2 * pairs, kPairThreads, smem, st, tm_w, tm_h, p);
     } else {
         const int grid = (int)(total < di.sm_count ? total : di.sm_count);
         launch_k(gemm_tc_kernel, grid, 192, smem, st, tm_w, tm_h, p);

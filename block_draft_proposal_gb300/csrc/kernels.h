@@ -102,8 +102,10 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
 dflash2_status launch_quant_rows_e4m3(const void *x, int32_t dtype, int64_t rows, int32_t cols,
                                       uint8_t *q, float *d, cudaStream_t st);
 
-// Epilogue warps of one fused launch (4 per CTA, every CTA resident at once),
-// or 0 when the device cannot hold such a launch.  Host-side, cached per device.
+// CTA pairs of one fused launch (every CTA resident at once) and their
+// epilogue warps, or 0 when the device cannot hold such a launch.  Host-side,
+// cached per device.
+int fused_pair_count(const DeviceInfo &di);
 int fused_epilogue_warps(const DeviceInfo &di);
 
 }  // namespace dflash2

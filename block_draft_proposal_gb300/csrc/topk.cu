@@ -635,7 +635,7 @@ bool use_fused(const DeviceInfo &di, const TopkLayout &L, int64_t rows, int bn, 
     const int64_t tok_tiles = (rows + bn - 1) / bn;
     const int64_t all_tiles = (int64_t)L.n_wtiles * tok_tiles;
     const int64_t filter_tiles = (int64_t)(L.n_wtiles - L.n_pilot) * tok_tiles;
-    const int64_t fused_pairs = std::min<int64_t>(all_tiles, fused_warps / 8);
+    const int64_t fused_pairs = std::min<int64_t>(all_tiles, fused_pair_count(di));
     if ((int64_t)L.n_pilot * tok_tiles > 2 * fused_pairs) return false;
     const int64_t filter_pairs = std::min<int64_t>(filter_tiles, di.sm_count / 2);
     if (filter_pairs < 1) return true;  // the pilot covers the vocab
