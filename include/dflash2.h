@@ -251,7 +251,7 @@ dflash2_status dflash2_selector_walk(const void *h, const void *proj, const void
 /*
  * The selector walk in two calls, so that the projection (which needs only h)
  * can run on another stream while the unary candidates are computed.  The
- * paper computes project(h) inside build_lattice; splitting it changes no
+ * sglang DFlash2 PR computes project(h) inside build_lattice; splitting it changes no
  * arithmetic: the two calls together give exactly what dflash2_selector_walk
  * gives for the same arguments.
  *
@@ -285,7 +285,7 @@ dflash2_status dflash2_selector_walk_projected(const void *A, const void *B, int
                                                void *stream);
 
 /*
- * Selector walk without a workspace argument.  The paper has no counterpart:
+ * Selector walk without a workspace argument.  The DFlash2 PR has no counterpart:
  * this is a library convenience for callers that cannot provide device
  * memory at call time, such as serving loops whose device memory belongs to
  * another allocator (a caching allocator that reserved its pool up front and

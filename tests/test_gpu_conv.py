@@ -75,7 +75,7 @@ EDGE = [
 def test_conv_edge_cases(cuda, case):
     c = dict(case)
     trim = c.pop("trim")
-    w = synth.CONFIGS[0].scaled(**c, x_std=1.0, seed=77)
+    w = synth.BY_NAME["tiny-fp32"].scaled(**c, x_std=1.0, seed=77)
     inp = synth.make(w, parts=("x", "base", "delta"))
     n = w.n_tokens - trim
     x, delta = inp["x"][:n].copy(), inp["delta"][:n].copy()
@@ -86,7 +86,7 @@ def test_conv_edge_cases(cuda, case):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_conv_misaligned_input_takes_scalar_path(cuda, dtype):
-    w = synth.CONFIGS[0].scaled(batch=4, dtype=dtype, x_std=1.0, seed=78)
+    w = synth.BY_NAME["tiny-fp32"].scaled(batch=4, dtype=dtype, x_std=1.0, seed=78)
     inp = synth.make(w, parts=("x", "base", "delta"))
     gpu = _run(w, cuda, inp["x"], inp["base"], inp["delta"], offset_elems=1)
     ref = oracle.conv(inp["x"], inp["base"], inp["delta"], w.block_size, w.group_size, w.taps)

@@ -67,7 +67,7 @@ SMALL = [
 @pytest.mark.parametrize("case", SMALL, ids=lambda c: f"m{c[0]}-h{c[1]}-v{c[2]}-k{c[4]}-{c[7]}")
 def test_unary_topk_small(cuda, case):
     rows, hidden, vd, vt, k, mult, cap, dtype = case
-    w = synth.CONFIGS[0].scaled(batch=rows, block_size=2, hidden=hidden, draft_vocab=vd,
+    w = synth.BY_NAME["tiny-fp32"].scaled(batch=rows, block_size=2, hidden=hidden, draft_vocab=vd,
                                 target_vocab=vt, top_k=k, mult=mult, cap=cap, dtype=dtype, seed=91)
     inp = synth.make(w, parts=("h", "lm_head"))
     ids, vals, err = _run(cuda, inp["h"], inp["lm_head"], vt, mult, cap, k)
@@ -96,7 +96,7 @@ def test_overflowing_candidate_lists_fall_back_exactly(cuda):
     # the minimum workspace leaves room for K candidates per row: every row
     # that meets a filter-pass survivor overflows and is recomputed exactly
     rows, hidden, vd, vt, k = 24, 128, 20000, 19900, 16
-    w = synth.CONFIGS[0].scaled(batch=rows, block_size=2, hidden=hidden, draft_vocab=vd,
+    w = synth.BY_NAME["tiny-fp32"].scaled(batch=rows, block_size=2, hidden=hidden, draft_vocab=vd,
                                 target_vocab=vt, top_k=k, dtype="bf16", seed=92)
     inp = synth.make(w, parts=("h", "lm_head"))
     ws = dflash2.unary_topk_workspace_min(rows, vd, k, dflash2.BF16)
@@ -136,7 +136,7 @@ def test_high_padded_logits_are_never_chosen(cuda):
 
 def test_k_equal_to_target_vocab_returns_every_valid_id(cuda):
     rows, hidden, vd, vt = 4, 64, 130, 100
-    w = synth.CONFIGS[0].scaled(batch=rows, block_size=2, hidden=hidden, draft_vocab=vd,
+    w = synth.BY_NAME["tiny-fp32"].scaled(batch=rows, block_size=2, hidden=hidden, draft_vocab=vd,
                                 target_vocab=vt, top_k=vt, dtype="bf16", seed=95)
     inp = synth.make(w, parts=("h", "lm_head"))
     ids, vals, err = _run(cuda, inp["h"], inp["lm_head"], vt, 1.0, 0.0, vt)
@@ -148,7 +148,7 @@ def test_k_equal_to_target_vocab_returns_every_valid_id(cuda):
 
 def test_zero_multiplier_ties_resolve_to_smallest_ids(cuda):
     rows, hidden, vd, k = 3, 64, 9000, 20
-    w = synth.CONFIGS[0].scaled(batch=rows, block_size=2, hidden=hidden, draft_vocab=vd,
+    w = synth.BY_NAME["tiny-fp32"].scaled(batch=rows, block_size=2, hidden=hidden, draft_vocab=vd,
                                 target_vocab=vd, top_k=k, dtype="bf16", seed=96)
     inp = synth.make(w, parts=("h", "lm_head"))
     ids, vals, err = _run(cuda, inp["h"], inp["lm_head"], vd, 0.0, 0.0, k)

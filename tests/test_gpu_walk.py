@@ -144,7 +144,7 @@ WALK_CASES = [
 
 @pytest.mark.parametrize("case", WALK_CASES, ids=lambda c: f"r{c['rank']}-k{c['top_k']}-{c['dtype']}")
 def test_walk_small_shapes(cuda, case):
-    w = synth.CONFIGS[0].scaled(draft_vocab=3000, target_vocab=3000, seed=97, **case)
+    w = synth.BY_NAME["tiny-fp32"].scaled(draft_vocab=3000, target_vocab=3000, seed=97, **case)
     inp, cand, cand_u = _random_candidates(w, 98, scale_ab=20.0)
     tokens, q, ps, err = _run_walk(cuda, inp, cand, cand_u)
     assert err == 0
@@ -152,7 +152,7 @@ def test_walk_small_shapes(cuda, case):
 
 
 def test_out_of_range_ids_set_the_error_bit_and_use_zero_rows(cuda):
-    w = synth.CONFIGS[0].scaled(batch=3, block_size=4, hidden=64, rank=16, top_k=8, dtype="bf16",
+    w = synth.BY_NAME["tiny-fp32"].scaled(batch=3, block_size=4, hidden=64, rank=16, top_k=8, dtype="bf16",
                                 draft_vocab=500, target_vocab=500, sampling="greedy", seed=99)
     inp, cand, cand_u = _random_candidates(w, 100, scale_ab=30.0)
     inp["anchors"] = inp["anchors"].copy()
@@ -169,7 +169,7 @@ def test_out_of_range_ids_set_the_error_bit_and_use_zero_rows(cuda):
 
 
 def test_greedy_rows_do_not_depend_on_other_rows(cuda):
-    w = synth.CONFIGS[0].scaled(batch=8, block_size=10, hidden=128, rank=32, top_k=16, dtype="bf16",
+    w = synth.BY_NAME["tiny-fp32"].scaled(batch=8, block_size=10, hidden=128, rank=32, top_k=16, dtype="bf16",
                                 draft_vocab=2000, target_vocab=2000, sampling="mixed",
                                 temperature=0.7, seed=101)
     inp, cand, cand_u = _random_candidates(w, 102, scale_ab=10.0)
@@ -190,7 +190,7 @@ def test_greedy_rows_do_not_depend_on_other_rows(cuda):
 def test_projection_then_walk_equals_the_one_call_walk(cuda, case):
     """dflash2_selector_project on one stream, then dflash2_selector_walk_projected
     on another (ordered by an event), give exactly what dflash2_selector_walk gives."""
-    w = synth.CONFIGS[0].scaled(draft_vocab=3000, target_vocab=3000, seed=97, **case)
+    w = synth.BY_NAME["tiny-fp32"].scaled(draft_vocab=3000, target_vocab=3000, seed=97, **case)
     inp, cand, cand_u = _random_candidates(w, 98, scale_ab=20.0)
     tokens, q, ps, err = _run_walk(cuda, inp, cand, cand_u)
     t = {k: dflash2.to_device(v, cuda) for k, v in inp.items() if v is not None}

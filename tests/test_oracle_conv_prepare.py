@@ -60,7 +60,7 @@ def test_matches_numpy_float64_product():
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_prepare_is_identity_at_module_init(dtype):
     # base_kernel[:, 0] = 1 and a zero projection: both convolutions pass x through
-    w = synth.CONFIGS[0].scaled(dtype=dtype)
+    w = synth.BY_NAME["tiny-fp32"].scaled(dtype=dtype)
     d = synth.make(w, parts=("x",))
     x = d["x"]
     base2 = np.zeros((2, w.taps, w.hidden), dtype=np.float32)
