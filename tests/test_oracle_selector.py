@@ -12,8 +12,6 @@ import os
 import numpy as np
 import pytest
 
-from block_draft_proposal_gb300 import synth
-
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "selector_tiny.txt")
 
 

@@ -9,7 +9,6 @@ constructed worst cases.
 import math
 
 import numpy as np
-import pytest
 
 from block_draft_proposal_gb300 import synth
 
