@@ -7,6 +7,7 @@ import torch
 
 import oracle
 from block_draft_proposal_gb300 import dflash2, synth
+from parity import check_step_against_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -40,20 +41,11 @@ def test_d2t_table_matches_oracle_bit_exact(cuda):
     np.testing.assert_array_equal(t_ids.cpu().numpy(), ref)
 
 
-def _pipeline_oracle(w, inp):
-    u = oracle.unary_rows(inp["h"], inp["lm_head"], w.target_vocab, w.mult, w.cap)
-    ids, vals = oracle.topk(u, w.top_k)
-    sel = oracle.selector(inp["h"], inp["proj"], inp["A"], inp["B"], inp["anchors"],
-                          ids.reshape(w.batch, w.slots, w.top_k),
-                          vals.reshape(w.batch, w.slots, w.top_k), inp["uniforms"],
-                          inp["temperatures"], inp["greedy"])
-    tgt, errors = oracle.d2t(sel["tokens"].reshape(-1), inp["d2t"], w.draft_vocab, w.target_vocab)
-    return ids, sel, tgt.reshape(w.batch, w.slots), errors
-
-
 @pytest.mark.parametrize("name,scale", [("tiny-fp32", {}),
                                         ("reduced-vocab-bs12-bf16", dict(batch=6)),
-                                        ("padded-vocab-bf16", dict(batch=2))])
+                                        ("padded-vocab-bf16", dict(batch=2)),
+                                        ("stress-bf16", dict(batch=3, draft_vocab=40000,
+                                                             target_vocab=40000))])
 def test_proposal_step_end_to_end(cuda, name, scale):
     w = synth.BY_NAME[name].scaled(**scale)
     inp = synth.make(w)
@@ -61,18 +53,8 @@ def test_proposal_step_end_to_end(cuda, name, scale):
     out = dflash2.proposal_step(w, t)
     torch.cuda.synchronize()
     assert int(out["err"].item()) & ~dflash2.DEVINFO_TOPK_FALLBACK == 0
-    ids, sel, tgt, errors = _pipeline_oracle(w, inp)
-    assert errors == 0
-    agree_ids = (out["cand_ids"].cpu().numpy() == ids).mean()
-    agree_tok = (out["tokens"].cpu().numpy() == sel["tokens"]).mean()
-    print(f"{name}: end-to-end agreement ids {agree_ids:.4f} tokens {agree_tok:.4f}")
-    # end to end, an accepted top-K near-tie may change a path; the staged
-    # tests pin each stage exactly.  Here most of the batch must agree.
-    assert agree_ids >= 0.99 and agree_tok >= 0.9
-    # the remap of the GPU's own tokens is exact
-    ref_tgt, _ = oracle.d2t(out["tokens"].cpu().numpy().reshape(-1), inp["d2t"], w.draft_vocab,
-                            w.target_vocab)
-    np.testing.assert_array_equal(out["target_ids"].cpu().numpy().reshape(-1), ref_tgt)
+    topk_ties, walk_ties = check_step_against_oracle(w, inp, out)
+    print(f"{name}: end-to-end near-ties accepted: top-K {topk_ties}, walk {walk_ties}")
 
 
 def test_captured_graph_replays_the_eager_step(cuda):

@@ -2,40 +2,38 @@
 
 Ids must equal the oracle's except documented near-ties (see parity.py);
 cand_u must lie within the fp32 forward-error bound of the exact u.  Small
-cases cover several tiles with ragged tails in every dimension; the named
-workloads run at full size with the oracle evaluated on sampled rows; the
-candidate-list overflow path, adversarial vocab orders, high padded logits and
-K equal to the logical vocab are covered explicitly."""
+cases cover several tiles with ragged tails in every dimension, compare every
+row, and pin which path (the fused cooperative launch or the split passes) each
+one takes; the named workloads run at full size with the oracle on every row
+(three workloads) or on at least 64 rows that include each token tile's first
+and last row (the padded-vocab and stress sizes); the candidate-list overflow
+path, adversarial vocab orders, high padded logits and K equal to the logical
+vocab are covered explicitly."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from block_draft_proposal_gb300 import dflash2, synth
-from parity import check_topk_row, u_error_bound
+from parity import compare_topk_rows
 
 pytestmark = pytest.mark.gpu
-
-
-def _f64(a):
-    return (synth.bf16_bits_to_f32(a) if a.dtype == np.uint16 else a).astype(np.float64)
 
 
 def _check(h, W, target_vocab, mult, cap, k, ids, vals, rows):
     u = oracle.unary_rows(h, W, target_vocab, mult, cap, rows=rows)
     ora_ids, _ = oracle.topk(u, k)
-    ties = 0
-    for r, m in enumerate(rows):
-        h64 = _f64(h[m])
-
-        def bound(sel, h64=h64, r=r):
-            sel = np.asarray(sel)
-            return u_error_bound(h64, _f64(W[sel]), np.arange(len(sel)), u[r][sel], mult)
-
-        ties += check_topk_row(ids[m], vals[m], ora_ids[r], u[r], bound, k)
-        assert np.all(ids[m] < target_vocab)
-        assert np.all(np.diff(vals[m]) <= 0)
+    ties, _ = compare_topk_rows(h, W, u, ora_ids, mult, k, ids, vals, rows, target_vocab)
     return ties
+
+
+def _launches(rows, vd, k, mult, dtype):
+    return dflash2.library().dflash2_unary_topk_launches(
+        rows, vd, k, mult, dflash2.BF16 if dtype == "bf16" else dflash2.F32)
+
+
+def _gb300():
+    return torch.cuda.get_device_properties(0).multi_processor_count == 152
 
 
 def _run(dev, h, W, target_vocab, mult, cap, k, ws_bytes=None):
@@ -48,25 +46,38 @@ def _run(dev, h, W, target_vocab, mult, cap, k, ws_bytes=None):
     return ids.cpu().numpy(), vals.cpu().numpy(), int(err.item())
 
 
+# The last column is the number of kernels dflash2_unary_topk_launches reports on
+# a 152-SM GB300: 2 = the fused cooperative launch (pilot, select and filter in
+# one GEMM launch, then finalize), 3 / 4 = the split passes (pilot, select,
+# filter when the pilot does not cover the vocab, finalize), None = fp32.  Every
+# case compares all of its rows with the oracle, so both bf16 paths are pinned
+# row by row.
 SMALL = [
-    # rows, hidden, draft_vocab, target_vocab, k, mult, cap, dtype
-    (37, 200, 5000, 4900, 16, 0.5, 30.0, "bf16"),      # ragged in every dimension, pilot-only
-    (300, 264, 40000, 39990, 32, 1.0, 0.0, "bf16"),    # filter pass active, two token tiles
-    (7, 512, 70000, 70000, 64, 1.0, 30.0, "bf16"),
-    (513, 128, 9000, 8800, 8, 2.0, 0.0, "bf16"),       # three token tiles
-    (5, 96, 3000, 2999, 128, 1.0, 0.0, "bf16"),        # K at its maximum; hidden below one stage
-    (9, 136, 1100, 1000, 16, 1.0, 10.0, "f32"),
-    (2100, 128, 9000, 8990, 24, 1.0, 30.0, "bf16"),   # nine token tiles over the CTA pairs
-    (1800, 136, 4000, 4000, 8, 0.7, 0.0, "bf16"),     # pilot of 8 of 16 units
-    (300, 136, 1500, 1450, 16, 1.0, 30.0, "bf16"),    # under 8 units: the pilot covers the vocab
-    (96, 256, 20000, 19990, 16, -0.5, 0.0, "bf16"),   # negative multiplier: order reversed
-    (40, 128, 12000, 12000, 8, -1.0, 30.0, "bf16"),   # negative multiplier with the soft cap
+    # rows, hidden, draft_vocab, target_vocab, k, mult, cap, dtype, launches
+    (37, 200, 5000, 4900, 16, 0.5, 30.0, "bf16", 2),      # ragged in every dimension
+    (300, 264, 40000, 39990, 32, 1.0, 0.0, "bf16", 4),    # filter pass active, two token tiles
+    (7, 512, 70000, 70000, 64, 1.0, 30.0, "bf16", 4),
+    (513, 128, 9000, 8800, 8, 2.0, 0.0, "bf16", 2),       # three token tiles
+    (5, 96, 3000, 2999, 128, 1.0, 0.0, "bf16", 4),        # K at its maximum; hidden below one stage
+    (9, 136, 1100, 1000, 16, 1.0, 10.0, "f32", None),
+    (2100, 128, 9000, 8990, 24, 1.0, 30.0, "bf16", 4),   # nine token tiles over the CTA pairs
+    (1800, 136, 4000, 4000, 8, 0.7, 0.0, "bf16", 2),     # pilot of 8 of 16 units
+    (300, 136, 1500, 1450, 16, 1.0, 30.0, "bf16", 3),    # under 8 units: the pilot covers the vocab
+    (96, 256, 20000, 19990, 16, -0.5, 0.0, "bf16", 4),   # negative multiplier: order reversed
+    (40, 128, 12000, 12000, 8, -1.0, 30.0, "bf16", 4),   # negative multiplier with the soft cap
+    # fused launch: 2432 rows = two rows for each of the 1216 select warps
+    # (76 CTA pairs x 16 epilogue warps), ten token tiles
+    (2432, 128, 10240, 10240, 16, 1.0, 30.0, "bf16", 2),
+    (1000, 200, 30000, 29990, 16, 0.7, 0.0, "bf16", 2),  # fused, ragged hidden and vocab
+    (300, 136, 70000, 69990, 32, 1.0, 30.0, "bf16", 2),  # fused with K = 32 (18 pilot units)
 ]
 
 
 @pytest.mark.parametrize("case", SMALL, ids=lambda c: f"m{c[0]}-h{c[1]}-v{c[2]}-k{c[4]}-{c[7]}")
 def test_unary_topk_small(cuda, case):
-    rows, hidden, vd, vt, k, mult, cap, dtype = case
+    rows, hidden, vd, vt, k, mult, cap, dtype, launches = case
+    if launches is not None and _gb300():
+        assert _launches(rows, vd, k, mult, dtype) == launches
     w = synth.BY_NAME["tiny-fp32"].scaled(batch=rows, block_size=2, hidden=hidden, draft_vocab=vd,
                                 target_vocab=vt, top_k=k, mult=mult, cap=cap, dtype=dtype, seed=91)
     inp = synth.make(w, parts=("h", "lm_head"))
@@ -76,20 +87,38 @@ def test_unary_topk_small(cuda, case):
     print(f"near-ties accepted: {ties}")
 
 
+def _sample_rows(w, n_min=64):
+    """At least n_min rows: the first and last row of every bf16 token tile (rows
+    in near-equal tiles of at most 256), then seeded random rows."""
+    n_tiles = (w.rows + 255) // 256
+    bn = ((w.rows + n_tiles - 1) // n_tiles + 15) // 16 * 16
+    rows = set()
+    for t in range(0, w.rows, bn):
+        rows.update((t, min(t + bn, w.rows) - 1))
+    rng = np.random.default_rng(5)
+    while len(rows) < n_min:
+        rows.add(int(rng.integers(0, w.rows)))
+    return sorted(rows)
+
+
+# all rows where the oracle finishes in seconds; otherwise every token tile's
+# first and last row plus random rows, 64 at least
+ALL_ROWS = {"tiny-fp32", "qwen3-8b-bf16", "reduced-vocab-bs12-bf16"}
+
+
 @pytest.mark.parametrize("name", [c.name for c in synth.CONFIGS])
 def test_unary_topk_named_workloads(cuda, name):
     w = synth.BY_NAME[name]
     inp = synth.make(w, parts=("h", "lm_head"))
     ids, vals, err = _run(cuda, inp["h"], inp["lm_head"], w.target_vocab, w.mult, w.cap, w.top_k)
     assert err == 0, hex(err)
-    rng = np.random.default_rng(5)
-    rows = sorted({0, w.rows - 1, *rng.integers(0, w.rows, size=2).tolist()})
+    rows = list(range(w.rows)) if name in ALL_ROWS else _sample_rows(w)
     ties = _check(inp["h"], inp["lm_head"], w.target_vocab, w.mult, w.cap, w.top_k, ids, vals, rows)
     # properties that hold for every row
     assert np.all(ids >= 0) and np.all(ids < w.target_vocab)
     assert np.all(np.diff(vals, axis=1) <= 0)
     assert all(len(set(r)) == w.top_k for r in ids.tolist())
-    print(f"{name}: near-ties accepted {ties}")
+    print(f"{name}: {len(rows)} rows compared, near-ties accepted {ties}")
 
 
 def test_overflowing_candidate_lists_fall_back_exactly(cuda):

@@ -12,36 +12,9 @@ import torch
 
 import oracle
 from block_draft_proposal_gb300 import dflash2, synth
+from parity import compare_walk
 
 pytestmark = pytest.mark.gpu
-EPS = 2.0 ** -24
-
-
-def _f64(a):
-    return (synth.bf16_bits_to_f32(a) if a.dtype == np.uint16 else a).astype(np.float64)
-
-
-def _edge_bound(inp, cand, anchors, hidden):
-    """Per-edge forward-error bound [B, S, K(prev), K(cur)] of the fp32 edges."""
-    batch, slots, k = cand.shape
-    A, B = _f64(inp["A"]), _f64(inp["B"])
-    r = A.shape[1]
-    habs = np.abs(_f64(inp["h"]))
-    gabs = habs @ np.abs(_f64(inp["proj"])).T                  # sum_i |h_i P_ji|
-    g = _f64(inp["h"]) @ _f64(inp["proj"]).T
-    gerr = (hidden + 2) * EPS * gabs                           # |g_gpu - g|
-    out = np.empty((batch, slots, k, k))
-    for b in range(batch):
-        for s in range(slots):
-            prev = np.full(k, anchors[b]) if s == 0 else cand[b, s - 1]
-            prev = np.clip(prev, 0, A.shape[0] - 1)
-            pa = np.abs(A[prev])                               # [k, r]
-            cb = np.abs(B[np.clip(cand[b, s], 0, B.shape[0] - 1)])
-            row = b * slots + s
-            lat = (pa * np.abs(g[row])[None, :]) @ cb.T        # sum |A g B|
-            lat_g = (pa * gerr[row][None, :]) @ cb.T
-            out[b, s] = (r + 4) * EPS * lat + lat_g
-    return out
 
 
 def _run_walk(dev, inp, cand, cand_u, with_ws=None):
@@ -56,47 +29,9 @@ def _run_walk(dev, inp, cand, cand_u, with_ws=None):
 
 
 def _compare(inp, cand, cand_u, tokens, q, ps, dtype, hidden):
-    batch, slots, k = cand.shape
     ora = oracle.selector(inp["h"], inp["proj"], inp["A"], inp["B"], inp["anchors"], cand, cand_u,
                           inp["uniforms"], inp["temperatures"], inp["greedy"])
-    bound = _edge_bound(inp, cand, inp["anchors"], hidden) + np.abs(cand_u)[:, :, None, :] * EPS
-    scores = ora["scores"]
-    q_tol = 1e-5 if dtype == "f32" else 2e-2
-    ties = 0
-    for b in range(batch):
-        greedy = bool(inp["greedy"][b])
-        prev = 0
-        diverged = False
-        for s in range(slots):
-            row = cand[b, s]
-            gi = int(np.nonzero(row == tokens[b, s])[0][0])     # GPU index (ids are distinct)
-            # edges the GPU read: the oracle lattice row of the GPU's predecessor
-            e_ref = scores[b, s, prev].astype(np.float64)
-            tol = bound[b, s, prev] + np.abs(e_ref) * EPS
-            assert np.all(np.abs(ps[b, s].astype(np.float64) - e_ref) <= tol), (b, s)
-            if greedy:
-                np.testing.assert_array_equal(q[b, s], np.eye(k, dtype=np.float32)[gi])
-            else:
-                assert abs(q[b, s].astype(np.float64).sum() - 1.0) <= 1e-6 * k
-            if not diverged:
-                oi = int(ora["chosen"][b, s])
-                if gi != oi:
-                    if greedy:
-                        gap = abs(float(e_ref[gi]) - float(e_ref[oi]))
-                        assert gap <= tol[gi] + tol[oi], (b, s, gi, oi, gap)
-                    else:
-                        t = max(float(inp["temperatures"][b]), 1e-5)
-                        p = ora["q"][b, s].astype(np.float64)
-                        cdf = np.cumsum(p)
-                        lo, hi = min(gi, oi), max(gi, oi)
-                        slack = k * 2.0 ** -23 + 4 * float(tol.max()) / t
-                        assert np.all(np.abs(inp["uniforms"][b, s] - cdf[lo:hi]) <= slack), (b, s)
-                    ties += 1
-                    diverged = True
-                else:
-                    assert abs(q[b, s] - ora["q"][b, s]).max() <= q_tol
-            prev = gi
-    return ties
+    return compare_walk(inp, ora, cand, cand_u, tokens, q, ps, dtype, hidden)
 
 
 def _named(name):
