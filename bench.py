@@ -9,10 +9,11 @@ the top-K), replayed from one captured CUDA graph.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                     [--workload NAME]
 
-The default workload is the Qwen3-8B-shaped bf16 draft (batch 32, block 16,
-hidden 4096, vocab 151936, rank 64, top-K 16, cap 30; even rows greedy, odd
-rows T = 0.7).  The metric is proposals per second (batch x slots proposed /
-step time).  L2 is flushed (a 256 MiB write) before every timed step and the
+The default workload is the largest one-GPU configuration, the large-batch,
+large-K stress draft (batch 512, block 16, hidden 7168 = 896 groups x 8, taps
+4, vocab 163840, rank 128, top-K 64, cap 30, mult 0.5, every row sampled at
+T = 0.6); the other named workloads run with --workload.  The metric is
+proposals per second (batch x slots proposed / step time).  L2 is flushed (a 256 MiB write) before every timed step and the
 flush is outside the timed events.  Prints ONE JSON line (rank 0).
 
 `--impl reference` times the CPU oracle (the method restated in plain C,
@@ -26,7 +27,6 @@ from __future__ import annotations
 import argparse
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -37,9 +37,11 @@ sys.path.insert(0, ROOT)
 
 METRIC = "draft blocks/sec (batch×slots proposed/s) + % HBM / tensor roofline per kernel"
 UNIT = "proposals/s"
-DEFAULT_WORKLOAD = "qwen3-8b-bf16"
+DEFAULT_WORKLOAD = "stress-bf16"
 L2_FLUSH_BYTES = 256 << 20
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "unary_topk_qwen3-8b-bf16.md")
+# DRAM bytes of the unary top-K stage per workload, from one ncu capture of
+# the stage's launches, keyed by the hash of the sources that make the stage
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
 def _dist():
@@ -151,26 +153,18 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def _profile_traffic(kernel_sources):
-    """DRAM bytes (read + write) of one unary_topk stage (all its launches)
-    from the committed ncu summary, or None when the kernel sources changed
-    since the capture."""
-    import hashlib
+def _profile_traffic(workload: str, src_hash: str):
+    """DRAM bytes (read + write) of one unary_topk stage (all its launches) of
+    `workload` from the committed ncu record, or None when there is none or
+    the stage's sources changed since the capture."""
     try:
-        text = open(PROFILE_SUMMARY).read()
-    except OSError:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
         return None
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    hm = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
-    if not m or not hm:
+    if not rec or rec.get("source_sha16") != src_hash:
         return None
-    h = hashlib.sha256()
-    for path in kernel_sources:
-        with open(path, "rb") as f:
-            h.update(f.read())
-    if h.hexdigest()[:16] != hm.group(1)[:16]:
-        return None
-    return float(m.group(1))
+    return float(rec["unary_topk_dram_bytes"])
 
 
 def kernel_source_hash():
@@ -375,9 +369,9 @@ def run_gpu(args, w):
     # the captured step on that set (each set has its own outputs), and reads
     # its tokens and q back into pinned host memory on a third stream, so the
     # next step's compute does not wait for the read-back.  Timed from the
-    # first copy to the last read-back over K steps; the 1.24 GB lm_head
-    # streams from HBM at every step (inputs larger than L2), so this loop runs
-    # without the flush.
+    # first copy to the last read-back over K steps; the lm_head (1.2 GB and
+    # more) streams from HBM at every step (inputs larger than L2), so this
+    # loop runs without the flush.
     in_keys = ("x", "delta", "h", "temperatures", "greedy", "anchors")
     host_in = {k: torch.from_numpy(inp[k].view(np.int16) if inp[k].dtype == np.uint16 else inp[k])
                .pin_memory() for k in in_keys}
@@ -578,8 +572,8 @@ def run_gpu(args, w):
     work = algorithmic_work(w)
     unary_ms = statistics.mean(stage_ms["unary_topk"])
     achieved_tf = work["gemm_flops"] / (unary_ms * 1e-3) / 1e12
-    src_hash, srcs = kernel_source_hash()
-    traffic = _profile_traffic(srcs)
+    src_hash, _ = kernel_source_hash()
+    traffic = _profile_traffic(w.name, src_hash)
     conv_ms = statistics.mean(stage_ms["conv"])
     walk_ms = statistics.mean(stage_ms["walk"])
     stages = {
@@ -619,7 +613,10 @@ def run_gpu(args, w):
     # CPU baseline: the oracle as it stands on a bounded sample (rank 0, N = 1)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        n_req = max(1, min(w.batch, 20))   # about 10-30 s of CPU work on 16 cores
+        # about 1.9e11 multiply-adds of the lm_head (10-20 s on 16 cores): 20
+        # requests of the Qwen3-8B-shaped draft, 10 of the stress draft
+        per_req = w.slots * w.draft_vocab * w.hidden
+        n_req = max(1, min(w.batch, 20, int(round(1.9e11 / per_req))))
         tc = oracle_sample_time(w, inp, n_req)
         import oracle
         threads = oracle.set_threads(0)
@@ -644,6 +641,7 @@ def run_gpu(args, w):
         "activations N(0,1); walk uniforms drawn on the device by Philox4x64-10)", "config": _config(w),
         "roofline": {"bound": "tensor", "achieved": achieved_tf, "peak": tf_burst,
                      "unit": "TFLOP/s", "frac": achieved_tf / tf_burst, "traffic": traffic,
+                     "traffic_source": "profiles/traffic.json" if traffic is not None else None,
                      "kernel": "unary_topk stage (fused pilot + select + filter GEMM, then "
                                "finalize), 2*M*V*H flops over the stage time",
                      "peak_kind": f"{peak_kind} bf16 burst"},
@@ -667,8 +665,8 @@ def run_gpu(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -21,8 +21,13 @@ namespace {
 // Upper bound of the scratch this entry point can use.  The walk's scratch
 // holds the hidden-split partial projections (k_splits x rows x rank fp32)
 // and, for top_k <= 32, the lattice (rows x top_k x (top_k + 3) x 4 bytes);
-// 4 MiB covers, for example, 480 rows at rank 64 and top_k 16 (1.2 MiB).
+// 4 MiB covers, for example, 480 rows at rank 64 and top_k 16 (1.2 MiB) or
+// 1408 rows at rank 64 and top_k 16 (2.3 MiB), but not 960 rows at top_k 32
+// (4.3 MiB of lattice) nor 7680 rows at rank 128.
 constexpr size_t kNoAllocScratchBytes = 4u << 20;
+// The walk's shape limits (include/dflash2.h, dflash2_selector_walk).
+constexpr int kNoAllocMaxRank = 256;
+constexpr int kNoAllocMaxK = 128;
 
 static __device__ __align__(256) unsigned char g_walk_scratch[kNoAllocScratchBytes];
 
@@ -33,6 +38,8 @@ void *g_scratch_addr[kMaxDevices];  // device address of g_walk_scratch, per dev
 // Looks up (once per device, with that device current) the device address of
 // the scratch array.  In host code the array's name is only a host-side
 // stand-in, never a device address, so it is not passed to kernels directly.
+// The address is kept for the life of the process: it stays valid as long as
+// the device's primary context is not reset (cudaDeviceReset) meanwhile.
 dflash2_status scratch_address(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -62,8 +69,17 @@ extern "C" dflash2_status dflash2_selector_walk_noalloc(
     int32_t slots, int32_t hidden, int32_t rank, int32_t top_k, int32_t dtype, int64_t *tokens,
     float *q, float *path_scores, int32_t *err_word, void *stream) {
     using namespace dflash2;
-    // The shapes decide how much scratch the walk needs; reject what does not
-    // fit before touching the device.
+    // The same shape checks as the workspace entry point, first, so that an
+    // invalid shape gets the same status from both; an empty batch queues
+    // nothing and needs no scratch.
+    if (dtype != DFLASH2_F32 && dtype != DFLASH2_BF16) return DFLASH2_ERR_UNSUPPORTED_DTYPE;
+    const int rank_mult = dtype == DFLASH2_BF16 ? 8 : 4;
+    if (batch < 0 || slots < 0 || hidden <= 0 || rank <= 0 || rank > kNoAllocMaxRank ||
+        rank % rank_mult != 0 || top_k <= 0 || top_k > kNoAllocMaxK || table_rows <= 0)
+        return DFLASH2_ERR_INVALID_ARG;
+    if (batch == 0 || slots == 0) return DFLASH2_OK;
+    // Then the scratch the shapes need: refuse what does not fit before
+    // touching the device.
     const size_t need =
         dflash2_selector_walk_workspace_size(batch, slots, hidden, rank, top_k, dtype);
     if (need > kNoAllocScratchBytes) return DFLASH2_ERR_WORKSPACE;

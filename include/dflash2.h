@@ -296,11 +296,17 @@ dflash2_status dflash2_selector_walk_projected(const void *A, const void *B, int
  * workspace and ws_bytes.  It allocates nothing: its scratch is a fixed
  * 4 MiB (4194304-byte) array in the library's device memory, held by every
  * GPU that loads the library until the process exits.
- *   - A call whose scratch need (dflash2_selector_walk_workspace_size of its
- *     shapes) exceeds 4 MiB returns DFLASH2_ERR_WORKSPACE and queues nothing.
+ *   - The arguments are checked first, as dflash2_selector_walk checks them
+ *     (an invalid shape returns INVALID_ARG or UNSUPPORTED_DTYPE; batch or
+ *     slots 0 queues nothing and touches no device state).  Then a call whose
+ *     scratch need (dflash2_selector_walk_workspace_size of its shapes: the
+ *     projection partials, plus the lattice when top_k <= 32) exceeds 4 MiB
+ *     returns DFLASH2_ERR_WORKSPACE and queues nothing.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and keeps it for the
+ *     life of the process; make that first call before any stream capture.
+ *     The kept address assumes the device's primary context is not reset
+ *     (cudaDeviceReset) while the library is loaded.
  *   - Every call, on every stream, shares the one array and overwrites what
  *     the previous call left there (nothing in it needs to start at zero).
  *     Calls whose work overlaps on the GPU, on different streams or from
@@ -385,9 +391,11 @@ dflash2_status dflash2_conv_finish(const void *y, const void *base2, const void 
  *               emitted token, then -1.
  * workspace     device, >= dflash2_verify_workspace_size(batch, slots, vocab)
  *               bytes, 16-byte aligned (per-chunk softmax partials).
- * Arithmetic: fp32; p = 2^(logit * log2(e) / T' - m) / Z with exp2f (the
- *   scaling is exact in real arithmetic); fixed reduction orders, so results
- *   are deterministic.
+ * Arithmetic: fp32; p = 2^(logit * log2(e) / T' - m) / Z with the hardware
+ *   base-2 exponential (PTX ex2.approx.ftz.f32; the change of base is exact in
+ *   real arithmetic, and the approximation is within the tolerance the
+ *   near-tie rule allows); fixed reduction orders, so results are
+ *   deterministic.
  * Errors: slots > 64, top_k outside [1, 128], vocab outside [1, 2^20] ->
  *   INVALID_ARG.  A draft that is not among its slot's candidates, or an id
  *   outside [0, vocab), sets DFLASH2_DEVERR_ID_RANGE and leaves that request's

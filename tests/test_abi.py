@@ -140,3 +140,23 @@ def test_workspace_sizes_are_host_arithmetic(lib):
     assert walk >= 32 * 15 * 64 * 4 + 32 * 15 * 16 * (16 + 3) * 4   # partials + the lattice
     # top_k above the lattice mode's 32 needs the partials only
     assert lib.dflash2_selector_walk_workspace_size(32, 15, 4096, 64, 64, 1) < walk
+
+
+def test_noalloc_walk_checks_arguments_before_its_scratch(lib):
+    """dflash2_selector_walk_noalloc gives an invalid shape the status the
+    workspace walk gives it, before comparing the shape's scratch need with
+    its fixed array; an empty batch touches no device state."""
+    null = None
+
+    def call(batch, slots, hidden, rank, top_k, dtype, table_rows=1000):
+        return lib.dflash2_selector_walk_noalloc(
+            null, null, null, null, table_rows, null, null, null, null, null, null, batch, slots,
+            hidden, rank, top_k, dtype, null, null, null, null, null)
+
+    assert call(4096, 15, 4096, 512, 16, 1) == 1      # rank above 256: INVALID_ARG, not WORKSPACE
+    assert call(4096, 15, 4096, 64, 200, 1) == 1      # top_k above 128
+    assert call(4096, 15, 4096, 60, 16, 1) == 1       # bf16 rank not a multiple of 8
+    assert call(8, 15, 4096, 64, 16, 7) == 2          # dtype
+    assert call(8, 15, 4096, 64, 16, 1, table_rows=0) == 1
+    assert call(0, 15, 4096, 64, 16, 1) == 0          # nothing to do
+    assert call(1024, 15, 4096, 256, 16, 1) == 4      # beyond the 4 MiB array: WORKSPACE
