@@ -8,6 +8,8 @@
 // coalesced 16-byte loads, so the taps re-read shared memory instead of L2.
 // One 16-byte vector is 8 bf16 (or 4 fp32) channels of one group, so the
 // per-token coefficient delta is one scalar per (token, tap, vector).
+#include <atomic>
+
 #include "common.cuh"
 
 namespace dflash2 {
@@ -39,6 +41,18 @@ template <> struct VecTraits<__nv_bfloat16> {
     }
     __device__ static float scalar(__nv_bfloat16 v) { return __bfloat162float(v); }
     __device__ static __nv_bfloat16 from(float v) { return __float2bfloat16_rn(v); }
+    __device__ static void unpack2(const uint4 &v, float2 (&f)[4]) {
+        const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) f[i] = __bfloat1622float2(p[i]);
+    }
+    __device__ static uint4 pack2(const float2 (&f)[4]) {
+        uint4 v;
+        __nv_bfloat162 *p = reinterpret_cast<__nv_bfloat162 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) p[i] = __float22bfloat162_rn(f[i]);
+        return v;
+    }
 };
 template <> struct VecTraits<float> {
     static constexpr int N = 4;
@@ -54,6 +68,14 @@ template <> struct VecTraits<float> {
     }
     __device__ static float scalar(float v) { return v; }
     __device__ static float from(float v) { return v; }
+    __device__ static void unpack2(const uint4 &v, float2 (&f)[2]) {
+        f[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+        f[1] = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+    }
+    __device__ static uint4 pack2(const float2 (&f)[2]) {
+        return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y), __float_as_uint(f[1].x),
+                          __float_as_uint(f[1].y));
+    }
 };
 
 __device__ __forceinline__ int64_t in_block_pos(int64_t i, int bs, bool pow2) {
@@ -170,6 +192,217 @@ __global__ void __launch_bounds__(kTileVecs *kTokenLanes)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Pipelined path.  Work items of kPipeTokens tokens x kPipeVecs vectors; a
+// persistent grid of CTAs takes items in turn, and each CTA keeps
+// kPipeStages items in flight: cp.async 16-byte copies stage an item's x rows
+// and its delta slice [token][tap][groups of the item] in shared memory while
+// the CTA computes an earlier item, so an SM's loads never wait behind its
+// arithmetic or stores.  When the block size divides the tile, every tile
+// starts a block and no tap reaches before it: no halo rows are loaded;
+// otherwise taps - 1 halo rows come first.  The taps are summed in the same
+// order as conv_vec_kernel (t = 0, 1, ...; fp32 fma), so both give the same
+// bits.
+// ---------------------------------------------------------------------------
+constexpr int kPipeVecs = 64;
+constexpr int kPipeTokens = 16;
+constexpr int kPipeThreads = 256;
+constexpr int kPipeStages = 4;
+constexpr int kPipeTokPerThread = kPipeTokens * kPipeVecs / kPipeThreads;
+constexpr int kPipeMaxTaps = 8;
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool valid) {
+    const uint32_t n = valid ? 16u : 0u;  // 0 source bytes: the 16 bytes are zero-filled
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)), "l"(gmem),
+                 "r"(n)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Shared-memory bytes of one pipeline stage.
+__host__ __device__ inline int pipe_stage_bytes(int halo, int taps, int gpv, int esz) {
+    return (kPipeTokens + halo) * kPipeVecs * 16 + kPipeTokens * taps * gpv * esz;
+}
+
+// Largest number of 16-byte delta chunks per (token, tap) and item: 64 / gs
+// with gs >= 8 for bf16 and >= 4 for fp32.
+template <typename T> __host__ __device__ constexpr int pipe_max_dch() { return sizeof(T) == 2 ? 8 : 16; }
+
+// Item iterator: token tile fastest, then the 64-vector strip; advancing by
+// the grid's size needs no division.
+struct PipeItem {
+    int tile, strip;
+    __device__ __forceinline__ void advance(int dq, int dr, int n_ttiles) {
+        tile += dr;
+        strip += dq;
+        if (tile >= n_ttiles) {
+            tile -= n_ttiles;
+            ++strip;
+        }
+    }
+};
+
+template <typename T, int KT>
+__global__ void __launch_bounds__(kPipeThreads, 2)
+    conv_pipe_kernel(const T *__restrict__ x, const T *__restrict__ base,
+                     const T *__restrict__ delta, int64_t dstride, T *__restrict__ out, int64_t n,
+                     int hidden, int group_size, int taps, int bs, bool pow2, int halo,
+                     int n_ttiles, int n_strips) {
+    grid_dep_wait();
+    using V = VecTraits<T>;
+    constexpr int VN = V::N;
+    constexpr int VP = VN / 2;                 // float2 pairs of a vector
+    constexpr int EPC = 16 / (int)sizeof(T);   // elements of a 16-byte chunk
+    constexpr int kDC = kPipeTokens * KT * pipe_max_dch<T>() / kPipeThreads;  // delta chunks a thread copies, at most
+    extern __shared__ __align__(16) uint8_t pipe_sm[];
+    const int nvec = hidden / VN;
+    const int groups = hidden / group_size;
+    const int gpv = kPipeVecs * VN / group_size;  // groups of one item
+    const int dch = gpv / EPC;                    // delta chunks per (token, tap)
+    const int per_tok = taps * dch;
+    const int xrows = kPipeTokens + halo;
+    const int xbytes = xrows * kPipeVecs * 16;
+    const int stage_bytes = pipe_stage_bytes(halo, taps, gpv, (int)sizeof(T));
+    const int tid = threadIdx.x;
+
+    // this thread's copies, the same for every item: x rows (tid >> 6) + 4 m
+    // of vector tid & 63, and delta chunks tid + 256 m as (token, offset)
+    int d_tt[kDC], d_q[kDC], d_off[kDC];
+#pragma unroll
+    for (int m = 0; m < kDC; ++m) {
+        const int c = tid + kPipeThreads * m;
+        const int tt = c / per_tok;
+        const int rem = c - tt * per_tok;
+        const int t = rem / dch;
+        d_tt[m] = c < kPipeTokens * per_tok ? tt : kPipeTokens;  // kPipeTokens: no chunk
+        d_q[m] = (rem - t * dch) * EPC;                          // group offset within the item
+        d_off[m] = t * groups + d_q[m];
+    }
+    const int xv = tid & (kPipeVecs - 1);
+    const int xr0 = tid / kPipeVecs;
+
+    auto issue = [&](const PipeItem &it, int stage) {
+        uint8_t *st = pipe_sm + (size_t)stage * stage_bytes;
+        const int64_t i0 = (int64_t)it.tile * kPipeTokens;
+        const int gv = it.strip * kPipeVecs + xv;
+        for (int r = xr0; r < xrows; r += kPipeThreads / kPipeVecs) {
+            const int64_t gi = i0 - halo + r;
+            const bool ok = gi >= 0 && gi < n && gv < nvec;
+            cp_async16(st + ((size_t)r * kPipeVecs + xv) * 16,
+                       ok ? x + gi * hidden + (int64_t)gv * VN : x, ok);
+        }
+        const int g0 = it.strip * gpv;
+        const T *drow = delta + i0 * dstride + g0;
+#pragma unroll
+        for (int m = 0; m < kDC; ++m) {
+            if (d_tt[m] < kPipeTokens) {
+                const int c = tid + kPipeThreads * m;
+                const int gg = g0 + d_q[m];
+                const bool ok = i0 + d_tt[m] < n && gg < groups;
+                cp_async16(st + xbytes + (size_t)c * 16,
+                           ok ? drow + (int64_t)d_tt[m] * dstride + d_off[m] : delta, ok);
+            }
+        }
+    };
+
+    const int vv = tid % kPipeVecs;
+    const int ty = tid / kPipeVecs;
+    const int tt0 = ty * kPipeTokPerThread;
+    const int gl = (vv * VN) / group_size;  // the vector's group within an item
+    const int grid = (int)gridDim.x;
+    const int dq = grid / n_ttiles, dr = grid - dq * n_ttiles;
+    PipeItem fetch{(int)blockIdx.x % n_ttiles, (int)blockIdx.x / n_ttiles};
+#pragma unroll
+    for (int st = 0; st < kPipeStages - 1; ++st) {
+        if (fetch.strip < n_strips) issue(fetch, st);
+        cp_async_commit();
+        fetch.advance(dq, dr, n_ttiles);
+    }
+    PipeItem cur{(int)blockIdx.x % n_ttiles, (int)blockIdx.x / n_ttiles};
+    for (int k = 0; cur.strip < n_strips; ++k, cur.advance(dq, dr, n_ttiles)) {
+        cp_async_wait<kPipeStages - 2>();
+        __syncthreads();  // item k is staged; every thread is done with item k - 1
+        if (fetch.strip < n_strips) issue(fetch, (k + kPipeStages - 1) % kPipeStages);
+        cp_async_commit();
+        fetch.advance(dq, dr, n_ttiles);
+
+        const int v = cur.strip * kPipeVecs + vv;
+        if (v >= nvec) continue;
+        const uint8_t *st = pipe_sm + (size_t)(k % kPipeStages) * stage_bytes;
+        const uint4 *xs = reinterpret_cast<const uint4 *>(st) + vv;
+        const T *ds = reinterpret_cast<const T *>(st + xbytes) + gl;
+        const int64_t i0 = (int64_t)cur.tile * kPipeTokens;
+        // block position of the thread's first token
+        int pos = pow2 ? (int)((i0 + tt0) & (int64_t)(bs - 1)) : (int)((i0 + tt0) % bs);
+        // the taps' base coefficients and a window of the last KT x rows of
+        // this vector: xw[t] is row tt - t of the token tt in hand (rows before
+        // the tile's staged range are never used: the block-position mask
+        // excludes them).  Up to four taps both are unpacked once; more taps
+        // keep the base packed and read x from shared memory at each use.
+        constexpr bool kFlat = KT <= 4;
+        constexpr int KF = kFlat ? KT : 1;
+        uint4 bq[KT];
+        float2 bf[KF][VP], xw[KF][VP];
+#pragma unroll
+        for (int t = 0; t < KT; ++t) {
+            bq[t] = t < taps ? __ldg(reinterpret_cast<const uint4 *>(base + (int64_t)t * hidden) + v)
+                             : make_uint4(0, 0, 0, 0);
+            if constexpr (kFlat) {
+                const int r = tt0 - t + halo;
+                V::unpack2(bq[t], bf[t]);
+                V::unpack2((t > 0 && t < taps && r >= 0) ? xs[r * kPipeVecs] : make_uint4(0, 0, 0, 0),
+                           xw[t]);
+            }
+        }
+        T *orow = out + (i0 + tt0) * hidden + (int64_t)v * VN;
+#pragma unroll
+        for (int j = 0; j < kPipeTokPerThread; ++j) {
+            const int tt = tt0 + j;
+            if (i0 + tt >= n) break;
+            if (j > 0) {
+                if (++pos == bs) pos = 0;
+                if constexpr (kFlat) {
+#pragma unroll
+                    for (int t = KT - 1; t > 0; --t)
+#pragma unroll
+                        for (int e = 0; e < VP; ++e) xw[t][e] = xw[t - 1][e];
+                }
+            }
+            if constexpr (kFlat) V::unpack2(xs[(tt + halo) * kPipeVecs], xw[0]);
+            float2 acc[VP];
+#pragma unroll
+            for (int e = 0; e < VP; ++e) acc[e] = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int t = 0; t < KT; ++t) {
+                if (t < taps && t <= pos) {
+                    const float dt = V::scalar(ds[(tt * taps + t) * gpv]);
+                    const float2 d2 = make_float2(dt, dt);
+                    float2 bt[VP], xt[VP];
+                    if constexpr (kFlat) {
+#pragma unroll
+                        for (int e = 0; e < VP; ++e) {
+                            bt[e] = bf[t][e];
+                            xt[e] = xw[t][e];
+                        }
+                    } else {
+                        V::unpack2(bq[t], bt);
+                        V::unpack2(xs[(tt + halo - t) * kPipeVecs], xt);
+                    }
+                    // acc = (base + delta) * x + acc, each lane rounded as fmaf(bf + dt, x, acc)
+#pragma unroll
+                    for (int e = 0; e < VP; ++e) acc[e] = __ffma2_rn(__fadd2_rn(bt[e], d2), xt[e], acc[e]);
+                }
+            }
+            *reinterpret_cast<uint4 *>(orow) = V::pack2(acc);
+            orow += hidden;
+        }
+    }
+    cp_async_wait<0>();
+}
+
 // General layout: one thread per output element.
 template <typename T>
 __global__ void conv_scalar_kernel(const T *__restrict__ x, const T *__restrict__ base,
@@ -196,6 +429,25 @@ __global__ void conv_scalar_kernel(const T *__restrict__ x, const T *__restrict_
     }
 }
 
+std::atomic<bool> g_pipe_attr[2][64];  // per element type and device; idempotent calls
+
+// Opt the pipelined kernels into more than 48 KB of dynamic shared memory.
+template <typename T> dflash2_status set_pipe_attrs(const DeviceInfo &di) {
+    const int ti = sizeof(T) == 2 ? 0 : 1;
+    if (di.device < 0 || di.device >= 64) return DFLASH2_ERR_CUDA;
+    if (g_pipe_attr[ti][di.device]) return DFLASH2_OK;
+    const int bytes = 227 * 1024;
+    if (cudaFuncSetAttribute(conv_pipe_kernel<T, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(conv_pipe_kernel<T, kPipeMaxTaps>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return DFLASH2_ERR_CUDA;
+    }
+    g_pipe_attr[ti][di.device] = true;
+    return DFLASH2_OK;
+}
+
 template <typename T>
 dflash2_status run_conv(const DeviceInfo &di, const void *x, const void *base, const void *delta,
                         int64_t dstride, void *out, int64_t n, int hidden, int gs, int taps, int bs,
@@ -205,6 +457,42 @@ dflash2_status run_conv(const DeviceInfo &di, const void *x, const void *base, c
     const bool pow2 = (bs & (bs - 1)) == 0;
     const bool vec_ok = (gs % VN) == 0 && aligned16(x) && aligned16(base) && aligned16(out) &&
                         taps_eff <= kMaxVecTaps;
+    // the pipelined path: whole 16-byte chunks of delta per (token, tap) and
+    // item, 16-byte aligned rows, and at most kPipeMaxTaps live taps
+    const int groups = hidden / gs;
+    const int gpv_num = kPipeVecs * VN;
+    const int esz = (int)sizeof(T);
+    const bool pipe_ok = vec_ok && taps_eff <= kPipeMaxTaps && gpv_num % gs == 0 &&
+                         ((gpv_num / gs) * esz) % 16 == 0 && (groups * esz) % 16 == 0 &&
+                         (dstride * esz) % 16 == 0 && aligned16(delta);
+    if (pipe_ok) {
+        const int gpv = gpv_num / gs;
+        const int halo = (kPipeTokens % bs == 0) ? 0 : taps_eff - 1;
+        const int nvec = hidden / VN;
+        const int64_t n_ttiles = (n + kPipeTokens - 1) / kPipeTokens;
+        const int n_strips = (nvec + kPipeVecs - 1) / kPipeVecs;
+        const int64_t n_items = n_ttiles * n_strips;
+        if (n_items > INT32_MAX / 2) return DFLASH2_ERR_INVALID_ARG;
+        const size_t smem = (size_t)kPipeStages * pipe_stage_bytes(halo, taps_eff, gpv, esz);
+        if (smem > 227 * 1024) return DFLASH2_ERR_INVALID_ARG;  // taps <= 8 keeps it below 160 KB
+        int per_sm = (int)((227 * 1024) / (smem + 1024));
+        if (per_sm > 2) per_sm = 2;
+        int64_t grid = (int64_t)di.sm_count * per_sm;
+        if (grid > n_items) grid = n_items;
+        const T *xp = static_cast<const T *>(x), *bp = static_cast<const T *>(base),
+                *dp = static_cast<const T *>(delta);
+        T *op = static_cast<T *>(out);
+        dflash2_status s = set_pipe_attrs<T>(di);
+        if (s != DFLASH2_OK) return s;
+        if (taps_eff <= 4)
+            launch_k(conv_pipe_kernel<T, 4>, (unsigned)grid, kPipeThreads, smem, st, xp, bp, dp,
+                     dstride, op, n, hidden, gs, taps_eff, bs, pow2, halo, (int)n_ttiles, n_strips);
+        else
+            launch_k(conv_pipe_kernel<T, kPipeMaxTaps>, (unsigned)grid, kPipeThreads, smem, st, xp,
+                     bp, dp, dstride, op, n, hidden, gs, taps_eff, bs, pow2, halo, (int)n_ttiles,
+                     n_strips);
+        return launch_status();
+    }
     if (vec_ok) {
         const int nvec = hidden / VN;
         const int64_t ctas = (int64_t)((nvec + kTileVecs - 1) / kTileVecs) *

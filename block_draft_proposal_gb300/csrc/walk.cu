@@ -186,6 +186,71 @@ __device__ __forceinline__ void issue_group(const WalkParams &p, const WalkLayou
     }
 }
 
+// The draw from one row of K edges held by one warp (lane owns candidates
+// k = lane + 32 i; invalid entries are k >= K), with warp shuffles only.
+// Greedy: the smallest index of the maximum, q one-hot.  Sampled: q =
+// softmax(e / T) (T already clamped to >= 1e-5; divide, do not multiply by
+// 1 / T), cdf = the inclusive prefix of q in candidate order (a blockwise
+// warp scan), index = min(#{k : u >= cdf_k}, K - 1).  Returns the index (the
+// same in every lane) and the lane's q values.
+template <int E>
+__device__ __forceinline__ int select_row(const float (&ev)[E], const bool (&valid)[E], bool greedy,
+                                          float temp, float u, int K, int lane, float (&qv)[E]) {
+    if (greedy) {
+        float best = -INFINITY;
+        int bi = INT32_MAX;
+#pragma unroll
+        for (int i = 0; i < E; ++i)
+            if (valid[i] && (bi == INT32_MAX || ev[i] > best)) {
+                best = ev[i];
+                bi = lane + 32 * i;
+            }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+            if (oi != INT32_MAX && (bi == INT32_MAX || ob > best || (ob == best && oi < bi))) {
+                best = ob;
+                bi = oi;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < E; ++i) qv[i] = (lane + 32 * i) == bi ? 1.0f : 0.0f;
+        return bi;
+    }
+    float sc[E];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+        sc[i] = valid[i] ? ev[i] / temp : -INFINITY;
+        mx = fmaxf(mx, sc[i]);
+    }
+    mx = warp_max(mx);
+    float local = 0.0f;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+        qv[i] = valid[i] ? expf(sc[i] - mx) : 0.0f;
+        local += qv[i];
+    }
+    const float total = warp_sum(local);
+    float offset = 0.0f;  // mass of the previous 32-candidate blocks
+    int count = 0;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+        qv[i] = qv[i] / total;
+        float incl = qv[i];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const float cdf = offset + incl;
+        count += __popc(__ballot_sync(0xFFFFFFFFu, valid[i] && u >= cdf));
+        if (i + 1 < E) offset = offset + __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    return count < K - 1 ? count : K - 1;
+}
+
 template <typename T, bool PA, int E>
 __global__ void __launch_bounds__(kMaxWarpsPerCta * 32)
     walk_kernel(const WalkParams p, int warps_per_cta, WalkLayout L) {
@@ -314,62 +379,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32)
         }
         // selection (warp shuffles only)
         float qv[E];
-        int index;
-        if (greedy) {
-            float best = -INFINITY;
-            int bi = INT32_MAX;
-#pragma unroll
-            for (int i = 0; i < E; ++i)
-                if (valid[i] && (bi == INT32_MAX || ev[i] > best)) {
-                    best = ev[i];
-                    bi = lane + 32 * i;
-                }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-                const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-                if (oi != INT32_MAX && (bi == INT32_MAX || ob > best || (ob == best && oi < bi))) {
-                    best = ob;
-                    bi = oi;
-                }
-            }
-            index = bi;
-#pragma unroll
-            for (int i = 0; i < E; ++i) qv[i] = (lane + 32 * i) == index ? 1.0f : 0.0f;
-        } else {
-            float sc[E];
-            float mx = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < E; ++i) {
-                sc[i] = valid[i] ? ev[i] / temp : -INFINITY;
-                mx = fmaxf(mx, sc[i]);
-            }
-            mx = warp_max(mx);
-            float local = 0.0f;
-#pragma unroll
-            for (int i = 0; i < E; ++i) {
-                qv[i] = valid[i] ? expf(sc[i] - mx) : 0.0f;
-                local += qv[i];
-            }
-            const float total = warp_sum(local);
-            const float u = uni[s];
-            float offset = 0.0f;  // mass of the previous 32-candidate blocks
-            int count = 0;
-#pragma unroll
-            for (int i = 0; i < E; ++i) {
-                qv[i] = qv[i] / total;
-                float incl = qv[i];
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                const float cdf = offset + incl;
-                count += __popc(__ballot_sync(0xFFFFFFFFu, valid[i] && u >= cdf));
-                if (i + 1 < E) offset = offset + __shfl_sync(0xFFFFFFFFu, incl, 31);
-            }
-            index = count < K - 1 ? count : K - 1;
-        }
+        const int index = select_row<E>(ev, valid, greedy, temp, uni[s], K, lane, qv);
 #pragma unroll
         for (int i = 0; i < E; ++i) {
             const int kk = lane + 32 * i;
@@ -381,6 +391,447 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32)
         if (lane == 0) p.tokens[row] = ids[(int64_t)s * K + index];
         prev = index;
         __syncwarp();  // w and this slot's buffer are rewritten next
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Chain mode (bf16, top_k in (32, 128], rank a multiple of 8 up to 256): one
+// CTA of four warps walks one request, so that every request of a large batch
+// is resident at once (one CTA per request, a few per SM) and the serial chain
+// of a slot is spread over 128 threads and touches shared memory only.
+//   - Every candidate id of the request is staged once (int32; -1 marks an id
+//     outside the table, whose rows are zero).
+//   - The A rows of slot s's candidates (the possible predecessors of slot
+//     s + 1) are copied into one of two A buffers about a slot and a half
+//     before slot s + 1 needs them, by warps 1-3 with 16-byte cp.async whose
+//     arrivals complete the buffer's mbarrier; so each slot reads its
+//     predecessor's row from shared memory.
+//   - The B rows of slot s (its candidates) are in a shared B buffer when its
+//     edges are formed.  With at most 8 16-byte chunks per thread (top_k <= 64,
+//     rank <= 128) each thread loads its own chunks of slot s + 2 into
+//     registers while slot s is drawn and stores them into the single B buffer
+//     after slot s + 1's edges; otherwise two B buffers are filled like the A
+//     buffers.
+//   - Edges: half-warp h owns candidates [h * CPH, (h + 1) * CPH); its lane
+//     l16 owns the rank chunks l16 + 16 i of 8 elements, so the 16 lanes read
+//     a B row's 256 contiguous bytes per chunk step (no bank conflicts).  Each
+//     lane multiplies its chunk of w = A[predecessor] * g (fp32) into the
+//     CPH rows, and a reduce-scatter over the 16 lanes leaves each candidate's
+//     sum on one lane (two when CPH = 8), which adds the unary value.
+//   - Warp 0 takes the slot's draw from the K edges (select_consecutive) and
+//     writes q and the path's edges while warps 1-3 issue the copies.
+// Measured on GB300 and not kept: one bulk (copy-engine) copy per row (64
+// engine operations per group slowed the shuffles and shared-memory loads of
+// every warp on the SM), and L2 prefetches of the rows ahead (slower, line
+// and bulk alike).
+// ---------------------------------------------------------------------------
+constexpr int kChainThreads = 128;
+constexpr int kChainCopyThreads = 96;  // warps 1-3 issue the cp.async copies
+
+struct ChainLayout {
+    int row_bytes;   // rank * 2
+    int regb;        // B rows staged through registers into one shared buffer
+    int slot_floats; // one entry of the slot-data ring: k_splits * rank partials, k unary values, the uniform
+    size_t bars, sdat, ids, chosen, esm, ctl, abuf, bbuf, total;
+};
+
+__host__ __device__ inline ChainLayout chain_layout(int slots, int k, int rank, int k_splits, bool regb) {
+    ChainLayout L;
+    L.row_bytes = rank * 2;
+    L.regb = regb ? 1 : 0;
+    L.slot_floats = (int)((k_splits * rank + k + 1 + 3) / 4 * 4);
+    L.bars = 0;                                              // A, B and slot-data mbarriers (2 each)
+    L.sdat = 64;                                             // [2][slot_floats] slot-data ring
+    L.ids = L.sdat + (size_t)2 * L.slot_floats * 4;          // [slots][k] ids (-1: outside the table)
+    L.chosen = L.ids + pad16((size_t)slots * k * 4);         // [slots] drawn index
+    L.esm = L.chosen + pad16((size_t)slots * 4);             // [k] the slot's edges
+    L.ctl = L.esm + pad16((size_t)k * 4);                    // abort flag
+    L.abuf = L.ctl + 16;                                     // [2][k] A rows of a slot's candidates
+    L.bbuf = L.abuf + (size_t)2 * k * L.row_bytes;           // [1 or 2][k] B rows
+    L.total = L.bbuf + (size_t)(regb ? 1 : 2) * k * L.row_bytes;
+    return L;
+}
+
+// The table rows tab[ids[c]] (c < K) into dst (row c at c * row_bytes) with
+// 16-byte cp.async by the copy threads (t in [0, kChainCopyThreads)); rows
+// whose id is -1 are zero-filled by the copies themselves.  Each copy thread
+// then arrives on `bar`, whose phase completes once every copy thread's
+// copies have landed.  nch = row_bytes / 16 chunks per row; lg = log2(nch)
+// when it is a power of two, else -1.
+__device__ __forceinline__ void chain_copy_rows(const int32_t *ids, int K, const __nv_bfloat16 *tab,
+                                                int R, int nch, int lg, uint8_t *dst, uint64_t *bar,
+                                                int t) {
+    for (int c = t; c < K * nch; c += kChainCopyThreads) {
+        const int row = lg >= 0 ? c >> lg : c / nch;
+        const int j = c - row * nch;
+        const int64_t id = ids[row];
+        cp_async16(dst + (size_t)c * 16,
+                   reinterpret_cast<const uint8_t *>(tab + (id >= 0 ? id : 0) * R) + 16 * j, id >= 0);
+    }
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ float redux_max(float v) {
+    float m;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(v));
+    return m;
+}
+
+// The draw from one row of K edges held by one warp, lane owning the E
+// consecutive candidates k = lane * E + i (invalid: k >= K).  Greedy: the
+// smallest index of the maximum, q one-hot.  Sampled: q = softmax(e / T) (T
+// already clamped to >= 1e-5; divide, do not multiply by 1 / T), cdf_k = the
+// prefix of exp(e / T - max) in candidate order over their total (one warp
+// scan of the lanes' sums), index = min(#{k : u >= cdf_k}, K - 1).  Returns
+// the index (the same in every lane) and the lane's q values.
+template <int E>
+__device__ __forceinline__ int select_consecutive(const float (&ev)[E], int K, int lane, bool greedy,
+                                                  float temp, float u, float (&qv)[E]) {
+    if (greedy) {
+        float best = -INFINITY;
+        int bi = -1;
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+            const int k = lane * E + i;
+            if (k < K && (bi < 0 || ev[i] > best)) {
+                best = ev[i];
+                bi = k;
+            }
+        }
+        const float m = redux_max(best);
+        // the lowest lane holding the maximum holds its smallest index
+        const uint32_t has = __ballot_sync(0xFFFFFFFFu, bi >= 0 && best == m);
+        const int index = __shfl_sync(0xFFFFFFFFu, bi, __ffs(has) - 1);
+#pragma unroll
+        for (int i = 0; i < E; ++i) qv[i] = (lane * E + i) == index ? 1.0f : 0.0f;
+        return index;
+    }
+    float sc[E];
+    float lm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+        sc[i] = lane * E + i < K ? ev[i] / temp : -INFINITY;
+        lm = fmaxf(lm, sc[i]);
+    }
+    const float m = redux_max(lm);
+    float ex[E];
+    float local = 0.0f;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+        ex[i] = lane * E + i < K ? expf(sc[i] - m) : 0.0f;
+        local += ex[i];
+    }
+    float incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const float total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    float run = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+    if (lane == 0) run = 0.0f;
+    int count = 0;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+        qv[i] = ex[i] / total;
+        run += ex[i];
+        count += __popc(__ballot_sync(0xFFFFFFFFu, lane * E + i < K && u >= run / total));
+    }
+    return count < K - 1 ? count : K - 1;
+}
+
+// One reduce-scatter step over a half-warp: of N partial sums, a lane keeps
+// the lower half (its bit o clear) or the upper half (set), adds the
+// partner's copy of the kept half, and moves it to positions [0, N / 2).
+template <int N, int CPH>
+__device__ __forceinline__ void rs_halve(float (&v)[CPH], int l16, int o) {
+    const bool upper = (l16 & o) != 0;
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+        const float send = upper ? v[i] : v[i + N / 2];
+        const float keep = upper ? v[i + N / 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+    }
+}
+
+// Sum of each of CPH partials over the 16 lanes of a half-warp.  Afterwards
+// lane l16 holds the total of candidate l16 (CPH = 16) or l16 >> 1 (CPH = 8;
+// lanes l16 and l16 ^ 1 hold the same value).
+template <int CPH>
+__device__ __forceinline__ float reduce_scatter16(float (&v)[CPH], int l16) {
+    static_assert(CPH == 8 || CPH == 16, "eight or sixteen candidates per half-warp");
+    if constexpr (CPH == 16) {
+        rs_halve<16>(v, l16, 8);
+        rs_halve<8>(v, l16, 4);
+        rs_halve<4>(v, l16, 2);
+        rs_halve<2>(v, l16, 1);
+    } else {
+        rs_halve<8>(v, l16, 8);
+        rs_halve<4>(v, l16, 4);
+        rs_halve<2>(v, l16, 2);
+        v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], 1);
+    }
+    return v[0];
+}
+
+// Bounded wait of the drain at the end of an aborted chain: the copies still
+// in flight into this CTA's shared memory land (or the limit passes) before
+// the CTA exits.
+__device__ __forceinline__ void chain_drain_wait(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > kWaitLimitNs) return;
+}
+
+// This thread's 16-byte B chunks of one slot (rows hw * CPH + i, chunk
+// l16 + 16 ch), from global memory into registers (zero past K, past the
+// rank, or for an id outside the table).
+// Slot-data entry of proposal row `row` into dst by the copy threads with
+// cp.async: the projection partials (16-byte copies), the unary values and
+// the uniform (4-byte copies); each copy thread then arrives on `bar`.
+__device__ __forceinline__ void chain_copy_slot(const WalkParams &p, int64_t row, float *dst, uint64_t *bar,
+                                                int t) {
+    const int pr4 = p.rank / 4;  // 16-byte chunks of one partial row
+    for (int c = t; c < p.k_splits * pr4; c += kChainCopyThreads) {
+        const int ks = c / pr4;
+        cp_async16(dst + 4 * c, p.g + ks * p.split_stride + row * p.rank + 4 * (c - ks * pr4), true);
+    }
+    float *du = dst + p.k_splits * p.rank;
+    for (int c = t; c <= p.k; c += kChainCopyThreads) {
+        const float *src = c < p.k ? p.cand_u + row * p.k + c : p.uniforms + row;
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(du + c)), "l"(src) : "memory");
+    }
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+template <int CPH, int CH>
+__device__ __forceinline__ void chain_load_b(const __nv_bfloat16 *B, const int32_t *ids, int K, int R,
+                                             int nch, int hw, int l16, uint4 (&bq)[CPH * CH]) {
+#pragma unroll
+    for (int i = 0; i < CPH; ++i) {
+        const int c = hw * CPH + i;
+        const int64_t id = c < K ? ids[c] : -1;
+#pragma unroll
+        for (int ch = 0; ch < CH; ++ch) {
+            const int j = l16 + 16 * ch;
+            bq[i * CH + ch] = (id >= 0 && j < nch) ? __ldg(reinterpret_cast<const uint4 *>(B + id * R) + j)
+                                                   : make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+template <int CPH, int CH>
+__device__ __forceinline__ void chain_store_b(uint8_t *bbuf, int row_bytes, int K, int nch, int hw, int l16,
+                                              const uint4 (&bq)[CPH * CH]) {
+#pragma unroll
+    for (int i = 0; i < CPH; ++i) {
+        const int c = hw * CPH + i;
+#pragma unroll
+        for (int ch = 0; ch < CH; ++ch) {
+            const int j = l16 + 16 * ch;
+            if (c < K && j < nch) *reinterpret_cast<uint4 *>(bbuf + (size_t)c * row_bytes + 16 * j) = bq[i * CH + ch];
+        }
+    }
+}
+
+template <int KM, int CH, bool REGB>
+__global__ void __launch_bounds__(kChainThreads, 4)
+    walk_chain_kernel(const WalkParams p, ChainLayout L) {
+    grid_dep_wait();
+    extern __shared__ __align__(128) uint8_t dyn[];
+    constexpr int CPH = KM / 8;  // candidates per half-warp
+    constexpr int E = KM / 32;   // candidates per lane of the selecting warp
+    constexpr int NBQ = REGB ? CPH * CH : 1;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int hw = tid >> 4, l16 = tid & 15;
+    const int ct = tid - 32;  // copy thread index (warps 1-3)
+    const int b = blockIdx.x;
+    const int S = p.slots, K = p.k, R = p.rank;
+    const int nch = R / 8;
+    const size_t gbytes = (size_t)K * L.row_bytes;  // one buffer of K rows
+    uint64_t *abar = reinterpret_cast<uint64_t *>(dyn + L.bars);  // [2]
+    uint64_t *bbar = abar + 2;                                     // [2], two-buffer B only
+    uint64_t *sbar = abar + 4;                                     // [2] slot-data ring
+    float *sdat = reinterpret_cast<float *>(dyn + L.sdat);
+    int32_t *ids = reinterpret_cast<int32_t *>(dyn + L.ids);
+    int32_t *chosen = reinterpret_cast<int32_t *>(dyn + L.chosen);
+    float *esm = reinterpret_cast<float *>(dyn + L.esm);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(dyn + L.ctl);
+    uint8_t *abuf = dyn + L.abuf;
+    uint8_t *bbuf = dyn + L.bbuf;
+    const int64_t row0 = (int64_t)b * S;
+    const __nv_bfloat16 *A = static_cast<const __nv_bfloat16 *>(p.A);
+    const __nv_bfloat16 *B = static_cast<const __nv_bfloat16 *>(p.B);
+
+    if (tid == 0) {
+        for (int i = 0; i < 6; ++i) mbar_init(&abar[i], kChainCopyThreads);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    const int lg = (nch & (nch - 1)) == 0 ? __ffs(nch) - 1 : -1;
+    // every candidate id of the request, once
+    bool bad = false;
+    for (int t = tid; t < S * K; t += kChainThreads) {
+        const int64_t id = p.cand[row0 * K + t];
+        const bool ok = id_ok(id, p.table_rows);
+        bad |= !ok;
+        ids[t] = ok ? (int32_t)id : -1;
+    }
+    const int64_t anchor = p.anchors[b];
+    const bool anchor_ok = id_ok(anchor, p.table_rows);
+    bad |= tid == 0 && !anchor_ok;
+    if (__syncthreads_or(bad) && tid == 0 && p.err) atomicOr(p.err, DFLASH2_DEVERR_ID_RANGE);
+    // slot 0's predecessor: the anchor's A row, as row 0 of A buffer 1
+    for (int j = tid; j < nch; j += kChainThreads)
+        reinterpret_cast<uint4 *>(abuf + gbytes)[j] =
+            anchor_ok ? __ldg(reinterpret_cast<const uint4 *>(A + anchor * R) + j) : make_uint4(0, 0, 0, 0);
+    // A rows of slot 0's candidates; B rows of slots 0 and 1
+    uint4 bq[NBQ];
+    if (warp > 0) {
+        chain_copy_slot(p, row0, sdat, &sbar[0], ct);
+        if (S > 1) chain_copy_slot(p, row0 + 1, sdat + L.slot_floats, &sbar[1], ct);
+        if (S > 1) chain_copy_rows(ids, K, A, R, nch, lg, abuf, &abar[0], ct);
+        if constexpr (!REGB) {
+            chain_copy_rows(ids, K, B, R, nch, lg, bbuf, &bbar[0], ct);
+            if (S > 1) chain_copy_rows(ids + K, K, B, R, nch, lg, bbuf + gbytes, &bbar[1], ct);
+        }
+    }
+    if constexpr (REGB) {
+        chain_load_b<CPH, CH>(B, ids, K, R, nch, hw, l16, bq);
+        chain_store_b<CPH, CH>(bbuf, L.row_bytes, K, nch, hw, l16, bq);
+        if (S > 1) chain_load_b<CPH, CH>(B, ids + K, K, R, nch, hw, l16, bq);
+    }
+
+    // the lane that adds the unary value and stores candidate cw's edge
+    const int iw = CPH == 16 ? l16 : (l16 >> 1);
+    const int cw = hw * CPH + iw;
+    const bool writer = (CPH == 16 || (l16 & 1) == 0) && cw < K;
+    const bool greedy = p.greedy[b] != 0;
+    float temp = p.temps[b];
+    if (!(temp >= 1e-5f)) temp = 1e-5f;
+    __syncthreads();  // the anchor row and slot 0's B rows (register path) are visible
+
+    int s = 0;
+    for (; s < S; ++s) {
+        const int64_t row = row0 + s;
+        // the slot's projection (its partials summed in split order), unary
+        // value and uniform, copied two slots ahead
+        mbar_wait(&sbar[s & 1], (uint32_t)(s >> 1) & 1u, abort_flag, p.err);
+        const float *sd = sdat + (size_t)(s & 1) * L.slot_floats;
+        float g[8 * CH];
+#pragma unroll
+        for (int ch = 0; ch < CH; ++ch) {
+            const int j = l16 + 16 * ch;
+            float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+            if (j < nch) {
+                lo = *reinterpret_cast<const float4 *>(sd + 8 * j);
+                hi = *reinterpret_cast<const float4 *>(sd + 8 * j + 4);
+                for (int ks = 1; ks < p.k_splits; ++ks) {
+                    const float4 a = *reinterpret_cast<const float4 *>(sd + ks * R + 8 * j);
+                    const float4 c = *reinterpret_cast<const float4 *>(sd + ks * R + 8 * j + 4);
+                    lo.x += a.x; lo.y += a.y; lo.z += a.z; lo.w += a.w;
+                    hi.x += c.x; hi.y += c.y; hi.z += c.z; hi.w += c.w;
+                }
+            }
+            g[8 * ch + 0] = lo.x; g[8 * ch + 1] = lo.y; g[8 * ch + 2] = lo.z; g[8 * ch + 3] = lo.w;
+            g[8 * ch + 4] = hi.x; g[8 * ch + 5] = hi.y; g[8 * ch + 6] = hi.z; g[8 * ch + 7] = hi.w;
+        }
+        const float cu = writer ? sd[p.k_splits * R + cw] : 0.0f;
+        const float uni = sd[p.k_splits * R + K];
+        // w = A[predecessor] * g on this lane's chunks: slot 0 reads the anchor
+        // (row 0 of A buffer 1), slot s the drawn row of A buffer (s - 1) % 2
+        if (s > 0) mbar_wait(&abar[(s - 1) & 1], (uint32_t)((s - 1) >> 1) & 1u, abort_flag, p.err);
+        const uint8_t *arow = abuf + (size_t)((s + 1) & 1) * gbytes +
+                              (size_t)(s > 0 ? chosen[s - 1] : 0) * L.row_bytes;
+        float2 w[4 * CH];
+#pragma unroll
+        for (int ch = 0; ch < CH; ++ch) {
+            const int j = l16 + 16 * ch;
+            const uint4 av = j < nch ? *reinterpret_cast<const uint4 *>(arow + 16 * j) : make_uint4(0, 0, 0, 0);
+            const __nv_bfloat162 *ap = reinterpret_cast<const __nv_bfloat162 *>(&av);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                w[4 * ch + e] = __fmul2_rn(__bfloat1622float2(ap[e]),
+                                           make_float2(g[8 * ch + 2 * e], g[8 * ch + 2 * e + 1]));
+        }
+        // the slot's B rows
+        const uint8_t *brows = bbuf;
+        if constexpr (!REGB) {
+            mbar_wait(&bbar[s & 1], (uint32_t)(s >> 1) & 1u, abort_flag, p.err);
+            brows = bbuf + (size_t)(s & 1) * gbytes;
+        }
+        float part[CPH];
+#pragma unroll
+        for (int i = 0; i < CPH; ++i) {
+            const int c = hw * CPH + i;
+            float2 acc = make_float2(0.0f, 0.0f);
+            if (c < K) {
+#pragma unroll
+                for (int ch = 0; ch < CH; ++ch) {
+                    const int j = l16 + 16 * ch;
+                    if (j < nch) {
+                        const uint4 bv = *reinterpret_cast<const uint4 *>(brows + (size_t)c * L.row_bytes + 16 * j);
+                        const __nv_bfloat162 *bp = reinterpret_cast<const __nv_bfloat162 *>(&bv);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc = __ffma2_rn(w[4 * ch + e], __bfloat1622float2(bp[e]), acc);
+                    }
+                }
+            }
+            part[i] = acc.x + acc.y;
+        }
+        const float total = reduce_scatter16<CPH>(part, l16);
+        if (writer) esm[cw] = total + cu;
+        __syncthreads();
+        if (*abort_flag) break;
+        if (warp == 0) {
+            float ev[E], qv[E];
+#pragma unroll
+            for (int i = 0; i < E; ++i) {
+                const int k = lane * E + i;
+                ev[i] = k < K ? esm[k] : -INFINITY;
+            }
+            const int index = select_consecutive<E>(ev, K, lane, greedy, temp, uni, qv);
+#pragma unroll
+            for (int i = 0; i < E; ++i) {
+                const int k = lane * E + i;
+                if (k < K) {
+                    p.q[row * K + k] = qv[i];
+                    if (p.path_scores) p.path_scores[row * K + k] = ev[i];
+                }
+            }
+            if (lane == 0) chosen[s] = index;
+        } else {
+            // A rows of slot s + 1's candidates into the buffer slot s - 1 used;
+            // slot s + 2's data and B rows into the entries slot s just read
+            if (s + 2 < S) {
+                chain_copy_rows(ids + (size_t)(s + 1) * K, K, A, R, nch, lg, abuf + (size_t)((s + 1) & 1) * gbytes,
+                                &abar[(s + 1) & 1], ct);
+                chain_copy_slot(p, row + 2, sdat + (size_t)(s & 1) * L.slot_floats, &sbar[s & 1], ct);
+            }
+            if constexpr (!REGB) {
+                if (s + 2 < S)
+                    chain_copy_rows(ids + (size_t)(s + 2) * K, K, B, R, nch, lg, bbuf + (size_t)(s & 1) * gbytes,
+                                    &bbar[s & 1], ct);
+            }
+        }
+        if constexpr (REGB) {
+            // slot s + 1's B chunks (loaded a slot ago) into the B buffer, then
+            // slot s + 2's from global memory
+            if (s + 1 < S) chain_store_b<CPH, CH>(bbuf, L.row_bytes, K, nch, hw, l16, bq);
+            if (s + 2 < S) chain_load_b<CPH, CH>(B, ids + (size_t)(s + 2) * K, K, R, nch, hw, l16, bq);
+        }
+        __syncthreads();
+    }
+    // the tokens of the walked slots: the raw candidate ids
+    for (int t = tid; t < s; t += kChainThreads)
+        p.tokens[row0 + t] = p.cand[(row0 + t) * K + chosen[t]];
+    // after an abort: let the copies still in flight land before exiting
+    if (s < S && tid == 32) {
+        for (int t = s - 1; t <= s + 1 && t < S; ++t) {
+            if (t >= 0 && t + 1 < S) chain_drain_wait(&abar[t & 1], (uint32_t)(t >> 1) & 1u);
+            if (!REGB && t >= 0) chain_drain_wait(&bbar[t & 1], (uint32_t)(t >> 1) & 1u);
+            if (t >= 0) chain_drain_wait(&sbar[t & 1], (uint32_t)(t >> 1) & 1u);
+        }
     }
 }
 
@@ -827,6 +1278,13 @@ dflash2_status set_walk_attributes(const DeviceInfo &di) {
     DFLASH2_LAT_ATTR(__nv_bfloat16, 32); DFLASH2_LAT_ATTR(float, 8);
     DFLASH2_LAT_ATTR(float, 16); DFLASH2_LAT_ATTR(float, 32);
 #undef DFLASH2_LAT_ATTR
+#define DFLASH2_CHAIN_ATTR(KM_, CH_, RB_)                                                       \
+    if (e == cudaSuccess)                                                                      \
+        e = cudaFuncSetAttribute(walk_chain_kernel<KM_, CH_, RB_>,                             \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
+    DFLASH2_CHAIN_ATTR(64, 1, true); DFLASH2_CHAIN_ATTR(64, 2, false);
+    DFLASH2_CHAIN_ATTR(128, 1, false); DFLASH2_CHAIN_ATTR(128, 2, false);
+#undef DFLASH2_CHAIN_ATTR
     if (e != cudaSuccess) {
         cudaGetLastError();
         return DFLASH2_ERR_CUDA;
@@ -854,6 +1312,16 @@ dflash2_status run_walk(const DeviceInfo &di, WalkParams wp, int32_t hidden, int
     parts = (slots + spp - 1) / spp;
     const RowsLayout RL = rows_layout(spp, top_k, rank, esz);
     const bool lattice = top_k <= kLatticeMaxK && RL.total <= kWalkSmemBytes;
+    // Chain mode (bf16 beyond the lattice): the deepest ring that still lets
+    // every request's CTA be resident at once, else the shallowest (the most
+    // CTAs per SM).
+    // Chain mode (bf16 beyond the lattice): B rows staged through registers
+    // when a thread's share is at most 8 chunks (top_k <= 64, rank <= 128),
+    // else two shared B buffers.
+    const bool regb = top_k <= 64 && rank <= 128;
+    const ChainLayout CL = chain_layout(slots, top_k, rank, ksplits, regb);
+    const bool chain = !lattice && dtype == DFLASH2_BF16 && rank % 8 == 0 && rank <= kMaxRank &&
+                       wp.table_rows <= INT32_MAX && CL.total <= kWalkSmemBytes;
     // One warp per request.  Among the shared-memory layouts that fit, take
     // the fewest waves of CTAs, then A-row prefetch, then the deepest
     // prefetch ring (every slot in flight at most).
@@ -882,9 +1350,10 @@ dflash2_status run_walk(const DeviceInfo &di, WalkParams wp, int32_t hidden, int
                 }
             }
         }
-        if (best_pa < 0 && !lattice) return DFLASH2_ERR_INVALID_ARG;  // one request's state exceeds shared memory
+        if (best_pa < 0 && !lattice && !chain) return DFLASH2_ERR_INVALID_ARG;  // one request's state exceeds shared memory
         // one mbarrier phase counts fewer than 2^20 transaction bytes
-        if (!lattice && (int64_t)ksplits * slots * rank * 4 + (int64_t)slots * top_k * 12 >= (1 << 20))
+        if (!lattice && !chain &&
+            (int64_t)ksplits * slots * rank * 4 + (int64_t)slots * top_k * 12 >= (1 << 20))
             return DFLASH2_ERR_INVALID_ARG;
         prefetch_a = best_pa != 0;
     }
@@ -920,6 +1389,18 @@ dflash2_status run_walk(const DeviceInfo &di, WalkParams wp, int32_t hidden, int
         if (s != DFLASH2_OK) return s;
         launch_k(walk_chase_kernel, (unsigned)batch, kChaseThreads,
                  (size_t)(slots * top_k + slots) * sizeof(int32_t), st, wp, lw);
+        return launch_status();
+    }
+    if (chain) {
+        const unsigned grid = (unsigned)batch;
+        if (regb)
+            launch_k(walk_chain_kernel<64, 1, true>, grid, kChainThreads, CL.total, st, wp, CL);
+        else if (top_k <= 64)
+            launch_k(walk_chain_kernel<64, 2, false>, grid, kChainThreads, CL.total, st, wp, CL);
+        else if (rank <= 128)
+            launch_k(walk_chain_kernel<128, 1, false>, grid, kChainThreads, CL.total, st, wp, CL);
+        else
+            launch_k(walk_chain_kernel<128, 2, false>, grid, kChainThreads, CL.total, st, wp, CL);
         return launch_status();
     }
     wp.bulk_ids = ((int64_t)slots * top_k) % 4 == 0 && aligned16(wp.cand) && aligned16(wp.cand_u);

@@ -68,6 +68,12 @@ EDGE = [
     dict(batch=3, block_size=16, hidden=60, group_size=6, taps=2, dtype="f32", trim=1),    # scalar path
     dict(batch=40, block_size=16, hidden=1024, group_size=8, taps=70, dtype="bf16", trim=9),  # taps > 64 clipped by block
     dict(batch=2, block_size=100, hidden=64, group_size=8, taps=70, dtype="bf16", trim=13),  # > 64 live taps: scalar path
+    # pipelined path: a block of 40 (halo rows before each 16-token tile) with 8
+    # taps over three 64-vector strips, the last one vector wide; fp32 with five
+    # taps and no halo; group size 16 with blocks of 32 (halo, 32 groups per strip)
+    dict(batch=3, block_size=40, hidden=1032, group_size=8, taps=8, dtype="bf16", trim=11),
+    dict(batch=6, block_size=16, hidden=512, group_size=8, taps=5, dtype="f32", trim=2),
+    dict(batch=7, block_size=32, hidden=2048, group_size=16, taps=4, dtype="bf16", trim=0),
 ]
 
 

@@ -74,6 +74,18 @@ WALK_CASES = [
     dict(batch=5, block_size=17, hidden=128, rank=256, top_k=128, dtype="bf16", sampling="mixed", temperature=0.5),
     dict(batch=3, block_size=2, hidden=64, rank=32, top_k=33, dtype="f32", sampling="sampled", temperature=2.0),
     dict(batch=7, block_size=8, hidden=256, rank=16, top_k=8, dtype="f32", sampling="mixed", temperature=1e-7),
+    # chain mode (bf16, 32 < top_k <= 128): ragged K under 64 with rank 40 (five
+    # rank chunks, most lanes idle); one slot with K = 100 and rank 136 (a lane
+    # with two chunks); 300 requests of K = 128 at rank 256 (whose buffers
+    # exceed shared memory: the one-warp path walk), greedy rows with T below
+    # its clamp
+    dict(batch=9, block_size=6, hidden=160, rank=40, top_k=47, dtype="bf16", sampling="mixed", temperature=0.8),
+    dict(batch=4, block_size=2, hidden=64, rank=136, top_k=100, dtype="bf16", sampling="sampled", temperature=0.3),
+    dict(batch=300, block_size=4, hidden=96, rank=256, top_k=128, dtype="bf16", sampling="mixed", temperature=1e-7),
+    dict(batch=5, block_size=16, hidden=128, rank=128, top_k=64, dtype="bf16", sampling="sampled", temperature=0.6),
+    # chain mode with two shared B buffers: K <= 64 at rank 200, and K = 96 at rank 64
+    dict(batch=7, block_size=7, hidden=96, rank=200, top_k=40, dtype="bf16", sampling="mixed", temperature=0.9),
+    dict(batch=6, block_size=11, hidden=64, rank=64, top_k=96, dtype="bf16", sampling="sampled", temperature=0.4),
 ]
 
 
@@ -103,10 +115,25 @@ def test_out_of_range_ids_set_the_error_bit_and_use_zero_rows(cuda):
     _compare(inp, cand, cand_u, tokens, q, ps, w.dtype, w.hidden)
 
 
-def test_greedy_rows_do_not_depend_on_other_rows(cuda):
-    w = synth.BY_NAME["tiny-fp32"].scaled(batch=8, block_size=10, hidden=128, rank=32, top_k=16, dtype="bf16",
-                                draft_vocab=2000, target_vocab=2000, sampling="mixed",
-                                temperature=0.7, seed=101)
+def test_chain_mode_out_of_range_ids_set_the_error_bit_and_use_zero_rows(cuda):
+    w = synth.BY_NAME["tiny-fp32"].scaled(batch=3, block_size=4, hidden=64, rank=16, top_k=40, dtype="bf16",
+                                draft_vocab=500, target_vocab=500, sampling="mixed", seed=104)
+    inp, cand, cand_u = _random_candidates(w, 105, scale_ab=30.0)
+    inp["anchors"] = inp["anchors"].copy()
+    inp["anchors"][1] = 10_000
+    cand[2, 1, 3] = -5
+    cand[0, 2, 39] = 500
+    tokens, q, ps, err = _run_walk(cuda, inp, cand, cand_u)
+    assert err & dflash2.DEVERR_ID_RANGE
+    np.testing.assert_allclose(ps[1, 0], cand_u[1, 0], rtol=0, atol=0)
+    _compare(inp, cand, cand_u, tokens, q, ps, w.dtype, w.hidden)
+
+
+@pytest.mark.parametrize("top_k", [16, 48])
+def test_greedy_rows_do_not_depend_on_other_rows(cuda, top_k):
+    w = synth.BY_NAME["tiny-fp32"].scaled(batch=8, block_size=10, hidden=128, rank=32, top_k=top_k,
+                                dtype="bf16", draft_vocab=2000, target_vocab=2000,
+                                sampling="mixed", temperature=0.7, seed=101)
     inp, cand, cand_u = _random_candidates(w, 102, scale_ab=10.0)
     t1, q1, _, _ = _run_walk(cuda, inp, cand, cand_u)
     rng = np.random.default_rng(103)
