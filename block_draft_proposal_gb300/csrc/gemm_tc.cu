@@ -149,6 +149,19 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams &p, const float 
                 if (i < ncols && m < p.rows_h) o[(int64_t)m * p.ldo] = z[i];
             }
         }
+    } else if (p.mode == kGemmStoreRows) {
+        if (v < p.rows_w) {
+            float *o = p.out + (int64_t)it.ks * p.split_stride + v * p.ldo + m0;
+            if (ncols == 32 && m0 + 32 <= p.rows_h) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 4)
+                    *reinterpret_cast<float4 *>(o + i) = make_float4(z[i], z[i + 1], z[i + 2], z[i + 3]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (i < ncols && m0 + i < p.rows_h) o[i] = z[i];
+            }
+        }
     } else if (p.mode == kGemmStoreBf16) {
         if (v < p.rows_w) {
             __nv_bfloat16 *o = p.out_bf16 + v;
@@ -606,7 +619,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kPairEpiWa
     // took bandwidth from the pilot.)
     if (p.mode != kGemmFilter || warp >= 2) grid_dep_wait();
     const uint32_t tmem = tmem_slot;
-    const int total = p.pass_tiles * p.n_tok_tiles;
+    const int total = p.pass_tiles * p.n_tok_tiles * p.k_splits;
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
     if (warp == 0) {
@@ -617,7 +630,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kPairEpiWa
                 const Item item = decode(p, w);
                 const int wrow = item.wt * p.unit + (int)rank * kGemmTileW;
                 const int hrow = item.nt * p.bn + (int)rank * half_bn;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                const int kb0 = item.ks * p.kb_per_split;
+                const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&empty_bar[s], ph, &abort_flag, p.err)) {
                         ok = false;
                         break;
@@ -659,7 +674,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kPairEpiWa
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)a * p.acc_cols;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                const Item item = decode(p, w);
+                const int kb0 = item.ks * p.kb_per_split;
+                const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&full_bar[s], ph, &abort_flag, p.err)) {
                         ok = false;
                         break;
@@ -667,10 +685,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kPairEpiWa
                     tc_fence_after();
                     if (p.fp8)
                         mma_stage_f8_pair(d_tmem, wd0 + s * w_st, hd0 + s * h_st, w_sub, h_sb,
-                                          idesc, kb > 0 ? 1u : 0u);
+                                          idesc, kb > kb0 ? 1u : 0u);
                     else
                         mma_stage<true>(d_tmem, wd0 + s * w_st, hd0 + s * h_st, w_sub, h_sb,
-                                        idesc, kb > 0 ? 1u : 0u);
+                                        idesc, kb > kb0 ? 1u : 0u);
                     tc_commit_pair_mc(&empty_bar[s], 0x3);
                     if (++s == (uint32_t)p.stages) {
                         s = 0;
@@ -873,7 +891,11 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     else
         p.pass_tiles = p.n_wtiles;
     if (p.pass_tiles <= 0) return DFLASH2_OK;
-    if (p.mode != kGemmStore) p.k_splits = 1;
+    if (p.mode != kGemmStore && p.mode != kGemmStoreRows) {
+        p.k_splits = 1;
+        p.kb_per_split = p.num_kb;
+    }
+    if (p.mode == kGemmStoreRows && (!pair || p.fp8 || p.ldo % 4 != 0)) return DFLASH2_ERR_INVALID_ARG;
     uint32_t acc = 32;
     while (acc < (uint32_t)p.bn) acc <<= 1;
     p.acc_cols = acc;

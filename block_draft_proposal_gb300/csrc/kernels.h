@@ -20,6 +20,12 @@ enum GemmMode : int32_t {
     // on, and every tile's candidates (the pilot tiles' from the accumulators
     // they kept) are taken against the thresholds
     kGemmFused = 4,
+    // fp32 C row by row, split over hidden: out[ks * split_stride + v * ldo + m]
+    // for weight row v and token m (CTA pairs).  The selector projection of a
+    // large batch runs with the tokens as the weight side (256 per pair), so
+    // each CTA streams 128 token rows and stages half of the small projection
+    // matrix.
+    kGemmStoreRows = 5,
 };
 
 constexpr int kGemmTileW = 128;  // weight rows per tile (MMA M)
@@ -51,7 +57,7 @@ struct GemmParams {
     int64_t target_vocab;
     float mult;
     float cap;
-    float *out;            // store: [k_splits][rows_h][ldo]; pilot: [rows_h][ldo]
+    float *out;            // store: [k_splits][rows_h][ldo]; store-rows: [k_splits][rows_w][ldo]; pilot: [rows_h][ldo]
     __nv_bfloat16 *out_bf16;  // store-bf16: [rows_h][ldo]
     int64_t ldo;
     int64_t split_stride;

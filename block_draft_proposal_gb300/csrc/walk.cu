@@ -422,8 +422,13 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32)
 //     writes q and the path's edges while warps 1-3 issue the copies.
 // Measured on GB300 and not kept: one bulk (copy-engine) copy per row (64
 // engine operations per group slowed the shuffles and shared-memory loads of
-// every warp on the SM), and L2 prefetches of the rows ahead (slower, line
-// and bulk alike).
+// every warp on the SM); L2 prefetches of the rows ahead (slower, line and
+// bulk alike); four-row copy-engine gathers of the A rows (no change); the
+// edges on one warp with the other three only copying, the warps meeting at
+// full/free mbarrier pairs instead of block barriers, the edges formed on
+// CUDA cores (88 us against 66 at batch 512 x 15 slots, K 64, rank 128) or on
+// the legacy tensor-core path (mma.sync on w split exactly into three bf16
+// parts: 80-90 us).
 // ---------------------------------------------------------------------------
 constexpr int kChainThreads = 128;
 constexpr int kChainCopyThreads = 96;  // warps 1-3 issue the cp.async copies
@@ -1162,27 +1167,48 @@ __global__ void __launch_bounds__(128)
     }
 }
 
-// Split of the hidden dimension for the tensor-core projection, so that
-// small batches still spread over the SMs; the walk sums the partials in a
-// fixed order.  Depends on the shape only, so the workspace size does not
-// depend on the device.
-inline void proj_tiling(int64_t rows, int hidden, int *bn, int *k_splits) {
-    *bn = rows >= 4096 ? 64 : 16;
-    const int64_t tiles = (rows + *bn - 1) / *bn;
+// Tiling of the tensor-core projection (bf16); it depends on the shape only,
+// so the workspace size does not depend on the device.
+//   - Batches of at least 4096 rows run on CTA pairs with the tokens as the
+//     weight side (256 rows a pair, 128 a CTA) and the projection matrix as
+//     one token tile: each CTA stages 128 token rows and half of the matrix
+//     per stage, so four stages keep 128 KB of h in flight per SM.  The
+//     hidden dimension is split so that the pairs cover a 152-SM GB300
+//     (76 pairs) about once.
+//   - Smaller batches run one CTA per tile of 16 tokens, split over hidden
+//     into enough items for the SMs.
+// The walk sums the partials in a fixed order.
+struct ProjTiling {
+    bool pairs;
+    int bn;
+    int k_splits;
+};
+
+inline ProjTiling proj_tiling(int64_t rows, int hidden, int rank) {
+    ProjTiling t{};
     const int num_kb = (hidden + kGemmStageK - 1) / kGemmStageK;
-    int64_t ks = (148 + tiles - 1) / tiles;
+    int64_t ks;
+    if (rows >= 4096) {
+        t.pairs = true;
+        t.bn = (rank + 15) / 16 * 16;
+        ks = 76 / ((rows + 2 * kGemmTileW - 1) / (2 * kGemmTileW));
+    } else {
+        t.pairs = false;
+        t.bn = 16;
+        const int64_t tiles = (rows + t.bn - 1) / t.bn;
+        ks = (148 + tiles - 1) / tiles;
+    }
     if (ks > num_kb) ks = num_kb;
     if (ks > 8) ks = 8;
     if (ks < 1) ks = 1;
-    *k_splits = (int)ks;
+    t.k_splits = (int)ks;
+    return t;
 }
 
 // Projection partials the workspace reserves (the tiling's split count before
 // the GEMM launcher trims it; 1 for fp32).
-inline int ksplits_ws(int64_t rows, int hidden, int32_t dtype) {
-    int bn = 32, ks = 1;
-    if (dtype == DFLASH2_BF16) proj_tiling(rows, hidden, &bn, &ks);
-    return ks;
+inline int ksplits_ws(int64_t rows, int hidden, int rank, int32_t dtype) {
+    return dtype == DFLASH2_BF16 ? proj_tiling(rows, hidden, rank).k_splits : 1;
 }
 
 std::atomic<bool> g_walk_attr[64];  // per device; the attribute calls are idempotent
@@ -1196,7 +1222,7 @@ extern "C" size_t dflash2_selector_walk_workspace_size(int32_t batch, int32_t sl
                                                        int32_t rank, int32_t top_k, int32_t dtype) {
     if (batch <= 0 || slots <= 0 || hidden <= 0 || rank <= 0 || top_k <= 0) return 0;
     const int64_t rows = (int64_t)batch * slots;
-    const size_t partials = (size_t)ksplits_ws(rows, hidden, dtype) * rows * rank * sizeof(float);
+    const size_t partials = (size_t)ksplits_ws(rows, hidden, rank, dtype) * rows * rank * sizeof(float);
     if (top_k > kLatticeMaxK) return partials;
     size_t o_lat, o_stat, o_nxt, o_end;
     lattice_ws_layout(rows, top_k, partials, &o_lat, &o_stat, &o_nxt, &o_end);
@@ -1218,10 +1244,9 @@ dflash2_status check_walk_shape(int32_t batch, int32_t slots, int32_t hidden, in
 
 // Projection partials the walk sums: the tiling's split count as the GEMM
 // launcher trims it (every split gets at least one pipeline stage).
-int kept_ksplits(int64_t rows, int hidden, int32_t dtype) {
+int kept_ksplits(int64_t rows, int hidden, int rank, int32_t dtype) {
     if (dtype != DFLASH2_BF16) return 1;
-    int bn_unused, ks;
-    proj_tiling(rows, hidden, &bn_unused, &ks);
+    const int ks = proj_tiling(rows, hidden, rank).k_splits;
     const int num_kb = (hidden + kGemmStageK - 1) / kGemmStageK;
     const int per = (num_kb + ks - 1) / ks;
     return (num_kb + per - 1) / per;
@@ -1233,19 +1258,24 @@ dflash2_status run_projection(const DeviceInfo &di, const void *h, const void *p
                               int32_t *err_word, cudaStream_t st) {
     if (dtype == DFLASH2_BF16) {
         if (hidden % 8 != 0 || !aligned16(h) || !aligned16(proj)) return DFLASH2_ERR_MISALIGNED;
-        int bn, ks;
-        proj_tiling(rows, hidden, &bn, &ks);
+        const ProjTiling t = proj_tiling(rows, hidden, rank);
         GemmParams p{};
-        p.rows_w = rank;
-        p.rows_h = (int32_t)rows;
         p.hidden = hidden;
-        p.mode = kGemmStore;
-        p.bn = bn;
-        p.k_splits = ks;
+        p.bn = t.bn;
+        p.k_splits = t.k_splits;
         p.out = g;
         p.ldo = rank;
         p.split_stride = rows * rank;
         p.err = err_word;
+        if (t.pairs) {  // g[m, :] row by row: the tokens on the weight side
+            p.rows_w = (int32_t)rows;
+            p.rows_h = rank;
+            p.mode = kGemmStoreRows;
+            return launch_gemm_tc(di, h, proj, p, st, /*pair=*/true);
+        }
+        p.rows_w = rank;
+        p.rows_h = (int32_t)rows;
+        p.mode = kGemmStore;
         return launch_gemm_tc(di, proj, h, p, st);
     }
     if ((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(proj)) % 4 != 0)
@@ -1299,7 +1329,7 @@ dflash2_status run_walk(const DeviceInfo &di, WalkParams wp, int32_t hidden, int
     const int batch = wp.batch, slots = wp.slots, rank = wp.rank, top_k = wp.k;
     const int esz = dtype == DFLASH2_BF16 ? 2 : 4;
     const int64_t rows = (int64_t)batch * slots;
-    const int ksplits = kept_ksplits(rows, hidden, dtype);
+    const int ksplits = kept_ksplits(rows, hidden, rank, dtype);
     // Lattice mode (top_k <= 32): the request's slots in parts of spp slots,
     // enough parts that the batch gives each SM about two CTAs, when a part's
     // rows fit in shared memory; the lattice itself lives in the workspace.
@@ -1365,7 +1395,7 @@ dflash2_status run_walk(const DeviceInfo &di, WalkParams wp, int32_t hidden, int
     if (lattice) {
         LatticeWs lw;
         size_t o_lat, o_stat, o_nxt, o_end;
-        lattice_ws_layout(rows, top_k, (size_t)ksplits_ws(rows, hidden, dtype) * rows * rank * 4,
+        lattice_ws_layout(rows, top_k, (size_t)ksplits_ws(rows, hidden, rank, dtype) * rows * rank * 4,
                           &o_lat, &o_stat, &o_nxt, &o_end);
         uint8_t *wsb = static_cast<uint8_t *>(workspace);
         lw.lat = reinterpret_cast<float *>(wsb + o_lat);

@@ -86,6 +86,11 @@ WALK_CASES = [
     # chain mode with two shared B buffers: K <= 64 at rank 200, and K = 96 at rank 64
     dict(batch=7, block_size=7, hidden=96, rank=200, top_k=40, dtype="bf16", sampling="mixed", temperature=0.9),
     dict(batch=6, block_size=11, hidden=64, rank=64, top_k=96, dtype="bf16", sampling="sampled", temperature=0.4),
+    # at least 4096 rows: the projection runs on CTA pairs with the tokens as the
+    # weight side, split over hidden; hidden off the 128-element stage (1000)
+    # and a rank off the 16-row tile (72), then chain mode at rank 128
+    dict(batch=300, block_size=16, hidden=1000, rank=72, top_k=24, dtype="bf16", sampling="mixed", temperature=0.8),
+    dict(batch=280, block_size=16, hidden=520, rank=128, top_k=48, dtype="bf16", sampling="sampled", temperature=0.7),
 ]
 
 
