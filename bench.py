@@ -7,14 +7,15 @@ C ABI (dflash2.proposal_step, the input-only work on a second stream beside
 the top-K), replayed from one captured CUDA graph.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload NAME]
+                    [--workload NAME] [--stage conv|unary_topk|projection|walk]
 
 The default workload is the largest one-GPU configuration, the large-batch,
 large-K stress draft (batch 512, block 16, hidden 7168 = 896 groups x 8, taps
 4, vocab 163840, rank 128, top-K 64, cap 30, mult 0.5, every row sampled at
 T = 0.6); the other named workloads run with --workload.  The metric is
-proposals per second (batch x slots proposed / step time).  L2 is flushed (a 256 MiB write) before every timed step and the
-flush is outside the timed events.  Prints ONE JSON line (rank 0).
+proposals per second (batch x slots proposed / step time).  L2 is flushed
+before every timed step (a 256 MiB write, then a read of the same buffer, so
+no dirty line is left) and the flush is outside the timed events.  Prints ONE JSON line (rank 0).
 
 `--impl reference` times the CPU oracle (the method restated in plain C,
 double accumulation) on a bounded sample of the same workload on the host
@@ -42,6 +43,16 @@ L2_FLUSH_BYTES = 256 << 20
 # DRAM bytes of the unary top-K stage per workload, from one ncu capture of
 # the stage's launches, keyed by the hash of the sources that make the stage
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def flush_l2(buf):
+    """Evicts the L2 before a timed call: writes `buf` (larger than the L2),
+    then reads it back, so that the L2 holds only clean lines of `buf` when the
+    timer starts (after the write alone the timed kernel would pay for writing
+    the flush's dirty lines back to HBM)."""
+    import torch
+    buf.zero_()
+    buf.view(torch.int64).sum()
 
 
 def _dist():
@@ -240,7 +251,8 @@ def _config(w):
             "draft_vocab": w.draft_vocab, "target_vocab": w.target_vocab, "rank": w.rank,
             "top_k": w.top_k, "mult": w.mult, "cap": w.cap, "sampling": w.sampling,
             "temperature": w.temperature,
-            "l2": "value: flushed before every timed step (256 MiB write, outside the timed events); "
+            "l2": "value: flushed before every timed step (256 MiB write then read back, outside the "
+                  "timed events); "
                   "e2e: a pipelined loop without flush, inputs larger than L2 (the lm_head streams "
                   "from HBM at every step)",
             "e2e": "double-buffered device inputs and outputs: the next step's H2D copy and the "
@@ -322,9 +334,9 @@ def run_gpu(args, w):
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            flush.zero_()
+            flush_l2(flush)
             graph.replay() if use_graph else step(False)
-            flush.zero_()
+            flush_l2(flush)
             step(True)
     stream.synchronize()
 
@@ -340,12 +352,12 @@ def run_gpu(args, w):
     with ClockSampler(local) as clocks:
         with torch.cuda.stream(stream):
             for i in range(args.steps):
-                flush.zero_()
+                flush_l2(flush)
                 gev[i][0].record(stream)
                 graph.replay() if use_graph else step(False)
                 gev[i][1].record(stream)
             for i in range(args.steps):
-                flush.zero_()
+                flush_l2(flush)
                 ev[:] = sev[i]
                 step(True)
         torch.cuda.synchronize()
@@ -456,7 +468,7 @@ def run_gpu(args, w):
             prep()
         with torch.cuda.stream(stream):
             for i in range(args.warmup + reps):
-                flush.zero_()
+                flush_l2(flush)
                 if i >= args.warmup:
                     pev[i - args.warmup][0].record(stream)
                 pgraph.replay()
@@ -501,7 +513,7 @@ def run_gpu(args, w):
                for _ in range(reps)]
         with torch.cuda.stream(stream):
             for i in range(args.warmup + reps):
-                flush.zero_()
+                flush_l2(flush)
                 if i >= args.warmup:
                     vev[i - args.warmup][0].record(stream)
                 vgraph.replay()
@@ -540,7 +552,7 @@ def run_gpu(args, w):
                for _ in range(reps)]
         with torch.cuda.stream(stream):
             for i in range(args.warmup + reps):
-                flush.zero_()
+                flush_l2(flush)
                 if i >= args.warmup:
                     fev[i - args.warmup][0].record(stream)
                 fgraph.replay()
@@ -662,6 +674,91 @@ def run_gpu(args, w):
     return 0
 
 
+def run_stage(args, w):
+    """One stage of the path alone, `--steps` timed calls with L2 flushed
+    before each (outside the events), on one stream; prints one JSON line with
+    the median and minimum call time and the stage's algorithmic rate.  The
+    walk runs on seeded synthetic candidates (distinct ids, descending u), so
+    no lm_head is allocated: the command the committed ncu summaries of the
+    conv, projection and walk kernels name."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__ as g
+    g.build_library()
+    from block_draft_proposal_gb300 import dflash2, synth
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    parts = {"conv": ("x", "base", "delta"),
+             "unary_topk": ("h", "lm_head"),
+             "projection": ("h", "proj"),
+             "walk": ("h", "A", "B", "proj", "uniforms", "anchors")}[args.stage]
+    inp = synth.make(w, parts=parts)
+    t = {k: dflash2.to_device(v, dev) for k, v in inp.items() if v is not None}
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    st = torch.cuda.Stream(device=dev)
+    code = dflash2.BF16 if w.dtype == "bf16" else dflash2.F32
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    work = algorithmic_work(w)
+    if args.stage == "conv":
+        out = torch.empty_like(t["x"])
+        fn = lambda: dflash2.grouped_conv(t["x"], t["base"], t["delta"], w.block_size,
+                                          w.group_size, w.taps, out=out, stream=st)
+        amount, unit = work["conv_bytes"], "GB/s"
+    elif args.stage == "unary_topk":
+        ids = torch.empty((w.rows, w.top_k), dtype=torch.int64, device=dev)
+        u = torch.empty((w.rows, w.top_k), dtype=torch.float32, device=dev)
+        ws = torch.empty(dflash2.unary_topk_workspace_size(w.rows, w.draft_vocab, w.top_k, code),
+                         dtype=torch.uint8, device=dev)
+        fn = lambda: dflash2.unary_topk(t["h"], t["lm_head"], w.target_vocab, w.mult, w.cap,
+                                        w.top_k, cand_ids=ids, cand_u=u, workspace=ws, err=err,
+                                        stream=st)
+        amount, unit = work["gemm_flops"], "TFLOP/s"
+    else:
+        ws = torch.empty(dflash2.selector_walk_workspace_size(w.batch, w.slots, w.hidden, w.rank,
+                                                              w.top_k, code),
+                         dtype=torch.uint8, device=dev)
+        e = 2 if w.dtype == "bf16" else 4
+        if args.stage == "projection":
+            fn = lambda: dflash2.selector_project(t["h"], t["proj"], w.batch, w.slots, w.top_k,
+                                                  ws, err=err, stream=st)
+            amount, unit = w.rows * w.hidden * e + w.rank * w.hidden * e, "GB/s"
+        else:
+            rng = np.random.default_rng(w.seed + 1)
+            cand = np.stack([rng.choice(w.draft_vocab, size=w.top_k, replace=False)
+                             for _ in range(w.rows)]).astype(np.int64)
+            cu = np.sort(rng.standard_normal((w.rows, w.top_k)).astype(np.float32),
+                         axis=1)[:, ::-1].copy()
+            tc = torch.from_numpy(cand).to(dev).view(w.batch, w.slots, w.top_k)
+            tu = torch.from_numpy(cu).to(dev).view(w.batch, w.slots, w.top_k)
+            tok = torch.empty((w.batch, w.slots), dtype=torch.int64, device=dev)
+            q = torch.empty((w.batch, w.slots, w.top_k), dtype=torch.float32, device=dev)
+            fn = lambda: dflash2.selector_walk(t["h"], t["proj"], t["A"], t["B"], t["anchors"], tc,
+                                               tu, t["temperatures"], t["greedy"], t["uniforms"],
+                                               tokens=tok, q=q, workspace=ws, err=err, stream=st)
+            amount, unit = work["walk_bytes"], "GB/s"
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):
+        for i in range(args.warmup + args.steps):
+            flush_l2(flush)
+            if i >= args.warmup:
+                evs[i - args.warmup][0].record(st)
+            fn()
+            if i >= args.warmup:
+                evs[i - args.warmup][1].record(st)
+    torch.cuda.synchronize()
+    us = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+    med = statistics.median(us)
+    scale = 1e3 if unit == "GB/s" else 1e6
+    print(json.dumps({"stage": args.stage, "workload": w.name, "calls": args.steps,
+                      "us_median": med, "us_min": us[0], unit: amount / (med * scale),
+                      "algorithmic": amount, "err": int(err.item())}), flush=True)
+    return 0 if int(err.item()) & ~dflash2.DEVINFO_TOPK_FALLBACK == 0 else 1
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -670,6 +767,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stage", choices=["conv", "unary_topk", "projection", "walk"],
+                    help="time one stage alone (one GPU) instead of the whole step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -677,6 +776,8 @@ def main():
     w = synth.BY_NAME[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.stage:
+        return run_stage(args, w)
     return run_gpu(args, w)
 
 

@@ -358,6 +358,38 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
             }
         }
         T *orow = out + (i0 + tt0) * hidden + (int64_t)v * VN;
+        if (kFlat && taps == KT && pos >= KT - 1 && pos + kPipeTokPerThread <= bs &&
+            i0 + tt0 + kPipeTokPerThread <= n) {
+            // Every tap of every token of this thread lies inside the token's
+            // block (the same for a whole warp: its 32 threads share tt0), so
+            // no tap needs its mask and the tokens' sums interleave freely.
+            // The arithmetic is the general loop's, tap by tap.
+#pragma unroll
+            for (int j = 0; j < kPipeTokPerThread; ++j) {
+                const int tt = tt0 + j;
+                if (j > 0) {
+#pragma unroll
+                    for (int t = KF - 1; t > 0; --t)
+#pragma unroll
+                        for (int e = 0; e < VP; ++e) xw[t][e] = xw[t - 1][e];
+                }
+                V::unpack2(xs[(tt + halo) * kPipeVecs], xw[0]);
+                float2 acc[VP];
+#pragma unroll
+                for (int e = 0; e < VP; ++e) acc[e] = make_float2(0.0f, 0.0f);
+#pragma unroll
+                for (int t = 0; t < KF; ++t) {
+                    const float dt = V::scalar(ds[(tt * KT + t) * gpv]);
+                    const float2 d2 = make_float2(dt, dt);
+#pragma unroll
+                    for (int e = 0; e < VP; ++e)
+                        acc[e] = __ffma2_rn(__fadd2_rn(bf[t][e], d2), xw[t][e], acc[e]);
+                }
+                *reinterpret_cast<uint4 *>(orow) = V::pack2(acc);
+                orow += hidden;
+            }
+            continue;
+        }
 #pragma unroll
         for (int j = 0; j < kPipeTokPerThread; ++j) {
             const int tt = tt0 + j;
