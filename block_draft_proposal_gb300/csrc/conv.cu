@@ -231,20 +231,6 @@ __host__ __device__ inline int pipe_stage_bytes(int halo, int taps, int gpv, int
 // with gs >= 8 for bf16 and >= 4 for fp32.
 template <typename T> __host__ __device__ constexpr int pipe_max_dch() { return sizeof(T) == 2 ? 8 : 16; }
 
-// Item iterator: token tile fastest, then the 64-vector strip; advancing by
-// the grid's size needs no division.
-struct PipeItem {
-    int tile, strip;
-    __device__ __forceinline__ void advance(int dq, int dr, int n_ttiles) {
-        tile += dr;
-        strip += dq;
-        if (tile >= n_ttiles) {
-            tile -= n_ttiles;
-            ++strip;
-        }
-    }
-};
-
 template <typename T, int KT>
 __global__ void __launch_bounds__(kPipeThreads, 2)
     conv_pipe_kernel(const T *__restrict__ x, const T *__restrict__ base,
@@ -284,17 +270,24 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     const int xv = tid & (kPipeVecs - 1);
     const int xr0 = tid / kPipeVecs;
 
-    auto issue = [&](const PipeItem &it, int stage) {
+    // Work split: CTA b keeps the 64-vector strip b % n_strips and takes
+    // its token tiles b / n_strips, + tstep, ... (the grid is a multiple of
+    // n_strips), so the strip's base coefficients are read once per CTA.
+    const int strip = (int)blockIdx.x % n_strips;
+    const int tstep = (int)gridDim.x / n_strips;
+    const int tile0 = (int)blockIdx.x / n_strips;
+    const int g0 = strip * gpv;
+
+    auto issue = [&](int tile, int stage) {
         uint8_t *st = pipe_sm + (size_t)stage * stage_bytes;
-        const int64_t i0 = (int64_t)it.tile * kPipeTokens;
-        const int gv = it.strip * kPipeVecs + xv;
+        const int64_t i0 = (int64_t)tile * kPipeTokens;
+        const int gv = strip * kPipeVecs + xv;
         for (int r = xr0; r < xrows; r += kPipeThreads / kPipeVecs) {
             const int64_t gi = i0 - halo + r;
             const bool ok = gi >= 0 && gi < n && gv < nvec;
             cp_async16(st + ((size_t)r * kPipeVecs + xv) * 16,
                        ok ? x + gi * hidden + (int64_t)gv * VN : x, ok);
         }
-        const int g0 = it.strip * gpv;
         const T *drow = delta + i0 * dstride + g0;
 #pragma unroll
         for (int m = 0; m < kDC; ++m) {
@@ -312,58 +305,65 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     const int ty = tid / kPipeVecs;
     const int tt0 = ty * kPipeTokPerThread;
     const int gl = (vv * VN) / group_size;  // the vector's group within an item
-    const int grid = (int)gridDim.x;
-    const int dq = grid / n_ttiles, dr = grid - dq * n_ttiles;
-    PipeItem fetch{(int)blockIdx.x % n_ttiles, (int)blockIdx.x / n_ttiles};
+    const int v = strip * kPipeVecs + vv;
+    const bool active = v < nvec;
+    int fetch = tile0;
 #pragma unroll
     for (int st = 0; st < kPipeStages - 1; ++st) {
-        if (fetch.strip < n_strips) issue(fetch, st);
+        if (fetch < n_ttiles) issue(fetch, st);
         cp_async_commit();
-        fetch.advance(dq, dr, n_ttiles);
+        fetch += tstep;
     }
-    PipeItem cur{(int)blockIdx.x % n_ttiles, (int)blockIdx.x / n_ttiles};
-    for (int k = 0; cur.strip < n_strips; ++k, cur.advance(dq, dr, n_ttiles)) {
+    // the taps' base coefficients of this thread's vector: up to four taps
+    // unpacked once for every item; more taps read at each use (L1 hits)
+    constexpr bool kFlat = KT <= 4;
+    constexpr int KF = kFlat ? KT : 1;
+    const uint4 *base_v = reinterpret_cast<const uint4 *>(base) + v;
+    float2 bf[KF][VP];
+    if constexpr (kFlat) {
+#pragma unroll
+        for (int t = 0; t < KT; ++t)
+            V::unpack2(active && t < taps ? __ldg(base_v + (int64_t)t * nvec)
+                                          : make_uint4(0, 0, 0, 0),
+                       bf[t]);
+    }
+    for (int k = 0, tile = tile0; tile < n_ttiles; ++k, tile += tstep) {
         cp_async_wait<kPipeStages - 2>();
         __syncthreads();  // item k is staged; every thread is done with item k - 1
-        if (fetch.strip < n_strips) issue(fetch, (k + kPipeStages - 1) % kPipeStages);
+        if (fetch < n_ttiles) issue(fetch, (k + kPipeStages - 1) % kPipeStages);
         cp_async_commit();
-        fetch.advance(dq, dr, n_ttiles);
+        fetch += tstep;
 
-        const int v = cur.strip * kPipeVecs + vv;
-        if (v >= nvec) continue;
+        if (!active) continue;
         const uint8_t *st = pipe_sm + (size_t)(k % kPipeStages) * stage_bytes;
         const uint4 *xs = reinterpret_cast<const uint4 *>(st) + vv;
         const T *ds = reinterpret_cast<const T *>(st + xbytes) + gl;
-        const int64_t i0 = (int64_t)cur.tile * kPipeTokens;
+        const int64_t i0 = (int64_t)tile * kPipeTokens;
         // block position of the thread's first token
         int pos = pow2 ? (int)((i0 + tt0) & (int64_t)(bs - 1)) : (int)((i0 + tt0) % bs);
-        // the taps' base coefficients and a window of the last KT x rows of
-        // this vector: xw[t] is row tt - t of the token tt in hand (rows before
-        // the tile's staged range are never used: the block-position mask
-        // excludes them).  Up to four taps both are unpacked once; more taps
-        // keep the base packed and read x from shared memory at each use.
-        constexpr bool kFlat = KT <= 4;
-        constexpr int KF = kFlat ? KT : 1;
-        uint4 bq[KT];
-        float2 bf[KF][VP], xw[KF][VP];
+        // a window of the last KT x rows of this vector: xw[t] is row tt - t
+        // of the token tt in hand (rows before the tile's staged range are
+        // never used: the block-position mask excludes them).  Up to four taps
+        // the window is unpacked once per row; more taps read x from shared
+        // memory at each use.
+        float2 xw[KF][VP];
+        if constexpr (kFlat) {
 #pragma unroll
-        for (int t = 0; t < KT; ++t) {
-            bq[t] = t < taps ? __ldg(reinterpret_cast<const uint4 *>(base + (int64_t)t * hidden) + v)
-                             : make_uint4(0, 0, 0, 0);
-            if constexpr (kFlat) {
+            for (int t = 1; t < KT; ++t) {
                 const int r = tt0 - t + halo;
-                V::unpack2(bq[t], bf[t]);
-                V::unpack2((t > 0 && t < taps && r >= 0) ? xs[r * kPipeVecs] : make_uint4(0, 0, 0, 0),
+                V::unpack2((t < taps && r >= 0) ? xs[r * kPipeVecs] : make_uint4(0, 0, 0, 0),
                            xw[t]);
             }
         }
         T *orow = out + (i0 + tt0) * hidden + (int64_t)v * VN;
-        if (kFlat && taps == KT && pos >= KT - 1 && pos + kPipeTokPerThread <= bs &&
-            i0 + tt0 + kPipeTokPerThread <= n) {
-            // Every tap of every token of this thread lies inside the token's
-            // block (the same for a whole warp: its 32 threads share tt0), so
-            // no tap needs its mask and the tokens' sums interleave freely.
-            // The arithmetic is the general loop's, tap by tap.
+        // Every tap of every token inside its block (full), or the thread's
+        // first token starting a block that its tokens do not leave (start):
+        // then the masks are known per (token, tap) without the position and
+        // the tokens' sums interleave freely.  The same for a whole warp: its
+        // 32 threads share tt0.  The arithmetic is the general loop's.
+        const bool full = pos >= KT - 1 && pos + kPipeTokPerThread <= bs;
+        const bool start = pos == 0 && kPipeTokPerThread <= bs;
+        if (kFlat && taps == KT && (full || start) && i0 + tt0 + kPipeTokPerThread <= n) {
 #pragma unroll
             for (int j = 0; j < kPipeTokPerThread; ++j) {
                 const int tt = tt0 + j;
@@ -379,11 +379,13 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
                 for (int e = 0; e < VP; ++e) acc[e] = make_float2(0.0f, 0.0f);
 #pragma unroll
                 for (int t = 0; t < KF; ++t) {
-                    const float dt = V::scalar(ds[(tt * KT + t) * gpv]);
-                    const float2 d2 = make_float2(dt, dt);
+                    if (t <= j || full) {
+                        const float dt = V::scalar(ds[(tt * KT + t) * gpv]);
+                        const float2 d2 = make_float2(dt, dt);
 #pragma unroll
-                    for (int e = 0; e < VP; ++e)
-                        acc[e] = __ffma2_rn(__fadd2_rn(bf[t][e], d2), xw[t][e], acc[e]);
+                        for (int e = 0; e < VP; ++e)
+                            acc[e] = __ffma2_rn(__fadd2_rn(bf[t][e], d2), xw[t][e], acc[e]);
+                    }
                 }
                 *reinterpret_cast<uint4 *>(orow) = V::pack2(acc);
                 orow += hidden;
@@ -420,7 +422,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
                             xt[e] = xw[t][e];
                         }
                     } else {
-                        V::unpack2(bq[t], bt);
+                        V::unpack2(__ldg(base_v + (int64_t)t * nvec), bt);
                         V::unpack2(xs[(tt + halo - t) * kPipeVecs], xt);
                     }
                     // acc = (base + delta) * x + acc, each lane rounded as fmaf(bf + dt, x, acc)
@@ -509,8 +511,12 @@ dflash2_status run_conv(const DeviceInfo &di, const void *x, const void *base, c
         if (smem > 227 * 1024) return DFLASH2_ERR_INVALID_ARG;  // taps <= 8 keeps it below 160 KB
         int per_sm = (int)((227 * 1024) / (smem + 1024));
         if (per_sm > 2) per_sm = 2;
-        int64_t grid = (int64_t)di.sm_count * per_sm;
-        if (grid > n_items) grid = n_items;
+        // a whole number of CTAs per strip (each CTA keeps one strip), at most
+        // the CTAs resident at once and at most one per item
+        int64_t per_strip = (int64_t)di.sm_count * per_sm / n_strips;
+        if (per_strip < 1) per_strip = 1;
+        if (per_strip > n_ttiles) per_strip = n_ttiles;
+        const int64_t grid = per_strip * n_strips;
         const T *xp = static_cast<const T *>(x), *bp = static_cast<const T *>(base),
                 *dp = static_cast<const T *>(delta);
         T *op = static_cast<T *>(out);
