@@ -88,6 +88,15 @@ def _load():
             lib.oracle_quantize_rows_e4m3.restype = None
             lib.oracle_unary_rows_fp8.argtypes = [P, P, P, P, P, i64, i32, i64, i64, f64, f64, P]
             lib.oracle_unary_rows_fp8.restype = None
+            lib.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+            lib.oracle_e2m1_decode.restype = f64
+            lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+            lib.oracle_e2m1_encode.restype = ctypes.c_uint8
+            lib.oracle_quantize_nvfp4.argtypes = [P, i64, i32, i32, i32, P, P, P]
+            lib.oracle_quantize_nvfp4.restype = None
+            lib.oracle_unary_rows_nvfp4.argtypes = [P, P, P, P, P, ctypes.c_float, P, i64, i32,
+                                                    i64, i64, f64, f64, P]
+            lib.oracle_unary_rows_nvfp4.restype = None
             _lib = lib
     return _lib
 
@@ -355,6 +364,61 @@ def unary_rows_fp8(qh, dh, qw, sw, target_vocab: int, mult: float, cap: float,
     u = np.empty((n_sel, vd), dtype=np.float64)
     _load().oracle_unary_rows_fp8(_ptr(qh), _ptr(dh), _ptr(qw), _ptr(sw), _ptr(sel), n_sel,
                                   hidden, vd, target_vocab, float(mult), float(cap), _ptr(u))
+    return u
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """Values (double) of E2M1 codes (the low 4 bits of a uint8 array)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    lib = _load()
+    return np.array([lib.oracle_e2m1_decode(int(b) & 15) for b in c.reshape(-1)],
+                    dtype=np.float64).reshape(c.shape)
+
+
+def e2m1_encode(x) -> np.ndarray:
+    """E2M1 codes (round to nearest even, saturating at 6) of float32 values."""
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    lib = _load()
+    return np.array([lib.oracle_e2m1_encode(float(v)) for v in a.reshape(-1)],
+                    dtype=np.uint8).reshape(a.shape)
+
+
+def quantize_nvfp4(x, per_tensor: bool = False):
+    """NVFP4 quantization of a float32 or bf16-bits matrix [rows, cols]
+    (cols a multiple of 16): packed codes uint8 [rows, cols/2], E4M3 block
+    scales uint8 [rows, cols/16], and the fp32 second-level scales (one per
+    row, or one for the tensor)."""
+    x, code = _elem(x)
+    rows, cols = x.shape
+    if cols % 16:
+        raise ValueError("cols must be a multiple of 16")
+    q = np.empty((rows, cols // 2), dtype=np.uint8)
+    s = np.empty((rows, cols // 16), dtype=np.uint8)
+    g = np.empty(1 if per_tensor else rows, dtype=np.float32)
+    _load().oracle_quantize_nvfp4(_ptr(x), rows, cols, code, int(per_tensor), _ptr(q), _ptr(s),
+                                  _ptr(g))
+    return q, s, (g[0] if per_tensor else g)
+
+
+def unary_rows_nvfp4(qh, sh, gh, qw, sw, gw: float, target_vocab: int, mult: float, cap: float,
+                     rows=None) -> np.ndarray:
+    """u (double) of the NVFP4 (W4A4) logits for the selected rows over the whole vocab."""
+    qh = np.ascontiguousarray(qh, dtype=np.uint8)
+    sh = np.ascontiguousarray(sh, dtype=np.uint8)
+    gh = np.ascontiguousarray(gh, dtype=np.float32)
+    qw = np.ascontiguousarray(qw, dtype=np.uint8)
+    sw = np.ascontiguousarray(sw, dtype=np.uint8)
+    hidden = qh.shape[1] * 2
+    vd = qw.shape[0]
+    if rows is None:
+        sel, n_sel = None, qh.shape[0]
+    else:
+        sel = np.ascontiguousarray(rows, dtype=np.int64)
+        n_sel = sel.shape[0]
+    u = np.empty((n_sel, vd), dtype=np.float64)
+    _load().oracle_unary_rows_nvfp4(_ptr(qh), _ptr(sh), _ptr(gh), _ptr(qw), _ptr(sw), float(gw),
+                                    _ptr(sel), n_sel, hidden, vd, target_vocab, float(mult),
+                                    float(cap), _ptr(u))
     return u
 
 

@@ -729,6 +729,146 @@ void oracle_unary_rows_fp8(const uint8_t *qh, const float *dh, const uint8_t *qw
     }
 }
 
+/* ---- (11) NVFP4 lm_head: E2M1 codes with E4M3 block scales ----------------
+ * The block-scaled 4-bit head (the vLLM DSpark review's padded-vocab draft
+ * is an NVFP4 checkpoint; the sglang DFlash2 PR rejects quantized heads).
+ * Plain definitions:
+ *   - E2M1 element (the FP4 element of the OCP microscaling formats): sign
+ *     bit, 2 exponent bits with bias 1, 1 mantissa bit; exponent field 0
+ *     holds 0 and 0.5; the magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6; no
+ *     infinities or NaN.  Encoding rounds to nearest, ties to the even code
+ *     (mantissa bit 0), and saturates at 6.  Codes are 4 bits; two per byte,
+ *     element 2i in the low nibble and element 2i+1 in the high nibble.
+ *   - Every 16 consecutive elements along hidden share one scale, a
+ *     non-negative E4M3 code (section 10's format), and every row of the
+ *     activations (dynamic) or the whole weight tensor shares an fp32
+ *     second-level scale.
+ *   - Quantizing a row (activations) or a tensor (weights) X with amax A over
+ *     it, all in fp32 (the values decide integer codes):
+ *       enc = 2688 / A and g = A / 2688 (2688 = 6 * 448; A == 0: both 1);
+ *       block b: a_b = max |x| over its 16 elements,
+ *                s_b = E4M3((a_b / 6) * enc), each operation rounded;
+ *                s_b == 0: the block's codes are 0; else
+ *                r_b = enc / dec(s_b) and q_j = E2M1(x_j * r_b).
+ *     Dequantized element: g * dec(s_b) * dec(q_j).
+ *   - Logits: z[m, v] = g_h[m] * g_w * sum_b dec(s_h[m, b]) * dec(s_w[v, b])
+ *     * sum_{j in b} dec(q_h[m, j]) * dec(q_w[v, j]), the sums in double
+ *     (exact: each term has at most 9 significant bits), then the transform
+ *     and mask of (3).
+ */
+double oracle_e2m1_decode(uint8_t c)
+{
+    const int s = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    const double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -v : v;
+}
+
+uint8_t oracle_e2m1_encode(float x)
+{
+    const uint8_t sign = signbit(x) ? 0x8 : 0x0;
+    const double a = fabs((double)x);
+    if (a < 1.0) /* 0 and 0.5: steps of 0.5; 2 steps is the smallest normal, 1.0 */
+        return sign | (uint8_t)nearbyint(2.0 * a);
+    int e;
+    (void)frexp(a, &e); /* a = f * 2^e, f in [0.5, 1): unbiased exponent e - 1 */
+    e -= 1;
+    double m = nearbyint(ldexp(a, 1 - e)); /* in [2, 4] */
+    if (m == 4.0) {
+        m = 2.0;
+        e += 1;
+    }
+    if (e > 2) /* past 6 (or the midpoint 7 rounding up): saturate */
+        return sign | 0x7;
+    return sign | (uint8_t)(((e + 1) << 1) | ((int)m - 2));
+}
+
+/* Quantize rows x [rows, cols] (cols a multiple of 16) to packed codes
+ * [rows, cols / 2], block scales [rows, cols / 16] and second-level scales
+ * g: one per row (per_tensor == 0) or one for the whole tensor (g[0]). */
+void oracle_quantize_nvfp4(const void *x, int64_t rows, int32_t cols, int32_t dtype,
+                           int32_t per_tensor, uint8_t *codes, uint8_t *scales, float *g)
+{
+    float amax_t = 0.0f;
+    if (per_tensor)
+        for (int64_t i = 0; i < rows * (int64_t)cols; ++i) {
+            const float a = fabsf((float)load_elem(x, i, dtype));
+            if (a > amax_t)
+                amax_t = a;
+        }
+    for (int64_t m = 0; m < rows; ++m) {
+        float amax = amax_t;
+        if (!per_tensor) {
+            amax = 0.0f;
+            for (int32_t j = 0; j < cols; ++j) {
+                const float a = fabsf((float)load_elem(x, m * cols + j, dtype));
+                if (a > amax)
+                    amax = a;
+            }
+        }
+        const float enc = amax == 0.0f ? 1.0f : 2688.0f / amax;
+        const float gm = amax == 0.0f ? 1.0f : amax / 2688.0f;
+        if (!per_tensor)
+            g[m] = gm;
+        else if (m == 0)
+            g[0] = gm;
+        for (int32_t b = 0; b < cols / 16; ++b) {
+            float ab = 0.0f;
+            for (int32_t j = 16 * b; j < 16 * b + 16; ++j) {
+                const float a = fabsf((float)load_elem(x, m * cols + j, dtype));
+                if (a > ab)
+                    ab = a;
+            }
+            float t = ab / 6.0f;
+            t = t * enc;
+            const uint8_t sb = oracle_e4m3_encode(t);
+            scales[m * (cols / 16) + b] = sb;
+            const float dsb = (float)oracle_e4m3_decode(sb);
+            const float r = dsb == 0.0f ? 0.0f : enc / dsb;
+            for (int32_t j = 16 * b; j < 16 * b + 16; j += 2) {
+                uint8_t lo = 0, hi = 0;
+                if (dsb != 0.0f) {
+                    lo = oracle_e2m1_encode((float)load_elem(x, m * cols + j, dtype) * r);
+                    hi = oracle_e2m1_encode((float)load_elem(x, m * cols + j + 1, dtype) * r);
+                }
+                codes[m * (cols / 2) + j / 2] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    }
+}
+
+void oracle_unary_rows_nvfp4(const uint8_t *qh, const uint8_t *sh, const float *gh,
+                             const uint8_t *qw, const uint8_t *sw, float gw, const int64_t *rows,
+                             int64_t n_sel, int32_t hidden, int64_t draft_vocab,
+                             int64_t target_vocab, double mult, double cap, double *u_out)
+{
+    const int32_t nb = hidden / 16, hb = hidden / 2;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t r = 0; r < n_sel; ++r) {
+        for (int64_t v = 0; v < draft_vocab; ++v) {
+            const int64_t m = rows ? rows[r] : r;
+            double u;
+            if (v >= target_vocab) {
+                u = -INFINITY;
+            } else {
+                double acc = 0.0;
+                for (int32_t b = 0; b < nb; ++b) {
+                    double blk = 0.0;
+                    for (int32_t j = 16 * b; j < 16 * b + 16; ++j) {
+                        const uint8_t ch = (qh[m * hb + j / 2] >> (4 * (j & 1))) & 15;
+                        const uint8_t cw = (qw[v * hb + j / 2] >> (4 * (j & 1))) & 15;
+                        blk += oracle_e2m1_decode(ch) * oracle_e2m1_decode(cw);
+                    }
+                    acc += oracle_e4m3_decode(sh[m * nb + b]) * oracle_e4m3_decode(sw[v * nb + b]) *
+                           blk;
+                }
+                const double z = (double)gh[m] * (double)gw * acc;
+                u = cap > 0.0 ? cap * tanh(mult * z / cap) : mult * z;
+            }
+            u_out[r * draft_vocab + v] = u;
+        }
+    }
+}
+
 /* Threads the OpenMP loops above use: n > 0 sets them, n <= 0 only asks.
  * Returns the count now in force (1 without OpenMP).  Timing aid only. */
 int oracle_set_threads(int n)
