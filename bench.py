@@ -563,6 +563,46 @@ def run_gpu(args, w):
                                        "calls": reps, "err": int(f_err.item())}
         del t_q8
 
+        # the NVFP4 head: W4A4 with E4M3 scales per 16 elements (activation
+        # quantization + kind::mxf4nvf4 block-scaled top-K), one captured call
+        if w.hidden % 64 == 0:
+            nq = synth.make(w, parts=("lm_head_nvfp4", "w_scales_nvfp4"))
+            t_q4 = dflash2.to_device(nq["lm_head_nvfp4"], dev)
+            t_s4 = dflash2.to_device(nq["w_scales_nvfp4"], dev)
+            g4 = synth.nvfp4_w_global(w)
+            del nq
+            n_ws = torch.empty(dflash2.unary_topk_nvfp4_workspace_size(w.rows, w.hidden,
+                                                                       w.draft_vocab, w.top_k),
+                               dtype=torch.uint8, device=dev)
+
+            def nvfp4():
+                dflash2.unary_topk_nvfp4(t["h"], t_q4, t_s4, g4, w.target_vocab, w.mult, w.cap,
+                                         w.top_k, cand_ids=f_ids, cand_u=f_u, workspace=n_ws,
+                                         err=f_err, stream=stream)
+
+            f_err.zero_()
+            with torch.cuda.stream(stream):
+                nvfp4()
+            stream.synchronize()
+            ngraph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(ngraph, stream=stream):
+                nvfp4()
+            nev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(reps)]
+            with torch.cuda.stream(stream):
+                for i in range(args.warmup + reps):
+                    flush_l2(flush)
+                    if i >= args.warmup:
+                        nev[i - args.warmup][0].record(stream)
+                    ngraph.replay()
+                    if i >= args.warmup:
+                        nev[i - args.warmup][1].record(stream)
+            torch.cuda.synchronize()
+            next_rows["unary_topk_nvfp4"] = {
+                "ms": statistics.mean(a.elapsed_time(b) for a, b in nev), "calls": reps,
+                "err": int(f_err.item())}
+            del t_q4, t_s4, n_ws
+
     # max over ranks
     if world > 1:
         ms, e2e = reduce_max_over_ranks([ms, e2e], device=dev)
@@ -621,6 +661,20 @@ def run_gpu(args, w):
         f8["what"] = ("unary top-K from an E4M3 head with per-row scales: activation "
                       "quantization + tcgen05 kind::f8f6f4 GEMM + top-K, one captured call "
                       "replayed; 2*M*V*H flops; peak = measured bf16 x 2 (nominal ratio)")
+
+    if "unary_topk_nvfp4" in next_rows:
+        f4 = next_rows["unary_topk_nvfp4"]
+        f4["TFLOP/s"] = work["gemm_flops"] / (f4["ms"] * 1e-3) / 1e12
+        # fp4 peak: the measured bf16 peak times the nominal dense fp4 / bf16
+        # ratio of GB300 (13.5 / 2.25 = 6)
+        f4["frac_fp4_burst"] = f4["TFLOP/s"] / (6 * tf_burst)
+        f4["frac_fp4_sustained"] = f4["TFLOP/s"] / (6 * tf_sust)
+        f4["speedup_vs_bf16_stage"] = unary_ms / f4["ms"]
+        f4["what"] = ("unary top-K from an NVFP4 head (E2M1 codes, E4M3 scale per 16 elements, "
+                      "fp32 tensor scale) with per-row NVFP4 activations: activation "
+                      "quantization + tcgen05 kind::mxf4nvf4 block-scaled GEMM + top-K, one "
+                      "captured call replayed; 2*M*V*H flops; peak = measured bf16 x 6 "
+                      "(nominal dense ratio)")
 
     # CPU baseline: the oracle as it stands on a bounded sample (rank 0, N = 1)
     cpu = None

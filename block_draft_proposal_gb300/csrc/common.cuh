@@ -399,6 +399,40 @@ __device__ __forceinline__ void tc_mma_f8_pair(uint32_t d_tmem, uint64_t a_desc,
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// The same for E2M1 operands with block scales (kind::mxf4nvf4, one E4M3
+// scale per 16 elements: K = 64 elements = 32 bytes per MMA).  The scales are
+// read from TMEM at sfa / sfb, laid out as measured on GB300 with tcgen05.st:
+// row i of a CTA's 128 weight rows in its lane i, column sfa + i / 32; token n
+// in column sfb + n / 32 of every lane quarter (lane 32q + n % 32), in each
+// CTA of the pair (both CTAs hold every token's scales); byte b of a 32-bit
+// cell scales elements 16b .. 16b + 15 of the MMA's 64.
+__device__ __forceinline__ void tc_mma_nvfp4_pair(uint32_t d_tmem, uint64_t a_desc,
+                                                  uint64_t b_desc, uint32_t idesc, uint32_t sfa,
+                                                  uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
+        "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+// Stores of 32-bit cells into TMEM: lane i of the warp writes lane
+// (its quarter's base + i), columns taddr .. taddr + N - 1.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2,
+                                         uint32_t v3) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+                 "r"(v0), "r"(v1), "r"(v2), "r"(v3)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Arrive once on the mbarrier at this shared offset in every CTA of `mask`
 // when the pair's tcgen05 operations issued so far complete.
 __device__ __forceinline__ void tc_commit_pair_mc(uint64_t *bar, uint16_t mask) {
@@ -438,6 +472,15 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n) {
     return (1u << 4)                      // accumulator format fp32
            | (0u << 7)                    // A format E4M3
            | (0u << 10)                   // B format E4M3
+           | ((uint32_t)(n >> 3) << 17)   // N / 8
+           | ((uint32_t)(m >> 4) << 24);  // M / 16
+}
+// Instruction descriptor of kind::mxf4nvf4 (block-scaled): E2M1 A and B
+// (format code 1), UE4M3 scales (bit 23 clear), scale-factor ids 0 (a 4X
+// scale vector fills the 32-bit cell), K-major operands, fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_nvfp4(int m, int n) {
+    return (1u << 7)                      // A format E2M1
+           | (1u << 10)                   // B format E2M1
            | ((uint32_t)(n >> 3) << 17)   // N / 8
            | ((uint32_t)(m >> 4) << 24);  // M / 16
 }

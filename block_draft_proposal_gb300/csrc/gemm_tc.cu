@@ -96,6 +96,20 @@ __device__ __forceinline__ void mma_stage_f8_pair(uint32_t d, uint64_t wd, uint6
     tc_mma_f8_pair(d, wd + wsub + 6, hd + hsub + 6, idesc, 1u);
 }
 
+// The 8 MMAs of one stage for E2M1 operands on a CTA pair (K = 64 elements =
+// 32 bytes per MMA), MMA i (= 4 * box + step) reading its scales from TMEM
+// columns sf + 4i (weight rows) and sf + 32 + 4i (tokens).
+__device__ __forceinline__ void mma_stage_nvfp4_pair(uint32_t d, uint64_t wd, uint64_t hd,
+                                                     uint32_t wsub, uint32_t hsub, uint32_t idesc,
+                                                     uint32_t acc0, uint32_t sf) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t off = (i >= 4 ? 1u : 0u), step = 2u * (uint32_t)(i & 3);
+        tc_mma_nvfp4_pair(d, wd + off * wsub + step, hd + off * hsub + step, idesc,
+                          sf + 4u * (uint32_t)i, sf + 32u + 4u * (uint32_t)i, i == 0 ? acc0 : 1u);
+    }
+}
+
 // Waits (bounded) until the last `stages` loads this producer issued have
 // landed, so no copy is still writing shared memory when the CTA leaves.
 __device__ __forceinline__ void drain_loads(uint64_t *full_bar, uint32_t issued, uint32_t stages) {
@@ -228,6 +242,13 @@ constexpr int kPairEpiWarps = 8;          // CTA pairs: two warps per TMEM lane 
 constexpr int kPairEpiCols = 128;         // each on half of the tile's columns
 using EpiScratchPair = EpiScratchT<kPairEpiCols>;
 constexpr int kPairThreads = 64 + 32 * kPairEpiWarps;  // producer, MMA issuer, epilogue
+// nvfp4: four more warps per CTA load the block scales into TMEM, whose
+// columns hold the two accumulators (<= 128 columns each) and then 64 scale
+// columns per stage: 32 for the weight rows (4 per MMA) and 32 for the tokens.
+constexpr int kPairThreadsNv = kPairThreads + 128;
+constexpr uint32_t kSfBase = 256;
+constexpr uint32_t kSfCols = 64;
+constexpr int kNvMaxStages = (512 - kSfBase) / kSfCols;
 
 // Moves the buffered survivors to their rows' candidate lists: one global
 // atomic per survivor, issued by all lanes together.
@@ -280,7 +301,7 @@ __device__ __forceinline__ void filter_chunk(const GemmParams &p, const float (&
         const int i = __ffs(cols) - 1;
         cols &= cols - 1;
         float zi = tmem_ld1_wait(tcol + (uint32_t)i);
-        if (p.fp8) zi *= __shfl_sync(0xFFFFFFFFu, asc, i) * wsv;  // as fp8_scale_chunk
+        if (p.fp8 || p.nvfp4) zi *= __shfl_sync(0xFFFFFFFFu, asc, i) * wsv;  // as fp8_scale_chunk
         const uint64_t th = shfl_u64(th_lane, i);
         bool pass = false;
         uint64_t key = 0;
@@ -557,7 +578,8 @@ __global__ void __launch_bounds__(192, 1)
 // accumulator-full barriers; both CTAs' epilogues (each reading its own 128
 // TMEM lanes) arrive on the leader's accumulator-empty barrier.
 // ---------------------------------------------------------------------------
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kPairEpiWarps, 1)
+template <bool NV>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NV ? kPairThreadsNv : kPairThreads, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_w,
                         const __grid_constant__ CUtensorMap tm_h, const GemmParams p) {
     extern __shared__ uint8_t dsmem[];
@@ -566,6 +588,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kPairEpiWa
     __shared__ uint64_t acc_full[2];
     __shared__ uint64_t acc_empty[2];
     __shared__ uint64_t drain_bar;
+    __shared__ uint64_t sf_full[NV ? kNvMaxStages : 1];  // nvfp4: a stage's scales are in TMEM
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -583,7 +606,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kPairEpiWa
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
-    const uint32_t tmem_cols = 2 * p.acc_cols;
+    const uint32_t tmem_cols = NV ? 512u : 2 * p.acc_cols;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -595,6 +618,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kPairEpiWa
             mbar_init(&acc_empty[a], 2 * kPairEpiWarps);  // every epilogue warp of the pair
         }
         mbar_init(&drain_bar, 1);
+        if (NV)
+            for (int s = 0; s < p.stages; ++s) mbar_init(&sf_full[s], 8);  // 4 warps x 2 CTAs
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -658,8 +683,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kPairEpiWa
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
-            const uint32_t idesc =
-                p.fp8 ? idesc_e4m3(2 * kGemmTileW, p.bn) : idesc_bf16(2 * kGemmTileW, p.bn);
+            const uint32_t idesc = NV     ? idesc_nvfp4(2 * kGemmTileW, p.bn)
+                                   : p.fp8 ? idesc_e4m3(2 * kGemmTileW, p.bn)
+                                           : idesc_bf16(2 * kGemmTileW, p.bn);
             const uint64_t wd0 = sw128_desc(smem_u32(w_smem)), hd0 = sw128_desc(smem_u32(h_smem));
             const uint32_t w_st = kWStageBytes >> 4, h_st = h_stage >> 4;  // descriptor units
             const uint32_t w_sub = kWTileBytes >> 4, h_sb = h_sub >> 4;
@@ -682,8 +708,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kPairEpiWa
                         ok = false;
                         break;
                     }
+                    if (NV && !mbar_wait(&sf_full[s], ph, &abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
-                    if (p.fp8)
+                    if (NV)
+                        mma_stage_nvfp4_pair(d_tmem, wd0 + s * w_st, hd0 + s * h_st, w_sub, h_sb,
+                                             idesc, kb > kb0 ? 1u : 0u,
+                                             tmem + kSfBase + s * kSfCols);
+                    else if (p.fp8)
                         mma_stage_f8_pair(d_tmem, wd0 + s * w_st, hd0 + s * h_st, w_sub, h_sb,
                                           idesc, kb > kb0 ? 1u : 0u);
                     else
@@ -701,6 +735,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kPairEpiWa
             if (!ok) {
                 tc_commit_pair(&drain_bar);
                 mbar_wait_drain(&drain_bar, 0);
+            }
+        }
+    } else if (NV && warp >= 2 + kPairEpiWarps) {
+        // nvfp4 scale loaders.  For every stage: the scales of this CTA's 128
+        // weight rows (the warp's lane quarter: one 32-bit cell of 4 scales
+        // per MMA, at column 4i + quarter) and of every token of the tile
+        // (columns 32 + 4i + token / 32, in each quarter), written into the
+        // stage's TMEM columns once the stage's previous MMAs are done; then
+        // an arrival on the leader's sf_full barrier.  Scales past a row's
+        // end, and of rows or tokens outside the problem, are zero (their
+        // codes are zero too).
+        const int q = warp & 3;  // the TMEM lane quarter this warp may access
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        const uint32_t sf_full_leader = mapa_shared(smem_u32(&sf_full[0]), 0);
+        uint32_t s = 0, ph = 1;  // the first pass finds every stage free
+        bool ok = true;
+        for (int w = pair; w < total && ok; w += npairs) {
+            const Item item = decode(p, w);
+            const int64_t vrow =
+                (int64_t)item.wt * p.unit + (int64_t)rank * kGemmTileW + q * 32 + lane;
+            const uint8_t *wsrc = vrow < p.rows_w ? p.sfw + vrow * p.n_sf : nullptr;
+            const uint8_t *hsrc[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = 32 * j + lane;
+                const int64_t m = (int64_t)item.nt * p.bn + c;
+                hsrc[j] = c < p.bn && m < p.rows_h ? p.sfh + m * p.n_sf : nullptr;
+            }
+            const int kb0 = item.ks * p.kb_per_split;
+            const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+            for (int kb = kb0; kb < kb1; ++kb) {
+                // the loads first: they touch no TMEM, so they overlap the wait
+                uint32_t a[8], b[4][8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int blk = kb * 32 + 4 * i;
+                    const bool in = blk < p.n_sf;
+                    a[i] = wsrc && in ? __ldg(reinterpret_cast<const uint32_t *>(wsrc + blk)) : 0u;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        b[j][i] = hsrc[j] && in
+                                      ? __ldg(reinterpret_cast<const uint32_t *>(hsrc[j] + blk))
+                                      : 0u;
+                }
+                if (!mbar_wait(&empty_bar[s], ph, &abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t col = tmem + lane_base + kSfBase + s * kSfCols;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) tmem_st1(col + 4u * (uint32_t)i + (uint32_t)q, a[i]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    tmem_st4(col + 32u + 4u * (uint32_t)i, b[0][i], b[1][i], b[2][i], b[3][i]);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(sf_full_leader + 8u * s);
+                if (++s == (uint32_t)p.stages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
         }
     } else {
@@ -725,9 +822,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kPairEpiWa
             }
             __syncwarp();
         };
-        // fp8: this thread's weight-row scale
+        // fp8: this thread's weight-row scale; nvfp4: the weights' one scale
+        const bool scaled = p.fp8 || NV;
         const auto row_scale = [&](int64_t v) {
-            return p.fp8 ? (v < p.rows_w ? __ldg(p.w_scale + v) : 0.0f) : 1.0f;
+            return p.fp8 ? (v < p.rows_w ? __ldg(p.w_scale + v) : 0.0f) : NV ? p.w_global : 1.0f;
         };
         const auto filter_tile = [&](const Item &item, int a) {
             const int m_tile = item.nt * p.bn;
@@ -738,7 +836,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kPairEpiWa
             for (int c0 = cb; c0 < ce; c0 += 32) {
                 float z[32];
                 tmem_ld32_wait(tbase + (uint32_t)c0, z);
-                const float asc = p.fp8 ? fp8_scale_chunk(p, z, m_tile + c0, wsv, lane) : 1.0f;
+                const float asc = scaled ? fp8_scale_chunk(p, z, m_tile + c0, wsv, lane) : 1.0f;
                 filter_chunk(p, z, v, m_tile + c0, c0 - cb, tbase + (uint32_t)c0, es, nbuf, lane,
                              asc, wsv);
             }
@@ -772,7 +870,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kPairEpiWa
                 for (int c0 = cb; c0 < ce; c0 += 32) {
                     float z[32];
                     tmem_ld32_wait(tbase + (uint32_t)c0, z);
-                    if (p.fp8) fp8_scale_chunk(p, z, item.nt * p.bn + c0, wsv, lane);
+                    if (scaled) fp8_scale_chunk(p, z, item.nt * p.bn + c0, wsv, lane);
                     group_max_chunk(p, z, valid, item.nt * p.bn + c0, min(32, p.bn - c0), g, lane);
                 }
                 counter_arrive(p.sync, lane);
@@ -805,7 +903,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kPairEpiWa
             for (int c0 = cb; c0 < ce; c0 += 32) {
                 float z[32];
                 tmem_ld32_wait(tbase + (uint32_t)c0, z);
-                if (p.fp8) fp8_scale_chunk(p, z, m_tile + c0, wsv, lane);
+                if (scaled) fp8_scale_chunk(p, z, m_tile + c0, wsv, lane);
                 epilogue_chunk(p, z, v, row_in_unit, m_tile + c0, min(32, p.bn - c0), item, lane);
             }
             tc_fence_before();
@@ -826,14 +924,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kPairEpiWa
 // Per-device caches; several host threads may fill them at once (the guarded
 // calls are idempotent).
 std::atomic<int> g_smem_set[64];
-std::atomic<int> g_fused_pairs[64];  // 0: not yet asked; -1: none
+std::atomic<int> g_fused_pairs[2][64];  // [nvfp4][device]; 0: not yet asked; -1: none
 
 dflash2_status set_gemm_attrs(const DeviceInfo &di) {
     if (di.device < 0 || di.device >= 64) return DFLASH2_ERR_CUDA;
     if (g_smem_set[di.device]) return DFLASH2_OK;
     if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kGemmSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(gemm_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(gemm_tc_pair_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kGemmSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_tc_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kGemmSmemBytes) != cudaSuccess) {
         cudaGetLastError();
         return DFLASH2_ERR_CUDA;
@@ -842,32 +943,38 @@ dflash2_status set_gemm_attrs(const DeviceInfo &di) {
     return DFLASH2_OK;
 }
 
-// CTA pairs of the pair kernel the device holds at once (its full shared
-// memory, so one CTA per SM), or 0.
-int fused_pairs(const DeviceInfo &di) {
+// CTA pairs of the pair kernel (nv: its nvfp4 form) the device holds at once
+// (its full shared memory, so one CTA per SM), or 0.
+int fused_pairs(const DeviceInfo &di, bool nv = false) {
     if (di.device < 0 || di.device >= 64) return 0;
-    if (g_fused_pairs[di.device] == 0) {
+    std::atomic<int> &slot = g_fused_pairs[nv ? 1 : 0][di.device];
+    if (slot == 0) {
         int n = 0;
         if (set_gemm_attrs(di) == DFLASH2_OK) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)(di.sm_count / 2 * 2));
-            cfg.blockDim = dim3(kPairThreads);
+            cfg.blockDim = dim3(nv ? kPairThreadsNv : kPairThreads);
             cfg.dynamicSmemBytes = kGemmSmemBytes;
-            if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_pair_kernel, &cfg) != cudaSuccess) {
+            const cudaError_t e =
+                nv ? cudaOccupancyMaxActiveClusters(&n, gemm_tc_pair_kernel<true>, &cfg)
+                   : cudaOccupancyMaxActiveClusters(&n, gemm_tc_pair_kernel<false>, &cfg);
+            if (e != cudaSuccess) {
                 cudaGetLastError();
                 n = 0;
             }
         }
-        g_fused_pairs[di.device] = n > 0 ? n : -1;
+        slot = n > 0 ? n : -1;
     }
-    const int n = g_fused_pairs[di.device];
+    const int n = slot;
     return n > 0 ? n : 0;
 }
 
 }  // namespace
 
-int fused_pair_count(const DeviceInfo &di) { return fused_pairs(di); }
-int fused_epilogue_warps(const DeviceInfo &di) { return fused_pairs(di) * 2 * kPairEpiWarps; }
+int fused_pair_count(const DeviceInfo &di, bool nv) { return fused_pairs(di, nv); }
+int fused_epilogue_warps(const DeviceInfo &di, bool nv) {
+    return fused_pairs(di, nv) * 2 * kPairEpiWarps;
+}
 
 dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h, GemmParams p,
                               cudaStream_t st, bool pair) {
@@ -876,10 +983,20 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     if (p.mode == kGemmStore) pair = false;  // the projection keeps one CTA per tile
     if (pair && di.sm_count < 2) return DFLASH2_ERR_UNSUPPORTED_DEVICE;  // the caller's layout assumes pairs
     if (p.fp8 && (!pair || p.hidden % 16 != 0)) return DFLASH2_ERR_INVALID_ARG;
+    const bool nv = p.nvfp4 != 0;
+    if (nv && (!pair || p.fp8 || p.bn > 128 || p.hidden % 64 != 0 || p.n_sf != p.hidden / 16 ||
+               !p.sfw || !p.sfh || reinterpret_cast<uintptr_t>(p.sfw) % 4 != 0 ||
+               reinterpret_cast<uintptr_t>(p.sfh) % 4 != 0 ||
+               (p.mode != kGemmPilot && p.mode != kGemmFilter && p.mode != kGemmFused)))
+        return DFLASH2_ERR_INVALID_ARG;
+    // The TMA boxes, the stages and their counts run over bytes of codes for
+    // 8-bit and 4-bit operands: one 128-byte row holds 64 bf16, 128 E4M3 codes
+    // or 256 E2M1 codes.
+    const int64_t kdim = nv ? p.hidden / 2 : p.hidden;
     p.unit = pair ? 2 * kGemmTileW : kGemmTileW;
     p.n_tok_tiles = (p.rows_h + p.bn - 1) / p.bn;
-    p.box_k = p.fp8 ? 2 * kGemmTileK : kGemmTileK;  // one 128-byte row: 128 codes or 64 bf16
-    p.num_kb = (p.hidden + 2 * p.box_k - 1) / (2 * p.box_k);
+    p.box_k = (p.fp8 || nv) ? 2 * kGemmTileK : kGemmTileK;
+    p.num_kb = (int32_t)((kdim + 2 * p.box_k - 1) / (2 * p.box_k));
     p.kb_per_split = (p.num_kb + p.k_splits - 1) / p.k_splits;
     p.k_splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;  // every split gets >= 1 block
     p.n_wtiles = (p.rows_w + p.unit - 1) / p.unit;
@@ -909,16 +1026,17 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
                                  : 0;
     int stages = (int)((kGemmSmemBytes - 1024 - epi_bytes) / stage_bytes);
     if (stages > kGemmMaxStages) stages = kGemmMaxStages;
+    if (nv && stages > kNvMaxStages) stages = kNvMaxStages;  // the scale columns of TMEM
     if (stages < 2) return DFLASH2_ERR_INVALID_ARG;  // bn <= 256 always leaves room for two
     p.stages = stages;
     const size_t smem = (size_t)stages * stage_bytes + epi_bytes + 1024;
 
     CUtensorMap tm_w, tm_h;
-    const uint32_t eb = p.fp8 ? 1 : 2;
+    const uint32_t eb = (p.fp8 || nv) ? 1 : 2;
     dflash2_status s =
-        encode_tmap_2d(&tm_w, w, (uint64_t)p.rows_w, (uint64_t)p.hidden, kGemmTileW, eb);
+        encode_tmap_2d(&tm_w, w, (uint64_t)p.rows_w, (uint64_t)kdim, kGemmTileW, eb);
     if (s != DFLASH2_OK) return s;
-    s = encode_tmap_2d(&tm_h, h, (uint64_t)p.rows_h, (uint64_t)p.hidden, h_rows, eb);
+    s = encode_tmap_2d(&tm_h, h, (uint64_t)p.rows_h, (uint64_t)kdim, h_rows, eb);
     if (s != DFLASH2_OK) return s;
 
     s = set_gemm_attrs(di);
@@ -927,14 +1045,14 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     if (fused) {
         // every CTA resident at once (its warps wait on one another): a
         // cooperative launch of at most the pairs the device holds together
-        const int64_t pairs_max = fused_pairs(di);
+        const int64_t pairs_max = fused_pairs(di, nv);
         if (pairs_max < 1) return DFLASH2_ERR_UNSUPPORTED_DEVICE;
         const int pairs = (int)(total < pairs_max ? total : pairs_max);
         // a pair keeps its pilot accumulators until the select: two at most
         if ((int64_t)p.n_pilot * p.n_tok_tiles > 2LL * pairs) return DFLASH2_ERR_INVALID_ARG;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(2 * pairs));
-        cfg.blockDim = dim3(kPairThreads);
+        cfg.blockDim = dim3(nv ? kPairThreadsNv : kPairThreads);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = st;
         cudaLaunchAttribute attr[2];
@@ -944,13 +1062,21 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
         attr[1].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
-        cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel, tm_w, tm_h, p);
+        if (nv)
+            cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<true>, tm_w, tm_h, p);
+        else
+            cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<false>, tm_w, tm_h, p);
         return launch_status();
     }
     if (pair) {
         const int64_t pairs_max = di.sm_count / 2;
         const int pairs = (int)(total < pairs_max ? total : pairs_max);
-        launch_k(gemm_tc_pair_kernel, 2 * pairs, kPairThreads, smem, st, tm_w, tm_h, p);
+        if (nv)
+            launch_k(gemm_tc_pair_kernel<true>, 2 * pairs, kPairThreadsNv, smem, st, tm_w, tm_h,
+                     p);
+        else
+            launch_k(gemm_tc_pair_kernel<false>, 2 * pairs, kPairThreads, smem, st, tm_w, tm_h,
+                     p);
     } else {
         const int grid = (int)(total < di.sm_count ? total : di.sm_count);
         launch_k(gemm_tc_kernel, grid, 192, smem, st, tm_w, tm_h, p);

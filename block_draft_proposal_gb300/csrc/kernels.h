@@ -81,6 +81,16 @@ struct GemmParams {
     int32_t box_k;  // hidden elements per TMA box (filled by launch_gemm_tc)
     const float *a_scale;
     const float *w_scale;
+    // nvfp4: E2M1 codes, two per byte (kind::mxf4nvf4 with one E4M3 scale per
+    // 16 elements, the scales in TMEM; CTA pairs, bn <= 128).  hidden counts
+    // elements; the codes rows are hidden / 2 bytes.  sfw [rows_w][n_sf] and
+    // sfh [rows_h][n_sf] hold the scales (n_sf = hidden / 16, a multiple of
+    // 4); C = acc * (a_scale[m] * w_global) before the epilogue.
+    int32_t nvfp4;
+    int32_t n_sf;
+    const uint8_t *sfw;
+    const uint8_t *sfh;
+    float w_global;
 };
 
 // Pilot tiling of a weight matrix with n_wtiles units of unit_rows rows:
@@ -107,11 +117,16 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
 // Per-row E4M3 quantization (quant.cu): q [rows, cols] codes, d [rows] scales.
 dflash2_status launch_quant_rows_e4m3(const void *x, int32_t dtype, int64_t rows, int32_t cols,
                                       uint8_t *q, float *d, cudaStream_t st);
+// Per-row NVFP4 quantization (quant.cu): codes [rows, cols / 2] (element 2i in
+// the low nibble), E4M3 block scales [rows, cols / 16], fp32 second-level
+// scales g [rows]; cols a multiple of 16.
+dflash2_status launch_quant_rows_nvfp4(const void *x, int32_t dtype, int64_t rows, int32_t cols,
+                                       uint8_t *codes, uint8_t *scales, float *g, cudaStream_t st);
 
 // CTA pairs of one fused launch (every CTA resident at once) and their
 // epilogue warps, or 0 when the device cannot hold such a launch.  Host-side,
 // cached per device.
-int fused_pair_count(const DeviceInfo &di);
-int fused_epilogue_warps(const DeviceInfo &di);
+int fused_pair_count(const DeviceInfo &di, bool nvfp4 = false);
+int fused_epilogue_warps(const DeviceInfo &di, bool nvfp4 = false);
 
 }  // namespace dflash2

@@ -7,6 +7,8 @@
 // A row of zeros gets code 0 everywhere and d = 1.  The divides and the
 // multiply are IEEE fp32 operations (no contraction), so the codes are fixed
 // by the inputs.  One CTA per row.
+#include <cuda_fp4.h>
+
 #include "kernels.h"
 
 namespace dflash2 {
@@ -50,7 +52,83 @@ __global__ void __launch_bounds__(kQuantThreads)
     if (threadIdx.x == 0) d[row] = __fdiv_rn(amax, 448.0f);
 }
 
+// Per-row NVFP4 quantization (the activations of the NVFP4-head unary path):
+//
+//   amax = max_j |x[m, j]|,  enc = 2688 / amax,  g[m] = amax / 2688   (fp32;
+//   2688 = 6 * 448; a row of zeros: enc = g = 1)
+//   block b of 16 elements: a_b = max |x| over it,
+//   s_b = E4M3((a_b / 6) * enc)  (round to nearest even, saturating),
+//   codes q_j = E2M1(x_j * (enc / dec(s_b)))  (round to nearest even,
+//   saturating at 6), all zero when s_b is zero.
+//
+// Each operation is one IEEE fp32 operation (no contraction), so the codes
+// and scales are fixed by the inputs.  One CTA per row; thread t takes blocks
+// t, t + 256, ...
+template <typename T>
+__global__ void __launch_bounds__(kQuantThreads)
+    quant_rows_nvfp4_kernel(const T *__restrict__ x, int cols, uint8_t *__restrict__ codes,
+                            uint8_t *__restrict__ scales, float *__restrict__ g) {
+    grid_dep_wait();
+    __shared__ float red[kQuantThreads / 32];
+    const int64_t row = blockIdx.x;
+    const T *xr = x + row * cols;
+    float amax = 0.0f;
+    for (int j = threadIdx.x; j < cols; j += kQuantThreads) amax = fmaxf(amax, fabsf(qf(xr[j])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+    const float enc = amax == 0.0f ? 1.0f : __fdiv_rn(2688.0f, amax);
+    const int nb = cols / 16;
+    for (int b = threadIdx.x; b < nb; b += kQuantThreads) {
+        float v[16];
+        float ab = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            v[e] = qf(xr[16 * b + e]);
+            ab = fmaxf(ab, fabsf(v[e]));
+        }
+        const float t = __fmul_rn(__fdiv_rn(ab, 6.0f), enc);
+        const __nv_fp8_storage_t sc = __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
+        __nv_fp8_e4m3 sv;
+        sv.__x = sc;
+        const float ds = static_cast<float>(sv);
+        uint32_t lo = 0, hi = 0;  // the 16 codes, 8 per word, element 2i in the low nibble
+        if (ds != 0.0f) {
+            const float r = __fdiv_rn(enc, ds);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const uint32_t c =
+                    (uint32_t)__nv_cvt_float_to_fp4(__fmul_rn(v[e], r), __NV_E2M1, cudaRoundNearest) &
+                    15u;
+                if (e < 8)
+                    lo |= c << (4 * e);
+                else
+                    hi |= c << (4 * (e - 8));
+            }
+        }
+        reinterpret_cast<uint2 *>(codes + row * (cols / 2))[b] = make_uint2(lo, hi);
+        scales[row * nb + b] = (uint8_t)sc;
+    }
+    if (threadIdx.x == 0) g[row] = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+}
+
 }  // namespace
+
+dflash2_status launch_quant_rows_nvfp4(const void *x, int32_t dtype, int64_t rows, int32_t cols,
+                                       uint8_t *codes, uint8_t *scales, float *g,
+                                       cudaStream_t st) {
+    if (dtype == DFLASH2_BF16)
+        launch_k(quant_rows_nvfp4_kernel<__nv_bfloat16>, (unsigned)rows, kQuantThreads, 0, st,
+                 static_cast<const __nv_bfloat16 *>(x), cols, codes, scales, g);
+    else
+        launch_k(quant_rows_nvfp4_kernel<float>, (unsigned)rows, kQuantThreads, 0, st,
+                 static_cast<const float *>(x), cols, codes, scales, g);
+    return launch_status();
+}
 
 dflash2_status launch_quant_rows_e4m3(const void *x, int32_t dtype, int64_t rows, int32_t cols,
                                       uint8_t *q, float *d, cudaStream_t st) {
@@ -80,4 +158,23 @@ extern "C" dflash2_status dflash2_quantize_rows_e4m3(const void *x, int64_t rows
     dflash2_status s = current_device(&di);
     if (s != DFLASH2_OK) return s;
     return launch_quant_rows_e4m3(x, dtype, rows, cols, q, scale, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" dflash2_status dflash2_quantize_rows_nvfp4(const void *x, int64_t rows, int32_t cols,
+                                                      int32_t dtype, uint8_t *codes,
+                                                      uint8_t *scales, float *g, void *stream) {
+    using namespace dflash2;
+    if (dtype != DFLASH2_F32 && dtype != DFLASH2_BF16) return DFLASH2_ERR_UNSUPPORTED_DTYPE;
+    if (rows < 0 || rows > INT32_MAX || cols <= 0 || cols % 16 != 0) return DFLASH2_ERR_INVALID_ARG;
+    if (rows == 0) return DFLASH2_OK;
+    if (!x || !codes || !scales || !g) return DFLASH2_ERR_INVALID_ARG;
+    const uintptr_t esz = dtype == DFLASH2_BF16 ? 2 : 4;
+    if (reinterpret_cast<uintptr_t>(x) % esz != 0 || reinterpret_cast<uintptr_t>(codes) % 8 != 0 ||
+        reinterpret_cast<uintptr_t>(g) % 4 != 0)
+        return DFLASH2_ERR_MISALIGNED;
+    DeviceInfo di;
+    dflash2_status s = current_device(&di);
+    if (s != DFLASH2_OK) return s;
+    return launch_quant_rows_nvfp4(x, dtype, rows, cols, codes, scales, g,
+                                   static_cast<cudaStream_t>(stream));
 }

@@ -346,6 +346,86 @@ __device__ int direct_row_topk(const T *__restrict__ hrow, const T *__restrict__
     return block_collect_sorted(buf, n, kth, k, sh);
 }
 
+// NVFP4 operands: packed E2M1 codes (two per byte, element 2i in the low
+// nibble) with one E4M3 scale per 16 elements and an fp32 second-level scale
+// (per row of h, one for the weights).
+struct E2M1x2 {
+    uint8_t bits;
+};
+struct NvScales {
+    const uint8_t *sfh;  // [rows][hidden / 16]
+    const uint8_t *sfw;  // [draft_vocab][hidden / 16]
+    float w_global;
+};
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+    const float m = (c & 1u) ? 1.5f : 1.0f;  // magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6
+    const uint32_t e = (c >> 1) & 3u;
+    const float v = e == 0 ? 0.5f * (float)(c & 1u) : m * (float)(1u << (e - 1));
+    return (c & 8u) ? -v : v;
+}
+__device__ __forceinline__ float e4m3_value(uint8_t c) {
+    __nv_fp8_e4m3 v;
+    v.__x = c;
+    return static_cast<float>(v);
+}
+__device__ __forceinline__ float nv_elem(const uint8_t *codes, const uint8_t *sf, int j) {
+    const uint32_t b = codes[j >> 1];
+    return e2m1_value((j & 1) ? b >> 4 : b & 15u) * e4m3_value(sf[j >> 4]);
+}
+
+// The exact top-k of one row for NVFP4 operands: as direct_row_topk, on the
+// block-scaled values (code times block scale, exact in fp32) and the
+// epilogue's second-level scale a_scale * w_global.
+__device__ int direct_row_topk_nvfp4(const uint8_t *__restrict__ hrow,
+                                     const uint8_t *__restrict__ sfh_row,
+                                     const uint8_t *__restrict__ w,
+                                     const uint8_t *__restrict__ sfw, int hidden,
+                                     int64_t draft_vocab, int64_t target_vocab, float mult,
+                                     float cap, int k, float *hs, uint64_t *buf, SelectShared &sh,
+                                     float scale) {
+    for (int j = threadIdx.x; j < hidden; j += blockDim.x) hs[j] = nv_elem(hrow, sfh_row, j);
+    if (threadIdx.x == 0) sh.count = 0;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
+    const int64_t vmax = draft_vocab < target_vocab ? draft_vocab : target_vocab;
+    const int nsf = hidden / 16;
+    uint64_t theta = 0;
+    for (int64_t v0 = 0; v0 < vmax; v0 += kDirectRows) {
+        for (int r = warp; r < kDirectRows; r += nwarps) {
+            const int64_t v = v0 + r;
+            if (v >= vmax) break;
+            const uint8_t *wr = w + v * (hidden / 2);
+            const uint8_t *sr = sfw + v * nsf;
+            float acc = 0.0f;
+            for (int j = lane; j < hidden; j += 32) acc = fmaf(hs[j], nv_elem(wr, sr, j), acc);
+            acc = warp_sum(acc);
+            acc *= scale;
+            if (lane == 0) {
+                const uint64_t key = make_key(unary_transform(acc, mult, cap), (uint32_t)v);
+                if (key >= theta) {
+                    const uint32_t slot = atomicAdd(&sh.count, 1u);
+                    buf[slot] = key;
+                }
+            }
+        }
+        __syncthreads();
+        const int n = (int)sh.count;
+        if (n > kDirectBuf - kDirectRows && n > k) {
+            const uint64_t kth = block_kth_largest(buf, n, k, sh);
+            const int got = block_collect_sorted(buf, n, kth, k, sh);
+            for (int i = threadIdx.x; i < got; i += blockDim.x) buf[i] = sh.top[i];
+            theta = kth;
+            __syncthreads();
+            if (threadIdx.x == 0) sh.count = (uint32_t)got;
+            __syncthreads();
+        }
+    }
+    const int n = (int)sh.count;
+    const uint64_t kth = n > k ? block_kth_largest(buf, n, k, sh) : 1;
+    return block_collect_sorted(buf, n, kth, k, sh);
+}
+
 // Shared-memory layout of the kernels that may take the exact path:
 // [SelectShared][hidden floats][kDirectBuf keys] (and the staged candidates
 // reuse the float + key area).
@@ -496,7 +576,8 @@ __global__ void __launch_bounds__(kSelThreads)
                     int cand_cap, int k, int64_t *ids, float *vals, int32_t *err,
                     const T *__restrict__ h, const T *__restrict__ w, int hidden,
                     int64_t draft_vocab, int64_t target_vocab, float mult, float cap,
-                    const float *__restrict__ a_scale, const float *__restrict__ w_scale) {
+                    const float *__restrict__ a_scale, const float *__restrict__ w_scale,
+                    NvScales nv) {
     grid_dep_wait();
     __shared__ SelectShared sh;
     extern __shared__ __align__(16) uint8_t dyn[];
@@ -506,9 +587,16 @@ __global__ void __launch_bounds__(kSelThreads)
         float *hs = reinterpret_cast<float *>(dyn);
         uint64_t *buf =
             reinterpret_cast<uint64_t *>(dyn + (((size_t)hidden * 4 + 15) & ~(size_t)15));
-        const int got = direct_row_topk<T>(h + row * hidden, w, hidden, draft_vocab, target_vocab,
-                                           mult, cap, k, hs, buf, sh, w_scale,
-                                           a_scale ? a_scale[row] : 1.0f);
+        int got;
+        if constexpr (std::is_same<T, E2M1x2>::value)
+            got = direct_row_topk_nvfp4(
+                reinterpret_cast<const uint8_t *>(h) + row * (hidden / 2),
+                nv.sfh + row * (hidden / 16), reinterpret_cast<const uint8_t *>(w), nv.sfw,
+                hidden, draft_vocab, target_vocab, mult, cap, k, hs, buf, sh,
+                a_scale[row] * nv.w_global);
+        else
+            got = direct_row_topk<T>(h + row * hidden, w, hidden, draft_vocab, target_vocab, mult,
+                                     cap, k, hs, buf, sh, w_scale, a_scale ? a_scale[row] : 1.0f);
         write_row(sh, got, k, row, ids, vals, err);
         if (threadIdx.x == 0 && err) atomicOr(err, DFLASH2_DEVINFO_TOPK_FALLBACK);
         return;
@@ -608,8 +696,8 @@ inline int64_t recommended_cap(const TopkLayout &L, int k) {
 }
 
 // Token tile of the bf16 path: the rows in near-equal tiles of at most 256.
-inline int token_tile(int64_t rows) {
-    const int64_t n_tiles = (rows + 255) / 256;
+inline int token_tile(int64_t rows, int max_bn = 256) {
+    const int64_t n_tiles = (rows + max_bn - 1) / max_bn;
     return (int)(((rows + n_tiles - 1) / n_tiles + 15) / 16 * 16);
 }
 
@@ -626,8 +714,8 @@ inline int token_tile(int64_t rows) {
 //     the bf16 workloads (measured on GB300: 7 us faster with one extra
 //     round, 11 us slower with two).
 bool use_fused(const DeviceInfo &di, const TopkLayout &L, int64_t rows, int bn, float mult,
-               int top_k) {
-    const int fused_warps = fused_epilogue_warps(di);
+               int top_k, bool nv = false) {
+    const int fused_warps = fused_epilogue_warps(di, nv);
     if (!(mult > 0.0f) || fused_warps <= 0 || rows > 2LL * fused_warps) return false;
     // its groups are 32-row slices of the pilot units; with fewer than 4 K of
     // them the threshold is loose and candidate lists overflow
@@ -635,7 +723,7 @@ bool use_fused(const DeviceInfo &di, const TopkLayout &L, int64_t rows, int bn, 
     const int64_t tok_tiles = (rows + bn - 1) / bn;
     const int64_t all_tiles = (int64_t)L.n_wtiles * tok_tiles;
     const int64_t filter_tiles = (int64_t)(L.n_wtiles - L.n_pilot) * tok_tiles;
-    const int64_t fused_pairs = std::min<int64_t>(all_tiles, fused_pair_count(di));
+    const int64_t fused_pairs = std::min<int64_t>(all_tiles, fused_pair_count(di, nv));
     if ((int64_t)L.n_pilot * tok_tiles > 2 * fused_pairs) return false;
     const int64_t filter_pairs = std::min<int64_t>(filter_tiles, di.sm_count / 2);
     if (filter_pairs < 1) return true;  // the pilot covers the vocab
@@ -653,6 +741,8 @@ dflash2_status set_select_attrs(int device) {
                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
         cudaFuncSetAttribute(finalize_kernel<__nv_fp8_e4m3>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
+        cudaFuncSetAttribute(finalize_kernel<E2M1x2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes) != cudaSuccess ||
         cudaFuncSetAttribute(pilot_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              bytes) != cudaSuccess ||
         cudaFuncSetAttribute(direct_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -679,7 +769,9 @@ dflash2_status run_tc_topk(const DeviceInfo &di, const void *h, const void *lm_h
                            const float *a_scale, const float *w_scale, int64_t rows, int hidden,
                            int64_t draft_vocab, int64_t target_vocab, float mult, float cap,
                            int top_k, int64_t *cand_ids, float *cand_u, void *workspace,
-                           size_t ws_bytes, int32_t *err_word, cudaStream_t st) {
+                           size_t ws_bytes, int32_t *err_word, cudaStream_t st,
+                           NvScales nvs = NvScales{}) {
+    constexpr bool kNv = std::is_same<T, E2M1x2>::value;
     dflash2_status s = DFLASH2_OK;
     const size_t dsm = direct_smem_bytes(hidden);
     const TopkLayout L = topk_layout(rows, draft_vocab);
@@ -695,7 +787,7 @@ dflash2_status run_tc_topk(const DeviceInfo &di, const void *h, const void *lm_h
     float *pilot_u = reinterpret_cast<float *>(ws + L.pilot_off);
     uint64_t *cand = reinterpret_cast<uint64_t *>(ws + L.cand_off);
 
-    const int bn = token_tile(rows);
+    const int bn = token_tile(rows, kNv ? 128 : 256);  // nvfp4: the scales' TMEM columns
 
     GemmParams p{};
     p.rows_w = (int32_t)draft_vocab;
@@ -710,6 +802,11 @@ dflash2_status run_tc_topk(const DeviceInfo &di, const void *h, const void *lm_h
     p.fp8 = std::is_same<T, __nv_fp8_e4m3>::value ? 1 : 0;
     p.a_scale = a_scale;
     p.w_scale = w_scale;
+    p.nvfp4 = kNv ? 1 : 0;
+    p.n_sf = hidden / 16;
+    p.sfw = nvs.sfw;
+    p.sfh = nvs.sfh;
+    p.w_global = nvs.w_global;
 
     const bool pairs = true;
     const int unit = unit_rows();
@@ -718,7 +815,7 @@ dflash2_status run_tc_topk(const DeviceInfo &di, const void *h, const void *lm_h
     if (fin_smem < dsm) fin_smem = dsm;
 
     // the pilot pass, select and filter pass in one cooperative launch?
-    if (use_fused(di, L, rows, bn, mult, top_k)) {
+    if (use_fused(di, L, rows, bn, mult, top_k, kNv)) {
         if (cudaMemsetAsync(sync, 0, 2 * sizeof(uint32_t), st) != cudaSuccess) {
             cudaGetLastError();
             return DFLASH2_ERR_CUDA;
@@ -740,7 +837,7 @@ dflash2_status run_tc_topk(const DeviceInfo &di, const void *h, const void *lm_h
         launch_k(finalize_kernel<T>, (unsigned)rows, kSelThreads, fin_smem, st, cnt, cand,
                  (int)cap_keys, top_k, cand_ids, cand_u, err_word, static_cast<const T *>(h),
                  static_cast<const T *>(lm_head), hidden, draft_vocab, target_vocab, mult, cap,
-                 a_scale, w_scale);
+                 a_scale, w_scale, nvs);
         return launch_status();
     }
 
@@ -782,7 +879,7 @@ dflash2_status run_tc_topk(const DeviceInfo &di, const void *h, const void *lm_h
     launch_k(finalize_kernel<T>, (unsigned)rows, kSelThreads, fin_smem, st, cnt, cand,
              (int)cap_keys, top_k, cand_ids, cand_u, err_word, static_cast<const T *>(h),
              static_cast<const T *>(lm_head), hidden, draft_vocab, target_vocab, mult, cap,
-             a_scale, w_scale);
+             a_scale, w_scale, nvs);
     return launch_status();
 }
 
@@ -829,6 +926,12 @@ extern "C" int32_t dflash2_unary_topk_launches(int64_t rows, int64_t draft_vocab
 namespace {
 inline size_t fp8_ws_prefix(int64_t rows, int32_t hidden) {
     return align256((size_t)rows * hidden) + align256((size_t)rows * 4);
+}
+// The NVFP4 path's quantized activations at the workspace's start: codes
+// [rows][hidden / 2], block scales [rows][hidden / 16], g [rows].
+inline size_t nvfp4_ws_prefix(int64_t rows, int32_t hidden) {
+    return align256((size_t)rows * (hidden / 2)) + align256((size_t)rows * (hidden / 16)) +
+           align256((size_t)rows * 4);
 }
 }  // namespace
 
@@ -937,4 +1040,51 @@ extern "C" dflash2_status dflash2_unary_topk(const void *h, const void *lm_head,
     return run_tc_topk<__nv_bfloat16>(di, h, lm_head, nullptr, nullptr, rows, hidden, draft_vocab,
                                       target_vocab, mult, cap, top_k, cand_ids, cand_u,
                                       workspace, ws_bytes, err_word, st);
+}
+
+extern "C" size_t dflash2_unary_topk_nvfp4_workspace_size(int64_t rows, int32_t hidden,
+                                                          int64_t draft_vocab, int32_t top_k) {
+    if (rows <= 0 || hidden <= 0 || draft_vocab <= 0 || top_k <= 0) return 0;
+    return nvfp4_ws_prefix(rows, hidden) +
+           dflash2_unary_topk_workspace_size(rows, draft_vocab, top_k, DFLASH2_BF16);
+}
+
+extern "C" dflash2_status dflash2_unary_topk_nvfp4(
+    const void *h, int32_t h_dtype, const uint8_t *lm_head_q, const uint8_t *w_scales,
+    float w_global, int64_t rows, int32_t hidden, int64_t draft_vocab, int64_t target_vocab,
+    float mult, float cap, int32_t top_k, int64_t *cand_ids, float *cand_u, void *workspace,
+    size_t ws_bytes, int32_t *err_word, void *stream) {
+    if (h_dtype != DFLASH2_F32 && h_dtype != DFLASH2_BF16) return DFLASH2_ERR_UNSUPPORTED_DTYPE;
+    if (rows < 0 || rows > INT32_MAX || hidden <= 0 || hidden > kMaxHidden || hidden % 64 != 0 ||
+        draft_vocab <= 0 || draft_vocab > INT32_MAX || target_vocab <= 0 || top_k <= 0 ||
+        top_k > kMaxTopK || top_k > target_vocab || top_k > draft_vocab || !(cap >= 0.0f) ||
+        !(w_global > 0.0f) || !(w_global < INFINITY))
+        return DFLASH2_ERR_INVALID_ARG;
+    if (rows == 0) return DFLASH2_OK;
+    if (!h || !lm_head_q || !w_scales || !cand_ids || !cand_u) return DFLASH2_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(cand_ids) % 8 != 0 ||
+        reinterpret_cast<uintptr_t>(cand_u) % 4 != 0 ||
+        reinterpret_cast<uintptr_t>(w_scales) % 4 != 0 ||
+        reinterpret_cast<uintptr_t>(h) % (h_dtype == DFLASH2_BF16 ? 2 : 4) != 0)
+        return DFLASH2_ERR_MISALIGNED;
+    if (!aligned16(lm_head_q)) return DFLASH2_ERR_MISALIGNED;  // TMA rows of codes
+    const size_t prefix = nvfp4_ws_prefix(rows, hidden);
+    if (!workspace || ws_bytes < prefix) return DFLASH2_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return DFLASH2_ERR_MISALIGNED;
+    DeviceInfo di;
+    dflash2_status s = current_device(&di);
+    if (s != DFLASH2_OK) return s;
+    s = set_select_attrs(di.device);
+    if (s != DFLASH2_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint8_t *qh = ws;
+    uint8_t *sh = ws + align256((size_t)rows * (hidden / 2));
+    float *gh = reinterpret_cast<float *>(sh + align256((size_t)rows * (hidden / 16)));
+    s = launch_quant_rows_nvfp4(h, h_dtype, rows, hidden, qh, sh, gh, st);
+    if (s != DFLASH2_OK) return s;
+    NvScales nvs{sh, w_scales, w_global};
+    return run_tc_topk<E2M1x2>(di, qh, lm_head_q, gh, nullptr, rows, hidden, draft_vocab,
+                               target_vocab, mult, cap, top_k, cand_ids, cand_u, ws + prefix,
+                               ws_bytes - prefix, err_word, st, nvs);
 }

@@ -29,7 +29,7 @@ DEVERR_ID_RANGE = 0x1
 DEVERR_TIMEOUT = 0x2
 DEVERR_SHORT = 0x4
 DEVINFO_TOPK_FALLBACK = 0x100
-ABI_VERSION = 7
+ABI_VERSION = 8
 
 # Every symbol include/dflash2.h declares.
 EXPORTS = (
@@ -41,6 +41,8 @@ EXPORTS = (
     "dflash2_verify", "dflash2_selector_project", "dflash2_selector_walk_projected",
     "dflash2_unary_topk_launches", "dflash2_topk_merge", "dflash2_quantize_rows_e4m3",
     "dflash2_unary_topk_fp8_workspace_size", "dflash2_unary_topk_fp8",
+    "dflash2_quantize_rows_nvfp4", "dflash2_unary_topk_nvfp4_workspace_size",
+    "dflash2_unary_topk_nvfp4",
 )
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -111,6 +113,13 @@ def library():
         lib.dflash2_unary_topk_fp8.argtypes = [P, i32, P, P, i64, i32, i64, i64, f32, f32, i32, P,
                                                P, P, sz, P, P]
         lib.dflash2_unary_topk_fp8.restype = i32
+        lib.dflash2_quantize_rows_nvfp4.argtypes = [P, i64, i32, i32, P, P, P, P]
+        lib.dflash2_quantize_rows_nvfp4.restype = i32
+        lib.dflash2_unary_topk_nvfp4_workspace_size.argtypes = [i64, i32, i64, i32]
+        lib.dflash2_unary_topk_nvfp4_workspace_size.restype = sz
+        lib.dflash2_unary_topk_nvfp4.argtypes = [P, i32, P, P, f32, i64, i32, i64, i64, f32, f32,
+                                                 i32, P, P, P, sz, P, P]
+        lib.dflash2_unary_topk_nvfp4.restype = i32
         lib.dflash2_topk_merge.argtypes = [P, P, P, i32, i64, i32, i32, P, P, P, P]
         lib.dflash2_topk_merge.restype = i32
         lib.dflash2_unary_topk_launches.argtypes = [i64, i64, i32, f32, i32]
@@ -252,6 +261,59 @@ def unary_topk_fp8(h, lm_head_q, w_scale, target_vocab: int, mult: float, cap: f
     _check("dflash2_unary_topk_fp8", library().dflash2_unary_topk_fp8(
         _ptr(h), _dtype_code(h), _ptr(lm_head_q), _ptr(w_scale), rows, hidden, draft_vocab,
         target_vocab, float(mult), float(cap), top_k, _ptr(cand_ids), _ptr(cand_u),
+        _ptr(workspace), workspace.numel(), _ptr(err), _stream(stream)))
+    return cand_ids, cand_u, err
+
+
+def quantize_rows_nvfp4(x, codes=None, scales=None, g=None, stream=None):
+    """dflash2_quantize_rows_nvfp4: per-row NVFP4 codes (uint8, two per byte),
+    E4M3 block scales (uint8, one per 16 elements) and fp32 second-level
+    scales of x."""
+    rows, cols = x.shape
+    _need(x, "x")
+    dev = x.device
+    if codes is None:
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev)
+    if g is None:
+        g = torch.empty(rows, dtype=torch.float32, device=dev)
+    _check("dflash2_quantize_rows_nvfp4", library().dflash2_quantize_rows_nvfp4(
+        _ptr(x), rows, cols, _dtype_code(x), _ptr(codes), _ptr(scales), _ptr(g),
+        _stream(stream)))
+    return codes, scales, g
+
+
+def unary_topk_nvfp4_workspace_size(rows: int, hidden: int, draft_vocab: int, top_k: int) -> int:
+    return int(library().dflash2_unary_topk_nvfp4_workspace_size(rows, hidden, draft_vocab,
+                                                                 top_k))
+
+
+def unary_topk_nvfp4(h, lm_head_q, w_scales, w_global: float, target_vocab: int, mult: float,
+                     cap: float, top_k: int, cand_ids=None, cand_u=None, workspace=None, err=None,
+                     stream=None):
+    """dflash2_unary_topk_nvfp4: top_k (ids, u) per row of h against an NVFP4
+    head (lm_head_q uint8 [draft_vocab, hidden / 2] codes, w_scales uint8
+    [draft_vocab, hidden / 16] E4M3 block scales, w_global its fp32 scale)."""
+    rows, hidden = h.shape
+    draft_vocab = lm_head_q.shape[0]
+    _need(h, "h")
+    _need(lm_head_q, "lm_head_q", torch.uint8, (draft_vocab, hidden // 2))
+    _need(w_scales, "w_scales", torch.uint8, (draft_vocab, hidden // 16))
+    dev = h.device
+    if cand_ids is None:
+        cand_ids = torch.empty((rows, top_k), dtype=torch.int64, device=dev)
+    if cand_u is None:
+        cand_u = torch.empty((rows, top_k), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(1, unary_topk_nvfp4_workspace_size(rows, hidden, draft_vocab,
+                                                                       top_k)),
+                                dtype=torch.uint8, device=dev)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check("dflash2_unary_topk_nvfp4", library().dflash2_unary_topk_nvfp4(
+        _ptr(h), _dtype_code(h), _ptr(lm_head_q), _ptr(w_scales), float(w_global), rows, hidden,
+        draft_vocab, target_vocab, float(mult), float(cap), top_k, _ptr(cand_ids), _ptr(cand_u),
         _ptr(workspace), workspace.numel(), _ptr(err), _stream(stream)))
     return cand_ids, cand_u, err
 

@@ -24,7 +24,8 @@ from dataclasses import dataclass, replace
 import numpy as np
 
 PARTS = ("x", "base", "delta", "h", "lm_head", "A", "B", "proj", "uniforms",
-         "d2t", "anchors", "w_kp", "base2", "lm_head_fp8", "w_scale")
+         "d2t", "anchors", "w_kp", "base2", "lm_head_fp8", "w_scale", "lm_head_nvfp4",
+         "w_scales_nvfp4")
 
 
 @dataclass(frozen=True)
@@ -148,6 +149,13 @@ DEFAULT_PARTS = PARTS[:11]  # the proposal step's inputs; w_kp / base2 feed the 
                             # lm_head_fp8 / w_scale the FP8 head
 
 
+def nvfp4_w_global(w: Workload) -> float:
+    """The tensor scale of the synthetic NVFP4 head: uniform codes have an rms
+    of about 3.2 and the block scales about 1, so the weights' rms is about
+    w_std."""
+    return float(w.w_std / 3.2)
+
+
 def make(w: Workload, parts=DEFAULT_PARTS) -> dict:
     """Draw the requested parts of a workload.  Floating parts are float32 for
     "f32" workloads and uint16 bf16 bits for "bf16" workloads."""
@@ -185,6 +193,15 @@ def make(w: Workload, parts=DEFAULT_PARTS) -> dict:
             # per-row dequantization scales: scale * code ~ N(0, w_std^2)
             out[p] = (rng(s, p).uniform(0.5, 1.5, size=w.draft_vocab)
                       * (w.w_std / 64.0)).astype(np.float32)
+        elif p == "lm_head_nvfp4":
+            # an NVFP4 checkpoint of the head: uniformly drawn E2M1 code bytes
+            # (two codes each) [draft_vocab, hidden / 2] ...
+            out[p] = rng(s, p).integers(0, 256, size=(w.draft_vocab, w.hidden // 2),
+                                        dtype=np.uint8)
+        elif p == "w_scales_nvfp4":
+            # ... and their E4M3 block scales, one per 16 elements, in [0.5, 1.5]
+            out[p] = fp8_codes(rng(s, p).uniform(0.5, 1.5, size=(w.draft_vocab, w.hidden // 16))
+                               .astype(np.float32))
         elif p == "anchors":
             hi = min(w.draft_vocab, w.target_vocab)
             out[p] = rng(s, p).integers(0, hi, size=w.batch, dtype=np.int64)

@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define DFLASH2_ABI_VERSION 7
+#define DFLASH2_ABI_VERSION 8
 
 typedef enum {
     DFLASH2_OK = 0,
@@ -199,6 +199,62 @@ dflash2_status dflash2_unary_topk_fp8(const void *h, int32_t h_dtype, const uint
                                       float cap, int32_t top_k, int64_t *cand_ids, float *cand_u,
                                       void *workspace, size_t ws_bytes, int32_t *err_word,
                                       void *stream);
+
+/*
+ * NVFP4 lm_head: the unary candidates of an NVFP4 head checkpoint (the vLLM
+ * DSpark review's padded-vocab draft ships one; the sglang DFlash2 PR lets a
+ * quantized head fall back to its eager path).  W4A4 on the block-scaled
+ * tensor cores (tcgen05.mma kind::mxf4nvf4, scale_vec::4X, CTA pairs):
+ *
+ *   E2M1 element: sign, 2 exponent bits (bias 1), 1 mantissa bit; magnitudes
+ *     0, 0.5, 1, 1.5, 2, 3, 4, 6.  Two codes per byte, element 2i in the low
+ *     nibble.  Every 16 consecutive elements along hidden share one E4M3
+ *     scale (non-negative).
+ *   activations, per row m of h (dflash2_quantize_rows_nvfp4), in fp32:
+ *     amax = max_j |h[m, j]|, enc = 2688 / amax, g_h[m] = amax / 2688
+ *     (2688 = 6 * 448; a row of zeros: enc = g_h = 1);
+ *     block b: a_b = max |h| over its 16 elements, s_b = E4M3((a_b / 6) * enc);
+ *     codes E2M1(h[m, j] * (enc / dec(s_b))) (round to nearest even,
+ *     saturating at 6), all 0 when s_b is 0.
+ *   weights: codes lm_head_q, scales w_scales, one fp32 w_global, quantized
+ *     the same way with the amax of the whole tensor (a checkpoint's format).
+ *   z[m, v] = g_h[m] * w_global * sum_b dec(s_h[m, b]) * dec(w_scales[v, b])
+ *             * sum_{j in b} dec(q_h[m, j]) * dec(lm_head_q[v, j])
+ *   then the transform, the padded-vocab mask and the top-K of
+ *   dflash2_unary_topk.
+ *
+ * dflash2_quantize_rows_nvfp4: x device [rows, cols] (dtype f32 or bf16),
+ *   cols % 16 == 0 -> codes device uint8 [rows, cols / 2] (8-byte aligned),
+ *   scales device uint8 [rows, cols / 16], g device float [rows].
+ *   Errors: dtype -> UNSUPPORTED_DTYPE; rows outside [0, 2^31), cols < 1 or
+ *   not a multiple of 16, or a null pointer -> INVALID_ARG; x, codes or g
+ *   misaligned -> MISALIGNED.  rows == 0 queues nothing.
+ * dflash2_unary_topk_nvfp4: h device [rows, hidden] (h_dtype f32 or bf16);
+ *   lm_head_q device uint8 [draft_vocab, hidden / 2], 16-byte aligned;
+ *   w_scales device uint8 [draft_vocab, hidden / 16], 4-byte aligned;
+ *   w_global > 0 and finite; hidden % 64 == 0; the other arguments as for
+ *   dflash2_unary_topk.  workspace device, 256-byte aligned, ws_bytes >=
+ *   dflash2_unary_topk_nvfp4_workspace_size(rows, hidden, draft_vocab,
+ *   top_k): the activation codes, scales and g, then a dflash2_unary_topk
+ *   workspace.  Queues the quantization kernel, then the pair GEMM (fused
+ *   with the select, or pilot, select and filter passes) and the final top-K.
+ *   Errors as for dflash2_unary_topk, plus INVALID_ARG for hidden % 64 != 0 or
+ *   a bad w_global, MISALIGNED for lm_head_q or w_scales.
+ * Arithmetic: exact products of codes, summed per 16-element block and
+ *   scaled by the two block scales in the tensor cores (fp32 accumulation),
+ *   then z = acc * (g_h[m] * w_global) in fp32.
+ */
+dflash2_status dflash2_quantize_rows_nvfp4(const void *x, int64_t rows, int32_t cols,
+                                           int32_t dtype, uint8_t *codes, uint8_t *scales,
+                                           float *g, void *stream);
+size_t dflash2_unary_topk_nvfp4_workspace_size(int64_t rows, int32_t hidden, int64_t draft_vocab,
+                                               int32_t top_k);
+dflash2_status dflash2_unary_topk_nvfp4(const void *h, int32_t h_dtype, const uint8_t *lm_head_q,
+                                        const uint8_t *w_scales, float w_global, int64_t rows,
+                                        int32_t hidden, int64_t draft_vocab, int64_t target_vocab,
+                                        float mult, float cap, int32_t top_k, int64_t *cand_ids,
+                                        float *cand_u, void *workspace, size_t ws_bytes,
+                                        int32_t *err_word, void *stream);
 
 /*
  * Selector lattice and walk.
