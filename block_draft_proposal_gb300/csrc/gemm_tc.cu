@@ -248,7 +248,28 @@ constexpr int kPairThreads = 64 + 32 * kPairEpiWarps;  // producer, MMA issuer, 
 constexpr int kPairThreadsNv = kPairThreads + 128;
 constexpr uint32_t kSfBase = 256;
 constexpr uint32_t kSfCols = 64;
-constexpr int kNvMaxStages = (512 - kSfBase) / kSfCols;
+constexpr int kNvStages = 3;                 // operand stages, TMEM scale slots and
+constexpr int kNvMaxStages = kNvStages;      // shared scale slots of the nvfp4 kernel
+constexpr uint32_t kNvSfStageBytes = 256 * 32;  // 128 weight rows + 128 tokens, 32 bytes each
+static_assert(kSfBase + kNvStages * kSfCols <= 512, "TMEM columns");
+
+// cp.async copies of 16 or 4 bytes (valid == false: zero-filled, nothing read)
+__device__ __forceinline__ void cpa16_zfill(void *smem, const void *gmem, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)), "l"(gmem),
+                 "r"(valid ? 16u : 0u)
+                 : "memory");
+}
+__device__ __forceinline__ void cpa4_zfill(void *smem, const void *gmem, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(smem)), "l"(gmem),
+                 "r"(valid ? 4u : 0u)
+                 : "memory");
+}
+__device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cpa_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Named barrier 1 of the four nvfp4 scale-loader warps.
+__device__ __forceinline__ void sf_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // Moves the buffered survivors to their rows' candidate lists: one global
 // atomic per survivor, issued by all lanes together.
@@ -738,68 +759,136 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NV ? kPairThreadsNv 
             }
         }
     } else if (NV && warp >= 2 + kPairEpiWarps) {
-        // nvfp4 scale loaders.  For every stage: the scales of this CTA's 128
-        // weight rows (the warp's lane quarter: one 32-bit cell of 4 scales
-        // per MMA, at column 4i + quarter) and of every token of the tile
-        // (columns 32 + 4i + token / 32, in each quarter), written into the
-        // stage's TMEM columns once the stage's previous MMAs are done; then
-        // an arrival on the leader's sf_full barrier.  Scales past a row's
-        // end, and of rows or tokens outside the problem, are zero (their
-        // codes are zero too).
+        // nvfp4 scale loaders (4 warps, 128 threads).  For every stage they
+        // stage in shared memory, by cp.async kNvStages - 1 stages ahead, the
+        // scales of this CTA's 128 weight rows (32 bytes each: one 4-scale
+        // cell per MMA) and of every token of the tile (each CTA holds them
+        // all), then, once the stage's previous MMAs are done, write them into
+        // the stage's TMEM columns: a weight row's cells at columns 4i +
+        // quarter of its own lane, a token's at 32 + 4i + token / 32 of lane
+        // 32 * quarter + token % 32, in every quarter; then arrive on the
+        // leader's sf_full barrier.  Rows and tokens outside the problem, and
+        // scales past a row's end, are zero (their codes are zero too).
         const int q = warp & 3;  // the TMEM lane quarter this warp may access
+        const int sft = (int)threadIdx.x - 32 * (2 + kPairEpiWarps);  // 0 .. 127
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const uint32_t sf_full_leader = mapa_shared(smem_u32(&sf_full[0]), 0);
-        uint32_t s = 0, ph = 1;  // the first pass finds every stage free
-        bool ok = true;
-        for (int w = pair; w < total && ok; w += npairs) {
-            const Item item = decode(p, w);
-            const int64_t vrow =
-                (int64_t)item.wt * p.unit + (int64_t)rank * kGemmTileW + q * 32 + lane;
-            const uint8_t *wsrc = vrow < p.rows_w ? p.sfw + vrow * p.n_sf : nullptr;
-            const uint8_t *hsrc[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int c = 32 * j + lane;
-                const int64_t m = (int64_t)item.nt * p.bn + c;
-                hsrc[j] = c < p.bn && m < p.rows_h ? p.sfh + m * p.n_sf : nullptr;
+        uint8_t *sf_smem = smem + p.sf_off;
+        const bool wide = (p.n_sf % 16) == 0 &&
+                          (reinterpret_cast<uintptr_t>(p.sfw) | reinterpret_cast<uintptr_t>(p.sfh)) %
+                                  16 == 0;
+        // the stage sequence of this CTA pair, as the producer and MMA see it
+        struct Seq {
+            int w, kb, kb1;
+            Item item;
+        };
+        const auto seq_start = [&](Seq &q_) {
+            q_.w = pair;
+            q_.kb = q_.kb1 = 0;
+            if (q_.w < total) {
+                q_.item = decode(p, q_.w);
+                q_.kb = q_.item.ks * p.kb_per_split;
+                q_.kb1 = min(p.num_kb, q_.kb + p.kb_per_split);
             }
-            const int kb0 = item.ks * p.kb_per_split;
-            const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
-            for (int kb = kb0; kb < kb1; ++kb) {
-                // the loads first: they touch no TMEM, so they overlap the wait
-                uint32_t a[8], b[4][8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int blk = kb * 32 + 4 * i;
-                    const bool in = blk < p.n_sf;
-                    a[i] = wsrc && in ? __ldg(reinterpret_cast<const uint32_t *>(wsrc + blk)) : 0u;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        b[j][i] = hsrc[j] && in
-                                      ? __ldg(reinterpret_cast<const uint32_t *>(hsrc[j] + blk))
-                                      : 0u;
+        };
+        const auto seq_next = [&](Seq &q_) {
+            if (++q_.kb < q_.kb1) return;
+            q_.w += npairs;
+            if (q_.w < total) {
+                q_.item = decode(p, q_.w);
+                q_.kb = q_.item.ks * p.kb_per_split;
+                q_.kb1 = min(p.num_kb, q_.kb + p.kb_per_split);
+            }
+        };
+        // copies of one stage's scales into ring slot `slot`: 256 rows of 32
+        // bytes (128 weight rows, then 128 token columns of the tile)
+        const auto issue = [&](const Seq &q_, int slot) {
+            uint8_t *dst = sf_smem + (size_t)slot * kNvSfStageBytes;
+            const int blk0 = q_.kb * 32;
+            const int64_t vbase = (int64_t)q_.item.wt * p.unit + (int64_t)rank * kGemmTileW;
+            const int64_t mbase = (int64_t)q_.item.nt * p.bn;
+            const int chunk = wide ? 16 : 4, per_row = 32 / chunk;
+            for (int c = sft; c < 256 * per_row; c += 128) {
+                const int r = c / per_row, off = (c - r * per_row) * chunk;
+                const uint8_t *src = nullptr;
+                if (r < 128) {
+                    const int64_t v = vbase + r;
+                    if (v < p.rows_w) src = p.sfw + v * p.n_sf;
+                } else {
+                    const int64_t m = mbase + (r - 128);
+                    if (r - 128 < p.bn && m < p.rows_h) src = p.sfh + m * p.n_sf;
                 }
-                if (!mbar_wait(&empty_bar[s], ph, &abort_flag, p.err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t col = tmem + lane_base + kSfBase + s * kSfCols;
+                const bool ok = src != nullptr && blk0 + off < p.n_sf;
+                const uint8_t *g = ok ? src + blk0 + off : p.sfw;
+                if (wide)
+                    cpa16_zfill(dst + r * 32 + off, g, ok);
+                else
+                    cpa4_zfill(dst + r * 32 + off, g, ok);
+            }
+        };
+        Seq fetch, cur;
+        seq_start(fetch);
+        seq_start(cur);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) tmem_st1(col + 4u * (uint32_t)i + (uint32_t)q, a[i]);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    tmem_st4(col + 32u + 4u * (uint32_t)i, b[0][i], b[1][i], b[2][i], b[3][i]);
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(sf_full_leader + 8u * s);
-                if (++s == (uint32_t)p.stages) {
+        for (int t = 0; t < kNvStages - 1; ++t) {
+            if (fetch.w < total) {
+                issue(fetch, t);
+                seq_next(fetch);
+            }
+            cpa_commit();
+        }
+        // Every loader runs the same number of iterations whatever happens, so
+        // the named barriers always meet: after a failed (timed-out) wait a
+        // warp only keeps the barriers and copies going.
+        uint32_t s = 0, ph = 1;  // the first pass finds every TMEM slot free
+        bool ok = true;
+        for (int g = 0; cur.w < total; ++g, seq_next(cur)) {
+            sf_bar_sync();  // every loader is done reading the slot refilled now
+            if (fetch.w < total) {
+                issue(fetch, (g + kNvStages - 1) % kNvStages);
+                seq_next(fetch);
+            }
+            cpa_commit();
+            cpa_wait<kNvStages - 1>();  // this thread's copies of stage g landed
+            sf_bar_sync();              // and everyone's
+            if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&empty_bar[s], ph, &abort_flag, p.err));
+            if (!ok) {
+                if (++s == (uint32_t)kNvStages) {
                     s = 0;
                     ph ^= 1u;
                 }
+                continue;
+            }
+            tc_fence_after();
+            const uint8_t *src = sf_smem + (size_t)s * kNvSfStageBytes;
+            const uint4 a0 = *reinterpret_cast<const uint4 *>(src + (q * 32 + lane) * 32);
+            const uint4 a1 = *reinterpret_cast<const uint4 *>(src + (q * 32 + lane) * 32 + 16);
+            const uint32_t col = tmem + lane_base + kSfBase + s * kSfCols;
+            const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) tmem_st1(col + 4u * (uint32_t)i + (uint32_t)q, aw[i]);
+            uint32_t bw[4][8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint8_t *tr = src + (128 + 32 * j + lane) * 32;
+                const uint4 b0 = *reinterpret_cast<const uint4 *>(tr);
+                const uint4 b1 = *reinterpret_cast<const uint4 *>(tr + 16);
+                bw[j][0] = b0.x; bw[j][1] = b0.y; bw[j][2] = b0.z; bw[j][3] = b0.w;
+                bw[j][4] = b1.x; bw[j][5] = b1.y; bw[j][6] = b1.z; bw[j][7] = b1.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                tmem_st4(col + 32u + 4u * (uint32_t)i, bw[0][i], bw[1][i], bw[2][i], bw[3][i]);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(sf_full_leader + 8u * s);
+            if (++s == (uint32_t)kNvStages) {
+                s = 0;
+                ph ^= 1u;
             }
         }
+        cpa_wait<0>();  // no copy still landing when the CTA leaves
     } else {
         const int quarter = warp & 3;  // TMEM lanes this warp may access
         const int row_in_unit = (int)rank * kGemmTileW + quarter * 32 + lane;
@@ -1026,10 +1115,18 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
                                  : 0;
     int stages = (int)((kGemmSmemBytes - 1024 - epi_bytes) / stage_bytes);
     if (stages > kGemmMaxStages) stages = kGemmMaxStages;
-    if (nv && stages > kNvMaxStages) stages = kNvMaxStages;  // the scale columns of TMEM
+    if (nv) {
+        // the TMEM scale columns and the shared scale ring hold kNvStages
+        stages = (int)((kGemmSmemBytes - 1024 - epi_bytes - kNvStages * kNvSfStageBytes) /
+                       stage_bytes);
+        if (stages < kNvStages) return DFLASH2_ERR_INVALID_ARG;
+        stages = kNvStages;
+    }
     if (stages < 2) return DFLASH2_ERR_INVALID_ARG;  // bn <= 256 always leaves room for two
     p.stages = stages;
-    const size_t smem = (size_t)stages * stage_bytes + epi_bytes + 1024;
+    p.sf_off = (int32_t)((size_t)stages * stage_bytes + epi_bytes);  // after the epilogue scratch
+    const size_t smem = (size_t)stages * stage_bytes + epi_bytes +
+                        (nv ? (size_t)kNvStages * kNvSfStageBytes : 0) + 1024;
 
     CUtensorMap tm_w, tm_h;
     const uint32_t eb = (p.fp8 || nv) ? 1 : 2;

@@ -91,6 +91,7 @@ struct GemmParams {
     const uint8_t *sfw;
     const uint8_t *sfh;
     float w_global;
+    int32_t sf_off;  // the scale ring's offset in dynamic shared memory (filled by launch_gemm_tc)
 };
 
 // Pilot tiling of a weight matrix with n_wtiles units of unit_rows rows:
