@@ -7,7 +7,8 @@ C ABI (dflash2.proposal_step, the input-only work on a second stream beside
 the top-K), replayed from one captured CUDA graph.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload NAME] [--stage conv|unary_topk|projection|walk]
+                    [--workload NAME] [--stage conv|unary_topk|unary_topk_fp8|
+                                               unary_topk_nvfp4|projection|walk]
 
 The default workload is the largest one-GPU configuration, the large-batch,
 large-K stress draft (batch 512, block 16, hidden 7168 = 896 groups x 8, taps
@@ -746,6 +747,8 @@ def run_stage(args, w):
     torch.cuda.set_device(dev)
     parts = {"conv": ("x", "base", "delta"),
              "unary_topk": ("h", "lm_head"),
+             "unary_topk_fp8": ("h", "lm_head_fp8", "w_scale"),
+             "unary_topk_nvfp4": ("h", "lm_head_nvfp4", "w_scales_nvfp4"),
              "projection": ("h", "proj"),
              "walk": ("h", "A", "B", "proj", "uniforms", "anchors")}[args.stage]
     inp = synth.make(w, parts=parts)
@@ -768,6 +771,27 @@ def run_stage(args, w):
         fn = lambda: dflash2.unary_topk(t["h"], t["lm_head"], w.target_vocab, w.mult, w.cap,
                                         w.top_k, cand_ids=ids, cand_u=u, workspace=ws, err=err,
                                         stream=st)
+        amount, unit = work["gemm_flops"], "TFLOP/s"
+    elif args.stage in ("unary_topk_fp8", "unary_topk_nvfp4"):
+        ids = torch.empty((w.rows, w.top_k), dtype=torch.int64, device=dev)
+        u = torch.empty((w.rows, w.top_k), dtype=torch.float32, device=dev)
+        if args.stage == "unary_topk_fp8":
+            ws = torch.empty(dflash2.unary_topk_fp8_workspace_size(w.rows, w.hidden, w.draft_vocab,
+                                                                   w.top_k),
+                             dtype=torch.uint8, device=dev)
+            fn = lambda: dflash2.unary_topk_fp8(t["h"], t["lm_head_fp8"], t["w_scale"],
+                                                w.target_vocab, w.mult, w.cap, w.top_k,
+                                                cand_ids=ids, cand_u=u, workspace=ws, err=err,
+                                                stream=st)
+        else:
+            ws = torch.empty(dflash2.unary_topk_nvfp4_workspace_size(w.rows, w.hidden,
+                                                                     w.draft_vocab, w.top_k),
+                             dtype=torch.uint8, device=dev)
+            g4 = synth.nvfp4_w_global(w)
+            fn = lambda: dflash2.unary_topk_nvfp4(t["h"], t["lm_head_nvfp4"], t["w_scales_nvfp4"],
+                                                  g4, w.target_vocab, w.mult, w.cap, w.top_k,
+                                                  cand_ids=ids, cand_u=u, workspace=ws, err=err,
+                                                  stream=st)
         amount, unit = work["gemm_flops"], "TFLOP/s"
     else:
         ws = torch.empty(dflash2.selector_walk_workspace_size(w.batch, w.slots, w.hidden, w.rank,
@@ -821,7 +845,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--stage", choices=["conv", "unary_topk", "projection", "walk"],
+    ap.add_argument("--stage", choices=["conv", "unary_topk", "unary_topk_fp8", "unary_topk_nvfp4",
+                                        "projection", "walk"],
                     help="time one stage alone (one GPU) instead of the whole step")
     args = ap.parse_args()
     if args.warmup < 3:
