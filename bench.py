@@ -569,7 +569,8 @@ def run_gpu(args, w):
         if w.hidden % 64 == 0:
             nq = synth.make(w, parts=("lm_head_nvfp4", "w_scales_nvfp4"))
             t_q4 = dflash2.to_device(nq["lm_head_nvfp4"], dev)
-            t_s4 = dflash2.to_device(nq["w_scales_nvfp4"], dev)
+            t_s4 = dflash2.nvfp4_tile_scales(dflash2.to_device(nq["w_scales_nvfp4"], dev),
+                                             w.hidden)
             g4 = synth.nvfp4_w_global(w)
             del nq
             n_ws = torch.empty(dflash2.unary_topk_nvfp4_workspace_size(w.rows, w.hidden,
@@ -788,7 +789,8 @@ def run_stage(args, w):
                                                                      w.draft_vocab, w.top_k),
                              dtype=torch.uint8, device=dev)
             g4 = synth.nvfp4_w_global(w)
-            fn = lambda: dflash2.unary_topk_nvfp4(t["h"], t["lm_head_nvfp4"], t["w_scales_nvfp4"],
+            tiles4 = dflash2.nvfp4_tile_scales(t["w_scales_nvfp4"], w.hidden)
+            fn = lambda: dflash2.unary_topk_nvfp4(t["h"], t["lm_head_nvfp4"], tiles4,
                                                   g4, w.target_vocab, w.mult, w.cap, w.top_k,
                                                   cand_ids=ids, cand_u=u, workspace=ws, err=err,
                                                   stream=st)

@@ -72,6 +72,8 @@ dflash2_status encode_tmap_bf16(CUtensorMap *map, const void *base, uint64_t row
                                 uint64_t cols, uint32_t box_rows);
 // The same for 1-byte (elem_bytes = 1, uint8 codes) or bf16 (2) elements: the
 // box is one 128-byte swizzle row wide (128 / elem_bytes columns).
+dflash2_status encode_tmap_bytes_2d(CUtensorMap *map, const void *base, uint64_t rows,
+                                    uint64_t cols, uint32_t box_cols, uint32_t box_rows);
 dflash2_status encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                               uint32_t box_rows, uint32_t elem_bytes);
 

@@ -242,34 +242,34 @@ constexpr int kPairEpiWarps = 8;          // CTA pairs: two warps per TMEM lane 
 constexpr int kPairEpiCols = 128;         // each on half of the tile's columns
 using EpiScratchPair = EpiScratchT<kPairEpiCols>;
 constexpr int kPairThreads = 64 + 32 * kPairEpiWarps;  // producer, MMA issuer, epilogue
-// nvfp4: four more warps per CTA load the block scales into TMEM, whose
-// columns hold the two accumulators (<= 128 columns each) and then 64 scale
-// columns per stage: 32 for the weight rows (4 per MMA) and 32 for the tokens.
-constexpr int kPairThreadsNv = kPairThreads + 128;
+// nvfp4: TMEM holds the two accumulators (<= 128 columns each) and then 64
+// scale columns per stage: 32 for the weight rows (4 per MMA) and 32 for
+// the tokens.  A stage's scales come with its operands: the producer's TMA
+// copies 8 scale tiles of each side (4 KB) into the stage's shared scale
+// slot, and the MMA warp moves them into TMEM with tcgen05.cp ahead of the
+// stage's MMAs, in issue order with them.  (Scale-loader warps that wrote
+// TMEM themselves made every stage wait for a software round trip: 0.52 ms
+// against 0.37 for bf16 at the Qwen3-8B size.)
 constexpr uint32_t kSfBase = 256;
 constexpr uint32_t kSfCols = 64;
-constexpr int kNvStages = 3;                 // operand stages, TMEM scale slots and
-constexpr int kNvMaxStages = kNvStages;      // shared scale slots of the nvfp4 kernel
-constexpr uint32_t kNvSfStageBytes = 256 * 32;  // 128 weight rows + 128 tokens, 32 bytes each
+constexpr int kNvStages = 3;                    // operand stages and TMEM scale slots
+constexpr uint32_t kNvSfStageBytes = 2 * 4096;  // 8 tiles of weight-row and of token scales
 static_assert(kSfBase + kNvStages * kSfCols <= 512, "TMEM columns");
 
-// cp.async copies of 16 or 4 bytes (valid == false: zero-filled, nothing read)
-__device__ __forceinline__ void cpa16_zfill(void *smem, const void *gmem, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)), "l"(gmem),
-                 "r"(valid ? 16u : 0u)
+// One 512-byte scale tile (32 rows x 16 bytes, no swizzle: core matrices of
+// 8 rows x 16 bytes, 128 bytes apart) from shared memory into TMEM columns
+// taddr .. taddr + 3 of every lane quarter, on both CTAs of the pair (each
+// from its own shared memory at the same offset).  Measured on GB300 to give
+// the layout the block-scaled MMA reads.
+__device__ __forceinline__ void tc_cp_sf_pair(uint32_t taddr, uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128 >> 4) << 16;  // leading byte offset
+    d |= (uint64_t)(128 >> 4) << 32;  // stride byte offset: 8 rows x 16 bytes
+    d |= (uint64_t)1 << 46;           // descriptor version for the sm_100 family
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d)
                  : "memory");
 }
-__device__ __forceinline__ void cpa4_zfill(void *smem, const void *gmem, bool valid) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(smem)), "l"(gmem),
-                 "r"(valid ? 4u : 0u)
-                 : "memory");
-}
-__device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N> __device__ __forceinline__ void cpa_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-// Named barrier 1 of the four nvfp4 scale-loader warps.
-__device__ __forceinline__ void sf_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // Moves the buffered survivors to their rows' candidate lists: one global
 // atomic per survivor, issued by all lanes together.
@@ -600,16 +600,17 @@ __global__ void __launch_bounds__(192, 1)
 // TMEM lanes) arrive on the leader's accumulator-empty barrier.
 // ---------------------------------------------------------------------------
 template <bool NV>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NV ? kPairThreadsNv : kPairThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tm_w,
-                        const __grid_constant__ CUtensorMap tm_h, const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tm_h,
+                        const __grid_constant__ CUtensorMap tm_sfw,
+                        const __grid_constant__ CUtensorMap tm_sfh, const GemmParams p) {
     extern __shared__ uint8_t dsmem[];
     __shared__ uint64_t full_bar[kGemmMaxStages];
     __shared__ uint64_t empty_bar[kGemmMaxStages];
     __shared__ uint64_t acc_full[2];
     __shared__ uint64_t acc_empty[2];
     __shared__ uint64_t drain_bar;
-    __shared__ uint64_t sf_full[NV ? kNvMaxStages : 1];  // nvfp4: a stage's scales are in TMEM
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -639,8 +640,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NV ? kPairThreadsNv 
             mbar_init(&acc_empty[a], 2 * kPairEpiWarps);  // every epilogue warp of the pair
         }
         mbar_init(&drain_bar, 1);
-        if (NV)
-            for (int s = 0; s < p.stages; ++s) mbar_init(&sf_full[s], 8);  // 4 warps x 2 CTAs
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -684,7 +683,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NV ? kPairThreadsNv 
                         break;
                     }
                     const uint32_t fb = mapa_shared(smem_u32(&full_bar[s]), 0);
-                    if (leader) mbar_arrive_expect_tx(&full_bar[s], 2 * (kWStageBytes + h_stage));
+                    if (leader)
+                        mbar_arrive_expect_tx(&full_bar[s], 2 * (kWStageBytes + h_stage +
+                                                                 (NV ? kNvSfStageBytes : 0u)));
                     uint8_t *ws = w_smem + s * kWStageBytes;
                     uint8_t *hs = h_smem + s * h_stage;
                     const int k0 = kb * 2 * p.box_k;  // boxes past `hidden` read zeros
@@ -692,6 +693,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NV ? kPairThreadsNv 
                     tma_load_2d_pair(ws + kWTileBytes, &tm_w, fb, k0 + p.box_k, wrow);
                     tma_load_2d_pair(hs, &tm_h, fb, k0, hrow);
                     tma_load_2d_pair(hs + h_sub, &tm_h, fb, k0 + p.box_k, hrow);
+                    if (NV) {
+                        // the stage's 8 scale tiles of this CTA's 128 weight rows and of
+                        // the tile's tokens (rows of 256 bytes in the tensor maps)
+                        uint8_t *sfs = smem + p.sf_off + (size_t)s * kNvSfStageBytes;
+                        const int yw = 2 * ((item.wt * 2 + (int)rank) * p.sf_nw8 + kb * 8);
+                        const int yh = 2 * (item.nt * p.sf_nw8 + kb * 8);
+                        tma_load_2d_pair(sfs, &tm_sfw, fb, 0, yw);
+                        tma_load_2d_pair(sfs + 4096, &tm_sfh, fb, 0, yh);
+                    }
                     ++issued;
                     if (++s == (uint32_t)p.stages) {
                         s = 0;
@@ -729,15 +739,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NV ? kPairThreadsNv 
                         ok = false;
                         break;
                     }
-                    if (NV && !mbar_wait(&sf_full[s], ph, &abort_flag, p.err)) {
-                        ok = false;
-                        break;
-                    }
                     tc_fence_after();
-                    if (NV)
+                    if (NV) {
+                        // the stage's scales into its TMEM slot, then its MMAs (in order;
+                        // the slot's previous MMAs finished before this stage's loads began)
+                        const uint32_t sft = tmem + kSfBase + s * kSfCols;
+                        const uint32_t sfs = smem_u32(smem + p.sf_off) + s * kNvSfStageBytes;
+#pragma unroll
+                        for (int m = 0; m < 8; ++m) {
+                            tc_cp_sf_pair(sft + 4u * (uint32_t)m, sfs + 512u * (uint32_t)m);
+                            tc_cp_sf_pair(sft + 32u + 4u * (uint32_t)m,
+                                          sfs + 4096u + 512u * (uint32_t)m);
+                        }
                         mma_stage_nvfp4_pair(d_tmem, wd0 + s * w_st, hd0 + s * h_st, w_sub, h_sb,
-                                             idesc, kb > kb0 ? 1u : 0u,
-                                             tmem + kSfBase + s * kSfCols);
+                                             idesc, kb > kb0 ? 1u : 0u, sft);
+                    }
                     else if (p.fp8)
                         mma_stage_f8_pair(d_tmem, wd0 + s * w_st, hd0 + s * h_st, w_sub, h_sb,
                                           idesc, kb > kb0 ? 1u : 0u);
@@ -758,137 +774,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NV ? kPairThreadsNv 
                 mbar_wait_drain(&drain_bar, 0);
             }
         }
-    } else if (NV && warp >= 2 + kPairEpiWarps) {
-        // nvfp4 scale loaders (4 warps, 128 threads).  For every stage they
-        // stage in shared memory, by cp.async kNvStages - 1 stages ahead, the
-        // scales of this CTA's 128 weight rows (32 bytes each: one 4-scale
-        // cell per MMA) and of every token of the tile (each CTA holds them
-        // all), then, once the stage's previous MMAs are done, write them into
-        // the stage's TMEM columns: a weight row's cells at columns 4i +
-        // quarter of its own lane, a token's at 32 + 4i + token / 32 of lane
-        // 32 * quarter + token % 32, in every quarter; then arrive on the
-        // leader's sf_full barrier.  Rows and tokens outside the problem, and
-        // scales past a row's end, are zero (their codes are zero too).
-        const int q = warp & 3;  // the TMEM lane quarter this warp may access
-        const int sft = (int)threadIdx.x - 32 * (2 + kPairEpiWarps);  // 0 .. 127
-        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        const uint32_t sf_full_leader = mapa_shared(smem_u32(&sf_full[0]), 0);
-        uint8_t *sf_smem = smem + p.sf_off;
-        const bool wide = (p.n_sf % 16) == 0 &&
-                          (reinterpret_cast<uintptr_t>(p.sfw) | reinterpret_cast<uintptr_t>(p.sfh)) %
-                                  16 == 0;
-        // the stage sequence of this CTA pair, as the producer and MMA see it
-        struct Seq {
-            int w, kb, kb1;
-            Item item;
-        };
-        const auto seq_start = [&](Seq &q_) {
-            q_.w = pair;
-            q_.kb = q_.kb1 = 0;
-            if (q_.w < total) {
-                q_.item = decode(p, q_.w);
-                q_.kb = q_.item.ks * p.kb_per_split;
-                q_.kb1 = min(p.num_kb, q_.kb + p.kb_per_split);
-            }
-        };
-        const auto seq_next = [&](Seq &q_) {
-            if (++q_.kb < q_.kb1) return;
-            q_.w += npairs;
-            if (q_.w < total) {
-                q_.item = decode(p, q_.w);
-                q_.kb = q_.item.ks * p.kb_per_split;
-                q_.kb1 = min(p.num_kb, q_.kb + p.kb_per_split);
-            }
-        };
-        // copies of one stage's scales into ring slot `slot`: 256 rows of 32
-        // bytes (128 weight rows, then 128 token columns of the tile)
-        const auto issue = [&](const Seq &q_, int slot) {
-            uint8_t *dst = sf_smem + (size_t)slot * kNvSfStageBytes;
-            const int blk0 = q_.kb * 32;
-            const int64_t vbase = (int64_t)q_.item.wt * p.unit + (int64_t)rank * kGemmTileW;
-            const int64_t mbase = (int64_t)q_.item.nt * p.bn;
-            const int chunk = wide ? 16 : 4, per_row = 32 / chunk;
-            for (int c = sft; c < 256 * per_row; c += 128) {
-                const int r = c / per_row, off = (c - r * per_row) * chunk;
-                const uint8_t *src = nullptr;
-                if (r < 128) {
-                    const int64_t v = vbase + r;
-                    if (v < p.rows_w) src = p.sfw + v * p.n_sf;
-                } else {
-                    const int64_t m = mbase + (r - 128);
-                    if (r - 128 < p.bn && m < p.rows_h) src = p.sfh + m * p.n_sf;
-                }
-                const bool ok = src != nullptr && blk0 + off < p.n_sf;
-                const uint8_t *g = ok ? src + blk0 + off : p.sfw;
-                if (wide)
-                    cpa16_zfill(dst + r * 32 + off, g, ok);
-                else
-                    cpa4_zfill(dst + r * 32 + off, g, ok);
-            }
-        };
-        Seq fetch, cur;
-        seq_start(fetch);
-        seq_start(cur);
-#pragma unroll
-        for (int t = 0; t < kNvStages - 1; ++t) {
-            if (fetch.w < total) {
-                issue(fetch, t);
-                seq_next(fetch);
-            }
-            cpa_commit();
-        }
-        // Every loader runs the same number of iterations whatever happens, so
-        // the named barriers always meet: after a failed (timed-out) wait a
-        // warp only keeps the barriers and copies going.
-        uint32_t s = 0, ph = 1;  // the first pass finds every TMEM slot free
-        bool ok = true;
-        for (int g = 0; cur.w < total; ++g, seq_next(cur)) {
-            sf_bar_sync();  // every loader is done reading the slot refilled now
-            if (fetch.w < total) {
-                issue(fetch, (g + kNvStages - 1) % kNvStages);
-                seq_next(fetch);
-            }
-            cpa_commit();
-            cpa_wait<kNvStages - 1>();  // this thread's copies of stage g landed
-            sf_bar_sync();              // and everyone's
-            if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&empty_bar[s], ph, &abort_flag, p.err));
-            if (!ok) {
-                if (++s == (uint32_t)kNvStages) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-                continue;
-            }
-            tc_fence_after();
-            const uint8_t *src = sf_smem + (size_t)s * kNvSfStageBytes;
-            const uint4 a0 = *reinterpret_cast<const uint4 *>(src + (q * 32 + lane) * 32);
-            const uint4 a1 = *reinterpret_cast<const uint4 *>(src + (q * 32 + lane) * 32 + 16);
-            const uint32_t col = tmem + lane_base + kSfBase + s * kSfCols;
-            const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) tmem_st1(col + 4u * (uint32_t)i + (uint32_t)q, aw[i]);
-            uint32_t bw[4][8];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint8_t *tr = src + (128 + 32 * j + lane) * 32;
-                const uint4 b0 = *reinterpret_cast<const uint4 *>(tr);
-                const uint4 b1 = *reinterpret_cast<const uint4 *>(tr + 16);
-                bw[j][0] = b0.x; bw[j][1] = b0.y; bw[j][2] = b0.z; bw[j][3] = b0.w;
-                bw[j][4] = b1.x; bw[j][5] = b1.y; bw[j][6] = b1.z; bw[j][7] = b1.w;
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                tmem_st4(col + 32u + 4u * (uint32_t)i, bw[0][i], bw[1][i], bw[2][i], bw[3][i]);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(sf_full_leader + 8u * s);
-            if (++s == (uint32_t)kNvStages) {
-                s = 0;
-                ph ^= 1u;
-            }
-        }
-        cpa_wait<0>();  // no copy still landing when the CTA leaves
     } else {
         const int quarter = warp & 3;  // TMEM lanes this warp may access
         const int row_in_unit = (int)rank * kGemmTileW + quarter * 32 + lane;
@@ -1042,7 +927,7 @@ int fused_pairs(const DeviceInfo &di, bool nv = false) {
         if (set_gemm_attrs(di) == DFLASH2_OK) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)(di.sm_count / 2 * 2));
-            cfg.blockDim = dim3(nv ? kPairThreadsNv : kPairThreads);
+            cfg.blockDim = dim3(kPairThreads);
             cfg.dynamicSmemBytes = kGemmSmemBytes;
             const cudaError_t e =
                 nv ? cudaOccupancyMaxActiveClusters(&n, gemm_tc_pair_kernel<true>, &cfg)
@@ -1074,8 +959,8 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     if (p.fp8 && (!pair || p.hidden % 16 != 0)) return DFLASH2_ERR_INVALID_ARG;
     const bool nv = p.nvfp4 != 0;
     if (nv && (!pair || p.fp8 || p.bn > 128 || p.hidden % 64 != 0 || p.n_sf != p.hidden / 16 ||
-               !p.sfw || !p.sfh || reinterpret_cast<uintptr_t>(p.sfw) % 4 != 0 ||
-               reinterpret_cast<uintptr_t>(p.sfh) % 4 != 0 ||
+               p.sf_nw8 != nvfp4_tile_cells(p.hidden) || !p.sfw || !p.sfh ||
+               !aligned16(p.sfw) || !aligned16(p.sfh) ||
                (p.mode != kGemmPilot && p.mode != kGemmFilter && p.mode != kGemmFused)))
         return DFLASH2_ERR_INVALID_ARG;
     // The TMA boxes, the stages and their counts run over bytes of codes for
@@ -1116,9 +1001,8 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     int stages = (int)((kGemmSmemBytes - 1024 - epi_bytes) / stage_bytes);
     if (stages > kGemmMaxStages) stages = kGemmMaxStages;
     if (nv) {
-        // the TMEM scale columns and the shared scale ring hold kNvStages
-        stages = (int)((kGemmSmemBytes - 1024 - epi_bytes - kNvStages * kNvSfStageBytes) /
-                       stage_bytes);
+        // the TMEM scale columns hold kNvStages; each stage brings its scales
+        stages = (int)((kGemmSmemBytes - 1024 - epi_bytes) / (stage_bytes + kNvSfStageBytes));
         if (stages < kNvStages) return DFLASH2_ERR_INVALID_ARG;
         stages = kNvStages;
     }
@@ -1126,7 +1010,7 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     p.stages = stages;
     p.sf_off = (int32_t)((size_t)stages * stage_bytes + epi_bytes);  // after the epilogue scratch
     const size_t smem = (size_t)stages * stage_bytes + epi_bytes +
-                        (nv ? (size_t)kNvStages * kNvSfStageBytes : 0) + 1024;
+                        (nv ? (size_t)stages * kNvSfStageBytes : 0) + 1024;
 
     CUtensorMap tm_w, tm_h;
     const uint32_t eb = (p.fp8 || nv) ? 1 : 2;
@@ -1135,6 +1019,16 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     if (s != DFLASH2_OK) return s;
     s = encode_tmap_2d(&tm_h, h, (uint64_t)p.rows_h, (uint64_t)kdim, h_rows, eb);
     if (s != DFLASH2_OK) return s;
+    CUtensorMap tm_sfw = tm_w, tm_sfh = tm_h;
+    if (nv) {
+        // the scale tiles as rows of 256 bytes; a stage's 8 tiles are 16 rows
+        const uint64_t rw = nvfp4_tiles_bytes(p.rows_w, p.hidden, kGemmTileW) / 256;
+        const uint64_t rh = nvfp4_tiles_bytes(p.rows_h, p.hidden, p.bn) / 256;
+        s = encode_tmap_bytes_2d(&tm_sfw, p.sfw, rw, 256, 256, 16);
+        if (s != DFLASH2_OK) return s;
+        s = encode_tmap_bytes_2d(&tm_sfh, p.sfh, rh, 256, 256, 16);
+        if (s != DFLASH2_OK) return s;
+    }
 
     s = set_gemm_attrs(di);
     if (s != DFLASH2_OK) return s;
@@ -1149,7 +1043,7 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
         if ((int64_t)p.n_pilot * p.n_tok_tiles > 2LL * pairs) return DFLASH2_ERR_INVALID_ARG;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(2 * pairs));
-        cfg.blockDim = dim3(nv ? kPairThreadsNv : kPairThreads);
+        cfg.blockDim = dim3(kPairThreads);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = st;
         cudaLaunchAttribute attr[2];
@@ -1160,20 +1054,20 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
         cfg.attrs = attr;
         cfg.numAttrs = 2;
         if (nv)
-            cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<true>, tm_w, tm_h, p);
+            cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<true>, tm_w, tm_h, tm_sfw, tm_sfh, p);
         else
-            cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<false>, tm_w, tm_h, p);
+            cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel<false>, tm_w, tm_h, tm_w, tm_h, p);
         return launch_status();
     }
     if (pair) {
         const int64_t pairs_max = di.sm_count / 2;
         const int pairs = (int)(total < pairs_max ? total : pairs_max);
         if (nv)
-            launch_k(gemm_tc_pair_kernel<true>, 2 * pairs, kPairThreadsNv, smem, st, tm_w, tm_h,
-                     p);
+            launch_k(gemm_tc_pair_kernel<true>, 2 * pairs, kPairThreads, smem, st, tm_w, tm_h,
+                     tm_sfw, tm_sfh, p);
         else
             launch_k(gemm_tc_pair_kernel<false>, 2 * pairs, kPairThreads, smem, st, tm_w, tm_h,
-                     p);
+                     tm_w, tm_h, p);
     } else {
         const int grid = (int)(total < di.sm_count ? total : di.sm_count);
         launch_k(gemm_tc_kernel, grid, 192, smem, st, tm_w, tm_h, p);

@@ -50,22 +50,28 @@ dflash2_status encode_tmap_bf16(CUtensorMap *map, const void *base, uint64_t row
     return encode_tmap_2d(map, base, rows, cols, box_rows, 2);
 }
 
+// Resolves cuTensorMapEncodeTiled once (through the runtime, so the
+// library needs no link against libcuda).
+static dflash2_status resolve_encode() {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn) {
+            cudaGetLastError();
+            return DFLASH2_ERR_CUDA;
+        }
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return DFLASH2_OK;
+}
+
 dflash2_status encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                               uint32_t box_rows, uint32_t elem_bytes) {
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_encode) {
-            void *fn = nullptr;
-            cudaDriverEntryPointQueryResult q;
-            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                 cudaEnableDefault, &q) != cudaSuccess ||
-                q != cudaDriverEntryPointSuccess || !fn) {
-                cudaGetLastError();
-                return DFLASH2_ERR_CUDA;
-            }
-            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
-        }
-    }
+    const dflash2_status st = resolve_encode();
+    if (st != DFLASH2_OK) return st;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols * elem_bytes};
     cuuint32_t box[2] = {128 / elem_bytes, box_rows};  // one 128-byte swizzle row wide
@@ -75,6 +81,23 @@ dflash2_status encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows,
     CUresult r = g_encode(map, type, 2, const_cast<void *>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+}
+
+// Plain (unswizzled) byte rows: box of box_cols bytes (<= 256, a multiple
+// of 16) x box_rows rows.
+dflash2_status encode_tmap_bytes_2d(CUtensorMap *map, const void *base, uint64_t rows,
+                                    uint64_t cols, uint32_t box_cols, uint32_t box_rows) {
+    const dflash2_status st = resolve_encode();
+    if (st != DFLASH2_OK) return st;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? DFLASH2_OK : DFLASH2_ERR_CUDA;
 }

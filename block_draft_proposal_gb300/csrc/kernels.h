@@ -88,11 +88,27 @@ struct GemmParams {
     // 4); C = acc * (a_scale[m] * w_global) before the epilogue.
     int32_t nvfp4;
     int32_t n_sf;
-    const uint8_t *sfw;
-    const uint8_t *sfh;
+    const uint8_t *sfw;  // weight scales in scale tiles of 128 rows (nvfp4_tiles_bytes)
+    const uint8_t *sfh;  // token scales in scale tiles of bn rows
     float w_global;
-    int32_t sf_off;  // the scale ring's offset in dynamic shared memory (filled by launch_gemm_tc)
+    int32_t sf_nw8;  // 4-scale cells per row in the scale tiles (a multiple of 8)
+    int32_t sf_off;  // the scale stages' offset in dynamic shared memory (filled by launch_gemm_tc)
 };
+
+// NVFP4 scale tiles: the layout in which the block-scaled GEMM copies a
+// stage's scales (TMA) and hands them to TMEM (tcgen05.cp 32x128b.warpx4).
+// Rows go in blocks of `block_rows` (<= 128); a row's scales in cells of 4
+// (one cell per MMA of 64 elements), nw8 = cells per row rounded up to a
+// multiple of 8.  Tile (rb, w) is 512 bytes at (rb * nw8 + w) * 512: row
+// rb * block_rows + l + 32 j (l < 32, j < 4) has its cell w at byte l * 16 +
+// j * 4.  Cells of rows past the end or past block_rows, and past the row's
+// scales, are zero.
+inline int32_t nvfp4_tile_cells(int32_t hidden) { return (hidden / 64 + 7) / 8 * 8; }
+inline size_t nvfp4_tiles_bytes(int64_t rows, int32_t hidden, int32_t block_rows) {
+    return (size_t)((rows + block_rows - 1) / block_rows) * nvfp4_tile_cells(hidden) * 512;
+}
+dflash2_status launch_nvfp4_tile_scales(const uint8_t *scales, int64_t rows, int32_t hidden,
+                                        int32_t block_rows, uint8_t *tiles, cudaStream_t st);
 
 // Pilot tiling of a weight matrix with n_wtiles units of unit_rows rows:
 // n_pilot units spaced pilot_stride apart, from unit 0.  A larger pilot gives

@@ -116,7 +116,39 @@ __global__ void __launch_bounds__(kQuantThreads)
     if (threadIdx.x == 0) g[row] = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
 }
 
+// Scale tiles from row-major scales [rows][hidden / 16]: one thread per
+// 32-bit cell of the tiles, zeros included, so the tiles need no clearing.
+__global__ void __launch_bounds__(256)
+    nvfp4_tile_kernel(const uint8_t *__restrict__ scales, int64_t rows, int n_sf,
+                      int block_rows, int nw8, int64_t cells, uint32_t *__restrict__ tiles) {
+    grid_dep_wait();
+    for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < cells;
+         c += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tile = c >> 7;  // 128 cells of 4 bytes per 512-byte tile
+        const int in = (int)(c & 127), l = in >> 2, j = in & 3;
+        const int64_t rb = tile / nw8;
+        const int w = (int)(tile - rb * nw8);
+        const int rl = l + 32 * j;
+        const int64_t row = rb * block_rows + rl;
+        uint32_t v = 0;
+        if (rl < block_rows && row < rows && 4 * w < n_sf)
+            v = __ldg(reinterpret_cast<const uint32_t *>(scales + row * n_sf) + w);
+        tiles[c] = v;
+    }
+}
+
 }  // namespace
+
+dflash2_status launch_nvfp4_tile_scales(const uint8_t *scales, int64_t rows, int32_t hidden,
+                                        int32_t block_rows, uint8_t *tiles, cudaStream_t st) {
+    const int nw8 = nvfp4_tile_cells(hidden);
+    const int64_t cells = (int64_t)nvfp4_tiles_bytes(rows, hidden, block_rows) / 4;
+    int64_t blocks = (cells + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    launch_k(nvfp4_tile_kernel, (unsigned)blocks, 256, 0, st, scales, rows, hidden / 16,
+             block_rows, nw8, cells, reinterpret_cast<uint32_t *>(tiles));
+    return launch_status();
+}
 
 dflash2_status launch_quant_rows_nvfp4(const void *x, int32_t dtype, int64_t rows, int32_t cols,
                                        uint8_t *codes, uint8_t *scales, float *g,
@@ -177,4 +209,25 @@ extern "C" dflash2_status dflash2_quantize_rows_nvfp4(const void *x, int64_t row
     if (s != DFLASH2_OK) return s;
     return launch_quant_rows_nvfp4(x, dtype, rows, cols, codes, scales, g,
                                    static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t dflash2_nvfp4_scale_tiles_size(int64_t rows, int32_t hidden) {
+    if (rows <= 0 || hidden <= 0 || hidden % 64 != 0) return 0;
+    return dflash2::nvfp4_tiles_bytes(rows, hidden, 128);
+}
+
+extern "C" dflash2_status dflash2_nvfp4_tile_scales(const uint8_t *scales, int64_t rows,
+                                                    int32_t hidden, uint8_t *tiles, void *stream) {
+    using namespace dflash2;
+    if (rows < 0 || rows > INT32_MAX || hidden <= 0 || hidden % 64 != 0)
+        return DFLASH2_ERR_INVALID_ARG;
+    if (rows == 0) return DFLASH2_OK;
+    if (!scales || !tiles) return DFLASH2_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(scales) % 4 != 0 || !aligned16(tiles))
+        return DFLASH2_ERR_MISALIGNED;
+    DeviceInfo di;
+    dflash2_status s = current_device(&di);
+    if (s != DFLASH2_OK) return s;
+    return launch_nvfp4_tile_scales(scales, rows, hidden, 128, tiles,
+                                    static_cast<cudaStream_t>(stream));
 }

@@ -353,8 +353,9 @@ struct E2M1x2 {
     uint8_t bits;
 };
 struct NvScales {
-    const uint8_t *sfh;  // [rows][hidden / 16]
-    const uint8_t *sfw;  // [draft_vocab][hidden / 16]
+    const uint8_t *sfh;        // [rows][hidden / 16]
+    const uint8_t *sfw_tiles;  // the weights' scale tiles (blocks of 128 rows)
+    const uint8_t *sfh_tiles;  // the tokens' scale tiles (blocks of the token tile)
     float w_global;
 };
 __device__ __forceinline__ float e2m1_value(uint32_t c) {
@@ -372,6 +373,12 @@ __device__ __forceinline__ float nv_elem(const uint8_t *codes, const uint8_t *sf
     const uint32_t b = codes[j >> 1];
     return e2m1_value((j & 1) ? b >> 4 : b & 15u) * e4m3_value(sf[j >> 4]);
 }
+// Scale of element j of weight row v, from scale tiles of 128-row blocks.
+__device__ __forceinline__ uint8_t tiled_scale(const uint8_t *tiles, int64_t v, int j, int nw8) {
+    const int64_t rb = v >> 7;
+    const int rl = (int)(v & 127), b = j >> 4;
+    return tiles[(rb * nw8 + (b >> 2)) * 512 + (rl & 31) * 16 + (rl >> 5) * 4 + (b & 3)];
+}
 
 // The exact top-k of one row for NVFP4 operands: as direct_row_topk, on the
 // block-scaled values (code times block scale, exact in fp32) and the
@@ -379,7 +386,7 @@ __device__ __forceinline__ float nv_elem(const uint8_t *codes, const uint8_t *sf
 __device__ int direct_row_topk_nvfp4(const uint8_t *__restrict__ hrow,
                                      const uint8_t *__restrict__ sfh_row,
                                      const uint8_t *__restrict__ w,
-                                     const uint8_t *__restrict__ sfw, int hidden,
+                                     const uint8_t *__restrict__ sfw_tiles, int hidden,
                                      int64_t draft_vocab, int64_t target_vocab, float mult,
                                      float cap, int k, float *hs, uint64_t *buf, SelectShared &sh,
                                      float scale) {
@@ -389,16 +396,20 @@ __device__ int direct_row_topk_nvfp4(const uint8_t *__restrict__ hrow,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nwarps = blockDim.x >> 5;
     const int64_t vmax = draft_vocab < target_vocab ? draft_vocab : target_vocab;
-    const int nsf = hidden / 16;
+    const int nw8 = (hidden / 64 + 7) / 8 * 8;
     uint64_t theta = 0;
     for (int64_t v0 = 0; v0 < vmax; v0 += kDirectRows) {
         for (int r = warp; r < kDirectRows; r += nwarps) {
             const int64_t v = v0 + r;
             if (v >= vmax) break;
             const uint8_t *wr = w + v * (hidden / 2);
-            const uint8_t *sr = sfw + v * nsf;
             float acc = 0.0f;
-            for (int j = lane; j < hidden; j += 32) acc = fmaf(hs[j], nv_elem(wr, sr, j), acc);
+            for (int j = lane; j < hidden; j += 32) {
+                const uint32_t b = wr[j >> 1];
+                const float wv = e2m1_value((j & 1) ? b >> 4 : b & 15u) *
+                                 e4m3_value(tiled_scale(sfw_tiles, v, j, nw8));
+                acc = fmaf(hs[j], wv, acc);
+            }
             acc = warp_sum(acc);
             acc *= scale;
             if (lane == 0) {
@@ -591,7 +602,7 @@ __global__ void __launch_bounds__(kSelThreads)
         if constexpr (std::is_same<T, E2M1x2>::value)
             got = direct_row_topk_nvfp4(
                 reinterpret_cast<const uint8_t *>(h) + row * (hidden / 2),
-                nv.sfh + row * (hidden / 16), reinterpret_cast<const uint8_t *>(w), nv.sfw,
+                nv.sfh + row * (hidden / 16), reinterpret_cast<const uint8_t *>(w), nv.sfw_tiles,
                 hidden, draft_vocab, target_vocab, mult, cap, k, hs, buf, sh,
                 a_scale[row] * nv.w_global);
         else
@@ -804,8 +815,9 @@ dflash2_status run_tc_topk(const DeviceInfo &di, const void *h, const void *lm_h
     p.w_scale = w_scale;
     p.nvfp4 = kNv ? 1 : 0;
     p.n_sf = hidden / 16;
-    p.sfw = nvs.sfw;
-    p.sfh = nvs.sfh;
+    p.sfw = nvs.sfw_tiles;
+    p.sfh = nvs.sfh_tiles;
+    p.sf_nw8 = nvfp4_tile_cells(hidden);
     p.w_global = nvs.w_global;
 
     const bool pairs = true;
@@ -846,7 +858,7 @@ dflash2_status run_tc_topk(const DeviceInfo &di, const void *h, const void *lm_h
     p.mode = kGemmPilot;
     p.out = pilot_u;
     p.ldo = (int64_t)L.n_pilot * unit;
-    {
+    if (!kNv) {  // nvfp4: the token scale tiles are cut at the filter's token tile
         int64_t want_tiles = (pairs ? di.sm_count / 2 : di.sm_count) / L.n_pilot;  // one wave
         if (want_tiles < 1) want_tiles = 1;
         int64_t per = (rows + want_tiles - 1) / want_tiles;
@@ -928,10 +940,12 @@ inline size_t fp8_ws_prefix(int64_t rows, int32_t hidden) {
     return align256((size_t)rows * hidden) + align256((size_t)rows * 4);
 }
 // The NVFP4 path's quantized activations at the workspace's start: codes
-// [rows][hidden / 2], block scales [rows][hidden / 16], g [rows].
+// [rows][hidden / 2], block scales [rows][hidden / 16], g [rows], and the
+// scales again as tiles of the token tile.
 inline size_t nvfp4_ws_prefix(int64_t rows, int32_t hidden) {
     return align256((size_t)rows * (hidden / 2)) + align256((size_t)rows * (hidden / 16)) +
-           align256((size_t)rows * 4);
+           align256((size_t)rows * 4) +
+           align256(nvfp4_tiles_bytes(rows, hidden, token_tile(rows, 128)));
 }
 }  // namespace
 
@@ -1050,7 +1064,7 @@ extern "C" size_t dflash2_unary_topk_nvfp4_workspace_size(int64_t rows, int32_t 
 }
 
 extern "C" dflash2_status dflash2_unary_topk_nvfp4(
-    const void *h, int32_t h_dtype, const uint8_t *lm_head_q, const uint8_t *w_scales,
+    const void *h, int32_t h_dtype, const uint8_t *lm_head_q, const uint8_t *w_scale_tiles,
     float w_global, int64_t rows, int32_t hidden, int64_t draft_vocab, int64_t target_vocab,
     float mult, float cap, int32_t top_k, int64_t *cand_ids, float *cand_u, void *workspace,
     size_t ws_bytes, int32_t *err_word, void *stream) {
@@ -1061,10 +1075,10 @@ extern "C" dflash2_status dflash2_unary_topk_nvfp4(
         !(w_global > 0.0f) || !(w_global < INFINITY))
         return DFLASH2_ERR_INVALID_ARG;
     if (rows == 0) return DFLASH2_OK;
-    if (!h || !lm_head_q || !w_scales || !cand_ids || !cand_u) return DFLASH2_ERR_INVALID_ARG;
+    if (!h || !lm_head_q || !w_scale_tiles || !cand_ids || !cand_u)
+        return DFLASH2_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(cand_ids) % 8 != 0 ||
-        reinterpret_cast<uintptr_t>(cand_u) % 4 != 0 ||
-        reinterpret_cast<uintptr_t>(w_scales) % 4 != 0 ||
+        reinterpret_cast<uintptr_t>(cand_u) % 4 != 0 || !aligned16(w_scale_tiles) ||
         reinterpret_cast<uintptr_t>(h) % (h_dtype == DFLASH2_BF16 ? 2 : 4) != 0)
         return DFLASH2_ERR_MISALIGNED;
     if (!aligned16(lm_head_q)) return DFLASH2_ERR_MISALIGNED;  // TMA rows of codes
@@ -1081,9 +1095,12 @@ extern "C" dflash2_status dflash2_unary_topk_nvfp4(
     uint8_t *qh = ws;
     uint8_t *sh = ws + align256((size_t)rows * (hidden / 2));
     float *gh = reinterpret_cast<float *>(sh + align256((size_t)rows * (hidden / 16)));
+    uint8_t *th = reinterpret_cast<uint8_t *>(gh) + align256((size_t)rows * 4);
     s = launch_quant_rows_nvfp4(h, h_dtype, rows, hidden, qh, sh, gh, st);
     if (s != DFLASH2_OK) return s;
-    NvScales nvs{sh, w_scales, w_global};
+    s = launch_nvfp4_tile_scales(sh, rows, hidden, token_tile(rows, 128), th, st);
+    if (s != DFLASH2_OK) return s;
+    NvScales nvs{sh, w_scale_tiles, th, w_global};
     return run_tc_topk<E2M1x2>(di, qh, lm_head_q, gh, nullptr, rows, hidden, draft_vocab,
                                target_vocab, mult, cap, top_k, cand_ids, cand_u, ws + prefix,
                                ws_bytes - prefix, err_word, st, nvs);

@@ -29,7 +29,7 @@ DEVERR_ID_RANGE = 0x1
 DEVERR_TIMEOUT = 0x2
 DEVERR_SHORT = 0x4
 DEVINFO_TOPK_FALLBACK = 0x100
-ABI_VERSION = 8
+ABI_VERSION = 9
 
 # Every symbol include/dflash2.h declares.
 EXPORTS = (
@@ -42,7 +42,7 @@ EXPORTS = (
     "dflash2_unary_topk_launches", "dflash2_topk_merge", "dflash2_quantize_rows_e4m3",
     "dflash2_unary_topk_fp8_workspace_size", "dflash2_unary_topk_fp8",
     "dflash2_quantize_rows_nvfp4", "dflash2_unary_topk_nvfp4_workspace_size",
-    "dflash2_unary_topk_nvfp4",
+    "dflash2_unary_topk_nvfp4", "dflash2_nvfp4_scale_tiles_size", "dflash2_nvfp4_tile_scales",
 )
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -120,6 +120,10 @@ def library():
         lib.dflash2_unary_topk_nvfp4.argtypes = [P, i32, P, P, f32, i64, i32, i64, i64, f32, f32,
                                                  i32, P, P, P, sz, P, P]
         lib.dflash2_unary_topk_nvfp4.restype = i32
+        lib.dflash2_nvfp4_scale_tiles_size.argtypes = [i64, i32]
+        lib.dflash2_nvfp4_scale_tiles_size.restype = sz
+        lib.dflash2_nvfp4_tile_scales.argtypes = [P, i64, i32, P, P]
+        lib.dflash2_nvfp4_tile_scales.restype = i32
         lib.dflash2_topk_merge.argtypes = [P, P, P, i32, i64, i32, i32, P, P, P, P]
         lib.dflash2_topk_merge.restype = i32
         lib.dflash2_unary_topk_launches.argtypes = [i64, i64, i32, f32, i32]
@@ -284,22 +288,39 @@ def quantize_rows_nvfp4(x, codes=None, scales=None, g=None, stream=None):
     return codes, scales, g
 
 
+def nvfp4_tile_scales(scales, hidden: int, tiles=None, stream=None):
+    """dflash2_nvfp4_tile_scales: the scale tiles of row-major E4M3 block
+    scales [rows, hidden / 16] (uint8), as the NVFP4 GEMM reads them."""
+    rows = scales.shape[0]
+    _need(scales, "scales", torch.uint8, (rows, hidden // 16))
+    if tiles is None:
+        tiles = torch.empty(max(1, int(library().dflash2_nvfp4_scale_tiles_size(rows, hidden))),
+                            dtype=torch.uint8, device=scales.device)
+    _check("dflash2_nvfp4_tile_scales", library().dflash2_nvfp4_tile_scales(
+        _ptr(scales), rows, hidden, _ptr(tiles), _stream(stream)))
+    return tiles
+
+
 def unary_topk_nvfp4_workspace_size(rows: int, hidden: int, draft_vocab: int, top_k: int) -> int:
     return int(library().dflash2_unary_topk_nvfp4_workspace_size(rows, hidden, draft_vocab,
                                                                  top_k))
 
 
-def unary_topk_nvfp4(h, lm_head_q, w_scales, w_global: float, target_vocab: int, mult: float,
+def unary_topk_nvfp4(h, lm_head_q, w_scale_tiles, w_global: float, target_vocab: int, mult: float,
                      cap: float, top_k: int, cand_ids=None, cand_u=None, workspace=None, err=None,
                      stream=None):
     """dflash2_unary_topk_nvfp4: top_k (ids, u) per row of h against an NVFP4
-    head (lm_head_q uint8 [draft_vocab, hidden / 2] codes, w_scales uint8
-    [draft_vocab, hidden / 16] E4M3 block scales, w_global its fp32 scale)."""
+    head (lm_head_q uint8 [draft_vocab, hidden / 2] codes, w_scale_tiles its
+    E4M3 block scales as nvfp4_tile_scales returns them, w_global its fp32
+    scale)."""
     rows, hidden = h.shape
     draft_vocab = lm_head_q.shape[0]
     _need(h, "h")
     _need(lm_head_q, "lm_head_q", torch.uint8, (draft_vocab, hidden // 2))
-    _need(w_scales, "w_scales", torch.uint8, (draft_vocab, hidden // 16))
+    _need(w_scale_tiles, "w_scale_tiles", torch.uint8)
+    need = int(library().dflash2_nvfp4_scale_tiles_size(draft_vocab, hidden))
+    if w_scale_tiles.numel() < need:
+        raise ValueError(f"w_scale_tiles: uint8 scale tiles of {need} bytes expected")
     dev = h.device
     if cand_ids is None:
         cand_ids = torch.empty((rows, top_k), dtype=torch.int64, device=dev)
@@ -312,7 +333,7 @@ def unary_topk_nvfp4(h, lm_head_q, w_scales, w_global: float, target_vocab: int,
     if err is None:
         err = torch.zeros(1, dtype=torch.int32, device=dev)
     _check("dflash2_unary_topk_nvfp4", library().dflash2_unary_topk_nvfp4(
-        _ptr(h), _dtype_code(h), _ptr(lm_head_q), _ptr(w_scales), float(w_global), rows, hidden,
+        _ptr(h), _dtype_code(h), _ptr(lm_head_q), _ptr(w_scale_tiles), float(w_global), rows, hidden,
         draft_vocab, target_vocab, float(mult), float(cap), top_k, _ptr(cand_ids), _ptr(cand_u),
         _ptr(workspace), workspace.numel(), _ptr(err), _stream(stream)))
     return cand_ids, cand_u, err

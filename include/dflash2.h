@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define DFLASH2_ABI_VERSION 8
+#define DFLASH2_ABI_VERSION 9
 
 typedef enum {
     DFLASH2_OK = 0,
@@ -216,8 +216,9 @@ dflash2_status dflash2_unary_topk_fp8(const void *h, int32_t h_dtype, const uint
  *     block b: a_b = max |h| over its 16 elements, s_b = E4M3((a_b / 6) * enc);
  *     codes E2M1(h[m, j] * (enc / dec(s_b))) (round to nearest even,
  *     saturating at 6), all 0 when s_b is 0.
- *   weights: codes lm_head_q, scales w_scales, one fp32 w_global, quantized
- *     the same way with the amax of the whole tensor (a checkpoint's format).
+ *   weights: codes lm_head_q, block scales, one fp32 w_global, quantized
+ *     the same way with the amax of the whole tensor (a checkpoint's format);
+ *     the block scales are handed over as scale tiles (below).
  *   z[m, v] = g_h[m] * w_global * sum_b dec(s_h[m, b]) * dec(w_scales[v, b])
  *             * sum_{j in b} dec(q_h[m, j]) * dec(lm_head_q[v, j])
  *   then the transform, the padded-vocab mask and the top-K of
@@ -229,17 +230,28 @@ dflash2_status dflash2_unary_topk_fp8(const void *h, int32_t h_dtype, const uint
  *   Errors: dtype -> UNSUPPORTED_DTYPE; rows outside [0, 2^31), cols < 1 or
  *   not a multiple of 16, or a null pointer -> INVALID_ARG; x, codes or g
  *   misaligned -> MISALIGNED.  rows == 0 queues nothing.
+ * dflash2_nvfp4_tile_scales: scales device uint8 [rows, hidden / 16]
+ *   (row-major, 4-byte aligned), hidden % 64 == 0 -> tiles device, 16-byte
+ *   aligned, dflash2_nvfp4_scale_tiles_size(rows, hidden) bytes, fully
+ *   written.  The layout the block-scaled GEMM copies from: rows in blocks of
+ *   128, a row's scales in cells of 4 bytes (64 elements), cells per row
+ *   rounded up to nw8 = a multiple of 8; tile (rb, w) is 512 bytes at
+ *   (rb * nw8 + w) * 512, row rb * 128 + l + 32 j (l < 32, j < 4) with its
+ *   cell w at byte l * 16 + j * 4; everything else zero.  Call once per
+ *   checkpoint.  Errors: INVALID_ARG (shape, null), MISALIGNED.
  * dflash2_unary_topk_nvfp4: h device [rows, hidden] (h_dtype f32 or bf16);
  *   lm_head_q device uint8 [draft_vocab, hidden / 2], 16-byte aligned;
- *   w_scales device uint8 [draft_vocab, hidden / 16], 4-byte aligned;
+ *   w_scale_tiles device: the weights' block scales as written by
+ *   dflash2_nvfp4_tile_scales, 16-byte aligned;
  *   w_global > 0 and finite; hidden % 64 == 0; the other arguments as for
  *   dflash2_unary_topk.  workspace device, 256-byte aligned, ws_bytes >=
  *   dflash2_unary_topk_nvfp4_workspace_size(rows, hidden, draft_vocab,
  *   top_k): the activation codes, scales and g, then a dflash2_unary_topk
- *   workspace.  Queues the quantization kernel, then the pair GEMM (fused
- *   with the select, or pilot, select and filter passes) and the final top-K.
+ *   workspace.  Queues the quantization and scale-tiling kernels, then the
+ *   pair GEMM (fused with the select, or pilot, select and filter passes)
+ *   and the final top-K.
  *   Errors as for dflash2_unary_topk, plus INVALID_ARG for hidden % 64 != 0 or
- *   a bad w_global, MISALIGNED for lm_head_q or w_scales.
+ *   a bad w_global, MISALIGNED for lm_head_q or w_scale_tiles.
  * Arithmetic: exact products of codes, summed per 16-element block and
  *   scaled by the two block scales in the tensor cores (fp32 accumulation),
  *   then z = acc * (g_h[m] * w_global) in fp32.
@@ -247,10 +259,13 @@ dflash2_status dflash2_unary_topk_fp8(const void *h, int32_t h_dtype, const uint
 dflash2_status dflash2_quantize_rows_nvfp4(const void *x, int64_t rows, int32_t cols,
                                            int32_t dtype, uint8_t *codes, uint8_t *scales,
                                            float *g, void *stream);
+size_t dflash2_nvfp4_scale_tiles_size(int64_t rows, int32_t hidden);
+dflash2_status dflash2_nvfp4_tile_scales(const uint8_t *scales, int64_t rows, int32_t hidden,
+                                         uint8_t *tiles, void *stream);
 size_t dflash2_unary_topk_nvfp4_workspace_size(int64_t rows, int32_t hidden, int64_t draft_vocab,
                                                int32_t top_k);
 dflash2_status dflash2_unary_topk_nvfp4(const void *h, int32_t h_dtype, const uint8_t *lm_head_q,
-                                        const uint8_t *w_scales, float w_global, int64_t rows,
+                                        const uint8_t *w_scale_tiles, float w_global, int64_t rows,
                                         int32_t hidden, int64_t draft_vocab, int64_t target_vocab,
                                         float mult, float cap, int32_t top_k, int64_t *cand_ids,
                                         float *cand_u, void *workspace, size_t ws_bytes,

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.dflash2_abi_version() == 8
+    assert lib.dflash2_abi_version() == 9
     assert lib.dflash2_status_string(0) == b"ok"
     for s in range(1, 7):
         assert lib.dflash2_status_string(s) not in (b"ok", b"unknown status")

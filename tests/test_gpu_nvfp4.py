@@ -101,7 +101,8 @@ CASES = [
 def test_nvfp4_topk_matches_the_oracle(cuda, case):
     rows, hidden, vd, vt, k, mult, cap, h_dtype = case
     hin, qw, sw, gw = _case(rows, hidden, vd, 7 * rows + hidden, h_dtype)
-    ids, vals, err = dflash2.unary_topk_nvfp4(_dev(hin, cuda), _dev(qw, cuda), _dev(sw, cuda), gw,
+    tiles = dflash2.nvfp4_tile_scales(_dev(sw, cuda), hidden)
+    ids, vals, err = dflash2.unary_topk_nvfp4(_dev(hin, cuda), _dev(qw, cuda), tiles, gw,
                                               vt, mult, cap, k)
     torch.cuda.synchronize()
     assert int(err.item()) & ~dflash2.DEVINFO_TOPK_FALLBACK == 0
@@ -118,8 +119,9 @@ def test_nvfp4_topk_at_the_qwen3_size_on_sampled_rows(cuda):
     h = synth.make(w, parts=("h",))["h"]
     wf = rng.normal(0, 0.02, (w.draft_vocab, w.hidden)).astype(np.float32)
     qw, sw, gw = oracle.quantize_nvfp4(wf, per_tensor=True)
-    ids, vals, err = dflash2.unary_topk_nvfp4(_dev(h, cuda), _dev(qw, cuda), _dev(sw, cuda),
-                                              float(gw), w.target_vocab, w.mult, w.cap, w.top_k)
+    tiles = dflash2.nvfp4_tile_scales(_dev(sw, cuda), w.hidden)
+    ids, vals, err = dflash2.unary_topk_nvfp4(_dev(h, cuda), _dev(qw, cuda), tiles, float(gw),
+                                              w.target_vocab, w.mult, w.cap, w.top_k)
     torch.cuda.synchronize()
     assert int(err.item()) & ~dflash2.DEVINFO_TOPK_FALLBACK == 0
     rows = np.array([0, 1, 127, 128, 239, 240, 479])
@@ -138,7 +140,8 @@ def test_nvfp4_overflowing_candidate_lists_fall_back_exactly(cuda):
     prefix = (dflash2.unary_topk_nvfp4_workspace_size(rows, hidden, vd, k)
               - dflash2.unary_topk_workspace_size(rows, vd, k, dflash2.BF16))
     ws = torch.empty(prefix + min_ws, dtype=torch.uint8, device=cuda)
-    ids, vals, err = dflash2.unary_topk_nvfp4(_dev(hin, cuda), _dev(qw, cuda), _dev(sw, cuda), gw,
+    tiles = dflash2.nvfp4_tile_scales(_dev(sw, cuda), hidden)
+    ids, vals, err = dflash2.unary_topk_nvfp4(_dev(hin, cuda), _dev(qw, cuda), tiles, gw,
                                               vt, 1.0, 0.0, k, workspace=ws)
     torch.cuda.synchronize()
     e = int(err.item())
@@ -157,10 +160,34 @@ def test_nvfp4_rejects_bad_arguments(cuda):
         dflash2.unary_topk_nvfp4(h, q, s, 1.0, 100, 1.0, 0.0, 4)
     h = torch.zeros((4, 128), dtype=torch.bfloat16, device=cuda)
     q = torch.zeros((100, 64), dtype=torch.uint8, device=cuda)
-    s = torch.zeros((100, 8), dtype=torch.uint8, device=cuda)
+    s = torch.zeros(int(lib.dflash2_nvfp4_scale_tiles_size(100, 128)), dtype=torch.uint8,
+                    device=cuda)
     for g in (0.0, -1.0, float("inf"), float("nan")):
         with pytest.raises(dflash2.Dflash2Error):
             dflash2.unary_topk_nvfp4(h, q, s, g, 100, 1.0, 0.0, 4)
     # cols not a multiple of 16
     assert lib.dflash2_quantize_rows_nvfp4(dflash2._ptr(h), 4, 120, dflash2.BF16, None, None,
                                            None, None) == 1
+
+
+@pytest.mark.parametrize("rows,hidden", [(5, 64), (300, 576), (128, 4096), (129, 1024)])
+def test_scale_tiles_follow_the_documented_layout(cuda, rows, hidden):
+    """dflash2_nvfp4_tile_scales against the layout of include/dflash2.h written
+    out with numpy: rows in blocks of 128, cells of 4 scales, nw8 cells per
+    row, tile (rb, w) of 512 bytes with row rb*128 + l + 32 j's cell at
+    l*16 + j*4; zeros elsewhere."""
+    rng = np.random.default_rng(rows + hidden)
+    nsf = hidden // 16
+    sc = rng.integers(1, 255, size=(rows, nsf), dtype=np.uint8)
+    tiles = dflash2.nvfp4_tile_scales(_dev(sc, cuda), hidden).cpu().numpy()
+    nw = nsf // 4
+    nw8 = (nw + 7) // 8 * 8
+    nrb = (rows + 127) // 128
+    ref = np.zeros(nrb * nw8 * 512, dtype=np.uint8)
+    for r in range(rows):
+        rb, rl = divmod(r, 128)
+        l, j = rl % 32, rl // 32
+        for w in range(nw):
+            o = (rb * nw8 + w) * 512 + l * 16 + j * 4
+            ref[o:o + 4] = sc[r, 4 * w:4 * w + 4]
+    np.testing.assert_array_equal(tiles, ref)
