@@ -179,6 +179,46 @@ def _profile_traffic(workload: str, src_hash: str):
     return float(rec["unary_topk_dram_bytes"])
 
 
+_NCU_BYTES = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12}
+
+
+def write_traffic(csv_path: str, workload: str, command: str):
+    """Records in TRAFFIC_FILE the DRAM bytes (dram__bytes_read.sum +
+    dram__bytes_write.sum) of every launch in an ncu --csv metrics log of one
+    unary_topk stage call, keyed by workload and by the current hash of the
+    stage's sources."""
+    import csv
+    with open(csv_path) as f:
+        rows = [r for r in csv.reader(f) if len(r) > 10]
+    head = rows[0]
+    ik, im, iu, iv = (head.index("Kernel Name"), head.index("Metric Name"),
+                      head.index("Metric Unit"), head.index("Metric Value"))
+    iid = head.index("ID")
+    total, kernels = 0.0, {}
+    for r in rows[1:]:
+        if r[im] in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            b = float(r[iv].replace(",", "")) * _NCU_BYTES[r[iu]]
+            total += b
+            kernels.setdefault(r[iid], [r[ik].split("(")[0].split("::")[-1], 0.0])[1] += b
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        rec = {}
+    src_hash, srcs = kernel_source_hash()
+    rec[workload] = {"unary_topk_dram_bytes": total,
+                     "launches": [{"kernel": k, "dram_bytes": v} for k, v in kernels.values()],
+                     "source_sha16": src_hash,
+                     "sources": [os.path.relpath(p, ROOT) for p in srcs],
+                     "command": command}
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(rec, f, indent=1, sort_keys=True)
+        f.write("\n")
+    print(json.dumps({"workload": workload, "unary_topk_dram_bytes": total,
+                      "launches": len(kernels)}))
+    return 0
+
+
 def kernel_source_hash():
     import hashlib
     srcs = [os.path.join(ROOT, "block_draft_proposal_gb300", "csrc", f)
@@ -847,12 +887,19 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--write-traffic", metavar="NCU_CSV",
+                    help="record the DRAM bytes of an ncu --csv log of one unary_topk stage call "
+                         "of --workload in profiles/traffic.json, then exit")
+    ap.add_argument("--traffic-command", default="",
+                    help="the ncu command that made the log (stored beside the bytes)")
     ap.add_argument("--stage", choices=["conv", "unary_topk", "unary_topk_fp8", "unary_topk_nvfp4",
                                         "projection", "walk"],
                     help="time one stage alone (one GPU) instead of the whole step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.write_traffic:
+        return write_traffic(args.write_traffic, args.workload, args.traffic_command)
     from block_draft_proposal_gb300 import synth
     w = synth.BY_NAME[args.workload]
     if args.impl == "reference":
