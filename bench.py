@@ -663,6 +663,13 @@ def run_gpu(args, w):
         return 0
 
     hbm, tf_burst, tf_sust, peak_kind = _peaks()
+    # The stage is timed across the whole eager phase: when that phase lasts
+    # seconds, the GPU runs at its power-capped sustained rate, so the
+    # sustained peak (a seconds-long cuBLAS loop) is the denominator; a short
+    # phase is compared with the burst peak.
+    eager_phase_s = statistics.mean(stage_ms["unary_topk"]) * 1e-3 * args.steps
+    roof_kind = "sustained" if eager_phase_s >= 1.0 else "burst"
+    roof_peak = tf_sust if roof_kind == "sustained" else tf_burst
     work = algorithmic_work(w)
     unary_ms = statistics.mean(stage_ms["unary_topk"])
     achieved_tf = work["gemm_flops"] / (unary_ms * 1e-3) / 1e12
@@ -747,12 +754,12 @@ def run_gpu(args, w):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded; weights N(0,0.02), "
         "activations N(0,1); walk uniforms drawn on the device by Philox4x64-10)", "config": _config(w),
-        "roofline": {"bound": "tensor", "achieved": achieved_tf, "peak": tf_burst,
-                     "unit": "TFLOP/s", "frac": achieved_tf / tf_burst, "traffic": traffic,
+        "roofline": {"bound": "tensor", "achieved": achieved_tf, "peak": roof_peak,
+                     "unit": "TFLOP/s", "frac": achieved_tf / roof_peak, "traffic": traffic,
                      "traffic_source": "profiles/traffic.json" if traffic is not None else None,
                      "kernel": "unary_topk stage (fused pilot + select + filter GEMM, then "
                                "finalize), 2*M*V*H flops over the stage time",
-                     "peak_kind": f"{peak_kind} bf16 burst"},
+                     "peak_kind": f"{peak_kind} bf16 {roof_kind}"},
         "stages": stages,
         "next_rows": next_rows,
         "cpu_baseline": cpu,
