@@ -130,6 +130,26 @@ def test_nvfp4_topk_at_the_qwen3_size_on_sampled_rows(cuda):
     print(f"qwen3 shape, vocab 60000: near-ties {ties}")
 
 
+def test_nvfp4_topk_at_the_stress_hidden_on_sampled_rows(cuda):
+    """hidden 7168 (14 stages of 512 elements), 960 rows (8 token tiles of
+    128), K 64, mult 0.5 with cap: the stress draft's shapes with a smaller
+    vocab."""
+    w = synth.BY_NAME["stress-bf16"].scaled(batch=64, draft_vocab=24000, target_vocab=24000)
+    rng = np.random.default_rng(707)
+    h = synth.make(w, parts=("h",))["h"]
+    wf = rng.normal(0, 0.02, (w.draft_vocab, w.hidden)).astype(np.float32)
+    qw, sw, gw = oracle.quantize_nvfp4(wf, per_tensor=True)
+    tiles = dflash2.nvfp4_tile_scales(_dev(sw, cuda), w.hidden)
+    ids, vals, err = dflash2.unary_topk_nvfp4(_dev(h, cuda), _dev(qw, cuda), tiles, float(gw),
+                                              w.target_vocab, w.mult, w.cap, w.top_k)
+    torch.cuda.synchronize()
+    assert int(err.item()) & ~dflash2.DEVINFO_TOPK_FALLBACK == 0
+    rows = np.array([0, 1, 127, 128, 511, 512, 895, 959])
+    ties = _check_nvfp4(h, qw, sw, float(gw), w.target_vocab, w.mult, w.cap, w.top_k,
+                        ids.cpu().numpy(), vals.cpu().numpy(), rows)
+    print(f"stress hidden, vocab 24000: near-ties {ties}")
+
+
 def test_nvfp4_overflowing_candidate_lists_fall_back_exactly(cuda):
     """The minimum workspace leaves room for K candidates per row: rows whose
     lists overflow are recomputed exactly on CUDA cores from the codes and
