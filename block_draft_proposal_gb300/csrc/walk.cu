@@ -401,17 +401,19 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32)
 // of a slot is spread over 128 threads and touches shared memory only.
 //   - Every candidate id of the request is staged once (int32; -1 marks an id
 //     outside the table, whose rows are zero).
-//   - The A rows of slot s's candidates (the possible predecessors of slot
-//     s + 1) are copied into one of two A buffers about a slot and a half
-//     before slot s + 1 needs them, by warps 1-3 with 16-byte cp.async whose
-//     arrivals complete the buffer's mbarrier; so each slot reads its
-//     predecessor's row from shared memory.
+//   - Only the predecessor's A row is read: as soon as warp 0 has drawn slot
+//     s, its lanes copy the drawn candidate's A row (16-byte cp.async per
+//     lane, arrivals on one of two mbarriers) into one of two row slots,
+//     which slot s + 1 waits for.  (Copying all K candidates' A rows a slot
+//     and a half ahead, the first design, moved 64 times the bytes and left
+//     each slot waiting about 3 us for them: 89 against 77 us for the walk
+//     stage at batch 512 x 15 slots, K 64, rank 128.)
 //   - The B rows of slot s (its candidates) are in a shared B buffer when its
 //     edges are formed.  With at most 8 16-byte chunks per thread (top_k <= 64,
 //     rank <= 128) each thread loads its own chunks of slot s + 2 into
 //     registers while slot s is drawn and stores them into the single B buffer
-//     after slot s + 1's edges; otherwise two B buffers are filled like the A
-//     buffers.
+//     after slot s + 1's edges; otherwise two B buffers are filled by warps
+//     1-3 with cp.async, a slot and a half ahead.
 //   - Edges: half-warp h owns candidates [h * CPH, (h + 1) * CPH); its lane
 //     l16 owns the rank chunks l16 + 16 i of 8 elements, so the 16 lanes read
 //     a B row's 256 contiguous bytes per chunk step (no bank conflicts).  Each
@@ -423,7 +425,8 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32)
 // Measured on GB300 and not kept: one bulk (copy-engine) copy per row (64
 // engine operations per group slowed the shuffles and shared-memory loads of
 // every warp on the SM); L2 prefetches of the rows ahead (slower, line and
-// bulk alike); four-row copy-engine gathers of the A rows (no change); the
+// bulk alike, also for the candidates' A rows ahead of the drawn-row copy);
+// four-row copy-engine gathers of the A rows (no change); the
 // edges on one warp with the other three only copying, the warps meeting at
 // full/free mbarrier pairs instead of block barriers, the edges formed on
 // CUDA cores (88 us against 66 at batch 512 x 15 slots, K 64, rank 128) or on
@@ -445,14 +448,14 @@ __host__ __device__ inline ChainLayout chain_layout(int slots, int k, int rank, 
     L.row_bytes = rank * 2;
     L.regb = regb ? 1 : 0;
     L.slot_floats = (int)((k_splits * rank + k + 1 + 3) / 4 * 4);
-    L.bars = 0;                                              // A, B and slot-data mbarriers (2 each)
+    L.bars = 0;                                              // chosen-A, B and slot-data mbarriers (2 each)
     L.sdat = 64;                                             // [2][slot_floats] slot-data ring
     L.ids = L.sdat + (size_t)2 * L.slot_floats * 4;          // [slots][k] ids (-1: outside the table)
     L.chosen = L.ids + pad16((size_t)slots * k * 4);         // [slots] drawn index
     L.esm = L.chosen + pad16((size_t)slots * 4);             // [k] the slot's edges
     L.ctl = L.esm + pad16((size_t)k * 4);                    // abort flag
-    L.abuf = L.ctl + 16;                                     // [2][k] A rows of a slot's candidates
-    L.bbuf = L.abuf + (size_t)2 * k * L.row_bytes;           // [1 or 2][k] B rows
+    L.abuf = L.ctl + 16;                                     // [3] A rows: anchor, chosen (2 slots)
+    L.bbuf = L.abuf + pad16((size_t)3 * L.row_bytes);        // [1 or 2][k] B rows
     L.total = L.bbuf + (size_t)(regb ? 1 : 2) * k * L.row_bytes;
     return L;
 }
@@ -669,7 +672,10 @@ __global__ void __launch_bounds__(kChainThreads, 4)
     const __nv_bfloat16 *B = static_cast<const __nv_bfloat16 *>(p.B);
 
     if (tid == 0) {
-        for (int i = 0; i < 6; ++i) mbar_init(&abar[i], kChainCopyThreads);
+        // abar[0..1]: the chosen A row, copied by the nch lanes of warp 0;
+        // bbar, sbar: the copy threads (warps 1-3)
+        for (int i = 0; i < 2; ++i) mbar_init(&abar[i], (uint32_t)(R / 8));
+        for (int i = 2; i < 6; ++i) mbar_init(&abar[i], kChainCopyThreads);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -686,16 +692,15 @@ __global__ void __launch_bounds__(kChainThreads, 4)
     const bool anchor_ok = id_ok(anchor, p.table_rows);
     bad |= tid == 0 && !anchor_ok;
     if (__syncthreads_or(bad) && tid == 0 && p.err) atomicOr(p.err, DFLASH2_DEVERR_ID_RANGE);
-    // slot 0's predecessor: the anchor's A row, as row 0 of A buffer 1
+    // slot 0's predecessor: the anchor's A row (row 0 of the A rows)
     for (int j = tid; j < nch; j += kChainThreads)
-        reinterpret_cast<uint4 *>(abuf + gbytes)[j] =
+        reinterpret_cast<uint4 *>(abuf)[j] =
             anchor_ok ? __ldg(reinterpret_cast<const uint4 *>(A + anchor * R) + j) : make_uint4(0, 0, 0, 0);
     // A rows of slot 0's candidates; B rows of slots 0 and 1
     uint4 bq[NBQ];
     if (warp > 0) {
         chain_copy_slot(p, row0, sdat, &sbar[0], ct);
         if (S > 1) chain_copy_slot(p, row0 + 1, sdat + L.slot_floats, &sbar[1], ct);
-        if (S > 1) chain_copy_rows(ids, K, A, R, nch, lg, abuf, &abar[0], ct);
         if constexpr (!REGB) {
             chain_copy_rows(ids, K, B, R, nch, lg, bbuf, &bbar[0], ct);
             if (S > 1) chain_copy_rows(ids + K, K, B, R, nch, lg, bbuf + gbytes, &bbar[1], ct);
@@ -744,10 +749,10 @@ __global__ void __launch_bounds__(kChainThreads, 4)
         const float cu = writer ? sd[p.k_splits * R + cw] : 0.0f;
         const float uni = sd[p.k_splits * R + K];
         // w = A[predecessor] * g on this lane's chunks: slot 0 reads the anchor
-        // (row 0 of A buffer 1), slot s the drawn row of A buffer (s - 1) % 2
+        // (A row 0), slot s the row drawn at slot s - 1 (A row 1 + (s - 1) % 2,
+        // copied by warp 0 as soon as it drew it)
         if (s > 0) mbar_wait(&abar[(s - 1) & 1], (uint32_t)((s - 1) >> 1) & 1u, abort_flag, p.err);
-        const uint8_t *arow = abuf + (size_t)((s + 1) & 1) * gbytes +
-                              (size_t)(s > 0 ? chosen[s - 1] : 0) * L.row_bytes;
+        const uint8_t *arow = abuf + (size_t)(s > 0 ? 1 + ((s - 1) & 1) : 0) * L.row_bytes;
         float2 w[4 * CH];
 #pragma unroll
         for (int ch = 0; ch < CH; ++ch) {
@@ -796,6 +801,17 @@ __global__ void __launch_bounds__(kChainThreads, 4)
                 ev[i] = k < K ? esm[k] : -INFINITY;
             }
             const int index = select_consecutive<E>(ev, K, lane, greedy, temp, uni, qv);
+            if (s + 1 < S && lane < nch) {
+                // the drawn candidate's A row, the next slot's predecessor (a row
+                // outside the table: zeros)
+                const int32_t id = ids[(size_t)s * K + index];
+                cp_async16(abuf + (size_t)(1 + (s & 1)) * L.row_bytes + 16 * lane,
+                           reinterpret_cast<const uint8_t *>(A + (id >= 0 ? id : 0) * R) + 16 * lane,
+                           id >= 0);
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
+                                 smem_u32(&abar[s & 1]))
+                             : "memory");
+            }
 #pragma unroll
             for (int i = 0; i < E; ++i) {
                 const int k = lane * E + i;
@@ -806,13 +822,9 @@ __global__ void __launch_bounds__(kChainThreads, 4)
             }
             if (lane == 0) chosen[s] = index;
         } else {
-            // A rows of slot s + 1's candidates into the buffer slot s - 1 used;
             // slot s + 2's data and B rows into the entries slot s just read
-            if (s + 2 < S) {
-                chain_copy_rows(ids + (size_t)(s + 1) * K, K, A, R, nch, lg, abuf + (size_t)((s + 1) & 1) * gbytes,
-                                &abar[(s + 1) & 1], ct);
+            if (s + 2 < S)
                 chain_copy_slot(p, row + 2, sdat + (size_t)(s & 1) * L.slot_floats, &sbar[s & 1], ct);
-            }
             if constexpr (!REGB) {
                 if (s + 2 < S)
                     chain_copy_rows(ids + (size_t)(s + 2) * K, K, B, R, nch, lg, bbuf + (size_t)(s & 1) * gbytes,
@@ -831,9 +843,9 @@ __global__ void __launch_bounds__(kChainThreads, 4)
     for (int t = tid; t < s; t += kChainThreads)
         p.tokens[row0 + t] = p.cand[(row0 + t) * K + chosen[t]];
     // after an abort: let the copies still in flight land before exiting
+    if (s < S && tid < nch) asm volatile("cp.async.wait_all;" ::: "memory");  // warp 0's row copies
     if (s < S && tid == 32) {
         for (int t = s - 1; t <= s + 1 && t < S; ++t) {
-            if (t >= 0 && t + 1 < S) chain_drain_wait(&abar[t & 1], (uint32_t)(t >> 1) & 1u);
             if (!REGB && t >= 0) chain_drain_wait(&bbar[t & 1], (uint32_t)(t >> 1) & 1u);
             if (t >= 0) chain_drain_wait(&sbar[t & 1], (uint32_t)(t >> 1) & 1u);
         }
