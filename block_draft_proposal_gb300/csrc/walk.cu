@@ -26,7 +26,6 @@ namespace {
 constexpr int kMaxK = 128;
 constexpr int kMaxRank = 256;
 constexpr int kMaxWarpsPerCta = 4;
-constexpr int kMaxSplits = 8;   // hidden splits of the tensor-core projection
 constexpr int kMaxRing = 8;     // prefetch groups per warp
 constexpr size_t kWalkSmemBytes = 224 * 1024;
 
@@ -646,7 +645,7 @@ template <int KM, int CH, bool REGB>
 __global__ void __launch_bounds__(kChainThreads, 4)
     walk_chain_kernel(const WalkParams p, ChainLayout L) {
     grid_dep_wait();
-    extern __shared__ __align__(128) uint8_t dyn[];
+    extern __shared__ __align__(16) uint8_t dyn[];
     constexpr int CPH = KM / 8;  // candidates per half-warp
     constexpr int E = KM / 32;   // candidates per lane of the selecting warp
     constexpr int NBQ = REGB ? CPH * CH : 1;
