@@ -197,6 +197,40 @@ __device__ __forceinline__ void epilogue_chunk(const GemmParams &p, const float 
     }
 }
 
+// Bf16 store of one 32 x 32 chunk on CTA pairs: the warp's weight rows v0 ..
+// v0 + 31 (lane i holds row v0 + i) and tokens m0 .. m0 + ncols - 1.  The
+// chunk goes through the warp's shared tile [32 tokens][32 rows] (rows of 64
+// bytes), so that each lane then writes 8 consecutive outputs of one token
+// row with one 16-byte store (vec: 16-byte aligned rows), instead of 32
+// two-byte stores per lane.
+__device__ __forceinline__ void store_bf16_chunk(const GemmParams &p, const float (&z)[32], int64_t v0,
+                                                 int m0, int ncols, bool vec, __nv_bfloat16 *tile,
+                                                 int lane) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) tile[i * 32 + lane] = __float2bfloat16_rn(z[i]);
+    __syncwarp();
+    const int64_t vq = v0 + 8 * (lane & 3);  // this lane's 8 consecutive rows
+    const bool full = vec && vq + 8 <= p.rows_w;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int r = 8 * j + (lane >> 2);  // the token of this store within the chunk
+        const int m = m0 + r;
+        if (r < ncols && m < p.rows_h) {
+            const uint4 val = *reinterpret_cast<const uint4 *>(tile + r * 32 + 8 * (lane & 3));
+            __nv_bfloat16 *o = p.out_bf16 + (int64_t)m * p.ldo + vq;
+            if (full) {
+                *reinterpret_cast<uint4 *>(o) = val;
+            } else {
+                const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&val);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (vq + q < p.rows_w) o[q] = e[q];
+            }
+        }
+    }
+    __syncwarp();  // the tile is rewritten by the next chunk
+}
+
 // Fused pilot tile: the warp's 32 vocab rows form group g; lane i stores the
 // order bits of the group's largest logit for token m0 + i (NaN and invalid
 // rows count as -inf).
@@ -242,6 +276,7 @@ constexpr int kPairEpiWarps = 8;          // CTA pairs: two warps per TMEM lane 
 constexpr int kPairEpiCols = 128;         // each on half of the tile's columns
 using EpiScratchPair = EpiScratchT<kPairEpiCols>;
 constexpr int kPairThreads = 64 + 32 * kPairEpiWarps;  // producer, MMA issuer, epilogue
+constexpr uint32_t kBf16TileBytes = 32 * 32 * 2;       // an epilogue warp's bf16 transpose tile
 // nvfp4: TMEM holds the two accumulators (<= 128 columns each) and then 64
 // scale columns per stage: 32 for the weight rows (4 per MMA) and 32 for
 // the tokens.  A stage's scales come with its operands: the producer's TMA
@@ -663,6 +698,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     // filter, start during the pilot pass was slower: the early filter CTAs
     // took bandwidth from the pilot.)
     if (p.mode != kGemmFilter || warp >= 2) grid_dep_wait();
+    // The store modes let the next kernel be scheduled now: its CTAs take the
+    // SMs this grid leaves idle (one CTA per SM here) and, as CTAs of this
+    // grid exit, the rest, and they wait for this grid's results in their own
+    // grid_dep_wait().
+    if (p.mode == kGemmStoreRows || p.mode == kGemmStoreBf16) grid_dep_launch();
     const uint32_t tmem = tmem_slot;
     const int total = p.pass_tiles * p.n_tok_tiles * p.k_splits;
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
@@ -777,9 +817,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     } else {
         const int quarter = warp & 3;  // TMEM lanes this warp may access
         const int row_in_unit = (int)rank * kGemmTileW + quarter * 32 + lane;
-        // the tile columns this warp takes: one half of them
-        const int cb = ((warp - 2) / 4) * kPairEpiCols;
-        const int ce = min(p.bn, cb + kPairEpiCols);
+        // the tile columns this warp takes: one half of them (the store modes
+        // split any tile evenly in chunks of 32; the candidate modes keep
+        // halves of kPairEpiCols, their scratch size)
+        const bool store_mode = p.mode == kGemmStoreRows || p.mode == kGemmStoreBf16;
+        const int half = store_mode ? (p.bn + 63) / 64 * 32 : kPairEpiCols;
+        const int cb = ((warp - 2) / 4) * half;
+        const int ce = min(p.bn, cb + half);
+        // bf16 stores: the warp's transpose tile after the stages
+        __nv_bfloat16 *bf_tile = reinterpret_cast<__nv_bfloat16 *>(
+            h_smem + (size_t)p.stages * h_stage + (size_t)(warp - 2) * kBf16TileBytes);
+        const bool bf_vec = (reinterpret_cast<uintptr_t>(p.out_bf16) & 15) == 0 && p.ldo % 8 == 0;
         EpiScratchPair &es = epi[warp - 2];
         const uint32_t acc_empty_leader[2] = {mapa_shared(smem_u32(&acc_empty[0]), 0),
                                               mapa_shared(smem_u32(&acc_empty[1]), 0)};
@@ -878,7 +926,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                 float z[32];
                 tmem_ld32_wait(tbase + (uint32_t)c0, z);
                 if (scaled) fp8_scale_chunk(p, z, m_tile + c0, wsv, lane);
-                epilogue_chunk(p, z, v, row_in_unit, m_tile + c0, min(32, p.bn - c0), item, lane);
+                if (p.mode == kGemmStoreBf16)
+                    store_bf16_chunk(p, z, v - lane, m_tile + c0, min(32, p.bn - c0), bf_vec, bf_tile,
+                                     lane);
+                else
+                    epilogue_chunk(p, z, v, row_in_unit, m_tile + c0, min(32, p.bn - c0), item, lane);
             }
             tc_fence_before();
             __syncwarp();
@@ -997,7 +1049,8 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
     const size_t epi_bytes = p.mode == kGemmFilter || fused
                                  ? (pair ? kPairEpiWarps * sizeof(EpiScratchPair)
                                          : 4 * sizeof(EpiScratch))
-                                 : 0;
+                             : p.mode == kGemmStoreBf16 && pair ? (size_t)kPairEpiWarps * kBf16TileBytes
+                                                                 : 0;
     int stages = (int)((kGemmSmemBytes - 1024 - epi_bytes) / stage_bytes);
     if (stages > kGemmMaxStages) stages = kGemmMaxStages;
     if (nv) {

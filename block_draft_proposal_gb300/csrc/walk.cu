@@ -44,6 +44,10 @@ struct WalkParams {
     const float *uniforms;
     int32_t batch, slots, rank, k;
     bool bulk_ids;
+    // launched right after this library's projection of the same call: the
+    // candidates, anchors and tables were complete before that projection
+    // started, so the walk may read them before its grid dependency wait
+    bool after_projection;
     int64_t *tokens;
     float *q;
     float *path_scores;
@@ -644,7 +648,7 @@ __device__ __forceinline__ void chain_store_b(uint8_t *bbuf, int row_bytes, int 
 template <int KM, int CH, bool REGB>
 __global__ void __launch_bounds__(kChainThreads, 4)
     walk_chain_kernel(const WalkParams p, ChainLayout L) {
-    grid_dep_wait();
+    if (!p.after_projection) grid_dep_wait();
     extern __shared__ __align__(16) uint8_t dyn[];
     constexpr int CPH = KM / 8;  // candidates per half-warp
     constexpr int E = KM / 32;   // candidates per lane of the selecting warp
@@ -695,20 +699,25 @@ __global__ void __launch_bounds__(kChainThreads, 4)
     for (int j = tid; j < nch; j += kChainThreads)
         reinterpret_cast<uint4 *>(abuf)[j] =
             anchor_ok ? __ldg(reinterpret_cast<const uint4 *>(A + anchor * R) + j) : make_uint4(0, 0, 0, 0);
-    // A rows of slot 0's candidates; B rows of slots 0 and 1
+    // B rows of slots 0 and 1
     uint4 bq[NBQ];
-    if (warp > 0) {
-        chain_copy_slot(p, row0, sdat, &sbar[0], ct);
-        if (S > 1) chain_copy_slot(p, row0 + 1, sdat + L.slot_floats, &sbar[1], ct);
-        if constexpr (!REGB) {
+    if constexpr (!REGB) {
+        if (warp > 0) {
             chain_copy_rows(ids, K, B, R, nch, lg, bbuf, &bbar[0], ct);
             if (S > 1) chain_copy_rows(ids + K, K, B, R, nch, lg, bbuf + gbytes, &bbar[1], ct);
         }
-    }
-    if constexpr (REGB) {
+    } else {
         chain_load_b<CPH, CH>(B, ids, K, R, nch, hw, l16, bq);
         chain_store_b<CPH, CH>(bbuf, L.row_bytes, K, nch, hw, l16, bq);
         if (S > 1) chain_load_b<CPH, CH>(B, ids + K, K, R, nch, hw, l16, bq);
+    }
+    // Up to here the kernel has read only the candidates, anchors and tables;
+    // the slot data (the projection partials, written by the kernel before
+    // this one) after the grid dependency.
+    grid_dep_wait();
+    if (warp > 0) {
+        chain_copy_slot(p, row0, sdat, &sbar[0], ct);
+        if (S > 1) chain_copy_slot(p, row0 + 1, sdat + L.slot_floats, &sbar[1], ct);
     }
 
     // the lane that adds the unary value and stores candidate cw's edge
@@ -1532,11 +1541,11 @@ extern "C" dflash2_status dflash2_selector_walk(
     s = run_projection(di, h, proj, (int64_t)batch * slots, hidden, rank, dtype,
                        static_cast<float *>(workspace), err_word, st);
     if (s != DFLASH2_OK) return s;
-    return run_walk(di,
-                    walk_params(A, B, table_rows, anchor_ids, cand_ids, cand_u, temperatures,
-                                greedy, uniforms, batch, slots, rank, top_k, tokens, q,
-                                path_scores, err_word),
-                    hidden, dtype, workspace, st);
+    WalkParams wp = walk_params(A, B, table_rows, anchor_ids, cand_ids, cand_u, temperatures, greedy,
+                                uniforms, batch, slots, rank, top_k, tokens, q, path_scores,
+                                err_word);
+    wp.after_projection = true;
+    return run_walk(di, wp, hidden, dtype, workspace, st);
 }
 
 extern "C" dflash2_status dflash2_selector_project(const void *h, const void *proj, int32_t batch,
