@@ -44,6 +44,7 @@ namespace {
 constexpr uint32_t kWTileBytes = kGemmTileW * kGemmTileK * 2;  // one weight box: 16 KiB
 constexpr uint32_t kWStageBytes = 2 * kWTileBytes;              // weight rows of one stage
 constexpr size_t kGemmSmemBytes = 220 * 1024;                   // dynamic shared memory cap
+constexpr double kTokGroupBytes = 64.0 * 1024 * 1024;          // token rows kept in L2 per group
 
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
     const uint64_t t0 = global_timer_ns();
@@ -142,8 +143,20 @@ __device__ __forceinline__ Item decode(const GemmParams &p, int w) {
     Item it;
     it.ks = w % p.k_splits;
     const int rest = w / p.k_splits;
-    it.nt = rest % p.n_tok_tiles;
-    it.j = rest / p.n_tok_tiles;
+    if (p.tok_group <= 0 || p.tok_group >= p.n_tok_tiles) {
+        it.nt = rest % p.n_tok_tiles;
+        it.j = rest / p.n_tok_tiles;
+    } else {
+        // groups of tok_group token tiles, each over every weight unit of the
+        // pass, token tiles fastest within a group
+        const int per = p.tok_group * p.pass_tiles;
+        const int q = rest / per;
+        const int r = rest - q * per;
+        const int t0 = q * p.tok_group;
+        const int gq = min(p.tok_group, p.n_tok_tiles - t0);
+        it.nt = t0 + r % gq;
+        it.j = r / gq;
+    }
     it.wt = pass_tile(p, it.j);
     it.pilot = p.mode == kGemmPilot || (p.mode == kGemmFused && it.j < p.n_pilot);
     it.filter = p.mode == kGemmFilter || (p.mode == kGemmFused && it.j >= p.n_pilot);
@@ -1039,6 +1052,18 @@ dflash2_status launch_gemm_tc(const DeviceInfo &di, const void *w, const void *h
         p.kb_per_split = p.num_kb;
     }
     if (p.mode == kGemmStoreRows && (!pair || p.fp8 || p.ldo % 4 != 0)) return DFLASH2_ERR_INVALID_ARG;
+    // Work order: the pairs take consecutive items, token tiles fastest, so a
+    // weight unit is read from DRAM once while every token tile passes over it
+    // from L2.  When the token tiles' rows exceed what the L2 keeps beside the
+    // weight units in flight, they go in groups, each group over the whole
+    // pass: the weights are read once per group, the tokens once.  (The fused
+    // mode keeps one group: its pilot items come first.)
+    p.tok_group = p.n_tok_tiles;
+    if (p.mode != kGemmFused) {
+        const double tile_bytes = (double)p.bn * (double)kdim * ((p.fp8 || nv) ? 1.0 : 2.0);
+        const int64_t groups = (int64_t)((p.n_tok_tiles * tile_bytes + kTokGroupBytes - 1) / kTokGroupBytes);
+        if (groups > 1) p.tok_group = (int32_t)((p.n_tok_tiles + groups - 1) / groups);
+    }
     uint32_t acc = 32;
     while (acc < (uint32_t)p.bn) acc <<= 1;
     p.acc_cols = acc;

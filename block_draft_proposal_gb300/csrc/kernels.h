@@ -51,6 +51,7 @@ struct GemmParams {
     int32_t pilot_stride;
     int32_t pass_tiles;
     int32_t unit;     // weight rows per work unit: 128 (one CTA) or 256 (a CTA pair)
+    int32_t tok_group; // token tiles per group of the work order (filled by launch_gemm_tc)
     int32_t stages;
     uint32_t acc_cols;
     // epilogue
