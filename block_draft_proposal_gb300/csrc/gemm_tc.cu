@@ -31,9 +31,11 @@
 //
 // Work items are ordered with the token tile fastest, so the CTAs that run
 // at the same time share weight tiles in L2 and the weight matrix streams
-// from HBM about once.  Modes: store (split-K fp32 partials), store-bf16, the
-// top-K's pilot and filter passes, and their fused cooperative launch (the
-// CTA-pair variant below).
+// from HBM about once per group of token tiles (the token rows go in groups
+// of at most 64 MB).  Modes: store (split-K fp32 partials), store-rows,
+// store-bf16, the top-K's pilot and filter passes, and their fused
+// cooperative launch (the CTA-pair variant below).  The store modes let the
+// next kernel on the stream launch at their entry.
 #include "kernels.h"
 
 #include <atomic>
